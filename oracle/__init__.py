@@ -1,0 +1,141 @@
+"""fp64 CPU oracle for y = x.W^T, r = r0 + y, out = RMSNorm(r).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
+CPU-baseline / reference leg may import this package; the library under
+``decoder_layer_projection_gb300`` never does.  The arithmetic lives in
+``oracle.c`` (plain C, fp64); this module compiles it with gcc and marshals
+numpy arrays through ctypes.  It shares no code with the CUDA path.
+
+The definitions it follows are cited in ``oracle.c``'s header (vLLM "TPSP
+Design", sections 1, 3 and 4; torch-spyre "Plugin Architecture", the
+GemmaRMSNorm / RowParallelLinear rows and "Transformers backend").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+NORM_STANDARD = 0
+NORM_GEMMA = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            p = ctypes.c_void_p
+            L = ctypes.c_long
+            lib.oracle_proj_add_rmsnorm.argtypes = [
+                p, p, p, p, ctypes.c_double, ctypes.c_int, L, L, L, p, L, p, p, p, ctypes.c_int]
+            lib.oracle_proj_add_rmsnorm.restype = ctypes.c_int
+            lib.oracle_add_rmsnorm.argtypes = [
+                p, p, p, ctypes.c_double, ctypes.c_int, L, L, p, p, p, ctypes.c_int]
+            lib.oracle_add_rmsnorm.restype = ctypes.c_int
+            lib.oracle_round_to_bf16.argtypes = [p, L, p]
+            lib.oracle_round_to_bf16.restype = None
+            lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+            lib.oracle_max_threads.argtypes = []
+            lib.oracle_max_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def _u16(a, shape):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("bf16 operands are passed as their uint16 bit patterns")
+    if a.shape != shape:
+        raise ValueError(f"expected shape {shape}, got {a.shape}")
+    return a
+
+
+def proj_add_rmsnorm(x, W, r0, gamma, eps, norm_kind, rows=None, nthreads=0):
+    """Return (r, o, ms) in float64 for the selected token rows (all if None).
+
+    x [T,K], W [H,K], r0 [T,H] are bf16 bit patterns (uint16); gamma [H] is
+    float32.  r = r0 + x.W^T, o = RMSNorm(r), ms = mean_h r^2.
+    """
+    lib = _load()
+    T, K = np.shape(x)
+    H = np.shape(W)[0]
+    x = _u16(x, (T, K))
+    W = _u16(W, (H, K))
+    r0 = _u16(r0, (T, H))
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    if gamma.shape != (H,):
+        raise ValueError("gamma must be [H]")
+    rows_arr = None
+    n = T
+    if rows is not None:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n = rows_arr.shape[0]
+    r = np.empty((n, H), np.float64)
+    o = np.empty((n, H), np.float64)
+    ms = np.empty((n,), np.float64)
+    rc = lib.oracle_proj_add_rmsnorm(_ptr(x), _ptr(W), _ptr(r0), _ptr(gamma), float(eps),
+                                     int(norm_kind), T, K, H, _ptr(rows_arr), n,
+                                     _ptr(r), _ptr(o), _ptr(ms), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return r, o, ms
+
+
+def add_rmsnorm(y, r0, gamma, eps, norm_kind, nthreads=0):
+    """Return (r, o, ms) in float64: r = r0 + y (both bf16), o = RMSNorm(r)."""
+    lib = _load()
+    T, H = np.shape(y)
+    y = _u16(y, (T, H))
+    r0 = _u16(r0, (T, H))
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    if gamma.shape != (H,):
+        raise ValueError("gamma must be [H]")
+    r = np.empty((T, H), np.float64)
+    o = np.empty((T, H), np.float64)
+    ms = np.empty((T,), np.float64)
+    rc = lib.oracle_add_rmsnorm(_ptr(y), _ptr(r0), _ptr(gamma), float(eps), int(norm_kind),
+                                T, H, _ptr(r), _ptr(o), _ptr(ms), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return r, o, ms
+
+
+def round_to_bf16(v):
+    """Round float64 values to bf16 bit patterns (nearest, ties to even)."""
+    lib = _load()
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, np.uint16)
+    lib.oracle_round_to_bf16(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())

@@ -1,0 +1,220 @@
+/*
+ * oracle.c -- fp64 CPU oracle for the dense decoder-layer region
+ *             y = x . W^T ; r = r0 + y ; out = RMSNorm(r)
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load this file's library.  The
+ * product path (libfusedln) never links, loads or calls it, and the two share
+ * no code, headers, tables or helpers.
+ *
+ * What it follows (vLLM "TPSP Design" page, and the torch-spyre "Plugin
+ * Architecture" page for the norm semantics):
+ *   - row-parallel projection o_proj / down_proj, F.linear semantics
+ *     y = x @ W^T with W stored [out, in] = [H, K]
+ *       ("Plugin Architecture", "Custom Op Replacement" table, RowParallelLinear
+ *        row; "Transposed linear weights");
+ *   - residual add then RMSNorm over the complete hidden dimension of each
+ *     token ("TPSP Design", section 1 "Motivation": local residual add and norm
+ *     keep the full hidden size per token; section 3 "Fusion regions");
+ *   - standard RMSNorm without norm bias ("TPSP Design", section 4
+ *     "Constraints"), computed in a wider type than the bf16 activations
+ *     ("Plugin Architecture", "Transformers backend": the fp16->fp32 upcast of
+ *     the native RMSNorm forward);
+ *   - Gemma RMSNorm: the same body with a trailing multiply by (1 + gamma),
+ *     gamma an fp32 [hidden] weight ("Plugin Architecture", table row
+ *     GemmaRMSNorm; "TPSP Design", section 5 "To-do", Gemma family).
+ *
+ * Readings where the pages print no formula (each listed in the design notes):
+ *   - RMSNorm(r)[h] = r[h] / sqrt(mean_h(r^2) + eps) * g[h], eps inside the
+ *     square root, mean over the full hidden dimension H;
+ *   - the projection output is not rounded before the residual add, and the
+ *     norm statistics come from the unrounded sum;
+ *   - g[h] = gamma[h] (standard) or 1 + gamma[h] (Gemma).
+ *
+ * Arithmetic: every bf16 input is widened exactly to double, the dot product
+ * is accumulated in double in ascending k, and nothing is blocked, fused or
+ * reordered beyond the definition above.  Rows are independent, so rows are
+ * spread over OpenMP threads; that changes no result bit.
+ *
+ * Pins (tests/test_oracle.py): hand-worked 2x2, 4x4 and 1x3x2 cases, the
+ * closed form of a constant row, the unit-RMS invariant, Gemma(0)==standard(1)
+ * bit for bit, linearity of the residual add, eps=0 scale invariance, column
+ * permutation of K, and the projection against numpy's float64 matmul.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_NORM_STANDARD 0
+#define ORACLE_NORM_GEMMA 1
+
+/* bf16 bit pattern -> double.  bf16 is the top half of an IEEE binary32, so
+ * the widening is exact. */
+static double bf16_bits_to_double(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* double -> bf16 bit pattern, round to nearest, ties to even, in one rounding
+ * step from the exact double value (no intermediate binary32).
+ * bf16: 1 sign bit, 8 exponent bits (bias 127), 7 stored fraction bits. */
+uint16_t oracle_double_to_bf16(double v)
+{
+    if (isnan(v))
+        return (uint16_t)0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0x0000;
+    double a = fabs(v);
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80);
+    if (a == 0.0)
+        return sign;
+    int e;
+    (void)frexp(a, &e);            /* a = m * 2^e, m in [0.5, 1) */
+    int exp_unbiased = e - 1;      /* a = 1.f * 2^exp_unbiased */
+    int quantum_exp;               /* spacing of representable values near a */
+    if (exp_unbiased >= -126)
+        quantum_exp = exp_unbiased - 7;  /* 8 significant bits */
+    else
+        quantum_exp = -126 - 7;          /* subnormal spacing 2^-133 */
+    double q = ldexp(a, -quantum_exp);   /* exact: scaling by a power of two */
+    double qi = nearbyint(q);            /* default mode: nearest, ties to even */
+    double rounded = ldexp(qi, quantum_exp);
+    if (rounded >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80); /* overflow to infinity */
+    /* rounded has at most 8 significant bits and lies in binary32 range, so
+     * the conversion to float is exact and its top 16 bits are the bf16. */
+    float f = (float)rounded;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (uint16_t)((u >> 16) & 0x7FFF));
+}
+
+void oracle_round_to_bf16(const double *v, long n, uint16_t *out)
+{
+    for (long i = 0; i < n; ++i)
+        out[i] = oracle_double_to_bf16(v[i]);
+}
+
+static double norm_weight(const float *gamma, long h, int norm_kind)
+{
+    double g = (double)gamma[h];
+    return norm_kind == ORACLE_NORM_GEMMA ? 1.0 + g : g;
+}
+
+/* RMSNorm of one row r[0..H) in place into o[0..H); returns mean square. */
+static double rmsnorm_row(const double *r, long H, const float *gamma, double eps,
+                          int norm_kind, double *o)
+{
+    double sum_sq = 0.0;
+    for (long h = 0; h < H; ++h)
+        sum_sq += r[h] * r[h];
+    double mean_sq = sum_sq / (double)H;
+    double inv_rms = 1.0 / sqrt(mean_sq + eps);
+    for (long h = 0; h < H; ++h)
+        o[h] = r[h] * inv_rms * norm_weight(gamma, h, norm_kind);
+    return mean_sq;
+}
+
+static int check_args(long T, long K, long H, int norm_kind, double eps)
+{
+    if (T < 0 || K < 0 || H <= 0)
+        return -1;
+    if (norm_kind != ORACLE_NORM_STANDARD && norm_kind != ORACLE_NORM_GEMMA)
+        return -1;
+    if (!(eps >= 0.0) || isinf(eps))
+        return -1;
+    return 0;
+}
+
+/*
+ * Full region for the selected token rows.
+ *   x      [T, K] bf16 bits, row-major
+ *   W      [H, K] bf16 bits, row-major ([out, in], F.linear layout)
+ *   r0     [T, H] bf16 bits, residual before the add
+ *   gamma  [H] fp32 norm weight
+ *   rows   indices of the token rows to compute, or NULL for all T rows
+ *   nrows  number of entries in rows (ignored when rows is NULL)
+ *   r_out  [n, H] double: r = r0 + x . W^T        (n = nrows or T)
+ *   o_out  [n, H] double: RMSNorm(r)
+ *   ms_out [n] double: mean over h of r^2, or NULL
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_proj_add_rmsnorm(const uint16_t *x, const uint16_t *W, const uint16_t *r0,
+                            const float *gamma, double eps, int norm_kind,
+                            long T, long K, long H, const long *rows, long nrows,
+                            double *r_out, double *o_out, double *ms_out, int nthreads)
+{
+    if (check_args(T, K, H, norm_kind, eps))
+        return -1;
+    long n = rows ? nrows : T;
+    for (long i = 0; rows && i < n; ++i)
+        if (rows[i] < 0 || rows[i] >= T)
+            return -1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long i = 0; i < n; ++i) {
+        long t = rows ? rows[i] : i;
+        const uint16_t *xt = x + t * K;
+        double *r = r_out + i * H;
+        for (long h = 0; h < H; ++h) {
+            const uint16_t *wh = W + h * K;
+            double y = 0.0;
+            for (long k = 0; k < K; ++k)
+                y += bf16_bits_to_double(xt[k]) * bf16_bits_to_double(wh[k]);
+            r[h] = bf16_bits_to_double(r0[t * H + h]) + y;
+        }
+        double ms = rmsnorm_row(r, H, gamma, eps, norm_kind, o_out + i * H);
+        if (ms_out)
+            ms_out[i] = ms;
+    }
+    return 0;
+}
+
+/*
+ * Add + RMSNorm alone, with a bf16 addend y (the unfused path's second step).
+ *   y [T, H] bf16, r0 [T, H] bf16, gamma [H] fp32; outputs as above.
+ */
+int oracle_add_rmsnorm(const uint16_t *y, const uint16_t *r0, const float *gamma,
+                       double eps, int norm_kind, long T, long H,
+                       double *r_out, double *o_out, double *ms_out, int nthreads)
+{
+    if (check_args(T, 0, H, norm_kind, eps))
+        return -1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(static)
+    for (long t = 0; t < T; ++t) {
+        double *r = r_out + t * H;
+        for (long h = 0; h < H; ++h)
+            r[h] = bf16_bits_to_double(r0[t * H + h]) + bf16_bits_to_double(y[t * H + h]);
+        double ms = rmsnorm_row(r, H, gamma, eps, norm_kind, o_out + t * H);
+        if (ms_out)
+            ms_out[t] = ms;
+    }
+    return 0;
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

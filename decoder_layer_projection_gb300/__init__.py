@@ -1,0 +1,220 @@
+"""GB300-native fused projection + residual add + RMSNorm (libfusedln).
+
+A thin ctypes binding over the C ABI declared in ``include/libfusedln.h``.
+The functions here carry the same names as the C entry points and only
+marshal arguments: tensor shapes and device pointers in, status codes out.
+Every step of the computation runs in the library's CUDA kernels; if the
+shared library is missing, the first call raises -- there is no CPU path.
+
+PyTorch provides the device memory and the streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfusedln.so")
+
+FLN_OK = 0
+FLN_ERR_INVALID_ARG = -1
+FLN_ERR_UNSUPPORTED = -2
+FLN_ERR_CUDA = -3
+FLN_ERR_DEVICE_TIMEOUT = -4
+FLN_ERR_NOT_TUNED = -5
+
+NORM_STANDARD = 0
+NORM_GEMMA = 1
+
+PATH_FUSED = 1
+PATH_PIPELINED = 2
+PATH_UNFUSED = 3
+
+KERNEL_NAMES = ("gemm_fused", "gemm_slot", "gemm_splitk", "norm_bf16", "norm_slot", "norm_splitk")
+
+EXPORTED_SYMBOLS = (
+    "fused_proj_add_rmsnorm", "add_rmsnorm", "fln_autotune", "fln_set_overrides", "fln_set_plan",
+    "fln_get_plan", "fln_device_status", "fln_last_error", "fln_release_workspace", "fln_launch_count",
+    "fln_profile_enable", "fln_profile_read", "fln_version",
+)
+
+
+class FlnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"libfusedln status {status}: {message}")
+        self.status = status
+        self.message = message
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("microchunk_tokens", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("gemm_ctas", ctypes.c_int), ("norm_ctas", ctypes.c_int), ("threshold_tokens", ctypes.c_int),
+                ("tuned_max_tokens", ctypes.c_int)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class ProfileStats(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_uint64 * 6), ("total_ms", ctypes.c_double * 6)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load libfusedln.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it first (python -m decoder_layer_projection_gb300._build)")
+        lib = ctypes.CDLL(p)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.fused_proj_add_rmsnorm.argtypes = [vp, vp, vp, vp, f, i, i, i, i, i, vp, vp]
+        lib.fused_proj_add_rmsnorm.restype = i
+        lib.add_rmsnorm.argtypes = [vp, vp, vp, f, i, i, i, vp, vp]
+        lib.add_rmsnorm.restype = i
+        lib.fln_autotune.argtypes = [i, i, i, i, vp]
+        lib.fln_autotune.restype = i
+        lib.fln_set_overrides.argtypes = [i, i]
+        lib.fln_set_overrides.restype = i
+        lib.fln_set_plan.argtypes = [i, i, i, ctypes.POINTER(Plan)]
+        lib.fln_set_plan.restype = i
+        lib.fln_get_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(Plan)]
+        lib.fln_get_plan.restype = i
+        lib.fln_device_status.argtypes = [vp]
+        lib.fln_device_status.restype = i
+        lib.fln_last_error.argtypes = []
+        lib.fln_last_error.restype = ctypes.c_char_p
+        lib.fln_release_workspace.argtypes = []
+        lib.fln_release_workspace.restype = None
+        lib.fln_launch_count.argtypes = []
+        lib.fln_launch_count.restype = ctypes.c_uint64
+        lib.fln_profile_enable.argtypes = [i]
+        lib.fln_profile_enable.restype = i
+        lib.fln_profile_read.argtypes = [ctypes.POINTER(ProfileStats)]
+        lib.fln_profile_read.restype = i
+        lib.fln_version.argtypes = []
+        lib.fln_version.restype = i
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != FLN_OK:
+        raise FlnError(status, load().fln_last_error().decode(errors="replace"))
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def fused_proj_add_rmsnorm(x, W, residual, gamma, eps: float, norm_kind: int = NORM_STANDARD,
+                           microchunk_tokens: int = 0, out=None, stream=None):
+    """residual += x @ W^T; out = RMSNorm(residual).  Tensors: x [T,K] bf16,
+    W [H,K] bf16, residual [T,H] bf16 (in place), gamma [H] fp32, out [T,H] bf16.
+    Returns out."""
+    T, K = x.shape
+    H = W.shape[0]
+    if out is None:
+        import torch
+        out = torch.empty((T, H), dtype=residual.dtype, device=residual.device)
+    _check(load().fused_proj_add_rmsnorm(_ptr(x), _ptr(W), _ptr(residual), _ptr(gamma), float(eps),
+                                         int(norm_kind), int(T), int(K), int(H), int(microchunk_tokens),
+                                         _ptr(out), _stream_ptr(stream)))
+    return out
+
+
+def fused_proj_add_rmsnorm_ptr(x_ptr, W_ptr, residual_ptr, gamma_ptr, eps, norm_kind, T, K, H,
+                               microchunk_tokens, out_ptr, stream_ptr) -> int:
+    """Raw-pointer form: returns the status code without raising."""
+    return load().fused_proj_add_rmsnorm(x_ptr, W_ptr, residual_ptr, gamma_ptr, float(eps), int(norm_kind),
+                                         int(T), int(K), int(H), int(microchunk_tokens), out_ptr, stream_ptr)
+
+
+def add_rmsnorm(y, residual, gamma, eps: float, norm_kind: int = NORM_STANDARD, out=None, stream=None):
+    """residual += y; out = RMSNorm(residual).  y, residual, out [T,H] bf16; gamma [H] fp32."""
+    T, H = y.shape
+    if out is None:
+        import torch
+        out = torch.empty((T, H), dtype=residual.dtype, device=residual.device)
+    _check(load().add_rmsnorm(_ptr(y), _ptr(residual), _ptr(gamma), float(eps), int(norm_kind), int(T), int(H),
+                              _ptr(out), _stream_ptr(stream)))
+    return out
+
+
+def add_rmsnorm_ptr(y_ptr, residual_ptr, gamma_ptr, eps, norm_kind, T, H, out_ptr, stream_ptr) -> int:
+    return load().add_rmsnorm(y_ptr, residual_ptr, gamma_ptr, float(eps), int(norm_kind), int(T), int(H),
+                              out_ptr, stream_ptr)
+
+
+def fln_autotune(K: int, H: int, norm_kind: int, max_tokens: int, stream=None):
+    _check(load().fln_autotune(int(K), int(H), int(norm_kind), int(max_tokens), _stream_ptr(stream)))
+
+
+def fln_set_overrides(microchunk_tokens: int = 0, threshold_tokens: int = 0):
+    _check(load().fln_set_overrides(int(microchunk_tokens), int(threshold_tokens)))
+
+
+def fln_set_plan(K: int, H: int, norm_kind: int, plan: Plan | dict | None):
+    if isinstance(plan, dict):
+        plan = Plan(**plan)
+    _check(load().fln_set_plan(int(K), int(H), int(norm_kind), ctypes.byref(plan) if plan is not None else None))
+
+
+def fln_get_plan(K: int, H: int, norm_kind: int, T: int, microchunk_tokens: int = 0) -> dict:
+    p = Plan()
+    _check(load().fln_get_plan(int(K), int(H), int(norm_kind), int(T), int(microchunk_tokens), ctypes.byref(p)))
+    return p.as_dict()
+
+
+def fln_device_status(stream=None):
+    _check(load().fln_device_status(_stream_ptr(stream)))
+
+
+def fln_last_error() -> str:
+    return load().fln_last_error().decode(errors="replace")
+
+
+def fln_release_workspace():
+    load().fln_release_workspace()
+
+
+def fln_launch_count() -> int:
+    return int(load().fln_launch_count())
+
+
+def fln_profile_enable(enable: bool = True):
+    _check(load().fln_profile_enable(1 if enable else 0))
+
+
+def fln_profile_read() -> dict:
+    s = ProfileStats()
+    _check(load().fln_profile_read(ctypes.byref(s)))
+    return {name: {"launches": int(s.launches[i]), "total_ms": float(s.total_ms[i])}
+            for i, name in enumerate(KERNEL_NAMES)}
+
+
+def fln_version() -> int:
+    return int(load().fln_version())
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)

@@ -1,0 +1,917 @@
+// fln_api.cu -- the C ABI of libfusedln: argument validation, per-device
+// workspace, plans (path, microchunk, tile width, SM-count targets, token
+// threshold), the microchunk scheduler with three slots on two streams, the
+// autotuner, overrides, error reporting and launch accounting.
+//
+// Behaviour follows the vLLM "TPSP Design" page: section 3 "Microchunk
+// pipeline" (chunk loop inside the native operator, GEMM then add/norm of a
+// chunk on a separate stream, three reusable slots guarded by readiness and
+// completion events, only valid rows written); section 3 "Profiling and
+// fallback" (tune microchunk size and SM-count targets per projection group,
+// numerical check of candidates before a token-threshold search, selection by
+// the actual token count, overrides that bypass the scan, errors propagate);
+// section 4 "Constraints" (microchunks capped at 4096 tokens, calls must fit
+// the profiled maximum, shared workspace assumes sequential calls).
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "fln_internal.h"
+#include "fln_ptx.cuh"
+#include "libfusedln.h"
+
+using namespace fln;
+
+namespace {
+
+constexpr int kMaxMicrochunk = 4096;   // per-call chunk cap ("TPSP Design", section 4)
+constexpr int kMaxUnfusedTokens = 256; // the split-K path puts T on the MMA's N side (N <= 256)
+constexpr int kMaxH = 32768;
+constexpr int kMaxK = 1 << 20;
+constexpr int kMaxT = 1 << 24;
+constexpr int kDefaultThreshold = kMaxUnfusedTokens + 1;
+
+thread_local std::string g_err;
+std::atomic<uint64_t> g_launches{0};
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(FLN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define FLN_CUDA(call, what)                         \
+  do {                                               \
+    cudaError_t e_ = (call);                         \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+// ------------------------------------------------------------------ workspace
+struct Workspace {
+  int device = -1;
+  int sms = 0;
+  unsigned int* err_word = nullptr;
+  float* psum = nullptr;
+  size_t psum_floats = 0;
+  unsigned int* flags = nullptr;
+  size_t flags_count = 0;
+  float* slots[3] = {nullptr, nullptr, nullptr};
+  size_t slot_floats = 0;
+  float* partial = nullptr;
+  size_t partial_floats = 0;
+  cudaStream_t stream_b = nullptr;
+  cudaEvent_t ev_ready[3] = {};
+  cudaEvent_t ev_free[3] = {};
+  cudaEvent_t ev_join = nullptr;
+  unsigned int gen = 0;
+  bool prepared[3][5] = {};
+};
+
+std::mutex g_mu;
+std::map<int, Workspace*> g_ws;
+
+struct GroupKey {
+  int K, H, kind;
+  bool operator<(const GroupKey& o) const { return std::tie(K, H, kind) < std::tie(o.K, o.H, o.kind); }
+};
+std::map<GroupKey, fln_plan> g_plans;
+int g_override_chunk = 0;
+int g_override_threshold = 0;
+
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+bool g_prof = false;
+std::vector<ProfRec> g_prof_recs;
+
+int bn_index(int bn) {
+  switch (bn) {
+    case 16: return 0;
+    case 32: return 1;
+    case 64: return 2;
+    case 128: return 3;
+    case 256: return 4;
+  }
+  return -1;
+}
+
+int get_ws(Workspace** out) {
+  int dev = 0;
+  FLN_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  auto it = g_ws.find(dev);
+  if (it != g_ws.end()) {
+    *out = it->second;
+    return FLN_OK;
+  }
+  Workspace* ws = new Workspace();
+  ws->device = dev;
+  cudaError_t e = cudaDeviceGetAttribute(&ws->sms, cudaDevAttrMultiProcessorCount, dev);
+  int major = 0, minor = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess) {
+    delete ws;
+    return cuda_fail(e, "device query");
+  }
+  if (major != 10 || minor != 3) {
+    delete ws;
+    return fail(FLN_ERR_UNSUPPORTED, "libfusedln is built for sm_103a (GB300); device %d is sm_%d%d", dev, major,
+                minor);
+  }
+  int lo = 0, hi = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&ws->stream_b, cudaStreamNonBlocking, hi);
+  for (int i = 0; i < 3 && e == cudaSuccess; ++i) {
+    e = cudaEventCreateWithFlags(&ws->ev_ready[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ws->ev_free[i], cudaEventDisableTiming);
+  }
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ws->ev_join, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaMalloc(&ws->err_word, sizeof(unsigned int));
+  if (e == cudaSuccess) e = cudaMemset(ws->err_word, 0, sizeof(unsigned int));
+  if (e != cudaSuccess) {
+    delete ws;  // partial handles leak only on a failing device
+    return cuda_fail(e, "workspace creation");
+  }
+  g_ws[dev] = ws;
+  *out = ws;
+  return FLN_OK;
+}
+
+// Grow a device buffer; waits for the device first because in-flight kernels
+// may still use the old one.
+template <typename T>
+int grow(T** p, size_t* cur, size_t need, bool zero, const char* what) {
+  if (need <= *cur) return FLN_OK;
+  FLN_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize before workspace growth");
+  if (*p) FLN_CUDA(cudaFree(*p), "cudaFree");
+  *p = nullptr;
+  *cur = 0;
+  FLN_CUDA(cudaMalloc(reinterpret_cast<void**>(p), need * sizeof(T)), what);
+  if (zero) FLN_CUDA(cudaMemset(*p, 0, need * sizeof(T)), what);
+  *cur = need;
+  return FLN_OK;
+}
+
+int prepare_kernel(Workspace* ws, int bn, EpilogueKind epi) {
+  const int bi = bn_index(bn);
+  if (bi < 0) return fail(FLN_ERR_UNSUPPORTED, "tile width %d", bn);
+  if (!ws->prepared[epi][bi]) {
+    FLN_CUDA(gemm_prepare(bn, epi), "cudaFuncSetAttribute(max dynamic shared memory)");
+    ws->prepared[epi][bi] = true;
+  }
+  return FLN_OK;
+}
+
+// ------------------------------------------------------------------ launches
+template <typename F>
+int launch_counted(int kind, cudaStream_t s, F&& fn, const char* what) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (g_prof) {
+    FLN_CUDA(cudaEventCreate(&a), "cudaEventCreate");
+    FLN_CUDA(cudaEventCreate(&b), "cudaEventCreate");
+    FLN_CUDA(cudaEventRecord(a, s), "cudaEventRecord");
+  }
+  cudaError_t e = fn();
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (g_prof) {
+    FLN_CUDA(cudaEventRecord(b, s), "cudaEventRecord");
+    g_prof_recs.push_back({kind, a, b});
+  }
+  return FLN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, inner] (inner contiguous) read in boxes of
+// 64 x box_rows elements with 128-byte swizzle; out-of-range elements read 0.
+int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return fail(FLN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FLN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return FLN_OK;
+}
+
+struct Call {
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* W;
+  __nv_bfloat16* residual;
+  const float* gamma;
+  float eps;
+  int kind;
+  int T, K, H;
+  __nv_bfloat16* out;
+  cudaStream_t stream;
+};
+
+int round_bn_tokens(int T) {
+  if (T <= 16) return 16;
+  if (T <= 32) return 32;
+  if (T <= 64) return 64;
+  if (T <= 128) return 128;
+  return 256;
+}
+
+// T <= 256: split-K GEMM with H on the MMA's M side, then reduce + add + norm.
+int run_unfused(Workspace* ws, const Call& c) {
+  const int bn = round_bn_tokens(c.T);
+  int rc = prepare_kernel(ws, bn, EPI_SPLITK_SWAP);
+  if (rc) return rc;
+  CUtensorMap tmA, tmB;
+  if ((rc = make_map(&tmA, c.W, c.K, c.H, 128))) return rc;
+  if ((rc = make_map(&tmB, c.x, c.K, c.T, bn))) return rc;
+  GemmParams p{};
+  p.M = c.H;
+  p.N = c.T;
+  p.K = c.K;
+  p.a_row0 = 0;
+  p.num_m_tiles = (c.H + 127) / 128;
+  p.num_n_tiles = 1;
+  p.num_k_blocks = (c.K + 63) / 64;
+  p.units_total = static_cast<long long>(p.num_m_tiles) * p.num_k_blocks;
+  const int G = static_cast<int>(std::min<long long>(ws->sms, p.units_total));
+  int max_split = 1;
+  for (int m = 0; m < p.num_m_tiles; ++m) {
+    const long long KB = p.num_k_blocks;
+    const int a = splitk_cta_of_unit(m * KB, p.units_total, G);
+    const int b = splitk_cta_of_unit((m + 1) * KB - 1, p.units_total, G);
+    max_split = std::max(max_split, b - a + 1);
+  }
+  p.max_split = max_split;
+  const size_t need = static_cast<size_t>(p.num_m_tiles) * max_split * c.T * 128;
+  if ((rc = grow(&ws->partial, &ws->partial_floats, need, false, "cudaMalloc(split-K partials)"))) return rc;
+  p.partial = ws->partial;
+  p.err = ws->err_word;
+  rc = launch_counted(FLN_KERNEL_GEMM_SPLITK, c.stream,
+                      [&] { return launch_gemm(EPI_SPLITK_SWAP, bn, tmA, tmB, p, G, c.stream); },
+                      "split-K GEMM launch");
+  if (rc) return rc;
+  NormParams np{};
+  np.partial = ws->partial;
+  np.max_split = max_split;
+  np.num_k_blocks = p.num_k_blocks;
+  np.gemm_grid = G;
+  np.units_total = p.units_total;
+  np.residual = c.residual;
+  np.out = c.out;
+  np.gamma = c.gamma;
+  np.eps = c.eps;
+  np.norm_kind = c.kind;
+  np.T = c.T;
+  np.row0 = 0;
+  np.H = c.H;
+  return launch_counted(FLN_KERNEL_NORM_SPLITK, c.stream,
+                        [&] { return launch_add_rmsnorm(NORM_SRC_SPLITK, np, 0, c.stream); },
+                        "split-K add+norm launch");
+}
+
+int gemm_grid(Workspace* ws, const fln_plan& pl, long long tiles) {
+  int g = pl.gemm_ctas > 0 ? std::min(pl.gemm_ctas, ws->sms) : ws->sms;
+  return static_cast<int>(std::max<long long>(1, std::min<long long>(g, tiles)));
+}
+
+// Per microchunk: one persistent GEMM whose epilogue does add + norm.
+int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
+  const int bn = pl.tile_n;
+  int rc = prepare_kernel(ws, bn, EPI_FUSED_NORM);
+  if (rc) return rc;
+  CUtensorMap tmA, tmB;
+  if ((rc = make_map(&tmA, c.x, c.K, c.T, 128))) return rc;
+  if ((rc = make_map(&tmB, c.W, c.K, c.H, bn))) return rc;
+  const int chunk = std::min(pl.microchunk_tokens, c.T);
+  const int mt = (chunk + 127) / 128;
+  const int nt = (c.H + bn - 1) / bn;
+  if ((rc = grow(&ws->psum, &ws->psum_floats, static_cast<size_t>(mt) * nt * 128, false, "cudaMalloc(row sums)")))
+    return rc;
+  if ((rc = grow(&ws->flags, &ws->flags_count, static_cast<size_t>(mt) * nt, true, "cudaMalloc(row flags)")))
+    return rc;
+  for (int c0 = 0; c0 < c.T; c0 += chunk) {
+    const int n = std::min(chunk, c.T - c0);
+    GemmParams p{};
+    p.M = n;
+    p.N = c.H;
+    p.K = c.K;
+    p.a_row0 = c0;
+    p.num_m_tiles = (n + 127) / 128;
+    p.num_n_tiles = nt;
+    p.num_k_blocks = (c.K + 63) / 64;
+    p.residual = c.residual;
+    p.out = c.out;
+    p.gamma = c.gamma;
+    p.eps = c.eps;
+    p.norm_kind = c.kind;
+    p.ld = c.H;
+    p.psum = ws->psum;
+    p.flags = ws->flags;
+    if (++ws->gen == 0) ++ws->gen;
+    p.gen = ws->gen;
+    p.err = ws->err_word;
+    // every CTA of the grid must be resident at once (they exchange row
+    // statistics), so the grid never exceeds one CTA per SM
+    const int G = gemm_grid(ws, pl, static_cast<long long>(p.num_m_tiles) * nt);
+    rc = launch_counted(FLN_KERNEL_GEMM_FUSED, c.stream,
+                        [&] { return launch_gemm(EPI_FUSED_NORM, bn, tmA, tmB, p, G, c.stream); },
+                        "fused GEMM launch");
+    if (rc) return rc;
+  }
+  return FLN_OK;
+}
+
+// Per microchunk: GEMM -> slot (caller's stream), add + norm of the slot on
+// the library's second stream; three slots guarded by events.
+int run_pipelined(Workspace* ws, const Call& c, const fln_plan& pl) {
+  const int bn = pl.tile_n;
+  int rc = prepare_kernel(ws, bn, EPI_STORE_F32);
+  if (rc) return rc;
+  CUtensorMap tmA, tmB;
+  if ((rc = make_map(&tmA, c.x, c.K, c.T, 128))) return rc;
+  if ((rc = make_map(&tmB, c.W, c.K, c.H, bn))) return rc;
+  const int chunk = std::min(pl.microchunk_tokens, c.T);
+  const size_t slot_need = static_cast<size_t>(chunk) * c.H;
+  if (slot_need > ws->slot_floats) {
+    FLN_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize before slot growth");
+    for (int i = 0; i < 3; ++i) {
+      if (ws->slots[i]) FLN_CUDA(cudaFree(ws->slots[i]), "cudaFree");
+      ws->slots[i] = nullptr;
+    }
+    ws->slot_floats = 0;
+    for (int i = 0; i < 3; ++i)
+      FLN_CUDA(cudaMalloc(&ws->slots[i], slot_need * sizeof(float)), "cudaMalloc(pipeline slots)");
+    ws->slot_floats = slot_need;
+  }
+  const int nt = (c.H + bn - 1) / bn;
+  int i = 0;
+  for (int c0 = 0; c0 < c.T; c0 += chunk, ++i) {
+    const int s = i % 3;
+    const int n = std::min(chunk, c.T - c0);
+    if (i >= 3) FLN_CUDA(cudaStreamWaitEvent(c.stream, ws->ev_free[s], 0), "cudaStreamWaitEvent(slot free)");
+    GemmParams p{};
+    p.M = n;
+    p.N = c.H;
+    p.K = c.K;
+    p.a_row0 = c0;
+    p.num_m_tiles = (n + 127) / 128;
+    p.num_n_tiles = nt;
+    p.num_k_blocks = (c.K + 63) / 64;
+    p.ld = c.H;
+    p.yout = ws->slots[s];
+    p.err = ws->err_word;
+    const int G = gemm_grid(ws, pl, static_cast<long long>(p.num_m_tiles) * nt);
+    rc = launch_counted(FLN_KERNEL_GEMM_SLOT, c.stream,
+                        [&] { return launch_gemm(EPI_STORE_F32, bn, tmA, tmB, p, G, c.stream); },
+                        "slot GEMM launch");
+    if (rc) return rc;
+    FLN_CUDA(cudaEventRecord(ws->ev_ready[s], c.stream), "cudaEventRecord(slot ready)");
+    FLN_CUDA(cudaStreamWaitEvent(ws->stream_b, ws->ev_ready[s], 0), "cudaStreamWaitEvent(slot ready)");
+    NormParams np{};
+    np.y_f32 = ws->slots[s];
+    np.residual = c.residual;
+    np.out = c.out;
+    np.gamma = c.gamma;
+    np.eps = c.eps;
+    np.norm_kind = c.kind;
+    np.T = n;
+    np.row0 = c0;
+    np.H = c.H;
+    rc = launch_counted(FLN_KERNEL_NORM_SLOT, ws->stream_b,
+                        [&] { return launch_add_rmsnorm(NORM_SRC_F32, np, pl.norm_ctas, ws->stream_b); },
+                        "slot add+norm launch");
+    if (rc) return rc;
+    FLN_CUDA(cudaEventRecord(ws->ev_free[s], ws->stream_b), "cudaEventRecord(slot free)");
+  }
+  FLN_CUDA(cudaEventRecord(ws->ev_join, ws->stream_b), "cudaEventRecord(join)");
+  FLN_CUDA(cudaStreamWaitEvent(c.stream, ws->ev_join, 0), "cudaStreamWaitEvent(join)");
+  return FLN_OK;
+}
+
+// ------------------------------------------------------------------ validation
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+int check_ptr(const char* name, const void* p) {
+  if (!p) return fail(FLN_ERR_INVALID_ARG, "%s is NULL", name);
+  if (reinterpret_cast<uintptr_t>(p) & 15u) return fail(FLN_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(FLN_ERR_INVALID_ARG, "%s: cudaPointerGetAttributes failed (%s)", name, cudaGetErrorName(e));
+  }
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+    return fail(FLN_ERR_INVALID_ARG, "%s is not a device pointer", name);
+  return FLN_OK;
+}
+
+int check_common(float eps, int kind, int T, int H) {
+  if (kind != FLN_NORM_STANDARD && kind != FLN_NORM_GEMMA)
+    return fail(FLN_ERR_INVALID_ARG, "norm_kind %d is neither standard (0) nor Gemma (1)", kind);
+  if (!(eps >= 0.0f) || std::isinf(eps)) return fail(FLN_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (T < 0 || T > kMaxT) return fail(FLN_ERR_INVALID_ARG, "T=%d outside [0, %d]", T, kMaxT);
+  if (H < 8 || (H & 7)) return fail(FLN_ERR_INVALID_ARG, "H=%d must be a positive multiple of 8", H);
+  if (H > kMaxH) return fail(FLN_ERR_UNSUPPORTED, "H=%d above the supported %d", H, kMaxH);
+  return FLN_OK;
+}
+
+fln_plan default_plan() {
+  fln_plan p;
+  p.path = FLN_PATH_FUSED;
+  p.microchunk_tokens = kMaxMicrochunk;
+  p.tile_n = 256;
+  p.gemm_ctas = 0;
+  p.norm_ctas = 0;
+  p.threshold_tokens = kDefaultThreshold;
+  p.tuned_max_tokens = 0;
+  return p;
+}
+
+int check_plan(const fln_plan& p) {
+  if (p.path != FLN_PATH_FUSED && p.path != FLN_PATH_PIPELINED)
+    return fail(FLN_ERR_INVALID_ARG, "plan.path must be FUSED or PIPELINED");
+  if (p.microchunk_tokens < 1 || p.microchunk_tokens > kMaxMicrochunk)
+    return fail(FLN_ERR_INVALID_ARG, "plan.microchunk_tokens must be in 1..%d", kMaxMicrochunk);
+  if (p.tile_n != 128 && p.tile_n != 256) return fail(FLN_ERR_INVALID_ARG, "plan.tile_n must be 128 or 256");
+  if (p.gemm_ctas < 0 || p.norm_ctas < 0) return fail(FLN_ERR_INVALID_ARG, "plan CTA targets must be >= 0");
+  if (p.threshold_tokens < 1 || p.threshold_tokens > kDefaultThreshold)
+    return fail(FLN_ERR_INVALID_ARG, "plan.threshold_tokens must be in 1..%d", kDefaultThreshold);
+  if (p.tuned_max_tokens < 0) return fail(FLN_ERR_INVALID_ARG, "plan.tuned_max_tokens must be >= 0");
+  return FLN_OK;
+}
+
+// The plan for a call: group plan (or default), then global overrides, then
+// the call's own microchunk; below the threshold the UNFUSED path.
+int resolve_plan(int K, int H, int kind, int T, int chunk_arg, fln_plan* out) {
+  auto it = g_plans.find({K, H, kind});
+  fln_plan p = it != g_plans.end() ? it->second : default_plan();
+  if (g_override_chunk > 0) p.microchunk_tokens = g_override_chunk;
+  if (g_override_threshold > 0) p.threshold_tokens = g_override_threshold;
+  if (chunk_arg > 0) {
+    p.microchunk_tokens = chunk_arg;
+  } else if (g_override_chunk == 0 && p.tuned_max_tokens > 0 && T > p.tuned_max_tokens) {
+    return fail(FLN_ERR_NOT_TUNED, "T=%d exceeds the profiled token maximum %d of group (K=%d, H=%d, kind=%d)", T,
+                p.tuned_max_tokens, K, H, kind);
+  }
+  if (T < p.threshold_tokens) p.path = FLN_PATH_UNFUSED;
+  *out = p;
+  return FLN_OK;
+}
+
+int run_plan(Workspace* ws, const Call& c, const fln_plan& pl) {
+  if (c.T == 0) return FLN_OK;
+  switch (pl.path) {
+    case FLN_PATH_UNFUSED:
+      if (c.T > kMaxUnfusedTokens) return fail(FLN_ERR_UNSUPPORTED, "UNFUSED path handles T <= %d", kMaxUnfusedTokens);
+      return run_unfused(ws, c);
+    case FLN_PATH_FUSED: return run_fused(ws, c, pl);
+    case FLN_PATH_PIPELINED: return run_pipelined(ws, c, pl);
+  }
+  return fail(FLN_ERR_INVALID_ARG, "unknown path %d", pl.path);
+}
+
+int validate_fused(const fln_bf16* x, const fln_bf16* W, fln_bf16* residual, const float* gamma, float eps,
+                   int kind, int T, int K, int H, int chunk, fln_bf16* out) {
+  int rc = check_common(eps, kind, T, H);
+  if (rc) return rc;
+  if (K < 8 || (K & 7)) return fail(FLN_ERR_INVALID_ARG, "K=%d must be a positive multiple of 8", K);
+  if (K > kMaxK) return fail(FLN_ERR_UNSUPPORTED, "K=%d above the supported %d", K, kMaxK);
+  if (chunk < 0 || chunk > kMaxMicrochunk)
+    return fail(FLN_ERR_INVALID_ARG, "microchunk_tokens=%d outside 0..%d", chunk, kMaxMicrochunk);
+  if (T == 0) return FLN_OK;
+  if ((rc = check_ptr("x", x)) || (rc = check_ptr("W", W)) || (rc = check_ptr("residual", residual)) ||
+      (rc = check_ptr("gamma", gamma)) || (rc = check_ptr("out", out)))
+    return rc;
+  const size_t bx = size_t(T) * K * 2, bw = size_t(H) * K * 2, br = size_t(T) * H * 2, bg = size_t(H) * 4;
+  if (overlaps(out, br, x, bx) || overlaps(out, br, W, bw) || overlaps(out, br, residual, br) ||
+      overlaps(out, br, gamma, bg))
+    return fail(FLN_ERR_INVALID_ARG, "out overlaps an input");
+  if (overlaps(residual, br, x, bx) || overlaps(residual, br, W, bw) || overlaps(residual, br, gamma, bg))
+    return fail(FLN_ERR_INVALID_ARG, "residual overlaps x, W or gamma");
+  return FLN_OK;
+}
+
+// ------------------------------------------------------------------ tuner
+__global__ void fill_pseudo_normal(__nv_bfloat16* p, size_t n, uint32_t seed, float scale, float shift) {
+  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x) {
+    // sum of four uniforms from an integer hash: mean 2, variance 1/3
+    float s = 0.f;
+    uint32_t h = static_cast<uint32_t>(i) * 0x9E3779B1u ^ seed ^ static_cast<uint32_t>(i >> 32) * 0x85EBCA77u;
+    for (int k = 0; k < 4; ++k) {
+      h ^= h >> 16;
+      h *= 0x7FEB352Du;
+      h ^= h >> 15;
+      h *= 0x846CA68Bu;
+      h ^= h >> 16;
+      s += static_cast<float>(h >> 8) * (1.0f / 16777216.0f);
+    }
+    p[i] = __float2bfloat16_rn((s - 2.0f) * 1.7320508f * scale + shift);
+  }
+}
+
+__global__ void fill_gamma(float* g, int n, int kind) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const float d = 0.25f * __sinf(0.37f * i);
+    g[i] = kind == FLN_NORM_GEMMA ? d : 1.0f + d;
+  }
+}
+
+struct DevBuf {
+  void* p = nullptr;
+  ~DevBuf() {
+    if (p) cudaFree(p);
+  }
+};
+
+struct TuneCtx {
+  Workspace* ws;
+  Call c;
+  const __nv_bfloat16* res0;  // pristine residual
+  void* flush;
+  size_t flush_bytes;
+  cudaEvent_t e0, e1;
+};
+
+// Restore the residual, flush L2, then time one call of `pl` on T tokens.
+int time_plan(TuneCtx& t, const fln_plan& pl, int T, float* ms) {
+  Call c = t.c;
+  c.T = T;
+  FLN_CUDA(cudaMemcpyAsync(c.residual, t.res0, size_t(T) * c.H * 2, cudaMemcpyDeviceToDevice, c.stream),
+           "tune: residual restore");
+  FLN_CUDA(cudaMemsetAsync(t.flush, T & 0xFF, t.flush_bytes, c.stream), "tune: L2 flush");
+  FLN_CUDA(cudaEventRecord(t.e0, c.stream), "cudaEventRecord");
+  int rc = run_plan(t.ws, c, pl);
+  if (rc) return rc;
+  FLN_CUDA(cudaEventRecord(t.e1, c.stream), "cudaEventRecord");
+  FLN_CUDA(cudaEventSynchronize(t.e1), "cudaEventSynchronize");
+  FLN_CUDA(cudaEventElapsedTime(ms, t.e0, t.e1), "cudaEventElapsedTime");
+  return FLN_OK;
+}
+
+int median_time(TuneCtx& t, const fln_plan& pl, int T, int reps, float* ms) {
+  std::vector<float> v;
+  for (int r = 0; r < reps + 1; ++r) {
+    float x = 0.f;
+    int rc = time_plan(t, pl, T, &x);
+    if (rc) return rc;
+    if (r > 0) v.push_back(x);  // first run warms up
+  }
+  std::sort(v.begin(), v.end());
+  *ms = v[v.size() / 2];
+  return FLN_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+int fused_proj_add_rmsnorm(const fln_bf16* x, const fln_bf16* W, fln_bf16* residual, const float* gamma,
+                           float eps, int norm_kind, int T, int K, int H, int microchunk_tokens, fln_bf16* out,
+                           fln_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = validate_fused(x, W, residual, gamma, eps, norm_kind, T, K, H, microchunk_tokens, out);
+  if (rc) return rc;
+  if (T == 0) return FLN_OK;
+  fln_plan pl;
+  if ((rc = resolve_plan(K, H, norm_kind, T, microchunk_tokens, &pl))) return rc;
+  Workspace* ws = nullptr;
+  if ((rc = get_ws(&ws))) return rc;
+  Call c{reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(W),
+         reinterpret_cast<__nv_bfloat16*>(residual), gamma, eps, norm_kind, T, K, H,
+         reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<cudaStream_t>(stream)};
+  return run_plan(ws, c, pl);
+}
+
+int add_rmsnorm(const fln_bf16* y, fln_bf16* residual, const float* gamma, float eps, int norm_kind, int T, int H,
+                fln_bf16* out, fln_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = check_common(eps, norm_kind, T, H);
+  if (rc) return rc;
+  if (T == 0) return FLN_OK;
+  if ((rc = check_ptr("y", y)) || (rc = check_ptr("residual", residual)) || (rc = check_ptr("gamma", gamma)) ||
+      (rc = check_ptr("out", out)))
+    return rc;
+  const size_t br = size_t(T) * H * 2;
+  if (overlaps(out, br, y, br) || overlaps(out, br, residual, br) || overlaps(out, br, gamma, size_t(H) * 4))
+    return fail(FLN_ERR_INVALID_ARG, "out overlaps an input");
+  if (overlaps(residual, br, y, br) || overlaps(residual, br, gamma, size_t(H) * 4))
+    return fail(FLN_ERR_INVALID_ARG, "residual overlaps y or gamma");
+  Workspace* ws = nullptr;
+  if ((rc = get_ws(&ws))) return rc;
+  NormParams np{};
+  np.y_bf16 = reinterpret_cast<const __nv_bfloat16*>(y);
+  np.residual = reinterpret_cast<__nv_bfloat16*>(residual);
+  np.out = reinterpret_cast<__nv_bfloat16*>(out);
+  np.gamma = gamma;
+  np.eps = eps;
+  np.norm_kind = norm_kind;
+  np.T = T;
+  np.row0 = 0;
+  np.H = H;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return launch_counted(FLN_KERNEL_NORM_BF16, s, [&] { return launch_add_rmsnorm(NORM_SRC_BF16, np, 0, s); },
+                        "add_rmsnorm launch");
+}
+
+int fln_set_overrides(int microchunk_tokens, int threshold_tokens) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (microchunk_tokens < 0 || microchunk_tokens > kMaxMicrochunk)
+    return fail(FLN_ERR_INVALID_ARG, "microchunk override %d outside 0..%d", microchunk_tokens, kMaxMicrochunk);
+  if (threshold_tokens < 0 || threshold_tokens > kDefaultThreshold)
+    return fail(FLN_ERR_INVALID_ARG, "threshold override %d outside 0..%d", threshold_tokens, kDefaultThreshold);
+  g_override_chunk = microchunk_tokens;
+  g_override_threshold = threshold_tokens;
+  return FLN_OK;
+}
+
+int fln_set_plan(int K, int H, int norm_kind, const fln_plan* plan) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (K < 8 || (K & 7) || H < 8 || (H & 7) || (norm_kind != 0 && norm_kind != 1))
+    return fail(FLN_ERR_INVALID_ARG, "bad group (K=%d, H=%d, kind=%d)", K, H, norm_kind);
+  if (!plan) {
+    g_plans.erase({K, H, norm_kind});
+    return FLN_OK;
+  }
+  int rc = check_plan(*plan);
+  if (rc) return rc;
+  g_plans[{K, H, norm_kind}] = *plan;
+  return FLN_OK;
+}
+
+int fln_get_plan(int K, int H, int norm_kind, int T, int microchunk_tokens, fln_plan* plan) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!plan) return fail(FLN_ERR_INVALID_ARG, "plan is NULL");
+  if (microchunk_tokens < 0 || microchunk_tokens > kMaxMicrochunk)
+    return fail(FLN_ERR_INVALID_ARG, "microchunk_tokens=%d outside 0..%d", microchunk_tokens, kMaxMicrochunk);
+  return resolve_plan(K, H, norm_kind, T, microchunk_tokens, plan);
+}
+
+int fln_autotune(int K, int H, int norm_kind, int max_tokens, fln_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = check_common(1e-5f, norm_kind, max_tokens, H);
+  if (rc) return rc;
+  if (K < 8 || (K & 7) || K > kMaxK) return fail(FLN_ERR_INVALID_ARG, "K=%d must be a multiple of 8 in [8, %d]", K, kMaxK);
+  if (max_tokens < 1 || max_tokens > 65536) return fail(FLN_ERR_INVALID_ARG, "max_tokens must be in 1..65536");
+  if (g_override_chunk > 0 && g_override_threshold > 0) return FLN_OK;  // both overrides: no scan, no check
+  Workspace* ws = nullptr;
+  if ((rc = get_ws(&ws))) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  FLN_CUDA(cudaStreamSynchronize(s), "tune: cudaStreamSynchronize");
+  const int T = max_tokens;
+  const int Tc = std::min(T, kMaxUnfusedTokens);  // rows used for the numerical check
+  DevBuf bx, bw, br0, br, bo, bg, bref_r, bref_o, bflush;
+  const size_t nx = size_t(T) * K, nw = size_t(H) * K, nr = size_t(T) * H;
+  const size_t flush_bytes = size_t(256) << 20;
+  FLN_CUDA(cudaMalloc(&bx.p, nx * 2), "tune: cudaMalloc");
+  FLN_CUDA(cudaMalloc(&bw.p, nw * 2), "tune: cudaMalloc");
+  FLN_CUDA(cudaMalloc(&br0.p, nr * 2), "tune: cudaMalloc");
+  FLN_CUDA(cudaMalloc(&br.p, nr * 2), "tune: cudaMalloc");
+  FLN_CUDA(cudaMalloc(&bo.p, nr * 2), "tune: cudaMalloc");
+  FLN_CUDA(cudaMalloc(&bg.p, size_t(H) * 4), "tune: cudaMalloc");
+  FLN_CUDA(cudaMalloc(&bref_r.p, size_t(Tc) * H * 2), "tune: cudaMalloc");
+  FLN_CUDA(cudaMalloc(&bref_o.p, size_t(Tc) * H * 2), "tune: cudaMalloc");
+  FLN_CUDA(cudaMalloc(&bflush.p, flush_bytes), "tune: cudaMalloc");
+  auto* x = static_cast<__nv_bfloat16*>(bx.p);
+  auto* w = static_cast<__nv_bfloat16*>(bw.p);
+  auto* r0 = static_cast<__nv_bfloat16*>(br0.p);
+  fill_pseudo_normal<<<1024, 256, 0, s>>>(x, nx, 0x1234u, 1.0f, 0.0f);
+  fill_pseudo_normal<<<1024, 256, 0, s>>>(w, nw, 0x5678u, 1.0f / std::sqrt(float(K)), 0.0f);
+  fill_pseudo_normal<<<1024, 256, 0, s>>>(r0, nr, 0x9ABCu, 2.0f, 0.0f);
+  fill_gamma<<<64, 256, 0, s>>>(static_cast<float*>(bg.p), H, norm_kind);
+  FLN_CUDA(cudaGetLastError(), "tune: fill launch");
+
+  TuneCtx t{};
+  t.ws = ws;
+  t.c = Call{x, w, static_cast<__nv_bfloat16*>(br.p), static_cast<float*>(bg.p), 1e-5f, norm_kind, T, K, H,
+             static_cast<__nv_bfloat16*>(bo.p), s};
+  t.res0 = r0;
+  t.flush = bflush.p;
+  t.flush_bytes = flush_bytes;
+  FLN_CUDA(cudaEventCreate(&t.e0), "cudaEventCreate");
+  FLN_CUDA(cudaEventCreate(&t.e1), "cudaEventCreate");
+  struct EvGuard {
+    TuneCtx& t;
+    ~EvGuard() {
+      cudaEventDestroy(t.e0);
+      cudaEventDestroy(t.e1);
+    }
+  } evg{t};
+
+  // reference for the numerical check: the UNFUSED path on the first Tc rows
+  fln_plan unf = default_plan();
+  unf.path = FLN_PATH_UNFUSED;
+  {
+    float ms;
+    if ((rc = time_plan(t, unf, Tc, &ms))) return rc;
+    FLN_CUDA(cudaMemcpy(bref_r.p, br.p, size_t(Tc) * H * 2, cudaMemcpyDeviceToDevice), "tune: copy");
+    FLN_CUDA(cudaMemcpy(bref_o.p, bo.p, size_t(Tc) * H * 2, cudaMemcpyDeviceToDevice), "tune: copy");
+  }
+  std::vector<uint16_t> ref_r(size_t(Tc) * H), ref_o(size_t(Tc) * H), got(size_t(Tc) * H);
+  FLN_CUDA(cudaMemcpy(ref_r.data(), bref_r.p, ref_r.size() * 2, cudaMemcpyDeviceToHost), "tune: D2H");
+  FLN_CUDA(cudaMemcpy(ref_o.data(), bref_o.p, ref_o.size() * 2, cudaMemcpyDeviceToHost), "tune: D2H");
+  auto bf = [](uint16_t b) {
+    uint32_t u = uint32_t(b) << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return f;
+  };
+  auto close_enough = [&](const std::vector<uint16_t>& a, const std::vector<uint16_t>& b) {
+    for (size_t i = 0; i < a.size(); ++i) {
+      const float u = bf(a[i]), v = bf(b[i]);
+      if (!(std::fabs(u - v) <= 2e-2f + std::fabs(v) * (1.0f / 64))) return false;
+    }
+    return true;
+  };
+
+  // candidate scan
+  std::vector<int> chunks;
+  for (int cch : {256, 512, 1024, 2048, 4096})
+    if (cch < T) chunks.push_back(cch);
+  chunks.push_back(std::min(T, kMaxMicrochunk));
+  std::sort(chunks.begin(), chunks.end());
+  chunks.erase(std::unique(chunks.begin(), chunks.end()), chunks.end());
+  std::vector<int> ctas = {ws->sms};
+  for (int g : {ws->sms - ws->sms % 16, ws->sms - 16})
+    if (g > 0 && g != ws->sms) ctas.push_back(g);
+  fln_plan best = default_plan();
+  float best_ms = 1e30f;
+  bool any = false;
+  for (int path : {FLN_PATH_FUSED, FLN_PATH_PIPELINED}) {
+    for (int tile : {256, 128}) {
+      for (int cch : chunks) {
+        for (int g : ctas) {
+          for (int nc : (path == FLN_PATH_PIPELINED ? std::vector<int>{0, ws->sms / 4} : std::vector<int>{0})) {
+            fln_plan pl = default_plan();
+            pl.path = path;
+            pl.tile_n = tile;
+            pl.microchunk_tokens = cch;
+            pl.gemm_ctas = g;
+            pl.norm_ctas = nc;
+            pl.threshold_tokens = 1;
+            // numerical check on the first Tc rows against the UNFUSED path
+            float ms;
+            fln_plan pc = pl;
+            pc.microchunk_tokens = std::min(cch, Tc);
+            if ((rc = time_plan(t, pc, Tc, &ms))) return rc;
+            FLN_CUDA(cudaMemcpy(got.data(), t.c.out, got.size() * 2, cudaMemcpyDeviceToHost), "tune: D2H");
+            bool ok = close_enough(got, ref_o);
+            FLN_CUDA(cudaMemcpy(got.data(), t.c.residual, got.size() * 2, cudaMemcpyDeviceToHost), "tune: D2H");
+            ok = ok && close_enough(got, ref_r);
+            if (!ok) continue;  // a candidate that disagrees is never selected
+            if ((rc = median_time(t, pl, T, 3, &ms))) return rc;
+            if (ms < best_ms) {
+              best_ms = ms;
+              best = pl;
+              any = true;
+            }
+          }
+        }
+      }
+    }
+  }
+  if (!any) return fail(FLN_ERR_CUDA, "tune: no candidate passed the numerical check for (K=%d, H=%d)", K, H);
+
+  // token-threshold search: UNFUSED vs the best prefill plan over a grid of T
+  std::vector<int> grid;
+  for (int v : {1, 2, 4, 8, 16, 32, 64, 96, 128, 192, 256})
+    if (v <= T) grid.push_back(v);
+  std::vector<bool> prefill_wins;
+  for (int v : grid) {
+    float mu = 0, mp = 0;
+    if ((rc = median_time(t, unf, v, 3, &mu))) return rc;
+    fln_plan pv = best;
+    pv.microchunk_tokens = std::min(best.microchunk_tokens, v);
+    if ((rc = median_time(t, pv, v, 3, &mp))) return rc;
+    prefill_wins.push_back(mp <= mu);
+  }
+  // threshold = the smallest grid point from which the prefill plan wins at
+  // every larger grid point; if it does not win at the largest one, UNFUSED
+  // serves every T it can (T <= 256)
+  int threshold = kDefaultThreshold;
+  size_t i0 = grid.size();
+  while (i0 > 0 && prefill_wins[i0 - 1]) --i0;
+  if (i0 < grid.size()) threshold = grid[i0];
+  best.threshold_tokens = threshold;
+  best.tuned_max_tokens = T;
+  g_plans[{K, H, norm_kind}] = best;
+  FLN_CUDA(cudaStreamSynchronize(s), "tune: cudaStreamSynchronize");
+  return FLN_OK;
+}
+
+int fln_device_status(fln_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace* ws = nullptr;
+  int rc = get_ws(&ws);
+  if (rc) return rc;
+  FLN_CUDA(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)), "cudaStreamSynchronize");
+  FLN_CUDA(cudaStreamSynchronize(ws->stream_b), "cudaStreamSynchronize(internal stream)");
+  unsigned int word = 0;
+  FLN_CUDA(cudaMemcpy(&word, ws->err_word, sizeof word, cudaMemcpyDeviceToHost), "read device error word");
+  if (word) {
+    FLN_CUDA(cudaMemset(ws->err_word, 0, sizeof word), "clear device error word");
+    return fail(FLN_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (device error bits 0x%x)", word);
+  }
+  return FLN_OK;
+}
+
+const char* fln_last_error(void) { return g_err.c_str(); }
+
+void fln_release_workspace(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_ws) {
+    Workspace* ws = kv.second;
+    cudaSetDevice(ws->device);
+    cudaDeviceSynchronize();
+    cudaFree(ws->err_word);
+    cudaFree(ws->psum);
+    cudaFree(ws->flags);
+    for (int i = 0; i < 3; ++i) cudaFree(ws->slots[i]);
+    cudaFree(ws->partial);
+    for (int i = 0; i < 3; ++i) {
+      cudaEventDestroy(ws->ev_ready[i]);
+      cudaEventDestroy(ws->ev_free[i]);
+    }
+    cudaEventDestroy(ws->ev_join);
+    cudaStreamDestroy(ws->stream_b);
+    delete ws;
+  }
+  g_ws.clear();
+  cudaSetDevice(cur);
+}
+
+uint64_t fln_launch_count(void) { return g_launches.load(); }
+
+int fln_profile_enable(int enable) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& r : g_prof_recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  g_prof_recs.clear();
+  g_prof = enable != 0;
+  return FLN_OK;
+}
+
+int fln_profile_read(fln_profile_stats* st) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!st) return fail(FLN_ERR_INVALID_ARG, "stats is NULL");
+  std::memset(st, 0, sizeof *st);
+  int rc = FLN_OK;
+  for (auto& r : g_prof_recs) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.a, r.b);
+    if (e != cudaSuccess && rc == FLN_OK) rc = cuda_fail(e, "profile event");
+    st->launches[r.kind] += 1;
+    st->total_ms[r.kind] += ms;
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  g_prof_recs.clear();
+  return rc;
+}
+
+int fln_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,471 @@
+// fln_gemm.cu -- the projection GEMM y = x . W^T on sm_103a tensor cores
+// (tcgen05 + TMEM + TMA), persistent and warp-specialised, with three
+// epilogues: the fused residual add + RMSNorm, an fp32 slot store for the
+// two-stream microchunk pipeline, and a stream-K split for the decode regime.
+//
+// What it computes follows the row-parallel projection of the vLLM "TPSP
+// Design" page (section 1: local projection, then residual add and norm over
+// the complete hidden size of each token; section 3 "Fusion regions":
+// o_proj / down_proj followed by residual add + norm) with F.linear's layout
+// (torch-spyre "Plugin Architecture", "Transposed linear weights": W is
+// [out, in] = [H, K], used K-major with no transpose).
+//
+// CTA layout (192 threads, one CTA per SM):
+//   warp 0      TMA producer (one lane): A and B tiles -> smem ring
+//   warp 1      TMEM owner; one lane issues tcgen05.mma into a double-buffered
+//               fp32 accumulator (2 x BN columns)
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator, one TMEM lane (= one
+//               result row) per thread
+//
+// Tiles: BM = 128 rows (MMA M), BN columns (MMA N), BK = 64 (one 128-byte
+// swizzle atom of bf16 per row).  Operands are K-major in shared memory with
+// 128-byte swizzle, exactly as TMA writes them.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fln_internal.h"
+#include "fln_ptx.cuh"
+
+namespace fln {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int NUM_THREADS = 192;
+constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KiB
+
+__host__ __device__ constexpr int stages_for(int bn) {
+  return bn >= 256 ? 4 : (bn >= 128 ? 6 : 8);
+}
+__host__ __device__ constexpr int stage_bytes(int bn) { return A_TILE_BYTES + bn * BK * 2; }
+__host__ __device__ constexpr int tmem_cols_for(int bn) {
+  return (2 * bn) <= 32 ? 32 : (2 * bn) <= 64 ? 64 : (2 * bn) <= 128 ? 128 : (2 * bn) <= 256 ? 256 : 512;
+}
+__host__ __device__ constexpr int smem_bytes_for(int bn) {
+  // ring + barriers/flags (256 B) + alignment slack for the 1024-byte swizzle base
+  return stages_for(bn) * stage_bytes(bn) + 256 + 1024;
+}
+
+// One unit of work: an output tile and the K-block range it accumulates.
+struct WorkItem {
+  int m_tile, n_tile, kb_begin, kb_end, split;
+};
+
+// Static persistent schedule shared verbatim by the three roles, so that they
+// agree on the sequence without communicating.
+template <int EPI>
+struct Scheduler {
+  const GemmParams& p;
+  int next_tile;       // prefill: next tile index
+  long long u, u_end;  // decode: stream-K unit cursor
+
+  __device__ explicit Scheduler(const GemmParams& prm) : p(prm) {
+    if (EPI == EPI_SPLITK_SWAP) {
+      const long long U = p.units_total;
+      u = U * blockIdx.x / gridDim.x;
+      u_end = U * (blockIdx.x + 1) / gridDim.x;
+      next_tile = 0;
+    } else {
+      next_tile = blockIdx.x;
+      u = u_end = 0;
+    }
+  }
+
+  __device__ bool next(WorkItem& w) {
+    if (EPI == EPI_SPLITK_SWAP) {
+      if (u >= u_end) return false;
+      const int KB = p.num_k_blocks;
+      w.m_tile = static_cast<int>(u / KB);
+      w.n_tile = 0;
+      w.kb_begin = static_cast<int>(u % KB);
+      const long long left = u_end - u;
+      w.kb_end = (KB - w.kb_begin) < left ? KB : w.kb_begin + static_cast<int>(left);
+      const int c_first = splitk_cta_of_unit(static_cast<long long>(w.m_tile) * KB, p.units_total, gridDim.x);
+      w.split = static_cast<int>(blockIdx.x) - c_first;
+      u += w.kb_end - w.kb_begin;
+      return true;
+    } else {
+      const int total = p.num_m_tiles * p.num_n_tiles;
+      if (next_tile >= total) return false;
+      w.m_tile = next_tile / p.num_n_tiles;  // row-block major: a row block's N-tiles run together
+      w.n_tile = next_tile % p.num_n_tiles;
+      w.kb_begin = 0;
+      w.kb_end = p.num_k_blocks;
+      w.split = 0;
+      next_tile += gridDim.x;
+      return true;
+    }
+  }
+};
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fln_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmParams p) {
+  constexpr int STAGES = stages_for(BN);
+  constexpr int STAGE_BYTES = stage_bytes(BN);
+  constexpr int TMEM_COLS = tmem_cols_for(BN);
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* acc_full = empty_bar + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain_bar = acc_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* epi_abort = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *epi_abort = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_a = (EPI == EPI_SPLITK_SWAP) ? l2_policy_evict_first() : l2_policy_evict_normal();
+    const uint64_t pol_b = (EPI == EPI_SPLITK_SWAP) ? l2_policy_evict_last() : l2_policy_evict_last();
+    Scheduler<EPI> sched(p);
+    WorkItem w;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_mask = 0;     // stages with a load issued
+    uint32_t issued_parity = 0;   // parity of that load's phase
+    bool ok = true;
+    while (ok && sched.next(w)) {
+      const int a_row = p.a_row0 + w.m_tile * BM;
+      const int b_row = w.n_tile * BN;
+      for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+        if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_EMPTY)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem + stage * STAGE_BYTES;
+        uint8_t* sb = sa + A_TILE_BYTES;
+        mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+        tma_load_2d(sa, &tmA, &full_bar[stage], kb * BK, a_row, pol_a);
+        tma_load_2d(sb, &tmB, &full_bar[stage], kb * BK, b_row, pol_b);
+        issued_mask |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      // unwinding: let every load already issued land before the CTA exits
+      for (int s = 0; s < STAGES; ++s) {
+        if (issued_mask & (1u << s)) {
+          volatile int no_abort = 0;
+          mbar_wait(&full_bar[s], (issued_parity >> s) & 1u, &no_abort, p.err, FLN_DEVERR_TIMEOUT_DRAIN);
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    Scheduler<EPI> sched(p);
+    WorkItem w;
+    int stage = 0;
+    uint32_t phase = 0;
+    int local = 0;
+    bool ok = true;
+    bool issued_any = false;
+    while (ok && sched.next(w)) {
+      const int b = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      if (!mbar_wait(&acc_empty[b], (use & 1u) ^ 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+      for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+        if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.err, FLN_DEVERR_TIMEOUT_FULL)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+        const uint32_t sb = sa + A_TILE_BYTES;
+        const uint64_t adesc = sw128_kmajor_desc(sa);
+        const uint64_t bdesc = sw128_kmajor_desc(sb);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          // advance 16 bf16 = 32 bytes along K inside the swizzle atom (encoded >> 4)
+          mma_bf16(d_tmem, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2), IDESC,
+                   (kb > w.kb_begin || kk > 0) ? 1u : 0u);
+        }
+        issued_any = true;
+        mma_commit(&empty_bar[stage]);  // frees the smem stage once these MMAs have read it
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      mma_commit(&acc_full[b]);  // accumulator ready for the epilogue
+      ++local;
+    }
+    if (!ok && issued_any) {
+      // unwinding: wait until the tensor core has finished with TMEM and smem
+      mma_commit(drain_bar);
+      volatile int no_abort = 0;
+      mbar_wait(drain_bar, 0, &no_abort, p.err, FLN_DEVERR_TIMEOUT_DRAIN);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int rl = q * 32 + lane;      // row within the tile
+    const int ep_tid = threadIdx.x - 64;
+    Scheduler<EPI> sched(p);
+    WorkItem w;
+    int local = 0;
+    while (sched.next(w)) {
+      const int b = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      // All 128 epilogue threads decide together whether to continue: a thread
+      // that leaves alone would strand the others at a named barrier.
+      if (!mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) *epi_abort = 1;
+      named_bar_sync(1, 128);
+      if (*epi_abort) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
+      const int row = w.m_tile * BM + rl;  // local row of the launch (A operand)
+      const bool vrow = row < p.M;
+
+      if (EPI == EPI_FUSED_NORM) {
+        const size_t grow = static_cast<size_t>(p.a_row0) + static_cast<size_t>(row);
+        const __nv_bfloat16* rrow = p.residual + grow * static_cast<size_t>(p.ld);
+        const int n0 = w.n_tile * BN;
+        // phase 1: r = r0 + acc, partial sum of squares over this tile's columns
+        float ss = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(tb + static_cast<uint32_t>(c), v);
+          if (vrow) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int col = n0 + c + 8 * h;
+              if (col < p.N) {
+                const uint4 u = *reinterpret_cast<const uint4*>(rrow + col);
+                float f[8];
+                bf16x8_to_f32(u, f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float r = f[j] + v[8 * h + j];
+                  ss = fmaf(r, r, ss);
+                }
+              }
+            }
+          }
+        }
+        // publish this tile's partial sums, then wait for the row block's others
+        const int nN = p.num_n_tiles;
+        float* ps = p.psum + (static_cast<size_t>(w.m_tile) * nN) * BM;
+        ps[static_cast<size_t>(w.n_tile) * BM + rl] = ss;
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (ep_tid == 0) st_release_gpu(&p.flags[w.m_tile * nN + w.n_tile], p.gen);
+        if (ep_tid < 32) {
+          bool ok = true;
+          for (int j = lane; j < nN; j += 32) {
+            const unsigned int* f = &p.flags[w.m_tile * nN + j];
+            if (ld_acquire_gpu(f) != p.gen) {
+              const uint64_t t0 = globaltimer_ns();
+              while (ld_acquire_gpu(f) != p.gen) {
+                if (*abort_flag || globaltimer_ns() - t0 > FLN_WAIT_TIMEOUT_NS) {
+                  ok = false;
+                  break;
+                }
+              }
+            }
+            if (!ok) break;
+          }
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok && lane == 0) {
+            if (!*abort_flag) atomicOr(p.err, FLN_DEVERR_TIMEOUT_ROWSTAT);
+            *abort_flag = 1;
+            *epi_abort = 1;
+          }
+        }
+        named_bar_sync(1, 128);
+        const bool go = (*epi_abort == 0);
+        // phase 2: normalise and store residual and out (bf16, 16-byte stores)
+        float tot = 0.f;
+        for (int j = 0; j < nN; ++j) tot += ld_cg_f32(&ps[static_cast<size_t>(j) * BM + rl]);
+        const float rstd = rsqrtf(tot / static_cast<float>(p.ld) + p.eps);
+        __nv_bfloat16* wrow = p.residual + grow * static_cast<size_t>(p.ld);
+        __nv_bfloat16* orow = p.out + grow * static_cast<size_t>(p.ld);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(tb + static_cast<uint32_t>(c), v);
+          if (vrow && go) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int col = n0 + c + 8 * h;
+              if (col < p.N) {
+                const uint4 u = *reinterpret_cast<const uint4*>(rrow + col);
+                float f[8];
+                bf16x8_to_f32(u, f);
+                const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + col));
+                const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + col + 4));
+                float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                float r[8], o[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  r[j] = f[j] + v[8 * h + j];
+                  const float gj = p.norm_kind ? 1.0f + g[j] : g[j];
+                  o[j] = r[j] * rstd * gj;
+                }
+                *reinterpret_cast<uint4*>(wrow + col) = f32x8_to_bf16(r);
+                *reinterpret_cast<uint4*>(orow + col) = f32x8_to_bf16(o);
+              }
+            }
+          }
+        }
+      } else if (EPI == EPI_STORE_F32) {
+        const int n0 = w.n_tile * BN;
+        float* yrow = p.yout + static_cast<size_t>(row) * static_cast<size_t>(p.ld);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(tb + static_cast<uint32_t>(c), v);
+          if (vrow) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int col = n0 + c + 8 * h;
+              if (col < p.N) {
+                float4* d = reinterpret_cast<float4*>(yrow + col);
+                d[0] = make_float4(v[8 * h + 0], v[8 * h + 1], v[8 * h + 2], v[8 * h + 3]);
+                d[1] = make_float4(v[8 * h + 4], v[8 * h + 5], v[8 * h + 6], v[8 * h + 7]);
+              }
+            }
+          }
+        }
+      } else {  // EPI_SPLITK_SWAP: TMEM lane = hidden index h, column = token t
+        float* dst = p.partial +
+                     static_cast<size_t>(w.m_tile * p.max_split + w.split) * static_cast<size_t>(p.N) * BM;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(tb + static_cast<uint32_t>(c), v);
+          if (vrow) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int t = c + j;
+              if (t < p.N) dst[static_cast<size_t>(t) * BM + rl] = v[j];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      ++local;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+template <int BN, int EPI>
+static cudaError_t prepare_one() {
+  return cudaFuncSetAttribute(fln_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem_bytes_for(BN));
+}
+
+template <int BN, int EPI>
+static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
+                              cudaStream_t stream) {
+  fln_gemm_kernel<BN, EPI><<<grid, NUM_THREADS, smem_bytes_for(BN), stream>>>(tmA, tmB, p);
+  return cudaGetLastError();
+}
+
+int gemm_smem_bytes(int bn) {
+  switch (bn) {
+    case 16: return smem_bytes_for(16);
+    case 32: return smem_bytes_for(32);
+    case 64: return smem_bytes_for(64);
+    case 128: return smem_bytes_for(128);
+    case 256: return smem_bytes_for(256);
+    default: return -1;
+  }
+}
+
+int gemm_stages(int bn) { return stages_for(bn); }
+
+#define FLN_BN_SWITCH(bn, EPI, CALL)                \
+  switch (bn) {                                     \
+    case 16: return CALL<16, EPI>();                \
+    case 32: return CALL<32, EPI>();                \
+    case 64: return CALL<64, EPI>();                \
+    case 128: return CALL<128, EPI>();              \
+    case 256: return CALL<256, EPI>();              \
+    default: return cudaErrorInvalidValue;          \
+  }
+
+cudaError_t gemm_prepare(int bn, EpilogueKind epi) {
+  switch (epi) {
+    case EPI_FUSED_NORM: FLN_BN_SWITCH(bn, EPI_FUSED_NORM, prepare_one)
+    case EPI_STORE_F32: FLN_BN_SWITCH(bn, EPI_STORE_F32, prepare_one)
+    case EPI_SPLITK_SWAP: FLN_BN_SWITCH(bn, EPI_SPLITK_SWAP, prepare_one)
+  }
+  return cudaErrorInvalidValue;
+}
+
+#undef FLN_BN_SWITCH
+#define FLN_BN_LAUNCH(bn, EPI)                                            \
+  switch (bn) {                                                           \
+    case 16: return launch_one<16, EPI>(tmA, tmB, p, grid, stream);       \
+    case 32: return launch_one<32, EPI>(tmA, tmB, p, grid, stream);       \
+    case 64: return launch_one<64, EPI>(tmA, tmB, p, grid, stream);       \
+    case 128: return launch_one<128, EPI>(tmA, tmB, p, grid, stream);     \
+    case 256: return launch_one<256, EPI>(tmA, tmB, p, grid, stream);     \
+    default: return cudaErrorInvalidValue;                                \
+  }
+
+cudaError_t launch_gemm(EpilogueKind epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                        const GemmParams& p, int grid, cudaStream_t stream) {
+  switch (epi) {
+    case EPI_FUSED_NORM: FLN_BN_LAUNCH(bn, EPI_FUSED_NORM)
+    case EPI_STORE_F32: FLN_BN_LAUNCH(bn, EPI_STORE_F32)
+    case EPI_SPLITK_SWAP: FLN_BN_LAUNCH(bn, EPI_SPLITK_SWAP)
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fln

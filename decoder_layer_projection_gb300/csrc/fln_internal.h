@@ -1,0 +1,89 @@
+// fln_internal.h -- types shared by the kernels and the host scheduler of
+// libfusedln.  Not part of the public ABI (that is include/libfusedln.h).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace fln {
+
+// What the GEMM epilogue does with the fp32 accumulator tile.
+enum EpilogueKind : int {
+  // r = r0 + acc; per-row sum of squares over the full hidden size, combined
+  // across the N-tiles of a row block through global partial sums and
+  // per-tile release flags; out = r * rsqrt(ms + eps) * g.  Writes residual
+  // (in place) and out, both bf16.
+  EPI_FUSED_NORM = 0,
+  // y (fp32) -> a pipeline slot [rows, ld]; the add + norm runs as a second
+  // stage on another stream.
+  EPI_STORE_F32 = 1,
+  // Swapped operands (A = W, B = x) with a stream-K split of the K loop:
+  // partial y^T tiles (fp32) go to a partial buffer, reduced by the
+  // add + norm kernel.
+  EPI_SPLITK_SWAP = 2,
+};
+
+struct GemmParams {
+  int M;             // valid rows of the A operand in this launch
+  int N;             // valid columns of the result (B rows)
+  int K;             // reduction length
+  int a_row0;        // TMA row coordinate of A's first row (chunk start)
+  int num_m_tiles;   // ceil(M / 128)
+  int num_n_tiles;   // ceil(N / BN)
+  int num_k_blocks;  // ceil(K / 64)
+  // fused-norm epilogue
+  __nv_bfloat16* residual;  // [rows, ld] bf16, global row = a_row0 + local row
+  __nv_bfloat16* out;       // [rows, ld] bf16
+  const float* gamma;       // [ld] fp32
+  float eps;
+  int norm_kind;            // 0 standard, 1 Gemma (1 + gamma)
+  int ld;                   // hidden size H (row stride in elements)
+  float* psum;              // [num_m_tiles, num_n_tiles, 128] row partial sums of squares
+  unsigned int* flags;      // [num_m_tiles, num_n_tiles] publication flags
+  unsigned int gen;         // value this launch writes into flags (never 0)
+  // store-f32 epilogue
+  float* yout;              // [M, ld] fp32 slot, local rows
+  // split-K swap epilogue
+  float* partial;           // [num_m_tiles * max_split, N, 128] fp32
+  int max_split;            // partial slots per m-tile
+  long long units_total;    // num_m_tiles * num_k_blocks
+  unsigned int* err;        // device error word
+};
+
+struct NormParams {
+  const __nv_bfloat16* y_bf16;  // [T, H] bf16 addend (plain add_rmsnorm)
+  const float* y_f32;           // [T, H] fp32 addend (pipeline slot), rows local to the launch
+  const float* partial;         // split-K partials (layout of GemmParams::partial)
+  int max_split;
+  int num_k_blocks;             // split-K bookkeeping (to find contributing CTAs)
+  int gemm_grid;
+  long long units_total;
+  __nv_bfloat16* residual;      // [T, H] in/out
+  __nv_bfloat16* out;           // [T, H]
+  const float* gamma;
+  float eps;
+  int norm_kind;
+  int T;                        // rows in this launch
+  int row0;                     // global row of local row 0 (residual/out/y_bf16)
+  int H;
+};
+
+// launchers (return cudaError_t of the launch)
+cudaError_t launch_gemm(EpilogueKind epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                        const GemmParams& p, int grid, cudaStream_t stream);
+int gemm_smem_bytes(int bn);
+int gemm_stages(int bn);
+cudaError_t gemm_prepare(int bn, EpilogueKind epi);  // sets max dynamic smem attributes
+
+enum NormSource : int { NORM_SRC_BF16 = 0, NORM_SRC_F32 = 1, NORM_SRC_SPLITK = 2 };
+cudaError_t launch_add_rmsnorm(NormSource src, const NormParams& p, int grid_cap, cudaStream_t stream);
+
+// split-K bookkeeping shared by the GEMM and the reducer: the CTA whose
+// unit range [c*U/G, (c+1)*U/G) contains unit u.
+__host__ __device__ inline int splitk_cta_of_unit(long long u, long long U, int G) {
+  return static_cast<int>(((u + 1) * G + U - 1) / U - 1);
+}
+
+}  // namespace fln

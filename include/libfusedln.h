@@ -1,0 +1,195 @@
+/*
+ * libfusedln.h -- C ABI of the GB300 (sm_103a) library for the dense
+ * decoder-layer region
+ *
+ *     y   = x . W^T                    row-parallel projection (o_proj / down_proj)
+ *     r   = r + y                      residual add, in place
+ *     out = RMSNorm(r)                 standard:  r / sqrt(mean_h r^2 + eps) * gamma
+ *                                      Gemma:     r / sqrt(mean_h r^2 + eps) * (1 + gamma)
+ *
+ * Sources (web pages; cited by title and section):
+ *   - vLLM "TPSP Design", section 1 "Motivation": the projection is followed by a
+ *     residual add and a norm that keeps the complete hidden dimension of every
+ *     token; section 3 "Fusion regions": o_proj -> add + post-attention norm and
+ *     down_proj -> add + next input norm; section 3 "Microchunk pipeline": per
+ *     chunk GEMM then add/norm on a second stream through three reusable slots,
+ *     only valid rows written; section 3 "Profiling and fallback": tuning of the
+ *     microchunk size and SM-count targets, candidate numerical checks, a
+ *     token-threshold search, overrides, errors that propagate; section 4
+ *     "Constraints": BF16, standard RMSNorm without bias, microchunks capped at
+ *     4096 tokens, calls must fit the profiled token maximum, a shared
+ *     workspace that assumes sequential calls.
+ *   - torch-spyre "Plugin Architecture": F.linear semantics, W stored [out, in]
+ *     ("Transposed linear weights"); GemmaRMSNorm's trailing fp32 weight
+ *     multiply and the fp32 upcast of RMSNorm ("Custom Op Replacement" table,
+ *     "Transformers backend").
+ *   On one GPU the pages' ReduceScatter / AllGather between the GEMM and the
+ *   add/norm are absent; everything else keeps its meaning.
+ *
+ * Conventions for every call
+ *   - Tensors are row-major with the last dimension contiguous.  bf16 tensors
+ *     are passed as pointers to their 16-bit storage (fln_bf16).  gamma is fp32.
+ *   - Pointers are CUDA device pointers on the current device, 16-byte
+ *     aligned.  The caller owns every tensor; the library never frees them.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     Work the library puts on its internal second stream is joined back into
+ *     `stream` before the call returns; nothing is synchronised on the host.
+ *   - Return value: FLN_OK, or a negative fln_status.  On an error nothing has
+ *     been launched, except FLN_ERR_CUDA from a failed launch in the middle of
+ *     a call.  fln_last_error() gives a message for the calling thread.
+ *     Errors are reported, never retried or routed around.
+ *   - The library owns a per-device workspace (row statistics, pipeline slots,
+ *     split-K partials, a device error word).  It is grown on demand with
+ *     cudaMalloc the first time a shape needs more (so make the first call for
+ *     a shape outside CUDA-graph capture), it is shared by all calls on a
+ *     device, and calls must therefore be issued sequentially: two host
+ *     threads calling concurrently on one device is unsupported.
+ */
+#ifndef LIBFUSEDLN_H
+#define LIBFUSEDLN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t fln_bf16;               /* storage of one bfloat16 value */
+typedef struct CUstream_st* fln_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  FLN_OK = 0,
+  FLN_ERR_INVALID_ARG = -1,    /* null/misaligned/host pointer, bad size, bad kind, bad eps, aliasing */
+  FLN_ERR_UNSUPPORTED = -2,    /* valid but outside what the kernels support (e.g. H > 32768) */
+  FLN_ERR_CUDA = -3,           /* a CUDA runtime call or launch failed */
+  FLN_ERR_DEVICE_TIMEOUT = -4, /* a kernel's bounded wait expired (reported by fln_device_status) */
+  FLN_ERR_NOT_TUNED = -5       /* automatic choice requested for T above the tuned token maximum */
+} fln_status;
+
+typedef enum { FLN_NORM_STANDARD = 0, FLN_NORM_GEMMA = 1 } fln_norm_kind;
+
+/* Execution paths (vLLM "TPSP Design", section 3 "Microchunk pipeline" and
+ * "Profiling and fallback").
+ *   FUSED      per microchunk, one persistent tcgen05 GEMM whose epilogue does
+ *              the residual add, the full-row sum of squares (combined across
+ *              the row's N-tiles through global partial sums) and the norm.
+ *   PIPELINED  per microchunk, the GEMM writes y (fp32) into one of three
+ *              reusable slots on the caller's stream; the add + norm of that
+ *              chunk runs on a second stream, overlapping the next GEMM.
+ *   UNFUSED    the conventional sequence for small token counts: a split-K
+ *              GEMM (H on the MMA's M side) then a separate add + norm pass. */
+typedef enum { FLN_PATH_FUSED = 1, FLN_PATH_PIPELINED = 2, FLN_PATH_UNFUSED = 3 } fln_path;
+
+/* How calls for one projection group (K, H, norm kind) execute. */
+typedef struct {
+  int path;              /* fln_path used when T >= threshold_tokens (FUSED or PIPELINED) */
+  int microchunk_tokens; /* 1..4096, the chunk of tokens per pipeline step */
+  int tile_n;            /* GEMM tile width on H: 128 or 256 */
+  int gemm_ctas;         /* SM-count target of the persistent GEMM grid; 0 = all SMs */
+  int norm_ctas;         /* CTA cap of the second-stream add + norm (PIPELINED); 0 = no cap */
+  int threshold_tokens;  /* T < threshold -> UNFUSED; 1..257 (UNFUSED handles T <= 256) */
+  int tuned_max_tokens;  /* largest T the plan was profiled for; 0 = not profiled */
+} fln_plan;
+
+/*
+ * fused_proj_add_rmsnorm -- y = x . W^T; residual += y; out = RMSNorm(residual)
+ *
+ *   x          [T, K] bf16 activations (input of o_proj / down_proj)
+ *   W          [H, K] bf16 weight, F.linear layout [out, in]
+ *   residual   [T, H] bf16, read and overwritten with r0 + y (rounded to bf16)
+ *   gamma      [H] fp32 norm weight
+ *   eps        finite, >= 0, added to the mean square inside the square root
+ *   norm_kind  FLN_NORM_STANDARD (x gamma) or FLN_NORM_GEMMA (x (1 + gamma))
+ *   T          tokens, 0 <= T <= 2^24 (T = 0 is an empty call)
+ *   K, H       multiples of 8 (16-byte rows); 8 <= K <= 2^20, 8 <= H <= 32768
+ *   microchunk_tokens  0 = automatic (the group's plan); else 1..4096
+ *   out        [T, H] bf16 normalised output; must not overlap x, W, residual
+ *
+ * The norm statistics and the normalised output are computed from the fp32
+ * sum r0 + y, before the residual is rounded to bf16.  Rows at or beyond T
+ * are never written.  With microchunk_tokens = 0 and a profiled plan whose
+ * tuned_max_tokens < T the call returns FLN_ERR_NOT_TUNED.
+ */
+int fused_proj_add_rmsnorm(const fln_bf16* x, const fln_bf16* W, fln_bf16* residual, const float* gamma,
+                           float eps, int norm_kind, int T, int K, int H, int microchunk_tokens, fln_bf16* out,
+                           fln_stream_t stream);
+
+/*
+ * add_rmsnorm -- residual += y; out = RMSNorm(residual)   (the add/norm step alone)
+ *
+ *   y [T, H] bf16 addend; residual [T, H] bf16 in/out; gamma [H] fp32;
+ *   out [T, H] bf16, must not overlap y or residual.  Other arguments as above.
+ */
+int add_rmsnorm(const fln_bf16* y, fln_bf16* residual, const float* gamma, float eps, int norm_kind, int T,
+                int H, fln_bf16* out, fln_stream_t stream);
+
+/*
+ * fln_autotune -- profile a projection group on the current device ("TPSP
+ * Design", section 3 "Profiling and fallback").  Sweeps path x microchunk x
+ * tile width x SM-count target on synthetic data of shape [max_tokens, K],
+ * [H, K]; checks every timed candidate numerically against the UNFUSED path;
+ * then searches the token threshold below which UNFUSED is faster.  Stores the
+ * winning plan for (K, H, norm_kind) with tuned_max_tokens = max_tokens.
+ * Synchronises `stream`.  Skipped (returns FLN_OK, plan untouched) when both
+ * overrides are set (fln_set_overrides).  1 <= max_tokens <= 65536.
+ */
+int fln_autotune(int K, int H, int norm_kind, int max_tokens, fln_stream_t stream);
+
+/*
+ * fln_set_overrides -- global overrides of the automatic choices ("TPSP
+ * Design", section 3: --tpsp-microchunk-tokens / --tpsp-threshold-tokens).
+ * 0 clears an override.  microchunk_tokens in 0..4096; threshold_tokens in
+ * 0..257.  An override is not evidence of benefit; when both are set,
+ * fln_autotune skips its scan and numerical check.
+ */
+int fln_set_overrides(int microchunk_tokens, int threshold_tokens);
+
+/* Install (or, with plan = NULL, remove) the plan of a group explicitly. */
+int fln_set_plan(int K, int H, int norm_kind, const fln_plan* plan);
+
+/* The plan a call with these arguments would use after overrides (path is
+ * FLN_PATH_UNFUSED when T is below the threshold).  Writes *plan. */
+int fln_get_plan(int K, int H, int norm_kind, int T, int microchunk_tokens, fln_plan* plan);
+
+/* Synchronise `stream` and the internal stream, read and clear the device
+ * error word.  FLN_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait. */
+int fln_device_status(fln_stream_t stream);
+
+/* Message for the last error on the calling thread ("" if none). */
+const char* fln_last_error(void);
+
+/* Free the workspace, streams and events of every device (synchronises the
+ * devices first).  The next call allocates again. */
+void fln_release_workspace(void);
+
+/* Number of kernels this library has launched since load (all devices). */
+uint64_t fln_launch_count(void);
+
+/* Per-kernel timing with CUDA events recorded on each kernel's own stream. */
+enum {
+  FLN_KERNEL_GEMM_FUSED = 0,   /* GEMM with the fused add + norm epilogue */
+  FLN_KERNEL_GEMM_SLOT = 1,    /* GEMM writing a pipeline slot */
+  FLN_KERNEL_GEMM_SPLITK = 2,  /* split-K GEMM of the UNFUSED path */
+  FLN_KERNEL_NORM_BF16 = 3,    /* add_rmsnorm */
+  FLN_KERNEL_NORM_SLOT = 4,    /* pipeline second stage */
+  FLN_KERNEL_NORM_SPLITK = 5,  /* split-K reduce + add + norm */
+  FLN_KERNEL_KINDS = 6
+};
+typedef struct {
+  uint64_t launches[FLN_KERNEL_KINDS];
+  double total_ms[FLN_KERNEL_KINDS];
+} fln_profile_stats;
+
+/* enable != 0 starts recording (and clears earlier records); 0 stops. */
+int fln_profile_enable(int enable);
+/* Synchronise the recorded events and return their per-kind sums; clears them. */
+int fln_profile_read(fln_profile_stats* stats);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fln_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LIBFUSEDLN_H */

@@ -1,0 +1,222 @@
+"""GPU parity: every path of libfusedln against the fp64 oracle, through the C ABI.
+
+Small cases run the oracle on every element (several tiles, ragged tails in
+T, K and H); the full-size workloads compare sampled token rows that the
+oracle computes one by one.  Chunk invariance is bitwise.  Guard rows after T
+must stay untouched on every call.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from synth import Workload, make_inputs, workload
+
+from .gpu_util import UNFUSED, Run, plan
+from .parity import compare
+
+pytestmark = pytest.mark.gpu
+
+fln = pytest.importorskip("decoder_layer_projection_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fln.build()
+    fln.load()
+    yield
+    fln.fln_set_overrides(0, 0)
+
+
+def check_rows(rb, ob, d, wl, rows=None, tight=True, name=""):
+    r, o, _ = oracle.proj_add_rmsnorm(d["x"], d["W"], d["r0"], d["gamma"], wl.eps, wl.norm_kind, rows=rows)
+    if rows is not None:
+        rb, ob = rb[rows], ob[rows]
+    sr = compare(rb, r, name + " residual", tight=tight)
+    so = compare(ob, o, name + " out", tight=tight)
+    return sr, so
+
+
+SMALL = [
+    Workload("ragged", T=300, K=320, H=640, eps=1e-5, r_sigma=2.0, seed=1),
+    Workload("ragged_k_h", T=130, K=200, H=264, eps=1e-6, r_sigma=1.0, seed=2),
+    Workload("gemma_small", T=257, K=448, H=3584, norm_kind=1, eps=1e-6, gamma_mode="plain", seed=3),
+    Workload("wide_k", T=129, K=2048, H=512, eps=1e-5, x_mode="silu_gu", r_sigma=2.0, seed=4),
+]
+
+
+def test_tiny_config_all_paths():
+    wl = workload("tiny")
+    d = make_inputs(wl)
+    run = Run(d, wl.eps, wl.norm_kind)
+    for p in (plan(fln.PATH_FUSED, chunk=16), plan(fln.PATH_PIPELINED, chunk=16),
+              plan(fln.PATH_FUSED, chunk=16, tile_n=128), UNFUSED):
+        rb, ob = run(p)
+        check_rows(rb, ob, d, wl, name=f"tiny {p}")
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("path,tile", [(1, 256), (1, 128), (2, 256), (2, 128)])
+def test_small_prefill_paths_full_parity(wl, path, tile):
+    d = make_inputs(wl)
+    run = Run(d, wl.eps, wl.norm_kind)
+    rb, ob = run(plan(path, chunk=128, tile_n=tile))
+    check_rows(rb, ob, d, wl, name=f"{wl.name} path={path} tile={tile}")
+
+
+@pytest.mark.parametrize("wl", SMALL[:3], ids=lambda w: w.name)
+@pytest.mark.parametrize("T", [1, 7, 16, 33, 128, 256])
+def test_small_unfused_full_parity(wl, T):
+    d = make_inputs(wl, T=T)
+    run = Run(d, wl.eps, wl.norm_kind)
+    rb, ob = run(UNFUSED)
+    check_rows(rb, ob, d, wl, name=f"{wl.name} unfused T={T}")
+
+
+def test_chunk_invariance_is_bitwise():
+    wl = Workload("chunks", T=700, K=256, H=512, eps=1e-5, r_sigma=2.0, seed=9)
+    d = make_inputs(wl)
+    run = Run(d, wl.eps, wl.norm_kind)
+    for path in (fln.PATH_FUSED, fln.PATH_PIPELINED):
+        res = [run(plan(path, chunk=c)) for c in (128, 256, 384, 700)]
+        for rb, ob in res[1:]:
+            assert np.array_equal(rb, res[0][0]) and np.array_equal(ob, res[0][1])
+        check_rows(res[0][0], res[0][1], d, wl, name=f"chunks path={path}")
+
+
+def test_call_microchunk_argument_and_overrides():
+    wl = Workload("args", T=520, K=128, H=256, eps=1e-5, seed=5)
+    d = make_inputs(wl)
+    run = Run(d, wl.eps, wl.norm_kind)
+    rb0, ob0 = run(plan(fln.PATH_FUSED, chunk=4096), chunk=0)
+    rb1, ob1 = run(plan(fln.PATH_FUSED, chunk=4096), chunk=200)   # the call's chunk wins
+    assert np.array_equal(rb0, rb1) and np.array_equal(ob0, ob1)
+    fln.fln_set_overrides(100, 0)
+    try:
+        rb2, ob2 = run(None, chunk=0)
+    finally:
+        fln.fln_set_overrides(0, 0)
+    assert np.array_equal(rb0, rb2) and np.array_equal(ob0, ob2)
+    check_rows(rb0, ob0, d, wl, name="args")
+
+
+def test_add_rmsnorm_matches_oracle():
+    import torch
+    from .gpu_util import dev_bf16, host_bits
+    for T, H, kind, eps in [(1, 256, 0, 1e-6), (37, 4096, 0, 1e-5), (300, 3584, 1, 1e-6), (5, 8192, 0, 1e-5),
+                            (3, 8, 1, 0.0), (2, 32768, 0, 1e-5)]:
+        wl = Workload("n", T=T, K=8, H=H, norm_kind=kind, eps=eps, r_sigma=2.0, seed=T,
+                      gamma_mode="plain" if kind else "one_plus")
+        d = make_inputs(wl)
+        y = make_inputs(wl, seed=100 + T)["r0"]
+        r_dev = dev_bf16(d["r0"], extra_rows=2)
+        out = dev_bf16(np.zeros_like(d["r0"]), extra_rows=2, fill_bits=0x7FC2)
+        fln.add_rmsnorm(dev_bf16(y), r_dev[:T], torch.from_numpy(d["gamma"]).cuda(), eps, kind, out=out[:T])
+        fln.fln_device_status()
+        rb, ob = host_bits(r_dev), host_bits(out)
+        assert np.all(rb[T:] == 0x7FC1) and np.all(ob[T:] == 0x7FC2)
+        r, o, _ = oracle.add_rmsnorm(y, d["r0"], d["gamma"], eps, kind)
+        compare(rb[:T], r, f"add_rmsnorm T={T} H={H} residual")
+        compare(ob[:T], o, f"add_rmsnorm T={T} H={H} out")
+
+
+def test_minimal_shapes():
+    for T, K, H in [(1, 8, 8), (2, 64, 16), (129, 8, 24)]:
+        wl = Workload("min", T=T, K=K, H=H, eps=1e-5, seed=T + K)
+        d = make_inputs(wl)
+        run = Run(d, wl.eps, wl.norm_kind)
+        for p in (plan(fln.PATH_FUSED), plan(fln.PATH_PIPELINED, tile_n=128), UNFUSED):
+            if p is UNFUSED and T > 256:
+                continue
+            rb, ob = run(p)
+            check_rows(rb, ob, d, wl, name=f"min {T}x{K}x{H} {p['path']}")
+
+
+def test_errors_reported_on_device():
+    import torch
+    wl = workload("tiny")
+    d = make_inputs(wl)
+    run = Run(d, wl.eps, wl.norm_kind)
+    out = torch.empty((16, 256), dtype=torch.bfloat16, device="cuda")
+    host_x = torch.zeros((16, 256), dtype=torch.bfloat16)
+    r = run.x.clone()
+    rc = fln.fused_proj_add_rmsnorm_ptr(host_x.data_ptr(), run.W.data_ptr(), r.data_ptr(), run.gamma.data_ptr(),
+                                        1e-6, 0, 16, 256, 256, 0, out.data_ptr(), 0)
+    assert rc == fln.FLN_ERR_INVALID_ARG and "device pointer" in fln.fln_last_error()
+    rc = fln.fused_proj_add_rmsnorm_ptr(run.x.data_ptr() + 2, run.W.data_ptr(), r.data_ptr(), run.gamma.data_ptr(),
+                                        1e-6, 0, 16, 256, 256, 0, out.data_ptr(), 0)
+    assert rc == fln.FLN_ERR_INVALID_ARG and "aligned" in fln.fln_last_error()
+    rc = fln.fused_proj_add_rmsnorm_ptr(run.x.data_ptr(), run.W.data_ptr(), r.data_ptr(), run.gamma.data_ptr(),
+                                        1e-6, 0, 16, 256, 256, 0, r.data_ptr(), 0)
+    assert rc == fln.FLN_ERR_INVALID_ARG and "overlap" in fln.fln_last_error()
+    fln.fln_set_plan(256, 256, 0, plan(fln.PATH_FUSED, tuned_max=8))
+    try:
+        rc = fln.fused_proj_add_rmsnorm_ptr(run.x.data_ptr(), run.W.data_ptr(), r.data_ptr(), run.gamma.data_ptr(),
+                                            1e-6, 0, 16, 256, 256, 0, out.data_ptr(), 0)
+        assert rc == fln.FLN_ERR_NOT_TUNED
+    finally:
+        fln.fln_set_plan(256, 256, 0, None)
+    fln.fln_device_status()
+
+
+def test_autotune_then_auto_calls():
+    wl = Workload("tune", T=1024, K=512, H=1024, eps=1e-5, r_sigma=2.0, seed=7)
+    fln.fln_autotune(wl.K, wl.H, wl.norm_kind, wl.T)
+    try:
+        p = fln.fln_get_plan(wl.K, wl.H, wl.norm_kind, wl.T)
+        assert p["tuned_max_tokens"] == wl.T
+        assert p["path"] in (fln.PATH_FUSED, fln.PATH_PIPELINED)
+        d = make_inputs(wl)
+        run = Run(d, wl.eps, wl.norm_kind)
+        for T in (1, 64, 300, 1024):
+            rb, ob = run(None, chunk=0, T=T)
+            dd = {k: (v[:T] if k in ("x", "r0") else v) for k, v in d.items()}
+            check_rows(rb, ob, dd, wl, name=f"tuned T={T}")
+        with pytest.raises(fln.FlnError) as e:
+            fln.fln_get_plan(wl.K, wl.H, wl.norm_kind, 1025)
+        assert e.value.status == fln.FLN_ERR_NOT_TUNED
+    finally:
+        fln.fln_set_plan(wl.K, wl.H, wl.norm_kind, None)
+
+
+# --------------------------------------------------------------- full sizes
+def _sample_rows(T, n=12, seed=0):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, min(127, T - 1), min(128, T - 1), T // 2, max(T - 129, 0), T - 1]
+    rows = sorted(set(fixed) | set(rng.choice(T, size=min(n, T), replace=False).tolist()))
+    return np.array(rows, np.int64)
+
+
+FULL = ["llama3_8b_oproj", "llama3_8b_down", "gemma2_9b_down"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_prefill_sampled_rows(name):
+    wl = workload(name)
+    d = make_inputs(wl)
+    run = Run(d, wl.eps, wl.norm_kind)
+    rows = _sample_rows(wl.T)
+    for p in (plan(fln.PATH_FUSED, chunk=min(wl.T, 4096)), plan(fln.PATH_PIPELINED, chunk=1024)):
+        rb, ob = run(p)
+        check_rows(rb, ob, d, wl, rows=rows, name=f"{name} path={p['path']}")
+
+
+def test_full_size_chunk_sweep_bitwise():
+    wl = workload("llama3_8b_oproj")
+    d = make_inputs(wl)
+    run = Run(d, wl.eps, wl.norm_kind)
+    base = run(plan(fln.PATH_FUSED, chunk=4096))
+    for c in (256, 512, 1024):
+        rb, ob = run(plan(fln.PATH_FUSED, chunk=c))
+        assert np.array_equal(rb, base[0]) and np.array_equal(ob, base[1]), c
+    check_rows(base[0], base[1], d, wl, rows=_sample_rows(wl.T, seed=3), name="oproj chunk sweep")
+
+
+@pytest.mark.parametrize("name", ["llama70b_oproj_decode", "llama70b_down_decode"])
+@pytest.mark.parametrize("T", [1, 8, 32, 128, 256])
+def test_full_size_decode_sampled_rows(name, T):
+    wl = workload(name)
+    d = make_inputs(wl, T=T)
+    run = Run(d, wl.eps, wl.norm_kind)
+    rows = _sample_rows(T, n=4, seed=T)
+    rb, ob = run(UNFUSED)
+    check_rows(rb, ob, d, wl, rows=rows, name=f"{name} T={T} unfused")

@@ -1,0 +1,428 @@
+"""Benchmark: fused projection + residual add + RMSNorm on GB300.
+
+One step = one fused_proj_add_rmsnorm call over one batch of T tokens
+(y = x W^T, residual += y, out = RMSNorm(residual)) through the C ABI, on
+inputs already resident in HBM.  The default workload is the Llama-3-8B-shaped
+o_proj prefill (T = K = H = 4096, standard RMSNorm, eps 1e-5); --config picks
+another row of the workload table.  Inputs are synthetic and seeded.
+
+Timing: W warm-up steps, then exactly K steps, each bracketed by CUDA events on
+the launching stream with an L2 flush (a 512 MiB device write) between steps,
+outside the events; a barrier and a device synchronize on both sides of the
+timed loop; the slowest rank's time counts.  The roofline fraction uses the
+dominant kernel's own per-launch CUDA-event durations, recorded by the library
+on the stream that launches it.
+
+--impl reference times the fp64 CPU oracle instead (host cores, bounded row
+sample per step, same metric and unit).
+
+Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused proj+add+RMSNorm TFLOP/s and tokens/s; % of roofline (tensor or HBM) on 1 GB300"
+DEFAULT_CONFIG = "llama3_8b_oproj"
+FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch of the dominant kernel, from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and by the
+# sha1 of the kernel source the capture was taken on; reported as null when
+# the source has changed since.
+NCU_TRAFFIC = {}
+
+
+# ------------------------------------------------------------------ distributed helpers
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each data-parallel replica draws its own batch."""
+    return int(base) + 1000003 * int(rank)
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def whole_job_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Aggregate throughput: all ranks' units over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ------------------------------------------------------------------ peaks / clocks
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, interval_ms: int = 20):
+        self.index = index
+        self.interval_ms = interval_ms
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms={self.interval_ms}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10], parts[5]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t0 - 0.05 <= r[0] <= self.t1 + 0.05] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import decoder_layer_projection_gb300 as fln
+    from synth import make_inputs, workload
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=device)
+
+    fln.build()
+    fln.load()
+    wl = workload(args.config)
+    if args.tokens:
+        wl = wl.with_tokens(args.tokens)
+    T, K, H = wl.T, wl.K, wl.H
+    d = make_inputs(wl, seed=rank_seed(wl.seed, rank))
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    x, W, r = up(d["x"]), up(d["W"]), up(d["r0"])
+    gamma = torch.from_numpy(d["gamma"]).to(device)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    # profile the group on this device, as the pages' runtime does after the weights load
+    t_tune = time.time()
+    if args.microchunk == 0:
+        fln.fln_autotune(K, H, wl.norm_kind, T, stream)
+    t_tune = time.time() - t_tune
+    plan = fln.fln_get_plan(K, H, wl.norm_kind, T, args.microchunk)
+
+    def step():
+        fln.fused_proj_add_rmsnorm(x, W, r, gamma, wl.eps, wl.norm_kind, args.microchunk, out, stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    fln.fln_device_status(stream)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    fln.fln_profile_enable(True)
+    launches0 = fln.fln_launch_count()
+    barrier(device)
+    torch.cuda.synchronize(device)
+    sampler.mark_begin()
+    for i in range(args.steps):
+        flush.fill_(float(i))  # L2 flush, outside the events
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    sampler.mark_end()
+    launches = fln.fln_launch_count() - launches0
+    prof = fln.fln_profile_read()
+    fln.fln_profile_enable(False)
+    clocks = sampler.stop()
+    fln.fln_device_status(stream)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    local_s = sum(step_ms) / 1e3
+    max_s = max_over_ranks(local_s, device)
+    ms_per_step = max_s * 1e3 / args.steps
+    flops = wl.flops()
+    value = whole_job_value(flops * args.steps, world, max_s) / 1e12
+    tokens_per_s = whole_job_value(T * args.steps, world, max_s)
+
+    # roofline of the dominant kernel (largest share of recorded device time)
+    peaks, peak_src = load_peaks()
+    kname = max(prof, key=lambda k: prof[k]["total_ms"])
+    kp = prof[kname]
+    avg_launch_ms = kp["total_ms"] / max(kp["launches"], 1)
+    launches_per_step = kp["launches"] / args.steps
+    if kname.startswith("gemm"):
+        units_per_launch = T / launches_per_step  # tokens per launch
+        achieved = 2.0 * units_per_launch * K * H / (avg_launch_ms * 1e-3) / 1e12
+        bound, unit, peak = "tensor", "TFLOP/s", peaks["bf16_tflops"]
+    else:
+        units_per_launch = T / launches_per_step
+        achieved = (units_per_launch * H * 8.0 + 4.0 * H) / (avg_launch_ms * 1e-3) / 1e9
+        bound, unit, peak = "hbm", "GB/s", peaks["hbm_gbs"]
+    src_hash = hashlib.sha1(open(os.path.join(ROOT, "decoder_layer_projection_gb300", "csrc",
+                                              "fln_gemm.cu"), "rb").read()).hexdigest()[:12]
+    traffic = NCU_TRAFFIC.get((args.config, kname, src_hash))
+    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kname,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback",
+                "kernel_ms_per_launch": round(avg_launch_ms, 5), "launches_per_step": launches_per_step}
+    # full-step roofline: the slower of FLOPs at tensor peak and bytes at HBM bandwidth
+    t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), wl.algorithmic_bytes() / (peaks["hbm_gbs"] * 1e9))
+    step_frac = t_roof / (ms_per_step * 1e-3)
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    e2e = run_e2e(args, wl, d, W, gamma, device, stream, fln)
+    comparator = run_comparator(args, wl, x, W, d, gamma, device, stream, fln, flush)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "T": T, "K": K, "H": H, "norm": "gemma" if wl.norm_kind else "standard",
+                   "eps": wl.eps, "global_batch_tokens": T * world, "parallelism": f"dp{world} (replicas)",
+                   "plan": plan, "microchunk_arg": args.microchunk, "tune_s": round(t_tune, 2),
+                   "l2": "flushed between timed steps (512 MiB write)"},
+        "tokens_per_s": round(tokens_per_s, 1),
+        "step_roofline_frac": round(step_frac, 4),
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "kernel_time_ms": {k: round(v["total_ms"] / args.steps, 5) for k, v in prof.items() if v["launches"]},
+        "comparator_unfused_cublas": comparator,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, d, args.cpu_seconds)
+    if world > 1:
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def run_e2e(args, wl, d, W, gamma, device, stream, fln):
+    import numpy as np
+    import torch
+    T, K, H = wl.T, wl.K, wl.H
+    hx = torch.from_numpy(np.ascontiguousarray(d["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hr = torch.from_numpy(np.ascontiguousarray(d["r0"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    ho = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    hr_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty((T, K), dtype=torch.bfloat16, device=device)
+    dr = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    do = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+
+    def step():
+        dx.copy_(hx, non_blocking=True)
+        dr.copy_(hr, non_blocking=True)
+        fln.fused_proj_add_rmsnorm(dx, W, dr, gamma, wl.eps, wl.norm_kind, args.microchunk, do, stream)
+        ho.copy_(do, non_blocking=True)
+        hr_out.copy_(dr, non_blocking=True)
+
+    for _ in range(max(2, args.warmup // 2)):
+        step()
+    n = max(5, args.steps // 4)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    s = max_over_ranks(e0.elapsed_time(e1) / 1e3, device)
+    _, world, _ = dist_env()
+    return {"value": round(whole_job_value(wl.flops() * n, world, s) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": 2 * T * K + 2 * T * H, "d2h_bytes_per_step": 4 * T * H, "steps": n,
+            "ms_per_step": round(s * 1e3 / n, 4), "weights": "W and gamma resident on the device"}
+
+
+def run_comparator(args, wl, x, W, d, gamma, device, stream, fln, flush):
+    """Unfused sequence: cuBLAS bf16 GEMM (torch.matmul) then the library's add_rmsnorm."""
+    import numpy as np
+    import torch
+    r = torch.from_numpy(np.ascontiguousarray(d["r0"]).view(np.int16)).view(torch.bfloat16).to(device)
+    out = torch.empty_like(r)
+    times = []
+    for i in range(args.warmup + max(5, args.steps // 4)):
+        flush.fill_(float(i))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        y = torch.matmul(x, W.t())
+        fln.add_rmsnorm(y, r, gamma, wl.eps, wl.norm_kind, out, stream)
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize(device)
+    ms = [a.elapsed_time(b) for a, b in times[args.warmup:]]
+    m = sum(ms) / len(ms)
+    return {"value": round(wl.flops() / (m * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(m, 5),
+            "what": "torch.matmul (cuBLAS, bf16 out) then add_rmsnorm; y rounded to bf16 before the add"}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def _oracle_rows_timed(wl, d, rows, nthreads=0):
+    import numpy as np
+    import oracle
+    t = time.time()
+    oracle.proj_add_rmsnorm(d["x"], d["W"], d["r0"], d["gamma"], wl.eps, wl.norm_kind,
+                            rows=np.asarray(rows, np.int64), nthreads=nthreads)
+    return time.time() - t
+
+
+def cpu_baseline(wl, d, seconds: float):
+    """The fp64 oracle as it stands, on this host's cores, on a bounded row sample."""
+    import oracle
+    cores = oracle.max_threads()
+    probe = min(wl.T, max(1, cores))
+    t = _oracle_rows_timed(wl, d, list(range(probe)))
+    rows = int(min(wl.T, max(probe, probe * seconds / max(t, 1e-6))))
+    t = _oracle_rows_timed(wl, d, list(range(rows)))
+    flops = 2.0 * rows * wl.K * wl.H
+    return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} of {wl.T} token rows of {wl.name} (fp64, OpenMP over rows), {t:.1f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle timed on host cores, same metric/unit/config."""
+    import oracle
+    from synth import make_inputs, workload
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    wl = workload(args.config)
+    if args.tokens:
+        wl = wl.with_tokens(args.tokens)
+    oracle.build()
+    d = make_inputs(wl)
+    cores = oracle.max_threads()
+    # rows per step sized so that warm-up + steps stay within about a minute
+    probe = min(wl.T, max(1, cores))
+    t = _oracle_rows_timed(wl, d, list(range(probe)))
+    per_step = float(args.cpu_seconds) / max(1, args.steps + args.warmup) * 4
+    rows = int(min(wl.T, max(1, probe * per_step / max(t, 1e-6))))
+    for i in range(args.warmup):
+        _oracle_rows_timed(wl, d, [(i * rows + j) % wl.T for j in range(rows)])
+    total = 0.0
+    for i in range(args.steps):
+        total += _oracle_rows_timed(wl, d, [(i * rows + j) % wl.T for j in range(rows)])
+    flops = 2.0 * rows * wl.K * wl.H * args.steps
+    value = flops / total / 1e12
+    sample = f"{rows} of {wl.T} token rows per step of {wl.name} (fp64 oracle, OpenMP over rows)"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "K": wl.K, "H": wl.H},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["libfusedln", "reference"], default="libfusedln")
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--tokens", type=int, default=0, help="override T of the workload")
+    ap.add_argument("--microchunk", type=int, default=0, help="0 = tuned plan")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -182,7 +182,7 @@ def test_autotune_then_auto_calls():
 def _sample_rows(T, n=12, seed=0):
     rng = np.random.default_rng(seed)
     fixed = [0, 1, min(127, T - 1), min(128, T - 1), T // 2, max(T - 129, 0), T - 1]
-    rows = sorted(set(fixed) | set(rng.choice(T, size=min(n, T), replace=False).tolist()))
+    rows = sorted({r for r in fixed if 0 <= r < T} | set(rng.choice(T, size=min(n, T), replace=False).tolist()))
     return np.array(rows, np.int64)
 
 

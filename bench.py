@@ -189,8 +189,15 @@ def run_gpu(args):
 
     # profile the group on this device, as the pages' runtime does after the weights load
     t_tune = time.time()
-    if args.microchunk == 0:
+    if args.plan == "auto":
         fln.fln_autotune(K, H, wl.norm_kind, T, stream)
+    else:
+        f = args.plan.split(":")
+        path = {"fused": fln.PATH_FUSED, "pipelined": fln.PATH_PIPELINED}[f[0]]
+        fln.fln_set_plan(K, H, wl.norm_kind, dict(
+            path=path, microchunk_tokens=int(f[1]), tile_n=int(f[2]), gemm_ctas=int(f[3]),
+            norm_ctas=int(f[4]) if len(f) > 4 else 0, threshold_tokens=1 if T > 256 else 257,
+            tuned_max_tokens=0))
     t_tune = time.time() - t_tune
     plan = fln.fln_get_plan(K, H, wl.norm_kind, T, args.microchunk)
 
@@ -267,7 +274,8 @@ def run_gpu(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "T": T, "K": K, "H": H, "norm": "gemma" if wl.norm_kind else "standard",
                    "eps": wl.eps, "global_batch_tokens": T * world, "parallelism": f"dp{world} (replicas)",
-                   "plan": plan, "microchunk_arg": args.microchunk, "tune_s": round(t_tune, 2),
+                   "plan": plan, "plan_arg": args.plan, "microchunk_arg": args.microchunk,
+                   "tune_s": round(t_tune, 2),
                    "l2": "flushed between timed steps (512 MiB write)"},
         "tokens_per_s": round(tokens_per_s, 1),
         "step_roofline_frac": round(step_frac, 4),
@@ -386,7 +394,7 @@ def run_reference(args):
     # rows per step sized so that warm-up + steps stay within about a minute
     probe = min(wl.T, max(1, cores))
     t = _oracle_rows_timed(wl, d, list(range(probe)))
-    per_step = float(args.cpu_seconds) / max(1, args.steps + args.warmup) * 4
+    per_step = float(args.ref_seconds) / max(1, args.steps + args.warmup)
     rows = int(min(wl.T, max(1, probe * per_step / max(t, 1e-6))))
     for i in range(args.warmup):
         _oracle_rows_timed(wl, d, [(i * rows + j) % wl.T for j in range(rows)])
@@ -414,7 +422,10 @@ def main(argv=None):
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--tokens", type=int, default=0, help="override T of the workload")
     ap.add_argument("--microchunk", type=int, default=0, help="0 = tuned plan")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--plan", default="auto",
+                    help="auto (tune the group) or path:chunk:tile:gemm_ctas[:norm_ctas], path fused|pipelined")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the cpu_baseline sample")
+    ap.add_argument("--ref-seconds", type=float, default=60.0, help="--impl reference: CPU work of the whole run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

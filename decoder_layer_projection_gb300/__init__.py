@@ -36,7 +36,7 @@ KERNEL_NAMES = ("gemm_fused", "gemm_slot", "gemm_splitk", "norm_bf16", "norm_slo
 EXPORTED_SYMBOLS = (
     "fused_proj_add_rmsnorm", "add_rmsnorm", "fln_autotune", "fln_set_overrides", "fln_set_plan",
     "fln_get_plan", "fln_device_status", "fln_last_error", "fln_release_workspace", "fln_launch_count",
-    "fln_profile_enable", "fln_profile_read", "fln_version",
+    "fln_profile_enable", "fln_profile_read", "fln_version", "fused_proj_add_rmsnorm_noalloc",
 )
 
 
@@ -105,6 +105,8 @@ def load(path: str | None = None):
         lib.fln_profile_read.restype = i
         lib.fln_version.argtypes = []
         lib.fln_version.restype = i
+        lib.fused_proj_add_rmsnorm_noalloc.argtypes = [vp, vp, vp, vp, f, i, i, i, i, vp, vp, vp]
+        lib.fused_proj_add_rmsnorm_noalloc.restype = i
         _lib = lib
         return lib
 
@@ -146,6 +148,31 @@ def fused_proj_add_rmsnorm_ptr(x_ptr, W_ptr, residual_ptr, gamma_ptr, eps, norm_
     """Raw-pointer form: returns the status code without raising."""
     return load().fused_proj_add_rmsnorm(x_ptr, W_ptr, residual_ptr, gamma_ptr, float(eps), int(norm_kind),
                                          int(T), int(K), int(H), int(microchunk_tokens), out_ptr, stream_ptr)
+
+
+def fused_proj_add_rmsnorm_noalloc(x, W, residual, gamma, eps: float, norm_kind: int = NORM_STANDARD, out=None,
+                                   device_error=None, stream=None):
+    """Same result as fused_proj_add_rmsnorm, through the entry point that never
+    allocates device memory (static scratch; FUSED path).  `out` must be given by
+    callers that cannot allocate; `device_error` is an optional int32/uint32
+    device tensor of one element that receives device error bits.  Returns out."""
+    T, K = x.shape
+    H = W.shape[0]
+    if out is None:
+        import torch
+        out = torch.empty((T, H), dtype=residual.dtype, device=residual.device)
+    _check(load().fused_proj_add_rmsnorm_noalloc(_ptr(x), _ptr(W), _ptr(residual), _ptr(gamma), float(eps),
+                                                 int(norm_kind), int(T), int(K), int(H), _ptr(out),
+                                                 _ptr(device_error), _stream_ptr(stream)))
+    return out
+
+
+def fused_proj_add_rmsnorm_noalloc_ptr(x_ptr, W_ptr, residual_ptr, gamma_ptr, eps, norm_kind, T, K, H, out_ptr,
+                                       device_error_ptr, stream_ptr) -> int:
+    """Raw-pointer form: returns the status code without raising."""
+    return load().fused_proj_add_rmsnorm_noalloc(x_ptr, W_ptr, residual_ptr, gamma_ptr, float(eps),
+                                                 int(norm_kind), int(T), int(K), int(H), out_ptr,
+                                                 device_error_ptr, stream_ptr)
 
 
 def add_rmsnorm(y, residual, gamma, eps: float, norm_kind: int = NORM_STANDARD, out=None, stream=None):

@@ -601,6 +601,63 @@ int median_time(TuneCtx& t, const fln_plan& pl, int T, int reps, float* ms) {
 
 }  // namespace
 
+// ------------------------------------------------------------------ no-allocation entry point
+// Scratch of fused_proj_add_rmsnorm_noalloc: the row statistics of one
+// 4096-token chunk (per-tile publication flags, then 128 partial sums of
+// squares per tile), behind a 256-byte header whose first word collects the
+// device error bits when the caller passes no error word of its own.  It is a
+// static device array, so every GPU that loads the library holds it
+// (1 057 024 bytes) until the process exits, and no call ever allocates.
+constexpr int kNoAllocMaxTiles = 2048;  // row blocks x 256-wide N-tiles of one chunk: H <= 16384 at T >= 3969
+constexpr size_t kNoAllocHeader = 256;
+constexpr size_t kNoAllocFlagsBytes = size_t(kNoAllocMaxTiles) * sizeof(unsigned int);
+constexpr size_t kNoAllocBytes = kNoAllocHeader + kNoAllocFlagsBytes + size_t(kNoAllocMaxTiles) * 128 * sizeof(float);
+constexpr int kNoAllocTile = 256;
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+
+struct NoAllocDevice {
+  bool ready = false;
+  unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int sms = 0;
+  unsigned int gen = 0;  // publication value of the next launch (flags start at 0, values start at 1)
+};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// Once per device, with that device current: find where the static scratch
+// lives on it (host code cannot use the array's name as an address), and set
+// the kernel's shared-memory limit.  Nothing here allocates.
+int noalloc_setup(NoAllocDevice** out) {
+  int dev = 0;
+  FLN_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(FLN_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kNoAllocMaxDevices - 1);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    FLN_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "device query");
+    FLN_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "device query");
+    FLN_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "device query");
+    if (major != 10 || minor != 3)
+      return fail(FLN_ERR_UNSUPPORTED, "libfusedln is built for sm_103a (GB300); device %d is sm_%d%d", dev, major,
+                  minor);
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+    FLN_CUDA(gemm_prepare(kNoAllocTile, EPI_FUSED_NORM), "cudaFuncSetAttribute(max dynamic shared memory)");
+    d.scratch = static_cast<unsigned char*>(p);
+    d.sms = sms;
+    d.ready = true;
+  }
+  *out = &d;
+  return FLN_OK;
+}
+
+}  // namespace
+
 // ====================================================================== C ABI
 extern "C" {
 
@@ -913,5 +970,71 @@ int fln_profile_read(fln_profile_stats* st) {
 }
 
 int fln_version(void) { return 100; }
+
+int fused_proj_add_rmsnorm_noalloc(const fln_bf16* x, const fln_bf16* W, fln_bf16* residual, const float* gamma,
+                                   float eps, int norm_kind, int T, int K, int H, fln_bf16* out,
+                                   unsigned int* device_error, fln_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = check_common(eps, norm_kind, T, H);
+  if (rc) return rc;
+  if (K < 8 || (K & 7)) return fail(FLN_ERR_INVALID_ARG, "K=%d must be a positive multiple of 8", K);
+  const int chunk = std::min(T, kMaxMicrochunk);
+  const int mt = (chunk + 127) / 128;
+  const int nt = (H + kNoAllocTile - 1) / kNoAllocTile;
+  if (static_cast<long long>(mt) * nt > kNoAllocMaxTiles)
+    return fail(FLN_ERR_UNSUPPORTED,
+                "no-allocation path: %d row blocks x %d N-tiles of row statistics exceed the static scratch of %d "
+                "tiles (H <= %d for chunks of %d tokens)",
+                mt, nt, kNoAllocMaxTiles, kNoAllocMaxTiles / 32 * kNoAllocTile, kMaxMicrochunk);
+  if (T == 0) return FLN_OK;
+  if ((rc = validate_fused(x, W, residual, gamma, eps, norm_kind, T, K, H, 0, out))) return rc;
+  if (device_error) {
+    if (reinterpret_cast<uintptr_t>(device_error) & 3u)
+      return fail(FLN_ERR_INVALID_ARG, "device_error is not 4-byte aligned");
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, device_error);
+    if (e != cudaSuccess || (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)) {
+      (void)cudaGetLastError();
+      return fail(FLN_ERR_INVALID_ARG, "device_error is not a device pointer");
+    }
+  }
+  NoAllocDevice* d = nullptr;
+  if ((rc = noalloc_setup(&d))) return rc;
+  CUtensorMap tmA, tmB;
+  if ((rc = make_map(&tmA, x, K, T, 128))) return rc;
+  if ((rc = make_map(&tmB, W, K, H, kNoAllocTile))) return rc;
+  unsigned int* err_word = device_error ? device_error : reinterpret_cast<unsigned int*>(d->scratch);
+  unsigned int* flags = reinterpret_cast<unsigned int*>(d->scratch + kNoAllocHeader);
+  float* psum = reinterpret_cast<float*>(d->scratch + kNoAllocHeader + kNoAllocFlagsBytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  for (int c0 = 0; c0 < T; c0 += chunk) {
+    const int n = std::min(chunk, T - c0);
+    GemmParams p{};
+    p.M = n;
+    p.N = H;
+    p.K = K;
+    p.a_row0 = c0;
+    p.num_m_tiles = (n + 127) / 128;
+    p.num_n_tiles = nt;
+    p.num_k_blocks = (K + 63) / 64;
+    p.residual = reinterpret_cast<__nv_bfloat16*>(residual);
+    p.out = reinterpret_cast<__nv_bfloat16*>(out);
+    p.gamma = gamma;
+    p.eps = eps;
+    p.norm_kind = norm_kind;
+    p.ld = H;
+    p.psum = psum;
+    p.flags = flags;
+    if (++d->gen == 0) ++d->gen;
+    p.gen = d->gen;
+    p.err = err_word;
+    const int G = std::max(1, std::min(d->sms, p.num_m_tiles * nt));
+    cudaError_t e = launch_gemm(EPI_FUSED_NORM, kNoAllocTile, tmA, tmB, p, G, s);
+    if (e != cudaSuccess) return cuda_fail(e, "no-allocation fused GEMM launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  return FLN_OK;
+}
+
 
 }  // extern "C"

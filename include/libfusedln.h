@@ -186,6 +186,46 @@ int fln_profile_enable(int enable);
 /* Synchronise the recorded events and return their per-kind sums; clears them. */
 int fln_profile_read(fln_profile_stats* stats);
 
+/*
+ * fused_proj_add_rmsnorm_noalloc -- the same projection + residual add + norm
+ * as fused_proj_add_rmsnorm, for callers that must not allocate device memory.
+ * (The pages have no counterpart; it exists for integration.)
+ *
+ * Who needs it: runtimes that own every byte of device memory through their
+ * own pool or budget (an inference server that reserved the GPU up front, where
+ * a cudaMalloc outside the pool can fail or break its accounting), and
+ * latency-critical loops where cudaMalloc / cudaFree would synchronise the
+ * device.  fused_proj_add_rmsnorm grows a library workspace with cudaMalloc the
+ * first time a shape needs more; this entry point never does, and never
+ * creates a stream or an event.
+ *
+ *   x, W, residual, gamma, eps, norm_kind, T, K, H, out, stream: as in
+ *   fused_proj_add_rmsnorm.  It always runs the FUSED path (tile width 256,
+ *   chunks of 4096 tokens, one CTA per SM); plans, tuning, the token threshold
+ *   and the overrides do not apply.
+ *   device_error: NULL, or a device pointer to one 4-byte word owned by the
+ *   caller; a kernel that gives up a bounded wait ORs its error bits into it
+ *   (the caller clears it and reads it after synchronising).
+ *
+ * Scratch: a static device array of 1 057 024 bytes, held by every GPU that
+ * loads the library until the process exits.  It holds the row statistics of
+ * at most 2048 tiles: ceil(min(T, 4096) / 128) * ceil(H / 256) <= 2048, i.e.
+ * H <= 16384 once T >= 3969.  Larger problems return FLN_ERR_UNSUPPORTED with a
+ * message before anything is launched.
+ * The first call on a device looks up where the array lives on that device
+ * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make that
+ * first call before any stream capture.
+ * Every call on a device shares the one array and it keeps the last call's
+ * contents: the publication flags start at zero when the library loads and
+ * each call writes a new per-device value into them, so stale flags are never
+ * taken for this call's; the partial sums are written before they are read.
+ * Calls whose GPU work overlaps (for example, issued on two streams without
+ * ordering) race on the array and give undefined results: order them.
+ */
+int fused_proj_add_rmsnorm_noalloc(const fln_bf16* x, const fln_bf16* W, fln_bf16* residual, const float* gamma,
+                                   float eps, int norm_kind, int T, int K, int H, fln_bf16* out,
+                                   unsigned int* device_error, fln_stream_t stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int fln_version(void);
 

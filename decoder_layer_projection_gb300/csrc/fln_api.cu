@@ -85,6 +85,7 @@ struct Workspace {
   cudaEvent_t ev_join = nullptr;
   unsigned int gen = 0;
   bool prepared[3][5] = {};
+  int pair_max[3] = {0, 0, 0};  // resident CTA pairs of the fused pair kernel, tile 128 / 192 / 256
 };
 
 std::mutex g_mu;
@@ -180,6 +181,21 @@ int prepare_kernel(Workspace* ws, int bn, EpilogueKind epi) {
     FLN_CUDA(gemm_prepare(bn, epi), "cudaFuncSetAttribute(max dynamic shared memory)");
     ws->prepared[epi][bi] = true;
   }
+  return FLN_OK;
+}
+
+int pair_index(int bn) { return bn == 128 ? 0 : bn == 192 ? 1 : bn == 256 ? 2 : -1; }
+
+int prepare_pair(Workspace* ws, int bn, int* max_pairs) {
+  const int i = pair_index(bn);
+  if (i < 0) return fail(FLN_ERR_UNSUPPORTED, "fused tile width %d", bn);
+  if (ws->pair_max[i] == 0) {
+    int mp = 0;
+    FLN_CUDA(pair_gemm_prepare(bn, &mp), "pair kernel set-up (shared memory limit, resident clusters)");
+    if (mp < 1) return fail(FLN_ERR_UNSUPPORTED, "no CTA pair of the fused kernel fits on this device");
+    ws->pair_max[i] = mp;
+  }
+  *max_pairs = ws->pair_max[i];
   return FLN_OK;
 }
 
@@ -309,23 +325,29 @@ int gemm_grid(Workspace* ws, const fln_plan& pl, long long tiles) {
   return static_cast<int>(std::max<long long>(1, std::min<long long>(g, tiles)));
 }
 
-// Per microchunk: one persistent GEMM whose epilogue does add + norm.
+// Per microchunk: one persistent CTA-pair GEMM whose epilogue does add + norm.
 int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
   const int bn = pl.tile_n;
-  int rc = prepare_kernel(ws, bn, EPI_FUSED_NORM);
+  int max_pairs = 0;
+  int rc = prepare_pair(ws, bn, &max_pairs);
   if (rc) return rc;
   CUtensorMap tmA, tmB;
   if ((rc = make_map(&tmA, c.x, c.K, c.T, 128))) return rc;
-  if ((rc = make_map(&tmB, c.W, c.K, c.H, bn))) return rc;
+  if ((rc = make_map(&tmB, c.W, c.K, c.H, bn / 2))) return rc;
   const int chunk = std::min(pl.microchunk_tokens, c.T);
-  const int mt = (chunk + 127) / 128;
+  const int mt_alloc = 2 * ((chunk + 255) / 256);  // 128-row blocks, rounded up to whole pairs
   const int nt = (c.H + bn - 1) / bn;
-  if ((rc = grow(&ws->psum, &ws->psum_floats, static_cast<size_t>(mt) * nt * 128, false, "cudaMalloc(row sums)")))
+  if ((rc = grow(&ws->psum, &ws->psum_floats, static_cast<size_t>(mt_alloc) * nt * 128, false,
+                 "cudaMalloc(row sums)")))
     return rc;
-  if ((rc = grow(&ws->flags, &ws->flags_count, static_cast<size_t>(mt) * nt, true, "cudaMalloc(row flags)")))
+  if ((rc = grow(&ws->flags, &ws->flags_count, static_cast<size_t>(mt_alloc) * nt, true, "cudaMalloc(row flags)")))
     return rc;
   for (int c0 = 0; c0 < c.T; c0 += chunk) {
     const int n = std::min(chunk, c.T - c0);
+    // the chunk's residual / output rows: TMA clips every store at row n
+    CUtensorMap tmR, tmO;
+    if ((rc = make_map(&tmR, c.residual + static_cast<size_t>(c0) * c.H, c.H, n, 128))) return rc;
+    if ((rc = make_map(&tmO, c.out + static_cast<size_t>(c0) * c.H, c.H, n, 128))) return rc;
     GemmParams p{};
     p.M = n;
     p.N = c.H;
@@ -345,12 +367,15 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     if (++ws->gen == 0) ++ws->gen;
     p.gen = ws->gen;
     p.err = ws->err_word;
-    // every CTA of the grid must be resident at once (they exchange row
-    // statistics), so the grid never exceeds one CTA per SM
-    const int G = gemm_grid(ws, pl, static_cast<long long>(p.num_m_tiles) * nt);
+    // every pair of the grid must be resident at once (they exchange row
+    // statistics), so the grid never exceeds the resident-pair count
+    const long long tiles = static_cast<long long>((p.num_m_tiles + 1) / 2) * nt;
+    int pairs = max_pairs;
+    if (pl.gemm_ctas > 0) pairs = std::min(pairs, std::max(1, pl.gemm_ctas / 2));
+    pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(pairs, tiles)));
     rc = launch_counted(FLN_KERNEL_GEMM_FUSED, c.stream,
-                        [&] { return launch_gemm(EPI_FUSED_NORM, bn, tmA, tmB, p, G, c.stream); },
-                        "fused GEMM launch");
+                        [&] { return launch_gemm_pair_fused(bn, tmA, tmB, tmR, tmO, p, pairs, c.stream); },
+                        "fused pair GEMM launch");
     if (rc) return rc;
   }
   return FLN_OK;
@@ -470,7 +495,10 @@ int check_plan(const fln_plan& p) {
     return fail(FLN_ERR_INVALID_ARG, "plan.path must be FUSED or PIPELINED");
   if (p.microchunk_tokens < 1 || p.microchunk_tokens > kMaxMicrochunk)
     return fail(FLN_ERR_INVALID_ARG, "plan.microchunk_tokens must be in 1..%d", kMaxMicrochunk);
-  if (p.tile_n != 128 && p.tile_n != 256) return fail(FLN_ERR_INVALID_ARG, "plan.tile_n must be 128 or 256");
+  if (p.tile_n != 128 && p.tile_n != 192 && p.tile_n != 256)
+    return fail(FLN_ERR_INVALID_ARG, "plan.tile_n must be 128, 192 or 256");
+  if (p.path == FLN_PATH_PIPELINED && p.tile_n == 192)
+    return fail(FLN_ERR_INVALID_ARG, "plan.tile_n 192 is available on the FUSED path only");
   if (p.gemm_ctas < 0 || p.norm_ctas < 0) return fail(FLN_ERR_INVALID_ARG, "plan CTA targets must be >= 0");
   if (p.threshold_tokens < 1 || p.threshold_tokens > kDefaultThreshold)
     return fail(FLN_ERR_INVALID_ARG, "plan.threshold_tokens must be in 1..%d", kDefaultThreshold);
@@ -833,7 +861,7 @@ int fln_autotune(int K, int H, int norm_kind, int max_tokens, fln_stream_t strea
   float best_ms = 1e30f;
   bool any = false;
   for (int path : {FLN_PATH_FUSED, FLN_PATH_PIPELINED}) {
-    for (int tile : {256, 128}) {
+    for (int tile : (path == FLN_PATH_FUSED ? std::vector<int>{256, 192, 128} : std::vector<int>{256, 128})) {
       for (int cch : chunks) {
         for (int g : ctas) {
           for (int nc : (path == FLN_PATH_PIPELINED ? std::vector<int>{0, ws->sms / 4} : std::vector<int>{0})) {

@@ -1,0 +1,431 @@
+// fln_gemm2.cu -- projection GEMM + residual add + RMSNorm on a CTA pair
+// (tcgen05 cta_group::2) for the prefill regime.
+//
+// Computes, per 4096-token chunk, y = x . W^T (vLLM "TPSP Design", section 1:
+// row-parallel projection; torch-spyre "Plugin Architecture", "Transposed
+// linear weights": W is [H, K], used K-major) and fuses the residual add and
+// the RMSNorm over the complete hidden size of each token ("TPSP Design",
+// sections 1 and 3 "Fusion regions"; standard or Gemma (1 + gamma) weight).
+//
+// A cluster of two CTAs (on two SMs) computes a 256 x BN output tile with one
+// MMA stream issued by the even CTA: each CTA loads its own 128 rows of x and
+// half of the BN rows of W into its shared memory, the tensor cores read both
+// halves, and each CTA's TMEM receives its own 128 rows.  Per SM this halves
+// the W traffic of a 128 x BN tile.
+//
+// Epilogue (warps 2-5 of each CTA, one TMEM lane = one row per thread): the
+// residual tile arrives by TMA in 128-byte-swizzled 128 x 64 boxes; phase 1
+// forms r = r0 + acc in fp32 and the row's partial sum of squares; the row
+// block's partial sums of all N-tiles are exchanged through global memory
+// (per-tile release flags, acquire by the others, fixed summation order);
+// phase 2 recomputes r, writes bf16(r) over the residual box in shared memory
+// and bf16(r * rstd * g) into a staging box, and TMA stores both.  TMA clips
+// rows past the chunk and columns past H, so only valid rows are written.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fln_internal.h"
+#include "fln_ptx.cuh"
+
+namespace fln {
+
+namespace pair {
+
+constexpr int BM = 128;  // rows per CTA (256 per pair)
+constexpr int BK = 64;
+constexpr int THREADS = 192;
+constexpr int SMEM_LIMIT = 232448;  // 227 KiB opt-in per block
+constexpr int BAR_BYTES = 512;
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;            // 16 KiB
+  static constexpr int B_BYTES = (BN / 2) * BK * 2;      // this CTA's half of the W tile
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int GROUPS = BN / 64;                 // 64-column epilogue boxes
+  static constexpr int BOX = BM * 64 * 2;                // one 128 x 64 bf16 box (16 KiB)
+  static constexpr int R_BYTES = GROUPS * BOX;           // residual tile
+  static constexpr int O_BYTES = 2 * BOX;                // double-buffered output box
+  static constexpr int RAW_STAGES = (SMEM_LIMIT - 1024 - BAR_BYTES - R_BYTES - O_BYTES) / STAGE;
+  static constexpr int STAGES = RAW_STAGES > 8 ? 8 : RAW_STAGES;
+  static constexpr int SMEM = STAGES * STAGE + R_BYTES + O_BYTES + BAR_BYTES + 1024;
+  static constexpr int TMEM_COLS = (2 * BN) <= 256 ? 256 : 512;
+  static_assert(BN % 64 == 0 && BN >= 128 && BN <= 256, "tile width");
+  static_assert(STAGES >= 3, "pipeline depth");
+  static_assert(SMEM <= SMEM_LIMIT, "shared memory");
+};
+
+// byte offset of the 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled box
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <int BN>
+__global__ void __launch_bounds__(THREADS, 1)
+    fln_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmO,
+                         const GemmParams p) {
+  using C = Cfg<BN>;
+  constexpr int STAGES = C::STAGES;
+  constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* sR = smem + STAGES * C::STAGE;
+  uint8_t* sO = sR + C::R_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sO + C::O_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* acc_full = empty_bar + STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* r_full = acc_empty + 2;
+  uint64_t* drain_bar = r_full + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* epi_abort = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair_id = static_cast<int>(cluster_id_x());
+  const int num_pairs = static_cast<int>(nclusters_x());
+  const int nN = p.num_n_tiles;
+  const int num_pm = (p.num_m_tiles + 1) / 2;
+  const int total = num_pm * nN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 8);  // 4 epilogue warps in each CTA of the pair
+    }
+    mbar_init(r_full, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *epi_abort = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmR);
+    tma_prefetch_desc(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    const uint64_t pol = l2_policy_evict_normal();
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_mask = 0, issued_parity = 0;
+    bool ok = true;
+    for (int t = pair_id; ok && t < total; t += num_pairs) {
+      const int pm = t / nN, nt = t % nN;
+      const int a_row = p.a_row0 + pm * 2 * BM + static_cast<int>(rank) * BM;
+      const int b_row = nt * BN + static_cast<int>(rank) * (BN / 2);
+      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_EMPTY)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = ring + stage * C::STAGE;
+        uint8_t* sb = sa + C::A_BYTES;
+        const uint32_t fb = map_to_cta(smem_u32(&full_bar[stage]), 0);
+        if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE);
+        tma_load_2d_pair(sa, &tmA, fb, kb * BK, a_row, pol);
+        tma_load_2d_pair(sb, &tmB, fb, kb * BK, b_row, pol);
+        issued_mask |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && leader) {
+      for (int s = 0; s < STAGES; ++s) {
+        if (issued_mask & (1u << s)) {
+          volatile int no_abort = 0;
+          mbar_wait(&full_bar[s], (issued_parity >> s) & 1u, &no_abort, p.err, FLN_DEVERR_TIMEOUT_DRAIN);
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    int stage = 0;
+    uint32_t phase = 0;
+    int local = 0;
+    bool ok = true, issued_any = false;
+    for (int t = pair_id; ok && t < total; t += num_pairs, ++local) {
+      const int b = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      if (!mbar_wait(&acc_empty[b], (use & 1u) ^ 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.err, FLN_DEVERR_TIMEOUT_FULL)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(ring + stage * C::STAGE);
+        const uint64_t adesc = sw128_kmajor_desc(sa);
+        const uint64_t bdesc = sw128_kmajor_desc(sa + C::A_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16_pair(d_tmem, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2), IDESC,
+                        (kb > 0 || kk > 0) ? 1u : 0u);
+        issued_any = true;
+        mma_commit_pair_mc(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      mma_commit_pair_mc(&acc_full[b], 0x3);  // accumulator ready in both CTAs
+    }
+    if (!ok && issued_any) {
+      mma_commit_pair(drain_bar);
+      volatile int no_abort = 0;
+      mbar_wait(drain_bar, 0, &no_abort, p.err, FLN_DEVERR_TIMEOUT_DRAIN);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;        // TMEM lane quarter of this warp
+    const int rl = q * 32 + lane;  // row within this CTA's 128 rows
+    const int ep_tid = threadIdx.x - 64;
+    const uint32_t acc_empty_leader = map_to_cta(smem_u32(&acc_empty[0]), 0);
+    const uint64_t pol_r = l2_policy_evict_first();
+    int local = 0;
+    // residual tile of this CTA's first tile
+    if (ep_tid == 0 && pair_id < total) {
+      const int t = pair_id;
+      const int m0 = (t / nN) * 2 * BM + static_cast<int>(rank) * BM;
+      const int n0 = (t % nN) * BN;
+      mbar_arrive_expect_tx(r_full, C::R_BYTES);
+      for (int g = 0; g < C::GROUPS; ++g) tma_load_2d(sR + g * C::BOX, &tmR, r_full, n0 + g * 64, m0, pol_r);
+    }
+    for (int t = pair_id; t < total; t += num_pairs, ++local) {
+      const int b = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      const int mtile = (t / nN) * 2 + static_cast<int>(rank);  // 128-row block index in the launch
+      const int nt = t % nN;
+      const int m0 = mtile * BM;
+      const int n0 = nt * BN;
+      bool okw = mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
+      okw = okw && mbar_wait(r_full, static_cast<uint32_t>(local) & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
+      if (!okw) *epi_abort = 1;
+      named_bar_sync(1, 128);
+      if (*epi_abort) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
+
+      // phase 1: r = r0 + acc in fp32, this tile's partial sum of squares
+      // (rows past the chunk and columns past H read zeros: acc and r0 are 0 there)
+      float ss = 0.f;
+#pragma unroll 1
+      for (int g = 0; g < C::GROUPS; ++g) {
+        const uint8_t* box = sR + g * C::BOX;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float v[16];
+          tmem_ld16(tb + static_cast<uint32_t>(g * 64 + c4 * 16), v);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 u = *reinterpret_cast<const uint4*>(box + swz(rl, c4 * 2 + h));
+            float f[8];
+            bf16x8_to_f32(u, f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float r = f[j] + v[8 * h + j];
+              ss = fmaf(r, r, ss);
+            }
+          }
+        }
+      }
+      float* ps = p.psum + static_cast<size_t>(mtile) * nN * BM;
+      ps[static_cast<size_t>(nt) * BM + rl] = ss;
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (ep_tid == 0) st_release_gpu(&p.flags[mtile * nN + nt], p.gen);
+      if (ep_tid < 32) {
+        bool ok = true;
+        for (int j = lane; j < nN; j += 32) {
+          const unsigned int* f = &p.flags[mtile * nN + j];
+          if (ld_acquire_gpu(f) != p.gen) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(f) != p.gen) {
+              if (*abort_flag || globaltimer_ns() - t0 > FLN_WAIT_TIMEOUT_NS) {
+                ok = false;
+                break;
+              }
+            }
+          }
+          if (!ok) break;
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0) {
+          if (!*abort_flag) atomicOr(p.err, FLN_DEVERR_TIMEOUT_ROWSTAT);
+          *abort_flag = 1;
+          *epi_abort = 1;
+        }
+      }
+      named_bar_sync(1, 128);
+      const bool go = (*epi_abort == 0);
+      float tot = 0.f;
+      for (int j = 0; j < nN; ++j) tot += ld_cg_f32(&ps[static_cast<size_t>(j) * BM + rl]);
+      const float rstd = rsqrtf(tot / static_cast<float>(p.ld) + p.eps);
+
+      // phase 2: normalise; bf16 residual and output boxes -> TMA stores
+#pragma unroll 1
+      for (int g = 0; g < C::GROUPS; ++g) {
+        uint8_t* rbox = sR + g * C::BOX;
+        uint8_t* obox = sO + (g & 1) * C::BOX;
+        if (g >= 2) {
+          // the store issued from this output box two groups ago has finished reading it
+          if (ep_tid == 0) bulk_wait_group_read<1>();
+          named_bar_sync(1, 128);
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float v[16];
+          tmem_ld16(tb + static_cast<uint32_t>(g * 64 + c4 * 16), v);
+          const int col = n0 + g * 64 + c4 * 16;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int cc = col + 8 * h;
+            uint4* rp = reinterpret_cast<uint4*>(rbox + swz(rl, c4 * 2 + h));
+            float f[8];
+            bf16x8_to_f32(*rp, f);
+            float gw[8];
+            if (cc < p.N) {
+              const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc));
+              const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc + 4));
+              gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
+              gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) gw[j] = 0.f;
+            }
+            float r[8], o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              r[j] = f[j] + v[8 * h + j];
+              const float gj = p.norm_kind ? 1.0f + gw[j] : gw[j];
+              o[j] = r[j] * rstd * gj;
+            }
+            *rp = f32x8_to_bf16(r);
+            *reinterpret_cast<uint4*>(obox + swz(rl, c4 * 2 + h)) = f32x8_to_bf16(o);
+          }
+        }
+        fence_proxy_async_smem();  // make the boxes visible to the TMA store
+        named_bar_sync(1, 128);
+        if (ep_tid == 0 && go) {
+          tma_store_2d(&tmR, rbox, n0 + g * 64, m0);
+          tma_store_2d(&tmO, obox, n0 + g * 64, m0);
+        }
+        if (ep_tid == 0) bulk_commit_group();
+      }
+      // TMEM reads of this tile are done: hand the accumulator back to the MMA issuer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_leader + static_cast<uint32_t>(b * 8));
+      // next residual tile, once every store has finished reading the boxes
+      if (ep_tid == 0) {
+        bulk_wait_group_read<0>();
+        const int tn = t + num_pairs;
+        if (tn < total) {
+          const int m0n = (tn / nN) * 2 * BM + static_cast<int>(rank) * BM;
+          const int n0n = (tn % nN) * BN;
+          mbar_arrive_expect_tx(r_full, C::R_BYTES);
+          for (int g = 0; g < C::GROUPS; ++g) tma_load_2d(sR + g * C::BOX, &tmR, r_full, n0n + g * 64, m0n, pol_r);
+        }
+      }
+    }
+    if (ep_tid == 0) bulk_wait_group<0>();  // stores complete before the CTA exits
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while its peer may still signal it
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+}
+
+template <int BN>
+static cudaError_t launch_pair_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmR,
+                                  const CUtensorMap& tmO, const GemmParams& p, int pairs, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fln_gemm_pair_kernel<BN>, tmA, tmB, tmR, tmO, p);
+}
+
+template <int BN>
+static cudaError_t prepare_pair_bn(int* max_pairs) {
+  cudaError_t e = cudaFuncSetAttribute(fln_gemm_pair_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<BN>::SMEM);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(max_pairs, fln_gemm_pair_kernel<BN>, &cfg);
+}
+
+}  // namespace pair
+
+cudaError_t pair_gemm_prepare(int bn, int* max_pairs) {
+  switch (bn) {
+    case 128: return pair::prepare_pair_bn<128>(max_pairs);
+    case 192: return pair::prepare_pair_bn<192>(max_pairs);
+    case 256: return pair::prepare_pair_bn<256>(max_pairs);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_pair_fused(int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmR,
+                                   const CUtensorMap& tmO, const GemmParams& p, int pairs, cudaStream_t stream) {
+  switch (bn) {
+    case 128: return pair::launch_pair_bn<128>(tmA, tmB, tmR, tmO, p, pairs, stream);
+    case 192: return pair::launch_pair_bn<192>(tmA, tmB, tmR, tmO, p, pairs, stream);
+    case 256: return pair::launch_pair_bn<256>(tmA, tmB, tmR, tmO, p, pairs, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fln

@@ -78,11 +78,13 @@ def test_plans_thresholds_and_profiled_maximum(lib):
     K, H = 1024, 768
     assert fln.fln_get_plan(K, H, 0, 4096)["path"] == fln.PATH_FUSED       # default plan
     assert fln.fln_get_plan(K, H, 0, 256)["path"] == fln.PATH_UNFUSED      # below default threshold
-    bad = dict(path=fln.PATH_FUSED, microchunk_tokens=512, tile_n=192, gemm_ctas=0, norm_ctas=0,
+    bad = dict(path=fln.PATH_FUSED, microchunk_tokens=512, tile_n=96, gemm_ctas=0, norm_ctas=0,
                threshold_tokens=1, tuned_max_tokens=0)
     with pytest.raises(fln.FlnError) as e:
         fln.fln_set_plan(K, H, 0, bad)
     assert e.value.status == fln.FLN_ERR_INVALID_ARG
+    with pytest.raises(fln.FlnError):
+        fln.fln_set_plan(K, H, 0, dict(bad, tile_n=192, path=fln.PATH_PIPELINED))  # 192: FUSED only
     good = dict(bad, tile_n=128, path=fln.PATH_PIPELINED, threshold_tokens=33, tuned_max_tokens=2048)
     fln.fln_set_plan(K, H, 0, good)
     try:

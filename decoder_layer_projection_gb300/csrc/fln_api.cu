@@ -344,10 +344,9 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     return rc;
   for (int c0 = 0; c0 < c.T; c0 += chunk) {
     const int n = std::min(chunk, c.T - c0);
-    // the chunk's residual / output rows: TMA clips every store at row n
-    CUtensorMap tmR, tmO;
+    // the chunk's residual rows: rows past the chunk read as zeros
+    CUtensorMap tmR;
     if ((rc = make_map(&tmR, c.residual + static_cast<size_t>(c0) * c.H, c.H, n, 128))) return rc;
-    if ((rc = make_map(&tmO, c.out + static_cast<size_t>(c0) * c.H, c.H, n, 128))) return rc;
     GemmParams p{};
     p.M = n;
     p.N = c.H;
@@ -374,7 +373,7 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     if (pl.gemm_ctas > 0) pairs = std::min(pairs, std::max(1, pl.gemm_ctas / 2));
     pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(pairs, tiles)));
     rc = launch_counted(FLN_KERNEL_GEMM_FUSED, c.stream,
-                        [&] { return launch_gemm_pair_fused(bn, tmA, tmB, tmR, tmO, p, pairs, c.stream); },
+                        [&] { return launch_gemm_pair_fused(bn, tmA, tmB, tmR, p, pairs, c.stream); },
                         "fused pair GEMM launch");
     if (rc) return rc;
   }

@@ -14,13 +14,16 @@
 // the W traffic of a 128 x BN tile.
 //
 // Epilogue (warps 2-5 of each CTA, one TMEM lane = one row per thread): the
-// residual tile arrives by TMA in 128-byte-swizzled 128 x 64 boxes; phase 1
-// forms r = r0 + acc in fp32 and the row's partial sum of squares; the row
-// block's partial sums of all N-tiles are exchanged through global memory
-// (per-tile release flags, acquire by the others, fixed summation order);
-// phase 2 recomputes r, writes bf16(r) over the residual box in shared memory
-// and bf16(r * rstd * g) into a staging box, and TMA stores both.  TMA clips
-// rows past the chunk and columns past H, so only valid rows are written.
+// residual streams through a ring of three 128-byte-swizzled 128 x 64 TMA
+// boxes, once for each phase; with 16 KiB of output staging the epilogue
+// holds 64 KiB of shared memory and the operand ring keeps 5 stages at
+// BN = 256.  Phase 1 forms r = r0 + acc in fp32
+// and the row's partial sum of squares; the row block's partial sums of all
+// N-tiles are exchanged through global memory (per-tile release flags,
+// acquire by the others, fixed summation order); phase 2 recomputes r, puts
+// bf16(r) and bf16(r * rstd * g) in shared memory and each warp writes its 32
+// rows back with coalesced 16-byte stores, rows past the chunk and columns
+// past H masked.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -44,16 +47,17 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;            // 16 KiB
   static constexpr int B_BYTES = (BN / 2) * BK * 2;      // this CTA's half of the W tile
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int GROUPS = BN / 64;                 // 64-column epilogue boxes
+  static constexpr int GROUPS = BN / 64;                 // 64-column residual boxes per tile
   static constexpr int BOX = BM * 64 * 2;                // one 128 x 64 bf16 box (16 KiB)
-  static constexpr int R_BYTES = GROUPS * BOX;           // residual tile
-  static constexpr int O_BYTES = 2 * BOX;                // double-buffered output box
-  static constexpr int RAW_STAGES = (SMEM_LIMIT - 1024 - BAR_BYTES - R_BYTES - O_BYTES) / STAGE;
+  static constexpr int NBOX = 3;                         // residual boxes in flight
+  static constexpr int OSTAGE = 4 * 32 * 128;            // 32 rows x 64 bf16 output staging per warp
+  static constexpr int E_BYTES = NBOX * BOX + OSTAGE;
+  static constexpr int RAW_STAGES = (SMEM_LIMIT - 1024 - BAR_BYTES - E_BYTES) / STAGE;
   static constexpr int STAGES = RAW_STAGES > 8 ? 8 : RAW_STAGES;
-  static constexpr int SMEM = STAGES * STAGE + R_BYTES + O_BYTES + BAR_BYTES + 1024;
+  static constexpr int SMEM = STAGES * STAGE + E_BYTES + BAR_BYTES + 1024;
   static constexpr int TMEM_COLS = (2 * BN) <= 256 ? 256 : 512;
   static_assert(BN % 64 == 0 && BN >= 128 && BN <= 256, "tile width");
-  static_assert(STAGES >= 3, "pipeline depth");
+  static_assert(STAGES >= 4, "pipeline depth");
   static_assert(SMEM <= SMEM_LIMIT, "shared memory");
 };
 
@@ -65,8 +69,7 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     fln_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmO,
-                         const GemmParams p) {
+                         const __grid_constant__ CUtensorMap tmR, const GemmParams p) {
   using C = Cfg<BN>;
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN);
@@ -74,14 +77,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint8_t* sR = smem + STAGES * C::STAGE;
-  uint8_t* sO = sR + C::R_BYTES;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sO + C::O_BYTES);
+  uint8_t* sE = smem + STAGES * C::STAGE;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sE + C::E_BYTES);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* acc_full = empty_bar + STAGES;
   uint64_t* acc_empty = acc_full + 2;
-  uint64_t* r_full = acc_empty + 2;
-  uint64_t* drain_bar = r_full + 1;
+  uint64_t* e_full = acc_empty + 2;
+  uint64_t* drain_bar = e_full + C::NBOX;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* epi_abort = abort_flag + 1;
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 8);  // 4 epilogue warps in each CTA of the pair
     }
-    mbar_init(r_full, 1);
+    for (int e = 0; e < C::NBOX; ++e) mbar_init(&e_full[e], 1);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     *epi_abort = 0;
@@ -114,7 +116,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmR);
-    tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
@@ -213,26 +214,35 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int rl = q * 32 + lane;  // row within this CTA's 128 rows
     const int ep_tid = threadIdx.x - 64;
     const uint32_t acc_empty_leader = map_to_cta(smem_u32(&acc_empty[0]), 0);
-    const uint64_t pol_r = l2_policy_evict_first();
+    const uint64_t pol_r = l2_policy_evict_normal();
+    constexpr int G = C::GROUPS;
+    constexpr int BOXES = 2 * G;  // residual boxes consumed per tile: G in each phase
+    // Box s of this CTA's sequence: local tile s / BOXES, group (s % BOXES) % G,
+    // buffer s % NBOX, phase parity (s / NBOX) & 1.  One thread issues the loads.
+    constexpr int NB = C::NBOX;
+    auto issue_box = [&](int s) {
+      const int k = s / BOXES;
+      const int g = (s % BOXES) % G;
+      const int t = pair_id + k * num_pairs;
+      if (t >= total) return;
+      const int m0 = ((t / nN) * 2 + static_cast<int>(rank)) * BM;
+      const int n0 = (t % nN) * BN + g * 64;
+      mbar_arrive_expect_tx(&e_full[s % NB], C::BOX);
+      tma_load_2d(sE + (s % NB) * C::BOX, &tmR, &e_full[s % NB], n0, m0, pol_r);
+    };
+    if (ep_tid == 0)
+      for (int k = 0; k < NB; ++k) issue_box(k);
+    int s = 0;  // next box to consume
     int local = 0;
-    // residual tile of this CTA's first tile
-    if (ep_tid == 0 && pair_id < total) {
-      const int t = pair_id;
-      const int m0 = (t / nN) * 2 * BM + static_cast<int>(rank) * BM;
-      const int n0 = (t % nN) * BN;
-      mbar_arrive_expect_tx(r_full, C::R_BYTES);
-      for (int g = 0; g < C::GROUPS; ++g) tma_load_2d(sR + g * C::BOX, &tmR, r_full, n0 + g * 64, m0, pol_r);
-    }
     for (int t = pair_id; t < total; t += num_pairs, ++local) {
       const int b = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       const int mtile = (t / nN) * 2 + static_cast<int>(rank);  // 128-row block index in the launch
       const int nt = t % nN;
-      const int m0 = mtile * BM;
       const int n0 = nt * BN;
-      bool okw = mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
-      okw = okw && mbar_wait(r_full, static_cast<uint32_t>(local) & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
-      if (!okw) *epi_abort = 1;
+      // All 128 epilogue threads decide together whether to continue: a thread
+      // that leaves alone would strand the others at a named barrier.
+      if (!mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) *epi_abort = 1;
       named_bar_sync(1, 128);
       if (*epi_abort) break;
       tc_fence_after();
@@ -242,8 +252,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       // (rows past the chunk and columns past H read zeros: acc and r0 are 0 there)
       float ss = 0.f;
 #pragma unroll 1
-      for (int g = 0; g < C::GROUPS; ++g) {
-        const uint8_t* box = sR + g * C::BOX;
+      for (int g = 0; g < G; ++g, ++s) {
+        mbar_wait(&e_full[s % NB], static_cast<uint32_t>(s / NB) & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
+        const uint8_t* box = sE + (s % NB) * C::BOX;
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           float v[16];
@@ -260,6 +271,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         }
+        named_bar_sync(1, 128);  // box s fully read
+        if (ep_tid == 0) issue_box(s + NB);
       }
       float* ps = p.psum + static_cast<size_t>(mtile) * nN * BM;
       ps[static_cast<size_t>(nt) * BM + rl] = ss;
@@ -289,30 +302,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       named_bar_sync(1, 128);
-      const bool go = (*epi_abort == 0);
+      const bool go_all = (*epi_abort == 0);
       float tot = 0.f;
       for (int j = 0; j < nN; ++j) tot += ld_cg_f32(&ps[static_cast<size_t>(j) * BM + rl]);
       const float rstd = rsqrtf(tot / static_cast<float>(p.ld) + p.eps);
 
-      // phase 2: normalise; bf16 residual and output boxes -> TMA stores
+      // phase 2: normalise.  r goes back into the residual box in place and
+      // the output into this warp's staging rows; then each warp reads its 32
+      // rows back row-major so that one 16-byte store per lane covers 4 rows x
+      // 128 contiguous bytes (rows past the chunk and columns past H masked).
+      uint8_t* ostage = sE + C::NBOX * C::BOX + q * (32 * 128);
 #pragma unroll 1
-      for (int g = 0; g < C::GROUPS; ++g) {
-        uint8_t* rbox = sR + g * C::BOX;
-        uint8_t* obox = sO + (g & 1) * C::BOX;
-        if (g >= 2) {
-          // the store issued from this output box two groups ago has finished reading it
-          if (ep_tid == 0) bulk_wait_group_read<1>();
-          named_bar_sync(1, 128);
-        }
+      for (int g = 0; g < G; ++g, ++s) {
+        mbar_wait(&e_full[s % NB], static_cast<uint32_t>(s / NB) & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
+        uint8_t* box = sE + (s % NB) * C::BOX;
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           float v[16];
           tmem_ld16(tb + static_cast<uint32_t>(g * 64 + c4 * 16), v);
-          const int col = n0 + g * 64 + c4 * 16;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int cc = col + 8 * h;
-            uint4* rp = reinterpret_cast<uint4*>(rbox + swz(rl, c4 * 2 + h));
+            const int chunk = c4 * 2 + h;
+            const int cc = n0 + g * 64 + chunk * 8;
+            uint4* rp = reinterpret_cast<uint4*>(box + swz(rl, chunk));
             float f[8];
             bf16x8_to_f32(*rp, f);
             float gw[8];
@@ -333,34 +345,45 @@ __global__ void __launch_bounds__(THREADS, 1)
               o[j] = r[j] * rstd * gj;
             }
             *rp = f32x8_to_bf16(r);
-            *reinterpret_cast<uint4*>(obox + swz(rl, c4 * 2 + h)) = f32x8_to_bf16(o);
+            *reinterpret_cast<uint4*>(ostage + swz(lane, chunk)) = f32x8_to_bf16(o);
           }
         }
-        fence_proxy_async_smem();  // make the boxes visible to the TMA store
-        named_bar_sync(1, 128);
-        if (ep_tid == 0 && go) {
-          tma_store_2d(&tmR, rbox, n0 + g * 64, m0);
-          tma_store_2d(&tmO, obox, n0 + g * 64, m0);
+        __syncwarp();
+        if (go_all) {
+#pragma unroll 2
+          for (int it = 0; it < 8; ++it) {
+            const int rr = it * 4 + (lane >> 3);  // row within this warp's 32
+            const int ch = lane & 7;
+            const int lrow = mtile * BM + q * 32 + rr;
+            const int col = n0 + g * 64 + ch * 8;
+            const uint4 rv = *reinterpret_cast<const uint4*>(box + swz(q * 32 + rr, ch));
+            const uint4 ov = *reinterpret_cast<const uint4*>(ostage + swz(rr, ch));
+            if (lrow < p.M && col < p.N) {
+              const size_t off = (static_cast<size_t>(p.a_row0) + lrow) * static_cast<size_t>(p.ld) + col;
+              *reinterpret_cast<uint4*>(p.residual + off) = rv;
+              __stcs(reinterpret_cast<uint4*>(p.out + off), ov);
+            }
+          }
         }
-        if (ep_tid == 0) bulk_commit_group();
+        named_bar_sync(1, 128);  // box s and the staging rows fully read
+        if (ep_tid == 0) issue_box(s + NB);
       }
       // TMEM reads of this tile are done: hand the accumulator back to the MMA issuer
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty_leader + static_cast<uint32_t>(b * 8));
-      // next residual tile, once every store has finished reading the boxes
-      if (ep_tid == 0) {
-        bulk_wait_group_read<0>();
-        const int tn = t + num_pairs;
-        if (tn < total) {
-          const int m0n = (tn / nN) * 2 * BM + static_cast<int>(rank) * BM;
-          const int n0n = (tn % nN) * BN;
-          mbar_arrive_expect_tx(r_full, C::R_BYTES);
-          for (int g = 0; g < C::GROUPS; ++g) tma_load_2d(sR + g * C::BOX, &tmR, r_full, n0n + g * 64, m0n, pol_r);
+    }
+    // unwinding or done: let residual boxes still in flight land before the CTA exits
+    if (ep_tid == 0) {
+      for (int k = 0; k < NB; ++k) {
+        const int sb = s + k;  // boxes issued but never consumed
+        const int kt = sb / BOXES;
+        if (pair_id + kt * num_pairs < total) {
+          volatile int no_abort = 0;
+          mbar_wait(&e_full[sb % NB], static_cast<uint32_t>(sb / NB) & 1u, &no_abort, p.err, FLN_DEVERR_TIMEOUT_DRAIN);
         }
       }
     }
-    if (ep_tid == 0) bulk_wait_group<0>();  // stores complete before the CTA exits
   }
 
   tc_fence_before();
@@ -372,7 +395,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 template <int BN>
 static cudaError_t launch_pair_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmR,
-                                  const CUtensorMap& tmO, const GemmParams& p, int pairs, cudaStream_t stream) {
+                                  const GemmParams& p, int pairs, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
@@ -385,7 +408,7 @@ static cudaError_t launch_pair_bn(const CUtensorMap& tmA, const CUtensorMap& tmB
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fln_gemm_pair_kernel<BN>, tmA, tmB, tmR, tmO, p);
+  return cudaLaunchKernelEx(&cfg, fln_gemm_pair_kernel<BN>, tmA, tmB, tmR, p);
 }
 
 template <int BN>
@@ -419,11 +442,11 @@ cudaError_t pair_gemm_prepare(int bn, int* max_pairs) {
 }
 
 cudaError_t launch_gemm_pair_fused(int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmR,
-                                   const CUtensorMap& tmO, const GemmParams& p, int pairs, cudaStream_t stream) {
+                                   const GemmParams& p, int pairs, cudaStream_t stream) {
   switch (bn) {
-    case 128: return pair::launch_pair_bn<128>(tmA, tmB, tmR, tmO, p, pairs, stream);
-    case 192: return pair::launch_pair_bn<192>(tmA, tmB, tmR, tmO, p, pairs, stream);
-    case 256: return pair::launch_pair_bn<256>(tmA, tmB, tmR, tmO, p, pairs, stream);
+    case 128: return pair::launch_pair_bn<128>(tmA, tmB, tmR, p, pairs, stream);
+    case 192: return pair::launch_pair_bn<192>(tmA, tmB, tmR, p, pairs, stream);
+    case 256: return pair::launch_pair_bn<256>(tmA, tmB, tmR, p, pairs, stream);
   }
   return cudaErrorInvalidValue;
 }

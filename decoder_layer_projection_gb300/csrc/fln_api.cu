@@ -337,10 +337,10 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
   const int chunk = std::min(pl.microchunk_tokens, c.T);
   const int mt_alloc = 2 * ((chunk + 255) / 256);  // 128-row blocks, rounded up to whole pairs
   const int nt = (c.H + bn - 1) / bn;
-  if ((rc = grow(&ws->psum, &ws->psum_floats, static_cast<size_t>(mt_alloc) * nt * 128, false,
+  // row partial sums: one 64-bit {generation, value} word per row and N-tile,
+  // zeroed once at allocation (no launch uses generation 0)
+  if ((rc = grow(&ws->psum, &ws->psum_floats, 2 * static_cast<size_t>(mt_alloc) * nt * 128, true,
                  "cudaMalloc(row sums)")))
-    return rc;
-  if ((rc = grow(&ws->flags, &ws->flags_count, static_cast<size_t>(mt_alloc) * nt, true, "cudaMalloc(row flags)")))
     return rc;
   for (int c0 = 0; c0 < c.T; c0 += chunk) {
     const int n = std::min(chunk, c.T - c0);
@@ -362,7 +362,6 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     p.norm_kind = c.kind;
     p.ld = c.H;
     p.psum = ws->psum;
-    p.flags = ws->flags;
     if (++ws->gen == 0) ++ws->gen;
     p.gen = ws->gen;
     p.err = ws->err_word;

@@ -83,7 +83,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* acc_full = empty_bar + STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* e_full = acc_empty + 2;
-  uint64_t* drain_bar = e_full + C::NBOX;
+  uint64_t* e_free = e_full + C::NBOX;
+  uint64_t* drain_bar = e_free + C::NBOX;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* epi_abort = abort_flag + 1;
@@ -107,7 +108,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 8);  // 4 epilogue warps in each CTA of the pair
     }
-    for (int e = 0; e < C::NBOX; ++e) mbar_init(&e_full[e], 1);
+    for (int e = 0; e < C::NBOX; ++e) {
+      mbar_init(&e_full[e], 1);
+      mbar_init(&e_free[e], 4);  // one arrival per epilogue warp once it has read the box
+    }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     *epi_abort = 0;
@@ -165,6 +169,38 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
+  } else if (warp == 0 && lane == 1) {
+    // ------------------------------------------------------------ residual loader (both CTAs)
+    // Box s of this CTA's sequence: local tile s / BOXES, group (s % BOXES) % G
+    // (each phase of a tile reads the G boxes once), buffer s % NBOX.
+    constexpr int G = C::GROUPS;
+    constexpr int BOXES = 2 * G;
+    constexpr int NB = C::NBOX;
+    const uint64_t pol_r = l2_policy_evict_normal();
+    int s = 0;
+    bool ok = true;
+    for (;; ++s) {
+      const int k = s / BOXES;
+      const int t = pair_id + k * num_pairs;
+      if (t >= total) break;
+      if (s >= NB && !mbar_wait(&e_free[s % NB], static_cast<uint32_t>(s / NB - 1) & 1u, abort_flag, p.err,
+                                FLN_DEVERR_TIMEOUT_EMPTY)) {
+        ok = false;
+        break;
+      }
+      const int g = (s % BOXES) % G;
+      const int m0 = ((t / nN) * 2 + static_cast<int>(rank)) * BM;
+      const int n0 = (t % nN) * BN + g * 64;
+      mbar_arrive_expect_tx(&e_full[s % NB], C::BOX);
+      tma_load_2d(sE + (s % NB) * C::BOX, &tmR, &e_full[s % NB], n0, m0, pol_r);
+    }
+    // let the last boxes land before the CTA can exit (they may be unconsumed after an abort)
+    for (int k = 1; k <= NB && s - k >= 0; ++k) {
+      const int sb = s - k;
+      volatile int no_abort = 0;
+      mbar_wait(&e_full[sb % NB], static_cast<uint32_t>(sb / NB) & 1u, &no_abort, p.err, FLN_DEVERR_TIMEOUT_DRAIN);
+    }
+    (void)ok;
   } else if (warp == 1 && lane == 0 && leader) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     int stage = 0;
@@ -212,27 +248,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;        // TMEM lane quarter of this warp
     const int rl = q * 32 + lane;  // row within this CTA's 128 rows
-    const int ep_tid = threadIdx.x - 64;
     const uint32_t acc_empty_leader = map_to_cta(smem_u32(&acc_empty[0]), 0);
-    const uint64_t pol_r = l2_policy_evict_normal();
     constexpr int G = C::GROUPS;
-    constexpr int BOXES = 2 * G;  // residual boxes consumed per tile: G in each phase
-    // Box s of this CTA's sequence: local tile s / BOXES, group (s % BOXES) % G,
-    // buffer s % NBOX, phase parity (s / NBOX) & 1.  One thread issues the loads.
     constexpr int NB = C::NBOX;
-    auto issue_box = [&](int s) {
-      const int k = s / BOXES;
-      const int g = (s % BOXES) % G;
-      const int t = pair_id + k * num_pairs;
-      if (t >= total) return;
-      const int m0 = ((t / nN) * 2 + static_cast<int>(rank)) * BM;
-      const int n0 = (t % nN) * BN + g * 64;
-      mbar_arrive_expect_tx(&e_full[s % NB], C::BOX);
-      tma_load_2d(sE + (s % NB) * C::BOX, &tmR, &e_full[s % NB], n0, m0, pol_r);
-    };
-    if (ep_tid == 0)
-      for (int k = 0; k < NB; ++k) issue_box(k);
-    int s = 0;  // next box to consume
+    uint8_t* ostage = sE + C::NBOX * C::BOX + q * (32 * 128);  // this warp's 32 output rows
+    unsigned long long* psum = reinterpret_cast<unsigned long long*>(p.psum);
+    const unsigned long long tag = static_cast<unsigned long long>(p.gen) << 32;
+    int s = 0;  // next residual box to consume
     int local = 0;
     for (int t = pair_id; t < total; t += num_pairs, ++local) {
       const int b = local & 1;
@@ -241,7 +263,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int nt = t % nN;
       const int n0 = nt * BN;
       // All 128 epilogue threads decide together whether to continue: a thread
-      // that leaves alone would strand the others at a named barrier.
+      // that leaves alone would strand the others at the named barrier.
       if (!mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) *epi_abort = 1;
       named_bar_sync(1, 128);
       if (*epi_abort) break;
@@ -271,47 +293,43 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         }
-        named_bar_sync(1, 128);  // box s fully read
-        if (ep_tid == 0) issue_box(s + NB);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&e_free[s % NB]);  // this warp is done with box s
       }
-      float* ps = p.psum + static_cast<size_t>(mtile) * nN * BM;
-      ps[static_cast<size_t>(nt) * BM + rl] = ss;
-      __threadfence();
-      named_bar_sync(1, 128);
-      if (ep_tid == 0) st_release_gpu(&p.flags[mtile * nN + nt], p.gen);
-      if (ep_tid < 32) {
-        bool ok = true;
-        for (int j = lane; j < nN; j += 32) {
-          const unsigned int* f = &p.flags[mtile * nN + j];
-          if (ld_acquire_gpu(f) != p.gen) {
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_gpu(f) != p.gen) {
-              if (*abort_flag || globaltimer_ns() - t0 > FLN_WAIT_TIMEOUT_NS) {
-                ok = false;
-                break;
-              }
+      // Row statistics across the row block's N-tiles: each row's partial sum
+      // is published as one 64-bit word {generation of this launch, value}, so a
+      // reader that sees this launch's generation also sees its value; no fence
+      // or flag is needed.  Partial sums are added in N-tile order.
+      unsigned long long* prow = psum + static_cast<size_t>(mtile) * nN * BM + rl;
+      st_relaxed_gpu_u64(prow + static_cast<size_t>(nt) * BM, tag | __float_as_uint(ss));
+      float tot = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nN && ok; ++j) {
+        const unsigned long long* f = prow + static_cast<size_t>(j) * BM;
+        unsigned long long v = ld_relaxed_gpu_u64(f);
+        if ((v >> 32) != p.gen) {
+          const uint64_t t0 = globaltimer_ns();
+          while (((v = ld_relaxed_gpu_u64(f)) >> 32) != p.gen) {
+            if (*abort_flag || globaltimer_ns() - t0 > FLN_WAIT_TIMEOUT_NS) {
+              ok = false;
+              break;
             }
           }
-          if (!ok) break;
         }
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok && lane == 0) {
-          if (!*abort_flag) atomicOr(p.err, FLN_DEVERR_TIMEOUT_ROWSTAT);
-          *abort_flag = 1;
-          *epi_abort = 1;
-        }
+        tot += __uint_as_float(static_cast<uint32_t>(v));
       }
-      named_bar_sync(1, 128);
-      const bool go_all = (*epi_abort == 0);
-      float tot = 0.f;
-      for (int j = 0; j < nN; ++j) tot += ld_cg_f32(&ps[static_cast<size_t>(j) * BM + rl]);
+      if (!ok) {
+        if (!*abort_flag) atomicOr(p.err, FLN_DEVERR_TIMEOUT_ROWSTAT);
+        *abort_flag = 1;
+        *epi_abort = 1;
+      }
+      const bool go = __all_sync(0xffffffffu, ok);
       const float rstd = rsqrtf(tot / static_cast<float>(p.ld) + p.eps);
 
       // phase 2: normalise.  r goes back into the residual box in place and
       // the output into this warp's staging rows; then each warp reads its 32
       // rows back row-major so that one 16-byte store per lane covers 4 rows x
       // 128 contiguous bytes (rows past the chunk and columns past H masked).
-      uint8_t* ostage = sE + C::NBOX * C::BOX + q * (32 * 128);
 #pragma unroll 1
       for (int g = 0; g < G; ++g, ++s) {
         mbar_wait(&e_full[s % NB], static_cast<uint32_t>(s / NB) & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
@@ -349,7 +367,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
         __syncwarp();
-        if (go_all) {
+        if (go) {
 #pragma unroll 2
           for (int it = 0; it < 8; ++it) {
             const int rr = it * 4 + (lane >> 3);  // row within this warp's 32
@@ -365,24 +383,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         }
-        named_bar_sync(1, 128);  // box s and the staging rows fully read
-        if (ep_tid == 0) issue_box(s + NB);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&e_free[s % NB]);  // box s and the staging rows are free
       }
       // TMEM reads of this tile are done: hand the accumulator back to the MMA issuer
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty_leader + static_cast<uint32_t>(b * 8));
-    }
-    // unwinding or done: let residual boxes still in flight land before the CTA exits
-    if (ep_tid == 0) {
-      for (int k = 0; k < NB; ++k) {
-        const int sb = s + k;  // boxes issued but never consumed
-        const int kt = sb / BOXES;
-        if (pair_id + kt * num_pairs < total) {
-          volatile int no_abort = 0;
-          mbar_wait(&e_full[sb % NB], static_cast<uint32_t>(sb / NB) & 1u, &no_abort, p.err, FLN_DEVERR_TIMEOUT_DRAIN);
-        }
-      }
     }
   }
 

@@ -40,8 +40,9 @@ struct GemmParams {
   float eps;
   int norm_kind;            // 0 standard, 1 Gemma (1 + gamma)
   int ld;                   // hidden size H (row stride in elements)
-  float* psum;              // [num_m_tiles, num_n_tiles, 128] row partial sums of squares
-  unsigned int* flags;      // [num_m_tiles, num_n_tiles] publication flags
+  float* psum;              // row partial sums of squares, [num_m_tiles, num_n_tiles, 128]: fp32 with
+                            // separate flags (CTA kernel), or 64-bit {gen, value} words (pair kernel)
+  unsigned int* flags;      // [num_m_tiles, num_n_tiles] publication flags (CTA kernel)
   unsigned int gen;         // value this launch writes into flags (never 0)
   // store-f32 epilogue
   float* yout;              // [M, ld] fp32 slot, local rows

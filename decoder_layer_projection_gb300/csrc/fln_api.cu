@@ -85,7 +85,7 @@ struct Workspace {
   cudaEvent_t ev_join = nullptr;
   unsigned int gen = 0;
   bool prepared[3][5] = {};
-  int pair_max[3] = {0, 0, 0};  // resident CTA pairs of the fused pair kernel, tile 128 / 192 / 256
+  int pair_max[4] = {0, 0, 0, 0};  // resident CTA pairs of the fused pair kernel, tile 128 / 192 / 224 / 256
 };
 
 std::mutex g_mu;
@@ -184,7 +184,7 @@ int prepare_kernel(Workspace* ws, int bn, EpilogueKind epi) {
   return FLN_OK;
 }
 
-int pair_index(int bn) { return bn == 128 ? 0 : bn == 192 ? 1 : bn == 256 ? 2 : -1; }
+int pair_index(int bn) { return bn == 128 ? 0 : bn == 192 ? 1 : bn == 224 ? 2 : bn == 256 ? 3 : -1; }
 
 int prepare_pair(Workspace* ws, int bn, int* max_pairs) {
   const int i = pair_index(bn);
@@ -493,10 +493,10 @@ int check_plan(const fln_plan& p) {
     return fail(FLN_ERR_INVALID_ARG, "plan.path must be FUSED or PIPELINED");
   if (p.microchunk_tokens < 1 || p.microchunk_tokens > kMaxMicrochunk)
     return fail(FLN_ERR_INVALID_ARG, "plan.microchunk_tokens must be in 1..%d", kMaxMicrochunk);
-  if (p.tile_n != 128 && p.tile_n != 192 && p.tile_n != 256)
-    return fail(FLN_ERR_INVALID_ARG, "plan.tile_n must be 128, 192 or 256");
-  if (p.path == FLN_PATH_PIPELINED && p.tile_n == 192)
-    return fail(FLN_ERR_INVALID_ARG, "plan.tile_n 192 is available on the FUSED path only");
+  if (p.tile_n != 128 && p.tile_n != 192 && p.tile_n != 224 && p.tile_n != 256)
+    return fail(FLN_ERR_INVALID_ARG, "plan.tile_n must be 128, 192, 224 or 256");
+  if (p.path == FLN_PATH_PIPELINED && (p.tile_n == 192 || p.tile_n == 224))
+    return fail(FLN_ERR_INVALID_ARG, "plan.tile_n 192 and 224 are available on the FUSED path only");
   if (p.gemm_ctas < 0 || p.norm_ctas < 0) return fail(FLN_ERR_INVALID_ARG, "plan CTA targets must be >= 0");
   if (p.threshold_tokens < 1 || p.threshold_tokens > kDefaultThreshold)
     return fail(FLN_ERR_INVALID_ARG, "plan.threshold_tokens must be in 1..%d", kDefaultThreshold);
@@ -859,7 +859,7 @@ int fln_autotune(int K, int H, int norm_kind, int max_tokens, fln_stream_t strea
   float best_ms = 1e30f;
   bool any = false;
   for (int path : {FLN_PATH_FUSED, FLN_PATH_PIPELINED}) {
-    for (int tile : (path == FLN_PATH_FUSED ? std::vector<int>{256, 192, 128} : std::vector<int>{256, 128})) {
+    for (int tile : (path == FLN_PATH_FUSED ? std::vector<int>{256, 224, 192, 128} : std::vector<int>{256, 128})) {
       for (int cch : chunks) {
         for (int g : ctas) {
           for (int nc : (path == FLN_PATH_PIPELINED ? std::vector<int>{0, ws->sms / 4} : std::vector<int>{0})) {

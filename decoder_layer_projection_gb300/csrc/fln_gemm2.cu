@@ -47,7 +47,7 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;            // 16 KiB
   static constexpr int B_BYTES = (BN / 2) * BK * 2;      // this CTA's half of the W tile
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int GROUPS = BN / 64;                 // 64-column residual boxes per tile
+  static constexpr int GROUPS = (BN + 63) / 64;          // 64-column residual boxes per tile (last may be half used)
   static constexpr int BOX = BM * 64 * 2;                // one 128 x 64 bf16 box (16 KiB)
   static constexpr int NBOX = 3;                         // residual boxes in flight
   static constexpr int OSTAGE = 4 * 32 * 128;            // 32 rows x 64 bf16 output staging per warp
@@ -56,7 +56,7 @@ struct Cfg {
   static constexpr int STAGES = RAW_STAGES > 8 ? 8 : RAW_STAGES;
   static constexpr int SMEM = STAGES * STAGE + E_BYTES + BAR_BYTES + 1024;
   static constexpr int TMEM_COLS = (2 * BN) <= 256 ? 256 : 512;
-  static_assert(BN % 64 == 0 && BN >= 128 && BN <= 256, "tile width");
+  static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile width");
   static_assert(STAGES >= 4, "pipeline depth");
   static_assert(SMEM <= SMEM_LIMIT, "shared memory");
 };
@@ -275,15 +275,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       float ss = 0.f;
 #pragma unroll 1
       for (int g = 0; g < G; ++g, ++s) {
+        const int halves = (BN - g * 64) >= 64 ? 2 : 1;  // 32-column halves of this box inside the tile
         mbar_wait(&e_full[s % NB], static_cast<uint32_t>(s / NB) & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
         const uint8_t* box = sE + (s % NB) * C::BOX;
+#pragma unroll 1
+        for (int c2 = 0; c2 < halves; ++c2) {
+          float v[32];
+          tmem_ld32(tb + static_cast<uint32_t>(g * 64 + c2 * 32), v);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          float v[16];
-          tmem_ld16(tb + static_cast<uint32_t>(g * 64 + c4 * 16), v);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint4 u = *reinterpret_cast<const uint4*>(box + swz(rl, c4 * 2 + h));
+          for (int h = 0; h < 4; ++h) {
+            const uint4 u = *reinterpret_cast<const uint4*>(box + swz(rl, c2 * 4 + h));
             float f[8];
             bf16x8_to_f32(u, f);
 #pragma unroll
@@ -299,24 +300,32 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Row statistics across the row block's N-tiles: each row's partial sum
       // is published as one 64-bit word {generation of this launch, value}, so a
       // reader that sees this launch's generation also sees its value; no fence
-      // or flag is needed.  Partial sums are added in N-tile order.
+      // or flag is needed.  The words are fetched eight at a time and added in
+      // N-tile order.
       unsigned long long* prow = psum + static_cast<size_t>(mtile) * nN * BM + rl;
       st_relaxed_gpu_u64(prow + static_cast<size_t>(nt) * BM, tag | __float_as_uint(ss));
       float tot = 0.f;
       bool ok = true;
-      for (int j = 0; j < nN && ok; ++j) {
-        const unsigned long long* f = prow + static_cast<size_t>(j) * BM;
-        unsigned long long v = ld_relaxed_gpu_u64(f);
-        if ((v >> 32) != p.gen) {
-          const uint64_t t0 = globaltimer_ns();
-          while (((v = ld_relaxed_gpu_u64(f)) >> 32) != p.gen) {
-            if (*abort_flag || globaltimer_ns() - t0 > FLN_WAIT_TIMEOUT_NS) {
-              ok = false;
-              break;
+      for (int j0 = 0; j0 < nN && ok; j0 += 8) {
+        unsigned long long v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          v[i] = (j0 + i < nN) ? ld_relaxed_gpu_u64(prow + static_cast<size_t>(j0 + i) * BM) : tag;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (j0 + i >= nN || !ok) continue;
+          if ((v[i] >> 32) != p.gen) {
+            const unsigned long long* f = prow + static_cast<size_t>(j0 + i) * BM;
+            const uint64_t t0 = globaltimer_ns();
+            while (((v[i] = ld_relaxed_gpu_u64(f)) >> 32) != p.gen) {
+              if (*abort_flag || globaltimer_ns() - t0 > FLN_WAIT_TIMEOUT_NS) {
+                ok = false;
+                break;
+              }
             }
           }
+          tot += __uint_as_float(static_cast<uint32_t>(v[i]));
         }
-        tot += __uint_as_float(static_cast<uint32_t>(v));
       }
       if (!ok) {
         if (!*abort_flag) atomicOr(p.err, FLN_DEVERR_TIMEOUT_ROWSTAT);
@@ -329,18 +338,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       // phase 2: normalise.  r goes back into the residual box in place and
       // the output into this warp's staging rows; then each warp reads its 32
       // rows back row-major so that one 16-byte store per lane covers 4 rows x
-      // 128 contiguous bytes (rows past the chunk and columns past H masked).
+      // 128 contiguous bytes (rows past the chunk, columns past H and columns of
+      // the next tile in a half-used last box are masked).
+      const int col_end = min(p.N, n0 + BN);
 #pragma unroll 1
       for (int g = 0; g < G; ++g, ++s) {
+        const int halves = (BN - g * 64) >= 64 ? 2 : 1;
         mbar_wait(&e_full[s % NB], static_cast<uint32_t>(s / NB) & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
         uint8_t* box = sE + (s % NB) * C::BOX;
+#pragma unroll 1
+        for (int c2 = 0; c2 < halves; ++c2) {
+          float v[32];
+          tmem_ld32(tb + static_cast<uint32_t>(g * 64 + c2 * 32), v);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          float v[16];
-          tmem_ld16(tb + static_cast<uint32_t>(g * 64 + c4 * 16), v);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int chunk = c4 * 2 + h;
+          for (int h = 0; h < 4; ++h) {
+            const int chunk = c2 * 4 + h;
             const int cc = n0 + g * 64 + chunk * 8;
             uint4* rp = reinterpret_cast<uint4*>(box + swz(rl, chunk));
             float f[8];
@@ -374,9 +386,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int ch = lane & 7;
             const int lrow = mtile * BM + q * 32 + rr;
             const int col = n0 + g * 64 + ch * 8;
-            const uint4 rv = *reinterpret_cast<const uint4*>(box + swz(q * 32 + rr, ch));
-            const uint4 ov = *reinterpret_cast<const uint4*>(ostage + swz(rr, ch));
-            if (lrow < p.M && col < p.N) {
+            if (lrow < p.M && col < col_end) {
+              const uint4 rv = *reinterpret_cast<const uint4*>(box + swz(q * 32 + rr, ch));
+              const uint4 ov = *reinterpret_cast<const uint4*>(ostage + swz(rr, ch));
               const size_t off = (static_cast<size_t>(p.a_row0) + lrow) * static_cast<size_t>(p.ld) + col;
               *reinterpret_cast<uint4*>(p.residual + off) = rv;
               __stcs(reinterpret_cast<uint4*>(p.out + off), ov);
@@ -443,6 +455,7 @@ cudaError_t pair_gemm_prepare(int bn, int* max_pairs) {
   switch (bn) {
     case 128: return pair::prepare_pair_bn<128>(max_pairs);
     case 192: return pair::prepare_pair_bn<192>(max_pairs);
+    case 224: return pair::prepare_pair_bn<224>(max_pairs);
     case 256: return pair::prepare_pair_bn<256>(max_pairs);
   }
   return cudaErrorInvalidValue;
@@ -453,6 +466,7 @@ cudaError_t launch_gemm_pair_fused(int bn, const CUtensorMap& tmA, const CUtenso
   switch (bn) {
     case 128: return pair::launch_pair_bn<128>(tmA, tmB, tmR, p, pairs, stream);
     case 192: return pair::launch_pair_bn<192>(tmA, tmB, tmR, p, pairs, stream);
+    case 224: return pair::launch_pair_bn<224>(tmA, tmB, tmR, p, pairs, stream);
     case 256: return pair::launch_pair_bn<256>(tmA, tmB, tmR, p, pairs, stream);
   }
   return cudaErrorInvalidValue;

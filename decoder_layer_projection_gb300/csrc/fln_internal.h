@@ -79,7 +79,7 @@ int gemm_stages(int bn);
 cudaError_t gemm_prepare(int bn, EpilogueKind epi);  // sets max dynamic smem attributes
 
 // CTA-pair (cta_group::2) fused GEMM + add + RMSNorm for tile widths 128,
-// 192, 256.  prepare sets the shared-memory limit and reports how many pairs
+// 192, 224, 256.  prepare sets the shared-memory limit and reports how many pairs
 // can be resident at once (the grid must not exceed it: the pairs exchange
 // row statistics).  tmR maps the chunk's residual rows (read in 128 x 64 boxes).
 cudaError_t pair_gemm_prepare(int bn, int* max_pairs);

@@ -49,13 +49,14 @@ def test_tiny_config_all_paths():
     d = make_inputs(wl)
     run = Run(d, wl.eps, wl.norm_kind)
     for p in (plan(fln.PATH_FUSED, chunk=16), plan(fln.PATH_PIPELINED, chunk=16),
-              plan(fln.PATH_FUSED, chunk=16, tile_n=128), plan(fln.PATH_FUSED, chunk=16, tile_n=192), UNFUSED):
+              plan(fln.PATH_FUSED, chunk=16, tile_n=128), plan(fln.PATH_FUSED, chunk=16, tile_n=192),
+              plan(fln.PATH_FUSED, chunk=16, tile_n=224), UNFUSED):
         rb, ob = run(p)
         check_rows(rb, ob, d, wl, name=f"tiny {p}")
 
 
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
-@pytest.mark.parametrize("path,tile", [(1, 256), (1, 192), (1, 128), (2, 256), (2, 128)])
+@pytest.mark.parametrize("path,tile", [(1, 256), (1, 224), (1, 192), (1, 128), (2, 256), (2, 128)])
 def test_small_prefill_paths_full_parity(wl, path, tile):
     d = make_inputs(wl)
     run = Run(d, wl.eps, wl.norm_kind)

@@ -285,6 +285,8 @@ int run_unfused(Workspace* ws, const Call& c) {
   p.num_k_blocks = (c.K + 63) / 64;
   p.units_total = static_cast<long long>(p.num_m_tiles) * p.num_k_blocks;
   const int G = static_cast<int>(std::min<long long>(ws->sms, p.units_total));
+  if ((p.units_total + 1) * G + p.units_total >= (1ll << 32))
+    return fail(FLN_ERR_UNSUPPORTED, "split-K path: K=%d, H=%d give too many work units", c.K, c.H);
   int max_split = 1;
   for (int m = 0; m < p.num_m_tiles; ++m) {
     const long long KB = p.num_k_blocks;
@@ -315,6 +317,7 @@ int run_unfused(Workspace* ws, const Call& c) {
   np.T = c.T;
   np.row0 = 0;
   np.H = c.H;
+  np.pdl = g_prof ? 0 : 1;  // timing events between the two launches would break the overlap
   return launch_counted(FLN_KERNEL_NORM_SPLITK, c.stream,
                         [&] { return launch_add_rmsnorm(NORM_SRC_SPLITK, np, 0, c.stream); },
                         "split-K add+norm launch");

@@ -35,10 +35,12 @@ constexpr int BK = 64;
 constexpr int NUM_THREADS = 192;
 constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KiB
 
-__host__ __device__ constexpr int stages_for(int bn) {
-  return bn >= 256 ? 4 : (bn >= 128 ? 6 : 8);
-}
 __host__ __device__ constexpr int stage_bytes(int bn) { return A_TILE_BYTES + bn * BK * 2; }
+// As many ring stages as fit in the 227 KiB a CTA may use (at most 16): the
+// decode shapes stream W from HBM and need many bytes in flight per SM.
+__host__ __device__ constexpr int stages_for(int bn) {
+  return (232448 - 256 - 1024) / stage_bytes(bn) > 16 ? 16 : (232448 - 256 - 1024) / stage_bytes(bn);
+}
 __host__ __device__ constexpr int tmem_cols_for(int bn) {
   return (2 * bn) <= 32 ? 32 : (2 * bn) <= 64 ? 64 : (2 * bn) <= 128 ? 128 : (2 * bn) <= 256 ? 256 : 512;
 }
@@ -121,6 +123,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // the split-K reducer may be scheduled right away: it waits for this grid to
+  // finish before it reads anything
+  if (EPI == EPI_SPLITK_SWAP) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {

@@ -69,6 +69,7 @@ struct NormParams {
   int T;                        // rows in this launch
   int row0;                     // global row of local row 0 (residual/out/y_bf16)
   int H;
+  int pdl;                      // launched as a programmatic dependent of the preceding kernel
 };
 
 // launchers (return cudaError_t of the launch)
@@ -90,9 +91,11 @@ enum NormSource : int { NORM_SRC_BF16 = 0, NORM_SRC_F32 = 1, NORM_SRC_SPLITK = 2
 cudaError_t launch_add_rmsnorm(NormSource src, const NormParams& p, int grid_cap, cudaStream_t stream);
 
 // split-K bookkeeping shared by the GEMM and the reducer: the CTA whose
-// unit range [c*U/G, (c+1)*U/G) contains unit u.
+// unit range [c*U/G, (c+1)*U/G) contains unit u.  32-bit arithmetic: the host
+// only launches the split-K path when (U + 1) * G + U < 2^32.
 __host__ __device__ inline int splitk_cta_of_unit(long long u, long long U, int G) {
-  return static_cast<int>(((u + 1) * G + U - 1) / U - 1);
+  const uint32_t uu = static_cast<uint32_t>(u), UU = static_cast<uint32_t>(U), GG = static_cast<uint32_t>(G);
+  return static_cast<int>(((uu + 1u) * GG + UU - 1u) / UU - 1u);
 }
 
 }  // namespace fln

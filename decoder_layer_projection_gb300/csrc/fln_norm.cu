@@ -16,7 +16,10 @@
 //   SPLITK  the fp32 stream-K partials of the decode GEMM, summed here in a
 //           fixed order (deterministic).
 // Each thread keeps its VPT 8-element vectors of r in registers between the
-// statistics pass and the normalisation pass, so every byte is read once.
+// statistics pass and the normalisation pass, so every byte is read once.  All
+// loads of a thread are independent and issued before their first use (the
+// split-K sum is unrolled to a compile-time bound of splits), so a row costs
+// about one memory latency, not one per split.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -26,9 +29,39 @@
 
 namespace fln {
 
-constexpr int NORM_THREADS = 256;
+// split-K: the hidden index h lives in m-tile h / 128, lane h % 128; the
+// CTAs that touched m-tile m wrote partial slots 0 .. n-1 in unit order; the
+// slots are summed in that order (at most MAXS of them).
+template <int MAXS>
+__device__ __forceinline__ void load_splitk8(const NormParams& p, int t, int h, float (&y)[8]) {
+  const int m = h >> 7;
+  const int hl = h & 127;
+  const long long KB = p.num_k_blocks;
+  const int c_first = splitk_cta_of_unit(static_cast<long long>(m) * KB, p.units_total, p.gemm_grid);
+  const int c_last = splitk_cta_of_unit(static_cast<long long>(m + 1) * KB - 1, p.units_total, p.gemm_grid);
+  const int n = c_last - c_first + 1;
+  float4 a[MAXS], b[MAXS];
+#pragma unroll
+  for (int s = 0; s < MAXS; ++s) {
+    if (s < n) {
+      const float4* src = reinterpret_cast<const float4*>(
+          p.partial + (static_cast<size_t>(m * p.max_split + s) * p.T + t) * 128 + hl);
+      a[s] = __ldcs(src);
+      b[s] = __ldcs(src + 1);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) y[j] = 0.f;
+#pragma unroll
+  for (int s = 0; s < MAXS; ++s) {
+    if (s < n) {
+      y[0] += a[s].x; y[1] += a[s].y; y[2] += a[s].z; y[3] += a[s].w;
+      y[4] += b[s].x; y[5] += b[s].y; y[6] += b[s].z; y[7] += b[s].w;
+    }
+  }
+}
 
-template <int SRC>
+template <int SRC, int MAXS>
 __device__ __forceinline__ void load_y8(const NormParams& p, int t, int h, float (&y)[8]) {
   if (SRC == NORM_SRC_BF16) {
     const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p.y_bf16 + (static_cast<size_t>(p.row0) + t) * p.H + h));
@@ -40,49 +73,43 @@ __device__ __forceinline__ void load_y8(const NormParams& p, int t, int h, float
     y[0] = a.x; y[1] = a.y; y[2] = a.z; y[3] = a.w;
     y[4] = b.x; y[5] = b.y; y[6] = b.z; y[7] = b.w;
   } else {
-    // split-K: the hidden index h lives in m-tile h / 128, lane h % 128; the
-    // CTAs that touched m-tile m wrote partial slots 0 .. n-1 in unit order.
-    const int m = h >> 7;
-    const int hl = h & 127;
-    const long long KB = p.num_k_blocks;
-    const int c_first = splitk_cta_of_unit(static_cast<long long>(m) * KB, p.units_total, p.gemm_grid);
-    const int c_last = splitk_cta_of_unit(static_cast<long long>(m + 1) * KB - 1, p.units_total, p.gemm_grid);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) y[j] = 0.f;
-    for (int s = 0; s <= c_last - c_first; ++s) {
-      const float4* src = reinterpret_cast<const float4*>(
-          p.partial + (static_cast<size_t>(m * p.max_split + s) * p.T + t) * 128 + hl);
-      const float4 a = __ldcs(src);
-      const float4 b = __ldcs(src + 1);
-      y[0] += a.x; y[1] += a.y; y[2] += a.z; y[3] += a.w;
-      y[4] += b.x; y[5] += b.y; y[6] += b.z; y[7] += b.w;
-    }
+    load_splitk8<MAXS>(p, t, h, y);
   }
 }
 
-template <int SRC, int VPT>
-__global__ void __launch_bounds__(NORM_THREADS) fln_add_rmsnorm_kernel(const NormParams p) {
-  __shared__ float warp_sums[NORM_THREADS / 32];
+template <int SRC, int VPT, int NT, int MAXS>
+__global__ void __launch_bounds__(NT) fln_add_rmsnorm_kernel(const NormParams p) {
+  __shared__ float warp_sums[NT / 32];
   __shared__ float row_total;
   const int tid = threadIdx.x;
   const int nvec = p.H >> 3;
+  // When launched as a programmatic dependent, wait until the producing
+  // kernel has finished and its writes are visible (a no-op otherwise).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
     const size_t grow = static_cast<size_t>(p.row0) + static_cast<size_t>(t);
     const __nv_bfloat16* r0 = p.residual + grow * p.H;
     float r[VPT][8];
     float ss = 0.f;
+    // all loads first
+    uint4 u[VPT];
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
-      const int vi = v * NORM_THREADS + tid;
+      const int vi = v * NT + tid;
       if (vi < nvec) {
-        const int h = vi << 3;
-        float y[8], f[8];
-        load_y8<SRC>(p, t, h, y);
-        const uint4 u = *reinterpret_cast<const uint4*>(r0 + h);
-        bf16x8_to_f32(u, f);
+        load_y8<SRC, MAXS>(p, t, vi << 3, r[v]);
+        u[v] = *reinterpret_cast<const uint4*>(r0 + (vi << 3));
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int vi = v * NT + tid;
+      if (vi < nvec) {
+        float f[8];
+        bf16x8_to_f32(u[v], f);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          r[v][j] = f[j] + y[j];
+          r[v][j] += f[j];
           ss = fmaf(r[v][j], r[v][j], ss);
         }
       }
@@ -94,7 +121,7 @@ __global__ void __launch_bounds__(NORM_THREADS) fln_add_rmsnorm_kernel(const Nor
     if (tid == 0) {
       float tot = 0.f;
 #pragma unroll
-      for (int w = 0; w < NORM_THREADS / 32; ++w) tot += warp_sums[w];
+      for (int w = 0; w < NT / 32; ++w) tot += warp_sums[w];
       row_total = tot;
     }
     __syncthreads();
@@ -103,7 +130,7 @@ __global__ void __launch_bounds__(NORM_THREADS) fln_add_rmsnorm_kernel(const Nor
     __nv_bfloat16* ow = p.out + grow * p.H;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
-      const int vi = v * NORM_THREADS + tid;
+      const int vi = v * NT + tid;
       if (vi < nvec) {
         const int h = vi << 3;
         const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + h));
@@ -123,17 +150,39 @@ __global__ void __launch_bounds__(NORM_THREADS) fln_add_rmsnorm_kernel(const Nor
   }
 }
 
-template <int SRC>
-static cudaError_t launch_src(const NormParams& p, int grid, cudaStream_t s) {
+template <int SRC, int VPT, int NT, int MAXS>
+static cudaError_t launch_k(const NormParams& p, int grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fln_add_rmsnorm_kernel<SRC, VPT, NT, MAXS>, p);
+}
+
+template <int SRC, int NT, int MAXS>
+static cudaError_t launch_nt(const NormParams& p, int grid, cudaStream_t s) {
   const int nvec = p.H / 8;
-  const int vpt = (nvec + NORM_THREADS - 1) / NORM_THREADS;
-  if (vpt <= 1) fln_add_rmsnorm_kernel<SRC, 1><<<grid, NORM_THREADS, 0, s>>>(p);
-  else if (vpt <= 2) fln_add_rmsnorm_kernel<SRC, 2><<<grid, NORM_THREADS, 0, s>>>(p);
-  else if (vpt <= 4) fln_add_rmsnorm_kernel<SRC, 4><<<grid, NORM_THREADS, 0, s>>>(p);
-  else if (vpt <= 8) fln_add_rmsnorm_kernel<SRC, 8><<<grid, NORM_THREADS, 0, s>>>(p);
-  else if (vpt <= 16) fln_add_rmsnorm_kernel<SRC, 16><<<grid, NORM_THREADS, 0, s>>>(p);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  const int vpt = (nvec + NT - 1) / NT;
+  if (vpt <= 1) return launch_k<SRC, 1, NT, MAXS>(p, grid, s);
+  if (vpt <= 2) return launch_k<SRC, 2, NT, MAXS>(p, grid, s);
+  if (vpt <= 4) return launch_k<SRC, 4, NT, MAXS>(p, grid, s);
+  if (vpt <= 8) return launch_k<SRC, 8, NT, MAXS>(p, grid, s);
+  if (vpt <= 16) return launch_k<SRC, 16, NT, MAXS>(p, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+// Block size: 512 threads when there are few rows (a row's loads spread over
+// more threads, so more of them are in flight), 256 otherwise.
+template <int SRC, int MAXS>
+static cudaError_t launch_src(const NormParams& p, int grid, cudaStream_t s) {
+  const bool wide = p.T <= 64 && p.H >= 8192;
+  return wide ? launch_nt<SRC, 512, MAXS>(p, grid, s) : launch_nt<SRC, 256, MAXS>(p, grid, s);
 }
 
 cudaError_t launch_add_rmsnorm(NormSource src, const NormParams& p, int grid_cap, cudaStream_t stream) {
@@ -141,9 +190,13 @@ cudaError_t launch_add_rmsnorm(NormSource src, const NormParams& p, int grid_cap
   int grid = p.T;
   if (grid_cap > 0 && grid > grid_cap) grid = grid_cap;
   switch (src) {
-    case NORM_SRC_BF16: return launch_src<NORM_SRC_BF16>(p, grid, stream);
-    case NORM_SRC_F32: return launch_src<NORM_SRC_F32>(p, grid, stream);
-    case NORM_SRC_SPLITK: return launch_src<NORM_SRC_SPLITK>(p, grid, stream);
+    case NORM_SRC_BF16: return launch_src<NORM_SRC_BF16, 1>(p, grid, stream);
+    case NORM_SRC_F32: return launch_src<NORM_SRC_F32, 1>(p, grid, stream);
+    case NORM_SRC_SPLITK:
+      if (p.max_split <= 4) return launch_src<NORM_SRC_SPLITK, 4>(p, grid, stream);
+      if (p.max_split <= 8) return launch_src<NORM_SRC_SPLITK, 8>(p, grid, stream);
+      if (p.max_split <= 16) return launch_src<NORM_SRC_SPLITK, 16>(p, grid, stream);
+      return cudaErrorInvalidValue;
   }
   return cudaErrorInvalidValue;
 }

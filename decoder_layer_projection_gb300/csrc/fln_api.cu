@@ -347,9 +347,12 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     return rc;
   for (int c0 = 0; c0 < c.T; c0 += chunk) {
     const int n = std::min(chunk, c.T - c0);
-    // the chunk's residual rows: rows past the chunk read as zeros
-    CUtensorMap tmR;
+    // the chunk's residual and output rows: rows past the chunk read as zeros
+    // and are never written (TMA clips every store at row n and column H)
+    CUtensorMap tmR, tmRs, tmOs;
     if ((rc = make_map(&tmR, c.residual + static_cast<size_t>(c0) * c.H, c.H, n, 128))) return rc;
+    if ((rc = make_map(&tmRs, c.residual + static_cast<size_t>(c0) * c.H, c.H, n, 32))) return rc;
+    if ((rc = make_map(&tmOs, c.out + static_cast<size_t>(c0) * c.H, c.H, n, 32))) return rc;
     GemmParams p{};
     p.M = n;
     p.N = c.H;
@@ -375,7 +378,7 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     if (pl.gemm_ctas > 0) pairs = std::min(pairs, std::max(1, pl.gemm_ctas / 2));
     pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(pairs, tiles)));
     rc = launch_counted(FLN_KERNEL_GEMM_FUSED, c.stream,
-                        [&] { return launch_gemm_pair_fused(bn, tmA, tmB, tmR, p, pairs, c.stream); },
+                        [&] { return launch_gemm_pair_fused(bn, tmA, tmB, tmR, tmRs, tmOs, p, pairs, c.stream); },
                         "fused pair GEMM launch");
     if (rc) return rc;
   }

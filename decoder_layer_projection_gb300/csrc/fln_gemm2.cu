@@ -38,7 +38,7 @@ namespace pair {
 
 constexpr int BM = 128;  // rows per CTA (256 per pair)
 constexpr int BK = 64;
-constexpr int THREADS = 192;
+constexpr int THREADS = 224;  // warps: 0 producer, 1 MMA / TMEM, 2-5 epilogue, 6 residual loader
 constexpr int SMEM_LIMIT = 232448;  // 227 KiB opt-in per block
 constexpr int BAR_BYTES = 512;
 
@@ -69,7 +69,8 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     fln_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const __grid_constant__ CUtensorMap tmR, const GemmParams p) {
+                         const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmRs,
+                         const __grid_constant__ CUtensorMap tmOs, const GemmParams p) {
   using C = Cfg<BN>;
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN);
@@ -120,6 +121,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmR);
+    tma_prefetch_desc(&tmRs);
+    tma_prefetch_desc(&tmOs);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
@@ -169,12 +172,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-  } else if (warp == 0 && lane == 1) {
+  } else if (warp == 6 && lane == 0) {
     // ------------------------------------------------------------ residual loader (both CTAs)
-    // Box s of this CTA's sequence: local tile s / BOXES, group (s % BOXES) % G
-    // (each phase of a tile reads the G boxes once), buffer s % NBOX.
+    // (a warp of its own: a lane spinning on a barrier would steal issue
+    // slots from a producer or MMA lane of the same warp)
+    // Box s of this CTA's sequence: local tile s / G, group s % G, buffer s % NBOX.
     constexpr int G = C::GROUPS;
-    constexpr int BOXES = 2 * G;
+    constexpr int BOXES = G;
     constexpr int NB = C::NBOX;
     const uint64_t pol_r = l2_policy_evict_normal();
     int s = 0;
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         ok = false;
         break;
       }
-      const int g = (s % BOXES) % G;
+      const int g = s % BOXES;
       const int m0 = ((t / nN) * 2 + static_cast<int>(rank)) * BM;
       const int n0 = (t % nN) * BN + g * 64;
       mbar_arrive_expect_tx(&e_full[s % NB], C::BOX);
@@ -244,7 +248,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       volatile int no_abort = 0;
       mbar_wait(drain_bar, 0, &no_abort, p.err, FLN_DEVERR_TIMEOUT_DRAIN);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;        // TMEM lane quarter of this warp
     const int rl = q * 32 + lane;  // row within this CTA's 128 rows
@@ -262,6 +266,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int mtile = (t / nN) * 2 + static_cast<int>(rank);  // 128-row block index in the launch
       const int nt = t % nN;
       const int n0 = nt * BN;
+      const int col_end = min(p.N, n0 + BN);
+      const int wrow0 = mtile * BM + q * 32;  // this warp's first row in the chunk
       // All 128 epilogue threads decide together whether to continue: a thread
       // that leaves alone would strand the others at the named barrier.
       if (!mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) *epi_abort = 1;
@@ -270,31 +276,64 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
 
-      // phase 1: r = r0 + acc in fp32, this tile's partial sum of squares
-      // (rows past the chunk and columns past H read zeros: acc and r0 are 0 there)
+      // phase 1: r = r0 + acc in fp32 and this tile's partial sum of squares.
+      // The fp32 r replaces the accumulator in TMEM (phase 2 reads it back) and
+      // bf16(r) replaces r0 in the residual box, from where each warp stores
+      // its 32 rows with one TMA store (rows past the chunk and columns past H
+      // are clipped by the tensor map).  A half-used last box (tile 224) is
+      // stored by the threads instead, so the next tile's columns stay intact.
+      // Rows past the chunk and columns past H read zeros: acc and r0 are 0.
       float ss = 0.f;
 #pragma unroll 1
       for (int g = 0; g < G; ++g, ++s) {
         const int halves = (BN - g * 64) >= 64 ? 2 : 1;  // 32-column halves of this box inside the tile
         mbar_wait(&e_full[s % NB], static_cast<uint32_t>(s / NB) & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
-        const uint8_t* box = sE + (s % NB) * C::BOX;
+        uint8_t* box = sE + (s % NB) * C::BOX;
 #pragma unroll 1
         for (int c2 = 0; c2 < halves; ++c2) {
           float v[32];
-          tmem_ld32(tb + static_cast<uint32_t>(g * 64 + c2 * 32), v);
+          const uint32_t ta = tb + static_cast<uint32_t>(g * 64 + c2 * 32);
+          tmem_ld32(ta, v);
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            const uint4 u = *reinterpret_cast<const uint4*>(box + swz(rl, c2 * 4 + h));
+            uint4* rp = reinterpret_cast<uint4*>(box + swz(rl, c2 * 4 + h));
             float f[8];
-            bf16x8_to_f32(u, f);
+            bf16x8_to_f32(*rp, f);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float r = f[j] + v[8 * h + j];
               ss = fmaf(r, r, ss);
+              v[8 * h + j] = r;
+            }
+            *rp = f32x8_to_bf16(&v[8 * h]);
+          }
+          tmem_st32(ta, v);
+        }
+        if (halves == 2) {
+          fence_proxy_async_smem();  // the box rows are visible to the TMA store
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmRs, box + q * (32 * 128), n0 + g * 64, wrow0);
+            bulk_commit_group();
+            bulk_wait_group_read<0>();  // the store has read the rows: the box may be refilled
+          }
+          __syncwarp();
+        } else {
+          __syncwarp();
+#pragma unroll 2
+          for (int it = 0; it < 8; ++it) {
+            const int rr = it * 4 + (lane >> 3);  // row within this warp's 32
+            const int ch = lane & 7;
+            const int lrow = wrow0 + rr;
+            const int col = n0 + g * 64 + ch * 8;
+            if (lrow < p.M && col < col_end) {
+              const size_t off = (static_cast<size_t>(p.a_row0) + lrow) * static_cast<size_t>(p.ld) + col;
+              *reinterpret_cast<uint4*>(p.residual + off) =
+                  *reinterpret_cast<const uint4*>(box + swz(q * 32 + rr, ch));
             }
           }
+          __syncwarp();
         }
-        __syncwarp();
         if (lane == 0) mbar_arrive(&e_free[s % NB]);  // this warp is done with box s
       }
       // Row statistics across the row block's N-tiles: each row's partial sum
@@ -335,17 +374,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool go = __all_sync(0xffffffffu, ok);
       const float rstd = rsqrtf(tot / static_cast<float>(p.ld) + p.eps);
 
-      // phase 2: normalise.  r goes back into the residual box in place and
-      // the output into this warp's staging rows; then each warp reads its 32
-      // rows back row-major so that one 16-byte store per lane covers 4 rows x
-      // 128 contiguous bytes (rows past the chunk, columns past H and columns of
-      // the next tile in a half-used last box are masked).
-      const int col_end = min(p.N, n0 + BN);
+      // phase 2: out = r * rstd * g from the fp32 r in TMEM, staged in this
+      // warp's 32 output rows and written by one TMA store per warp and box
+      // (threads store a half-used last box themselves).
+      tmem_wait_st();
 #pragma unroll 1
-      for (int g = 0; g < G; ++g, ++s) {
+      for (int g = 0; g < G; ++g) {
         const int halves = (BN - g * 64) >= 64 ? 2 : 1;
-        mbar_wait(&e_full[s % NB], static_cast<uint32_t>(s / NB) & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
-        uint8_t* box = sE + (s % NB) * C::BOX;
 #pragma unroll 1
         for (int c2 = 0; c2 < halves; ++c2) {
           float v[32];
@@ -354,9 +389,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int h = 0; h < 4; ++h) {
             const int chunk = c2 * 4 + h;
             const int cc = n0 + g * 64 + chunk * 8;
-            uint4* rp = reinterpret_cast<uint4*>(box + swz(rl, chunk));
-            float f[8];
-            bf16x8_to_f32(*rp, f);
             float gw[8];
             if (cc < p.N) {
               const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc));
@@ -367,42 +399,50 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 8; ++j) gw[j] = 0.f;
             }
-            float r[8], o[8];
+            float o[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              r[j] = f[j] + v[8 * h + j];
               const float gj = p.norm_kind ? 1.0f + gw[j] : gw[j];
-              o[j] = r[j] * rstd * gj;
+              o[j] = v[8 * h + j] * rstd * gj;
             }
-            *rp = f32x8_to_bf16(r);
             *reinterpret_cast<uint4*>(ostage + swz(lane, chunk)) = f32x8_to_bf16(o);
           }
         }
-        __syncwarp();
-        if (go) {
+        if (halves == 2) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (go) {
+              tma_store_2d(&tmOs, ostage, n0 + g * 64, wrow0);
+              bulk_commit_group();
+            }
+            bulk_wait_group_read<0>();  // staging rows read: the next box may overwrite them
+          }
+          __syncwarp();
+        } else {
+          __syncwarp();
+          if (go) {
 #pragma unroll 2
-          for (int it = 0; it < 8; ++it) {
-            const int rr = it * 4 + (lane >> 3);  // row within this warp's 32
-            const int ch = lane & 7;
-            const int lrow = mtile * BM + q * 32 + rr;
-            const int col = n0 + g * 64 + ch * 8;
-            if (lrow < p.M && col < col_end) {
-              const uint4 rv = *reinterpret_cast<const uint4*>(box + swz(q * 32 + rr, ch));
-              const uint4 ov = *reinterpret_cast<const uint4*>(ostage + swz(rr, ch));
-              const size_t off = (static_cast<size_t>(p.a_row0) + lrow) * static_cast<size_t>(p.ld) + col;
-              *reinterpret_cast<uint4*>(p.residual + off) = rv;
-              __stcs(reinterpret_cast<uint4*>(p.out + off), ov);
+            for (int it = 0; it < 8; ++it) {
+              const int rr = it * 4 + (lane >> 3);
+              const int ch = lane & 7;
+              const int lrow = wrow0 + rr;
+              const int col = n0 + g * 64 + ch * 8;
+              if (lrow < p.M && col < col_end) {
+                const size_t off = (static_cast<size_t>(p.a_row0) + lrow) * static_cast<size_t>(p.ld) + col;
+                __stcs(reinterpret_cast<uint4*>(p.out + off), *reinterpret_cast<const uint4*>(ostage + swz(rr, ch)));
+              }
             }
           }
+          __syncwarp();
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&e_free[s % NB]);  // box s and the staging rows are free
       }
       // TMEM reads of this tile are done: hand the accumulator back to the MMA issuer
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty_leader + static_cast<uint32_t>(b * 8));
     }
+    if (lane == 0) bulk_wait_group<0>();  // this warp's stores have completed before the CTA exits
   }
 
   tc_fence_before();
@@ -414,7 +454,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 template <int BN>
 static cudaError_t launch_pair_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmR,
-                                  const GemmParams& p, int pairs, cudaStream_t stream) {
+                                  const CUtensorMap& tmRs, const CUtensorMap& tmOs, const GemmParams& p, int pairs,
+                                  cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
@@ -427,7 +468,7 @@ static cudaError_t launch_pair_bn(const CUtensorMap& tmA, const CUtensorMap& tmB
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fln_gemm_pair_kernel<BN>, tmA, tmB, tmR, p);
+  return cudaLaunchKernelEx(&cfg, fln_gemm_pair_kernel<BN>, tmA, tmB, tmR, tmRs, tmOs, p);
 }
 
 template <int BN>
@@ -462,12 +503,13 @@ cudaError_t pair_gemm_prepare(int bn, int* max_pairs) {
 }
 
 cudaError_t launch_gemm_pair_fused(int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmR,
-                                   const GemmParams& p, int pairs, cudaStream_t stream) {
+                                   const CUtensorMap& tmRs, const CUtensorMap& tmOs, const GemmParams& p, int pairs,
+                                   cudaStream_t stream) {
   switch (bn) {
-    case 128: return pair::launch_pair_bn<128>(tmA, tmB, tmR, p, pairs, stream);
-    case 192: return pair::launch_pair_bn<192>(tmA, tmB, tmR, p, pairs, stream);
-    case 224: return pair::launch_pair_bn<224>(tmA, tmB, tmR, p, pairs, stream);
-    case 256: return pair::launch_pair_bn<256>(tmA, tmB, tmR, p, pairs, stream);
+    case 128: return pair::launch_pair_bn<128>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
+    case 192: return pair::launch_pair_bn<192>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
+    case 224: return pair::launch_pair_bn<224>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
+    case 256: return pair::launch_pair_bn<256>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -82,10 +82,13 @@ cudaError_t gemm_prepare(int bn, EpilogueKind epi);  // sets max dynamic smem at
 // CTA-pair (cta_group::2) fused GEMM + add + RMSNorm for tile widths 128,
 // 192, 224, 256.  prepare sets the shared-memory limit and reports how many pairs
 // can be resident at once (the grid must not exceed it: the pairs exchange
-// row statistics).  tmR maps the chunk's residual rows (read in 128 x 64 boxes).
+// row statistics).  tmR maps the chunk's residual rows (read in 128 x 64
+// boxes), tmRs / tmOs the chunk's residual and output rows in 32 x 64 boxes
+// (stores).
 cudaError_t pair_gemm_prepare(int bn, int* max_pairs);
 cudaError_t launch_gemm_pair_fused(int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmR,
-                                   const GemmParams& p, int pairs, cudaStream_t stream);
+                                   const CUtensorMap& tmRs, const CUtensorMap& tmOs, const GemmParams& p, int pairs,
+                                   cudaStream_t stream);
 
 enum NormSource : int { NORM_SRC_BF16 = 0, NORM_SRC_F32 = 1, NORM_SRC_SPLITK = 2 };
 cudaError_t launch_add_rmsnorm(NormSource src, const NormParams& p, int grid_cap, cudaStream_t stream);

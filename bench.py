@@ -41,9 +41,9 @@ FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes per launch of the dominant kernel, from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and by the
-# sha1 of the kernel source the capture was taken on; reported as null when
-# the source has changed since.
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, kernel,
+# tile width and the sha1 of the kernel sources the capture was taken on;
+# reported as null when the sources have changed since.
 NCU_TRAFFIC = {}
 
 
@@ -270,9 +270,11 @@ def run_gpu(args):
         # add + norm: residual read and written, output written, gamma
         achieved = (tokens_per_launch * H * 6.0 + 4.0 * H) / (avg_launch_ms * 1e-3) / 1e9
         bound, unit, peak = "hbm", "GB/s", peaks["hbm_gbs"]
-    src_hash = hashlib.sha1(open(os.path.join(ROOT, "decoder_layer_projection_gb300", "csrc",
-                                              "fln_gemm.cu"), "rb").read()).hexdigest()[:12]
-    traffic = NCU_TRAFFIC.get((args.config, kname, src_hash))
+    h = hashlib.sha1()
+    for f in ("fln_gemm.cu", "fln_gemm2.cu", "fln_norm.cu", "fln_ptx.cuh"):
+        h.update(open(os.path.join(ROOT, "decoder_layer_projection_gb300", "csrc", f), "rb").read())
+    src_hash = h.hexdigest()[:12]
+    traffic = NCU_TRAFFIC.get((args.config, kname, plan["tile_n"], src_hash))
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kname,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback",

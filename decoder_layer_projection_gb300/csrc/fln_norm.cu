@@ -177,6 +177,92 @@ static cudaError_t launch_nt(const NormParams& p, int grid, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
+// Few rows: each row is split over a cluster of CL CTAs (one slice of H/CL
+// columns each, one 8-column vector per thread), so a row's loads come from
+// CL SMs at once; the slices' sums of squares are combined through
+// distributed shared memory in rank order.
+template <int SRC, int CL, int MAXS>
+__global__ void __launch_bounds__(256) fln_add_rmsnorm_cluster_kernel(const NormParams p) {
+  __shared__ float warp_sums[8];
+  __shared__ float slice_ss;
+  __shared__ float row_total;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int tid = threadIdx.x;
+  const uint32_t rank = cluster_ctarank();
+  const int t = static_cast<int>(cluster_id_x());
+  const int slice = p.H / CL;             // columns of this CTA
+  const int nvec = slice >> 3;
+  const int vi = tid;
+  const bool active = vi < nvec;
+  const int h = static_cast<int>(rank) * slice + (vi << 3);
+  const size_t grow = static_cast<size_t>(p.row0) + static_cast<size_t>(t);
+  float r[8];
+  float ss = 0.f;
+  if (active) {
+    uint4 u = *reinterpret_cast<const uint4*>(p.residual + grow * p.H + h);
+    load_y8<SRC, MAXS>(p, t, h, r);
+    float f[8];
+    bf16x8_to_f32(u, f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      r[j] += f[j];
+      ss = fmaf(r[j], r[j], ss);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((tid & 31) == 0) warp_sums[tid >> 5] = ss;
+  __syncthreads();
+  if (tid == 0) {
+    float tot = 0.f;
+    for (int w = 0; w < (blockDim.x + 31) / 32; ++w) tot += warp_sums[w];
+    slice_ss = tot;
+  }
+  cluster_sync();  // every slice's sum is in its CTA's shared memory
+  if (tid == 0) {
+    float tot = 0.f;
+    const uint32_t a = smem_u32(&slice_ss);
+    for (uint32_t k = 0; k < CL; ++k) {
+      float v;
+      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(map_to_cta(a, k)) : "memory");
+      tot += v;
+    }
+    row_total = tot;
+  }
+  cluster_sync();  // peers have read this CTA's slice sum; row_total is visible
+  if (active) {
+    const float rstd = rsqrtf(row_total / static_cast<float>(p.H) + p.eps);
+    const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + h));
+    const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + h + 4));
+    const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    float o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = r[j] * rstd * (p.norm_kind ? 1.0f + g[j] : g[j]);
+    *reinterpret_cast<uint4*>(p.residual + grow * p.H + h) = f32x8_to_bf16(r);
+    __stcs(reinterpret_cast<uint4*>(p.out + grow * p.H + h), f32x8_to_bf16(o));
+  }
+}
+
+template <int SRC, int CL, int MAXS>
+static cudaError_t launch_cluster(const NormParams& p, cudaStream_t s) {
+  const int nvec = p.H / CL / 8;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.T * CL, 1, 1);
+  cfg.blockDim = dim3(((nvec + 31) / 32) * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, fln_add_rmsnorm_cluster_kernel<SRC, CL, MAXS>, p);
+}
+
 // Block size: 512 threads when there are few rows (a row's loads spread over
 // more threads, so more of them are in flight), 256 otherwise.
 template <int SRC, int MAXS>
@@ -189,6 +275,18 @@ cudaError_t launch_add_rmsnorm(NormSource src, const NormParams& p, int grid_cap
   if (p.T <= 0) return cudaSuccess;
   int grid = p.T;
   if (grid_cap > 0 && grid > grid_cap) grid = grid_cap;
+  // few long rows: one 8-CTA cluster per row (slices of H/8 columns, at most
+  // 256 vectors of 8 per CTA)
+  if (p.T <= 64 && p.H % 64 == 0 && p.H / 64 <= 256 && p.H >= 2048 && grid_cap == 0) {
+    switch (src) {
+      case NORM_SRC_BF16: return launch_cluster<NORM_SRC_BF16, 8, 1>(p, stream);
+      case NORM_SRC_F32: return launch_cluster<NORM_SRC_F32, 8, 1>(p, stream);
+      case NORM_SRC_SPLITK:
+        if (p.max_split <= 4) return launch_cluster<NORM_SRC_SPLITK, 8, 4>(p, stream);
+        if (p.max_split <= 8) return launch_cluster<NORM_SRC_SPLITK, 8, 8>(p, stream);
+        break;
+    }
+  }
   switch (src) {
     case NORM_SRC_BF16: return launch_src<NORM_SRC_BF16, 1>(p, grid, stream);
     case NORM_SRC_F32: return launch_src<NORM_SRC_F32, 1>(p, grid, stream);

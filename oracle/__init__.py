@@ -42,26 +42,50 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(path):
+    lib = ctypes.CDLL(path)
+    p = ctypes.c_void_p
+    L = ctypes.c_long
+    lib.oracle_proj_add_rmsnorm.argtypes = [
+        p, p, p, p, ctypes.c_double, ctypes.c_int, L, L, L, p, L, p, p, p, ctypes.c_int]
+    lib.oracle_proj_add_rmsnorm.restype = ctypes.c_int
+    lib.oracle_add_rmsnorm.argtypes = [
+        p, p, p, ctypes.c_double, ctypes.c_int, L, L, p, p, p, ctypes.c_int]
+    lib.oracle_add_rmsnorm.restype = ctypes.c_int
+    lib.oracle_round_to_bf16.argtypes = [p, L, p]
+    lib.oracle_round_to_bf16.restype = None
+    lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+    lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
+class using_library:
+    """Temporarily route this module's functions to another build of oracle.c
+    (the tests use it to check that the pins catch planted mistakes)."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        _load()
+        self.saved = _lib
+        _lib = _bind(self.path)
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            p = ctypes.c_void_p
-            L = ctypes.c_long
-            lib.oracle_proj_add_rmsnorm.argtypes = [
-                p, p, p, p, ctypes.c_double, ctypes.c_int, L, L, L, p, L, p, p, p, ctypes.c_int]
-            lib.oracle_proj_add_rmsnorm.restype = ctypes.c_int
-            lib.oracle_add_rmsnorm.argtypes = [
-                p, p, p, ctypes.c_double, ctypes.c_int, L, L, p, p, p, ctypes.c_int]
-            lib.oracle_add_rmsnorm.restype = ctypes.c_int
-            lib.oracle_round_to_bf16.argtypes = [p, L, p]
-            lib.oracle_round_to_bf16.restype = None
-            lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
-            lib.oracle_double_to_bf16.restype = ctypes.c_uint16
-            lib.oracle_max_threads.argtypes = []
-            lib.oracle_max_threads.restype = ctypes.c_int
-            _lib = lib
+            _lib = _bind(build())
     return _lib
 
 

@@ -1,0 +1,82 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a copy of oracle.c (on the CPU), builds it,
+routes the oracle module to it, and runs the pins of test_oracle.py: at least
+one pin must fail.  The untouched source must pass them all.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+
+from . import test_oracle as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "eps_outside_root": ("double inv_rms = 1.0 / sqrt(mean_sq + eps);", "double inv_rms = 1.0 / sqrt(mean_sq) + eps;"),
+    "eps_dropped": ("double inv_rms = 1.0 / sqrt(mean_sq + eps);", "double inv_rms = 1.0 / sqrt(mean_sq);"),
+    "mean_off_by_one": ("double mean_sq = sum_sq / (double)H;", "double mean_sq = sum_sq / (double)(H + 1);"),
+    "gemma_without_one": ("return norm_kind == ORACLE_NORM_GEMMA ? 1.0 + g : g;", "return g;"),
+    "gemma_always": ("return norm_kind == ORACLE_NORM_GEMMA ? 1.0 + g : g;", "return 1.0 + g;"),
+    "residual_dropped": ("r[h] = bf16_bits_to_double(r0[t * H + h]) + y;", "r[h] = y;"),
+    "residual_subtracted": ("r[h] = bf16_bits_to_double(r0[t * H + h]) + y;",
+                            "r[h] = bf16_bits_to_double(r0[t * H + h]) - y;"),
+    "weight_transposed": ("y += bf16_bits_to_double(xt[k]) * bf16_bits_to_double(wh[k]);",
+                          "y += bf16_bits_to_double(xt[k]) * bf16_bits_to_double(W[(k % H) * K + (h % K)]);"),
+    "weight_index_shift": ("y += bf16_bits_to_double(xt[k]) * bf16_bits_to_double(wh[k]);",
+                           "y += bf16_bits_to_double(xt[k]) * bf16_bits_to_double(wh[(k + 1) % K]);"),
+    "single_precision_dot": ("            double y = 0.0;", "            float y = 0.0f;"),
+    "sum_of_abs": ("sum_sq += r[h] * r[h];", "sum_sq += fabs(r[h]);"),
+    "norm_weight_ignored": ("o[h] = r[h] * inv_rms * norm_weight(gamma, h, norm_kind);", "o[h] = r[h] * inv_rms;"),
+    "add_path_drops_y": ("r[h] = bf16_bits_to_double(r0[t * H + h]) + bf16_bits_to_double(y[t * H + h]);",
+                         "r[h] = bf16_bits_to_double(r0[t * H + h]);"),
+    "round_truncates": ("double qi = nearbyint(q);", "double qi = trunc(q);"),
+    "round_ties_away": ("double qi = nearbyint(q);", "double qi = round(q);"),
+}
+
+
+def _pin_calls():
+    calls = [(f"hand[{c['name']}]", (lambda c=c: pins.test_hand_worked_cases(c))) for c in pins._load_cases()]
+    for name in dir(pins):
+        if name.startswith("test_") and name != "test_hand_worked_cases":
+            calls.append((name, getattr(pins, name)))
+    return calls
+
+
+def _failing_pins():
+    failed = []
+    for name, fn in _pin_calls():
+        try:
+            fn()
+        except (AssertionError, ValueError, pytest.fail.Exception):
+            failed.append(name)
+    return failed
+
+
+def _build(tmp_path, text, tag):
+    src = tmp_path / f"oracle_{tag}.c"
+    src.write_text(text)
+    so = tmp_path / f"liboracle_{tag}.so"
+    subprocess.run(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11", "-fno-fast-math",
+                    "-ffp-contract=off", str(src), "-o", str(so), "-lm"], check=True)
+    return str(so)
+
+
+def test_unmodified_source_passes_every_pin(tmp_path):
+    so = _build(tmp_path, open(SRC).read(), "clean")
+    with oracle.using_library(so):
+        assert _failing_pins() == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(tmp_path, name):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation anchor for {name} not unique"
+    so = _build(tmp_path, text.replace(old, new), name)
+    with oracle.using_library(so):
+        failed = _failing_pins()
+    assert failed, f"no pin caught the planted mistake {name}"

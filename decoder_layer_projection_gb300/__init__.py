@@ -37,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "fused_proj_add_rmsnorm", "add_rmsnorm", "fln_autotune", "fln_set_overrides", "fln_set_plan",
     "fln_get_plan", "fln_device_status", "fln_last_error", "fln_release_workspace", "fln_launch_count",
     "fln_profile_enable", "fln_profile_read", "fln_version", "fused_proj_add_rmsnorm_noalloc",
+    "fln_debug_stall_next_call",
 )
 
 
@@ -105,6 +106,8 @@ def load(path: str | None = None):
         lib.fln_profile_read.restype = i
         lib.fln_version.argtypes = []
         lib.fln_version.restype = i
+        lib.fln_debug_stall_next_call.argtypes = [i]
+        lib.fln_debug_stall_next_call.restype = i
         lib.fused_proj_add_rmsnorm_noalloc.argtypes = [vp, vp, vp, vp, f, i, i, i, i, vp, vp, vp]
         lib.fused_proj_add_rmsnorm_noalloc.restype = i
         _lib = lib
@@ -236,6 +239,11 @@ def fln_profile_read() -> dict:
     _check(load().fln_profile_read(ctypes.byref(s)))
     return {name: {"launches": int(s.launches[i]), "total_ms": float(s.total_ms[i])}
             for i, name in enumerate(KERNEL_NAMES)}
+
+
+def fln_debug_stall_next_call(enable: bool = True):
+    """Test switch: the next FUSED launch's bounded row-statistics wait runs out."""
+    _check(load().fln_debug_stall_next_call(1 if enable else 0))
 
 
 def fln_version() -> int:

@@ -98,6 +98,7 @@ struct GroupKey {
 std::map<GroupKey, fln_plan> g_plans;
 int g_override_chunk = 0;
 int g_override_threshold = 0;
+bool g_stall_next = false;  // test switch, see fln_debug_stall_next_call
 
 struct ProfRec {
   int kind;
@@ -371,6 +372,8 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     if (++ws->gen == 0) ++ws->gen;
     p.gen = ws->gen;
     p.err = ws->err_word;
+    p.stall_rowstat = g_stall_next ? 1 : 0;
+    g_stall_next = false;
     // every pair of the grid must be resident at once (they exchange row
     // statistics), so the grid never exceeds the resident-pair count
     const long long tiles = static_cast<long long>((p.num_m_tiles + 1) / 2) * nt;
@@ -1002,6 +1005,12 @@ int fln_profile_read(fln_profile_stats* st) {
 }
 
 int fln_version(void) { return 100; }
+
+int fln_debug_stall_next_call(int enable) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_stall_next = enable != 0;
+  return FLN_OK;
+}
 
 int fused_proj_add_rmsnorm_noalloc(const fln_bf16* x, const fln_bf16* W, fln_bf16* residual, const float* gamma,
                                    float eps, int norm_kind, int T, int K, int H, fln_bf16* out,

@@ -353,10 +353,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (j0 + i >= nN || !ok) continue;
-          if ((v[i] >> 32) != p.gen) {
+          // (the test switch makes slot 0 wait for a generation nobody publishes)
+          const unsigned int want = (p.stall_rowstat && j0 + i == 0) ? p.gen + 1u : p.gen;
+          if ((v[i] >> 32) != want) {
             const unsigned long long* f = prow + static_cast<size_t>(j0 + i) * BM;
             const uint64_t t0 = globaltimer_ns();
-            while (((v[i] = ld_relaxed_gpu_u64(f)) >> 32) != p.gen) {
+            while (((v[i] = ld_relaxed_gpu_u64(f)) >> 32) != want) {
               if (*abort_flag || globaltimer_ns() - t0 > FLN_WAIT_TIMEOUT_NS) {
                 ok = false;
                 break;

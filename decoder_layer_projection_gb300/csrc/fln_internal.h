@@ -44,6 +44,7 @@ struct GemmParams {
                             // separate flags (CTA kernel), or 64-bit {gen, value} words (pair kernel)
   unsigned int* flags;      // [num_m_tiles, num_n_tiles] publication flags (CTA kernel)
   unsigned int gen;         // value this launch writes into flags (never 0)
+  int stall_rowstat;        // test switch: wait for a generation nobody publishes (bounded wait runs out)
   // store-f32 epilogue
   float* yout;              // [M, ld] fp32 slot, local rows
   // split-K swap epilogue

@@ -226,6 +226,14 @@ int fused_proj_add_rmsnorm_noalloc(const fln_bf16* x, const fln_bf16* W, fln_bf1
                                    float eps, int norm_kind, int T, int K, int H, fln_bf16* out,
                                    unsigned int* device_error, fln_stream_t stream);
 
+/* Test switch for failure reporting: with enable != 0, the next launch of
+ * the FUSED path waits, in its exchange of row statistics, for a value that no
+ * CTA publishes.  That bounded wait gives up after about two seconds, the
+ * kernel unwinds without writing the affected rows, and fln_device_status
+ * returns FLN_ERR_DEVICE_TIMEOUT; the device stays usable.  The switch clears
+ * itself after one launch.  No fault, trap or unbounded wait is involved. */
+int fln_debug_stall_next_call(int enable);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int fln_version(void);
 

@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // stored by the threads instead, so the next tile's columns stay intact.
       // Rows past the chunk and columns past H read zeros: acc and r0 are 0.
       float ss = 0.f;
+      int pending = -1;  // box whose TMA store may still be reading it (freed one box later)
 #pragma unroll 1
       for (int g = 0; g < G; ++g, ++s) {
         const int halves = (BN - g * 64) >= 64 ? 2 : 1;  // 32-column halves of this box inside the tile
@@ -315,8 +316,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (lane == 0) {
             tma_store_2d(&tmRs, box + q * (32 * 128), n0 + g * 64, wrow0);
             bulk_commit_group();
-            bulk_wait_group_read<0>();  // the store has read the rows: the box may be refilled
+            if (pending >= 0) {
+              bulk_wait_group_read<1>();           // the previous box's store has read its rows
+              mbar_arrive(&e_free[pending % NB]);  // this warp is done with that box
+            }
           }
+          pending = s;
           __syncwarp();
         } else {
           __syncwarp();
@@ -333,8 +338,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
           __syncwarp();
+          if (lane == 0) mbar_arrive(&e_free[s % NB]);  // this warp is done with box s
         }
-        if (lane == 0) mbar_arrive(&e_free[s % NB]);  // this warp is done with box s
+      }
+      if (lane == 0 && pending >= 0) {
+        bulk_wait_group_read<0>();
+        mbar_arrive(&e_free[pending % NB]);
       }
       // Row statistics across the row block's N-tiles: each row's partial sum
       // is published as one 64-bit word {generation of this launch, value}, so a
@@ -383,42 +392,47 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll 1
       for (int g = 0; g < G; ++g) {
         const int halves = (BN - g * 64) >= 64 ? 2 : 1;
-#pragma unroll 1
-        for (int c2 = 0; c2 < halves; ++c2) {
-          float v[32];
-          tmem_ld32(tb + static_cast<uint32_t>(g * 64 + c2 * 32), v);
+        uint4 ob[8];  // this box's bf16 outputs, computed before waiting for the staging rows
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int chunk = c2 * 4 + h;
-            const int cc = n0 + g * 64 + chunk * 8;
-            float gw[8];
-            if (cc < p.N) {
-              const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc));
-              const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc + 4));
-              gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
-              gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
-            } else {
+        for (int c2 = 0; c2 < 2; ++c2) {
+          if (c2 < halves) {
+            float v[32];
+            tmem_ld32(tb + static_cast<uint32_t>(g * 64 + c2 * 32), v);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) gw[j] = 0.f;
+            for (int h = 0; h < 4; ++h) {
+              const int chunk = c2 * 4 + h;
+              const int cc = n0 + g * 64 + chunk * 8;
+              float gw[8];
+              if (cc < p.N) {
+                const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc));
+                const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc + 4));
+                gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
+                gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
+              } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) gw[j] = 0.f;
+              }
+              float o[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float gj = p.norm_kind ? 1.0f + gw[j] : gw[j];
+                o[j] = v[8 * h + j] * rstd * gj;
+              }
+              ob[chunk] = f32x8_to_bf16(o);
             }
-            float o[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float gj = p.norm_kind ? 1.0f + gw[j] : gw[j];
-              o[j] = v[8 * h + j] * rstd * gj;
-            }
-            *reinterpret_cast<uint4*>(ostage + swz(lane, chunk)) = f32x8_to_bf16(o);
           }
         }
+        if (lane == 0) bulk_wait_group_read<0>();  // the previous box's store has read the staging rows
+        __syncwarp();
+#pragma unroll
+        for (int chunk = 0; chunk < 8; ++chunk)
+          if (chunk < halves * 4) *reinterpret_cast<uint4*>(ostage + swz(lane, chunk)) = ob[chunk];
         if (halves == 2) {
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            if (go) {
-              tma_store_2d(&tmOs, ostage, n0 + g * 64, wrow0);
-              bulk_commit_group();
-            }
-            bulk_wait_group_read<0>();  // staging rows read: the next box may overwrite them
+          if (lane == 0 && go) {
+            tma_store_2d(&tmOs, ostage, n0 + g * 64, wrow0);
+            bulk_commit_group();
           }
           __syncwarp();
         } else {

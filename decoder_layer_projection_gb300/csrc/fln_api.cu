@@ -79,6 +79,7 @@ struct Workspace {
   size_t slot_floats = 0;
   float* partial = nullptr;
   size_t partial_floats = 0;
+  unsigned int* dyn_counter = nullptr;  // split-K dynamic chunk draws; each GEMM launch leaves it at zero
   cudaStream_t stream_b = nullptr;
   cudaEvent_t ev_ready[3] = {};
   cudaEvent_t ev_free[3] = {};
@@ -151,6 +152,8 @@ int get_ws(Workspace** out) {
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ws->ev_join, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaMalloc(&ws->err_word, sizeof(unsigned int));
   if (e == cudaSuccess) e = cudaMemset(ws->err_word, 0, sizeof(unsigned int));
+  if (e == cudaSuccess) e = cudaMalloc(&ws->dyn_counter, sizeof(unsigned int));
+  if (e == cudaSuccess) e = cudaMemset(ws->dyn_counter, 0, sizeof(unsigned int));
   if (e != cudaSuccess) {
     delete ws;  // partial handles leak only on a failing device
     return cuda_fail(e, "workspace creation");
@@ -284,22 +287,54 @@ int run_unfused(Workspace* ws, const Call& c) {
   p.num_m_tiles = (c.H + 127) / 128;
   p.num_n_tiles = 1;
   p.num_k_blocks = (c.K + 63) / 64;
-  p.units_total = static_cast<long long>(p.num_m_tiles) * p.num_k_blocks;
-  const int G = static_cast<int>(std::min<long long>(ws->sms, p.units_total));
+  // Dynamic balancing: CTAs finish their static share at different times
+  // (about +-10 % around the median), so about a fifth of each m-tile's
+  // K-blocks (the last ones) is handed out at run time in chunks of >= 4
+  // blocks, each chunk with its own partial slot.  That pays where a CTA's
+  // share is long (K >= 16384) and the extra partial slots are small (<= 32
+  // tokens); measured on the 70B down projection (K = 28672): 91 -> 88 us at
+  // 1-32 tokens, a loss at 64; no gain at K = 8192.
+  const int KB = p.num_k_blocks;
+  int kc = 0, cpm = 0;
+  if (c.T <= 32 && KB >= 256) {
+    const double kd = 0.2 * KB;
+    kc = std::max(4, static_cast<int>(std::ceil(kd / 8.0)));
+    cpm = std::min(8, std::max(1, static_cast<int>(std::lround(kd / kc))));
+  }
+  p.dyn_kc = kc;
+  p.dyn_cpm = cpm;
+  p.kb_static = KB - kc * cpm;
+  p.units_total = static_cast<long long>(p.num_m_tiles) * p.kb_static;
+  // grid: one CTA per SM, fewer when an m-tile would be split over more
+  // partial slots than the reducer sums (16, static and dynamic together;
+  // happens for few m-tiles and long K)
+  const long long KBs = p.kb_static;
+  auto slots_for = [&](int g) {
+    int ms = 1;
+    for (int m = 0; m < p.num_m_tiles; ++m) {
+      const int a = splitk_cta_of_unit(m * KBs, p.units_total, g);
+      const int b = splitk_cta_of_unit((m + 1) * KBs - 1, p.units_total, g);
+      ms = std::max(ms, b - a + 1);
+    }
+    return ms;
+  };
+  int G = static_cast<int>(std::min<long long>(ws->sms, p.units_total));
   if ((p.units_total + 1) * G + p.units_total >= (1ll << 32))
     return fail(FLN_ERR_UNSUPPORTED, "split-K path: K=%d, H=%d give too many work units", c.K, c.H);
-  int max_split = 1;
-  for (int m = 0; m < p.num_m_tiles; ++m) {
-    const long long KB = p.num_k_blocks;
-    const int a = splitk_cta_of_unit(m * KB, p.units_total, G);
-    const int b = splitk_cta_of_unit((m + 1) * KB - 1, p.units_total, G);
-    max_split = std::max(max_split, b - a + 1);
+  int max_split = slots_for(G);
+  while (max_split + cpm > 16 && G > 1) {
+    G = std::max(1, G - std::max(1, G / 16));
+    max_split = slots_for(G);
   }
+  if (max_split + cpm > 16)
+    return fail(FLN_ERR_UNSUPPORTED, "split-K path: %d partial slots per m-tile (at most 16)", max_split + cpm);
   p.max_split = max_split;
-  const size_t need = static_cast<size_t>(p.num_m_tiles) * max_split * c.T * 128;
+  p.slot_stride = max_split + cpm;
+  const size_t need = static_cast<size_t>(p.num_m_tiles) * p.slot_stride * c.T * 128;
   if ((rc = grow(&ws->partial, &ws->partial_floats, need, false, "cudaMalloc(split-K partials)"))) return rc;
   p.partial = ws->partial;
   p.err = ws->err_word;
+  p.dyn_counter = ws->dyn_counter;
   rc = launch_counted(FLN_KERNEL_GEMM_SPLITK, c.stream,
                       [&] { return launch_gemm(EPI_SPLITK_SWAP, bn, tmA, tmB, p, G, c.stream); },
                       "split-K GEMM launch");
@@ -307,7 +342,9 @@ int run_unfused(Workspace* ws, const Call& c) {
   NormParams np{};
   np.partial = ws->partial;
   np.max_split = max_split;
-  np.num_k_blocks = p.num_k_blocks;
+  np.slot_stride = p.slot_stride;
+  np.dyn_cpm = cpm;
+  np.num_k_blocks = p.kb_static;
   np.gemm_grid = G;
   np.units_total = p.units_total;
   np.residual = c.residual;
@@ -960,6 +997,7 @@ void fln_release_workspace(void) {
     cudaFree(ws->flags);
     for (int i = 0; i < 3; ++i) cudaFree(ws->slots[i]);
     cudaFree(ws->partial);
+    cudaFree(ws->dyn_counter);
     for (int i = 0; i < 3; ++i) {
       cudaEventDestroy(ws->ev_ready[i]);
       cudaEventDestroy(ws->ev_free[i]);

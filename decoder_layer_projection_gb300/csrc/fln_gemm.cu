@@ -39,14 +39,14 @@ __host__ __device__ constexpr int stage_bytes(int bn) { return A_TILE_BYTES + bn
 // As many ring stages as fit in the 227 KiB a CTA may use (at most 16): the
 // decode shapes stream W from HBM and need many bytes in flight per SM.
 __host__ __device__ constexpr int stages_for(int bn) {
-  return (232448 - 256 - 1024) / stage_bytes(bn) > 16 ? 16 : (232448 - 256 - 1024) / stage_bytes(bn);
+  return (232448 - 512 - 1024) / stage_bytes(bn) > 16 ? 16 : (232448 - 512 - 1024) / stage_bytes(bn);
 }
 __host__ __device__ constexpr int tmem_cols_for(int bn) {
   return (2 * bn) <= 32 ? 32 : (2 * bn) <= 64 ? 64 : (2 * bn) <= 128 ? 128 : (2 * bn) <= 256 ? 256 : 512;
 }
 __host__ __device__ constexpr int smem_bytes_for(int bn) {
-  // ring + barriers/flags (256 B) + alignment slack for the 1024-byte swizzle base
-  return stages_for(bn) * stage_bytes(bn) + 256 + 1024;
+  // ring + barriers/flags/work queue (512 B) + alignment slack for the 1024-byte swizzle base
+  return stages_for(bn) * stage_bytes(bn) + 512 + 1024;
 }
 
 // One unit of work: an output tile and the K-block range it accumulates.
@@ -55,7 +55,21 @@ struct WorkItem {
 };
 
 // Static persistent schedule shared verbatim by the three roles, so that they
-// agree on the sequence without communicating.
+// agree on the sequence without communicating.  (The split-K mode appends
+// dynamic chunks after it; those the producer hands to the others.)
+// Dynamic chunk j of the split-K mode: m-tile j / dyn_cpm, K-blocks
+// [kb_static + i * dyn_kc, ...) with i = j % dyn_cpm, partial slot max_split + i.
+__device__ __forceinline__ WorkItem dyn_item(const GemmParams& p, int j) {
+  WorkItem w;
+  const int i = j % p.dyn_cpm;
+  w.m_tile = j / p.dyn_cpm;
+  w.n_tile = 0;
+  w.kb_begin = p.kb_static + i * p.dyn_kc;
+  w.kb_end = min(p.num_k_blocks, w.kb_begin + p.dyn_kc);
+  w.split = p.max_split + i;
+  return w;
+}
+
 template <int EPI>
 struct Scheduler {
   const GemmParams& p;
@@ -76,8 +90,9 @@ struct Scheduler {
 
   __device__ bool next(WorkItem& w) {
     if (EPI == EPI_SPLITK_SWAP) {
+      // static part: units (m-tile, K-block < kb_static) in m-major order
       if (u >= u_end) return false;
-      const int KB = p.num_k_blocks;
+      const int KB = p.kb_static;
       w.m_tile = static_cast<int>(u / KB);
       w.n_tile = 0;
       w.kb_begin = static_cast<int>(u % KB);
@@ -101,6 +116,95 @@ struct Scheduler {
   }
 };
 
+// The sequence of work items one role processes: the static schedule, then
+// (split-K with dynamic chunks) the chunks the producer draws from a global
+// counter and passes on through a 4-entry queue in shared memory.  Each CTA
+// draws until it gets an id past the end, so one launch makes exactly
+// (chunks + CTAs) draws; whoever makes the last one puts the counter back to
+// zero, so every launch (a graph replay too) starts from zero.
+template <int EPI>
+struct WorkSource {
+  Scheduler<EPI> sched;
+  bool dyn = false;   // static part done
+  bool done = false;  // this CTA has taken its id past the end
+  int q = 0;
+  __device__ explicit WorkSource(const GemmParams& prm) : sched(prm) {}
+
+  __device__ bool has_dynamic() const { return EPI == EPI_SPLITK_SWAP && sched.p.dyn_cpm > 0; }
+
+  // one draw; returns the chunk id or -1 past the end
+  __device__ int draw() {
+    const GemmParams& p = sched.p;
+    const unsigned int nc = static_cast<unsigned int>(p.num_m_tiles * p.dyn_cpm);
+    const unsigned int j = atomicAdd(p.dyn_counter, 1u);
+    if (j < nc) return static_cast<int>(j);
+    if (j == nc + gridDim.x - 1) atomicExch(p.dyn_counter, 0u);  // the launch's last draw
+    done = true;
+    return -1;
+  }
+
+  // producer: take the next chunk id and publish it; ok = false on a timeout
+  __device__ bool next_producer(WorkItem& w, bool& ok, uint64_t* wq_full, uint64_t* wq_empty, volatile int* wq,
+                                volatile int* abort_flag) {
+    if (!dyn) {
+      if (sched.next(w)) return true;
+      if (!has_dynamic()) return false;
+      dyn = true;
+    }
+    const GemmParams& p = sched.p;
+    const int slot = q & 3;
+    if (q >= 4 && !mbar_wait(&wq_empty[slot], static_cast<uint32_t>((q >> 2) - 1) & 1u, abort_flag, p.err,
+                             FLN_DEVERR_TIMEOUT_EMPTY)) {
+      ok = false;
+      return false;
+    }
+    const int jj = draw();
+    wq[slot] = jj;
+    mbar_arrive(&wq_full[slot]);
+    ++q;
+    if (jj < 0) return false;
+    w = dyn_item(p, jj);
+    return true;
+  }
+
+  // unwinding after a timeout: keep drawing until past the end, so that the
+  // launch still makes exactly (chunks + CTAs) draws and the counter returns
+  // to zero
+  __device__ void drain_ids() {
+    if (!has_dynamic()) return;
+    while (!done) draw();
+  }
+
+  // MMA issuer (one thread, whole_warp = false) / epilogue warps (all 32
+  // lanes, lane 0 arrives): the next item; ok = false on a timeout
+  __device__ bool next_consumer(WorkItem& w, bool& ok, uint64_t* wq_full, uint64_t* wq_empty, volatile int* wq,
+                                volatile int* abort_flag, bool whole_warp) {
+    if (!dyn) {
+      if (sched.next(w)) return true;
+      if (!has_dynamic()) return false;
+      dyn = true;
+    }
+    const GemmParams& p = sched.p;
+    const int slot = q & 3;
+    if (!mbar_wait(&wq_full[slot], static_cast<uint32_t>(q >> 2) & 1u, abort_flag, p.err,
+                   FLN_DEVERR_TIMEOUT_FULL)) {
+      ok = false;
+      return false;
+    }
+    const int jj = wq[slot];
+    if (whole_warp) {
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&wq_empty[slot]);
+    } else {
+      mbar_arrive(&wq_empty[slot]);
+    }
+    ++q;
+    if (jj < 0) return false;
+    w = dyn_item(p, jj);
+    return true;
+  }
+};
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fln_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -117,9 +221,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* acc_full = empty_bar + STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain_bar = acc_empty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint64_t* wq_full = drain_bar + 1;   // dynamic split-K chunks: producer -> MMA and epilogue
+  uint64_t* wq_empty = wq_full + 4;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(wq_empty + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* epi_abort = abort_flag + 1;
+  volatile int* wq = epi_abort + 1;     // 4 queued chunk ids (-1 = no more)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -137,6 +244,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
     }
     mbar_init(drain_bar, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&wq_full[i], 1);
+      mbar_init(&wq_empty[i], 5);  // the MMA issuer and the four epilogue warps
+    }
     *abort_flag = 0;
     *epi_abort = 0;
     fence_mbar_init();
@@ -157,14 +268,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ producer
     const uint64_t pol_a = (EPI == EPI_SPLITK_SWAP) ? l2_policy_evict_first() : l2_policy_evict_normal();
     const uint64_t pol_b = (EPI == EPI_SPLITK_SWAP) ? l2_policy_evict_last() : l2_policy_evict_last();
-    Scheduler<EPI> sched(p);
+    WorkSource<EPI> src(p);
     WorkItem w;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0;     // stages with a load issued
     uint32_t issued_parity = 0;   // parity of that load's phase
     bool ok = true;
-    while (ok && sched.next(w)) {
+    while (ok && src.next_producer(w, ok, wq_full, wq_empty, wq, abort_flag)) {
       const int a_row = p.a_row0 + w.m_tile * BM;
       const int b_row = w.n_tile * BN;
       for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
@@ -185,6 +296,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
+    if (!ok) src.drain_ids();
     if (!ok) {
       // unwinding: let every load already issued land before the CTA exits
       for (int s = 0; s < STAGES; ++s) {
@@ -196,14 +308,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    Scheduler<EPI> sched(p);
+    WorkSource<EPI> src(p);
     WorkItem w;
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
     bool ok = true;
     bool issued_any = false;
-    while (ok && sched.next(w)) {
+    while (ok && src.next_consumer(w, ok, wq_full, wq_empty, wq, abort_flag, false)) {
       const int b = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(&acc_empty[b], (use & 1u) ^ 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) {
@@ -250,17 +362,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int rl = q * 32 + lane;      // row within the tile
     const int ep_tid = threadIdx.x - 64;
-    Scheduler<EPI> sched(p);
+    WorkSource<EPI> src(p);
     WorkItem w;
     int local = 0;
-    while (sched.next(w)) {
+    bool failed = false;  // a row-statistics wait of this CTA gave up
+    for (;;) {
+      bool okq = true;
+      const bool have = src.next_consumer(w, okq, wq_full, wq_empty, wq, abort_flag, true);
       const int b = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       // All 128 epilogue threads decide together whether to continue: a thread
       // that leaves alone would strand the others at a named barrier.
-      if (!mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) *epi_abort = 1;
-      named_bar_sync(1, 128);
-      if (*epi_abort) break;
+      bool stop = !have || !okq || failed;
+      if (!stop && !mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) stop = true;
+      if (named_bar_any(1, 128, stop)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
       const int row = w.m_tile * BM + rl;  // local row of the launch (A operand)
@@ -300,6 +415,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __threadfence();
         named_bar_sync(1, 128);
         if (ep_tid == 0) st_release_gpu(&p.flags[w.m_tile * nN + w.n_tile], p.gen);
+        bool rs_fail = false;
         if (ep_tid < 32) {
           bool ok = true;
           for (int j = lane; j < nN; j += 32) {
@@ -319,11 +435,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!ok && lane == 0) {
             if (!*abort_flag) atomicOr(p.err, FLN_DEVERR_TIMEOUT_ROWSTAT);
             *abort_flag = 1;
-            *epi_abort = 1;
           }
+          rs_fail = !ok;
         }
-        named_bar_sync(1, 128);
-        const bool go = (*epi_abort == 0);
+        const bool go = !named_bar_any(1, 128, rs_fail);
+        if (!go) failed = true;
         // phase 2: normalise and store residual and out (bf16, 16-byte stores)
         float tot = 0.f;
         for (int j = 0; j < nN; ++j) tot += ld_cg_f32(&ps[static_cast<size_t>(j) * BM + rl]);
@@ -379,7 +495,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       } else {  // EPI_SPLITK_SWAP: TMEM lane = hidden index h, column = token t
         float* dst = p.partial +
-                     static_cast<size_t>(w.m_tile * p.max_split + w.split) * static_cast<size_t>(p.N) * BM;
+                     static_cast<size_t>(w.m_tile * p.slot_stride + w.split) * static_cast<size_t>(p.N) * BM;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           float v[16];

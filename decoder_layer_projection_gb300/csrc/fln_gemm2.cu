@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const unsigned long long tag = static_cast<unsigned long long>(p.gen) << 32;
     int s = 0;  // next residual box to consume
     int local = 0;
+    bool failed = false;  // a row-statistics wait of this warp gave up
     for (int t = pair_id; t < total; t += num_pairs, ++local) {
       const int b = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -270,9 +271,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int wrow0 = mtile * BM + q * 32;  // this warp's first row in the chunk
       // All 128 epilogue threads decide together whether to continue: a thread
       // that leaves alone would strand the others at the named barrier.
-      if (!mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) *epi_abort = 1;
-      named_bar_sync(1, 128);
-      if (*epi_abort) break;
+      bool stop = failed;
+      if (!stop && !mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) stop = true;
+      if (named_bar_any(1, 128, stop)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
 
@@ -380,7 +381,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) {
         if (!*abort_flag) atomicOr(p.err, FLN_DEVERR_TIMEOUT_ROWSTAT);
         *abort_flag = 1;
-        *epi_abort = 1;
+        failed = true;  // this warp; the next top-of-loop barrier stops all four
       }
       const bool go = __all_sync(0xffffffffu, ok);
       const float rstd = rsqrtf(tot / static_cast<float>(p.ld) + p.eps);

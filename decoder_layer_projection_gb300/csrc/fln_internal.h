@@ -47,10 +47,17 @@ struct GemmParams {
   int stall_rowstat;        // test switch: wait for a generation nobody publishes (bounded wait runs out)
   // store-f32 epilogue
   float* yout;              // [M, ld] fp32 slot, local rows
-  // split-K swap epilogue
-  float* partial;           // [num_m_tiles * max_split, N, 128] fp32
-  int max_split;            // partial slots per m-tile
-  long long units_total;    // num_m_tiles * num_k_blocks
+  // split-K swap epilogue.  Each m-tile's first kb_static K-blocks are split
+  // statically (stream-K over the grid); the remaining K-blocks form dyn_cpm
+  // chunks of dyn_kc blocks, handed out at run time through an atomic counter.
+  float* partial;           // [num_m_tiles * slot_stride, N, 128] fp32
+  int max_split;            // static partial slots per m-tile (dynamic chunk i uses slot max_split + i)
+  int slot_stride;          // partial slots per m-tile: max_split + dyn_cpm
+  long long units_total;    // num_m_tiles * kb_static
+  int kb_static;            // statically split K-blocks per m-tile
+  int dyn_cpm;              // dynamic chunks per m-tile (0: none)
+  int dyn_kc;               // K-blocks per dynamic chunk
+  unsigned int* dyn_counter;  // chunk counter: zero before and after every launch
   unsigned int* err;        // device error word
 };
 
@@ -58,10 +65,13 @@ struct NormParams {
   const __nv_bfloat16* y_bf16;  // [T, H] bf16 addend (plain add_rmsnorm)
   const float* y_f32;           // [T, H] fp32 addend (pipeline slot), rows local to the launch
   const float* partial;         // split-K partials (layout of GemmParams::partial)
-  int max_split;
-  int num_k_blocks;             // split-K bookkeeping (to find contributing CTAs)
+  int max_split;                // static slots per m-tile
+  int slot_stride;              // slots per m-tile (static + dynamic)
+  int dyn_cpm;                  // dynamic chunk slots per m-tile
+  int num_k_blocks;             // statically split K-blocks per m-tile (to find contributing CTAs)
   int gemm_grid;
   long long units_total;
+
   __nv_bfloat16* residual;      // [T, H] in/out
   __nv_bfloat16* out;           // [T, H]
   const float* gamma;

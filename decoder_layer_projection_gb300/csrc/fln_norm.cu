@@ -30,8 +30,9 @@
 namespace fln {
 
 // split-K: the hidden index h lives in m-tile h / 128, lane h % 128; the
-// CTAs that touched m-tile m wrote partial slots 0 .. n-1 in unit order; the
-// slots are summed in that order (at most MAXS of them).
+// CTAs that touched m-tile m in the static split wrote partial slots
+// 0 .. n-1 in unit order, the dynamic chunks slots max_split .. max_split +
+// dyn_cpm - 1; the slots are summed in that fixed order (at most MAXS).
 template <int MAXS>
 __device__ __forceinline__ void load_splitk8(const NormParams& p, int t, int h, float (&y)[8]) {
   const int m = h >> 7;
@@ -40,12 +41,14 @@ __device__ __forceinline__ void load_splitk8(const NormParams& p, int t, int h, 
   const int c_first = splitk_cta_of_unit(static_cast<long long>(m) * KB, p.units_total, p.gemm_grid);
   const int c_last = splitk_cta_of_unit(static_cast<long long>(m + 1) * KB - 1, p.units_total, p.gemm_grid);
   const int n = c_last - c_first + 1;
+  const int total = n + p.dyn_cpm;
   float4 a[MAXS], b[MAXS];
 #pragma unroll
   for (int s = 0; s < MAXS; ++s) {
-    if (s < n) {
+    if (s < total) {
+      const int slot = s < n ? s : p.max_split + (s - n);
       const float4* src = reinterpret_cast<const float4*>(
-          p.partial + (static_cast<size_t>(m * p.max_split + s) * p.T + t) * 128 + hl);
+          p.partial + (static_cast<size_t>(m * p.slot_stride + slot) * p.T + t) * 128 + hl);
       a[s] = __ldcs(src);
       b[s] = __ldcs(src + 1);
     }
@@ -54,7 +57,7 @@ __device__ __forceinline__ void load_splitk8(const NormParams& p, int t, int h, 
   for (int j = 0; j < 8; ++j) y[j] = 0.f;
 #pragma unroll
   for (int s = 0; s < MAXS; ++s) {
-    if (s < n) {
+    if (s < total) {
       y[0] += a[s].x; y[1] += a[s].y; y[2] += a[s].z; y[3] += a[s].w;
       y[4] += b[s].x; y[5] += b[s].y; y[6] += b[s].z; y[7] += b[s].w;
     }
@@ -179,14 +182,15 @@ static cudaError_t launch_nt(const NormParams& p, int grid, cudaStream_t s) {
 
 // Few rows: each row is split over a cluster of CL CTAs (one slice of H/CL
 // columns each, one 8-column vector per thread), so a row's loads come from
-// CL SMs at once; the slices' sums of squares are combined through
-// distributed shared memory in rank order.
+// CL SMs at once.  Each CTA writes its slice's sum of squares into every
+// CTA of the cluster (distributed shared memory), one cluster barrier later
+// every CTA adds the CL sums in rank order (the same float in all of them).
+// Residual and gamma are read before waiting for the addend: no kernel that
+// this one depends on programmatically writes them.
 template <int SRC, int CL, int MAXS>
 __global__ void __launch_bounds__(256) fln_add_rmsnorm_cluster_kernel(const NormParams p) {
   __shared__ float warp_sums[8];
-  __shared__ float slice_ss;
-  __shared__ float row_total;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float slice_ss[CL];
   const int tid = threadIdx.x;
   const uint32_t rank = cluster_ctarank();
   const int t = static_cast<int>(cluster_id_x());
@@ -196,10 +200,18 @@ __global__ void __launch_bounds__(256) fln_add_rmsnorm_cluster_kernel(const Norm
   const bool active = vi < nvec;
   const int h = static_cast<int>(rank) * slice + (vi << 3);
   const size_t grow = static_cast<size_t>(p.row0) + static_cast<size_t>(t);
+  uint4 u = make_uint4(0u, 0u, 0u, 0u);
+  float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0;
+  if (active) {
+    u = *reinterpret_cast<const uint4*>(p.residual + grow * p.H + h);
+    g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + h));
+    g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + h + 4));
+  }
+  // when launched as a programmatic dependent, wait for the producing kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   float r[8];
   float ss = 0.f;
   if (active) {
-    uint4 u = *reinterpret_cast<const uint4*>(p.residual + grow * p.H + h);
     load_y8<SRC, MAXS>(p, t, h, r);
     float f[8];
     bf16x8_to_f32(u, f);
@@ -213,27 +225,19 @@ __global__ void __launch_bounds__(256) fln_add_rmsnorm_cluster_kernel(const Norm
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((tid & 31) == 0) warp_sums[tid >> 5] = ss;
   __syncthreads();
-  if (tid == 0) {
+  if (tid < CL) {
+    // thread k sends this slice's sum to CTA k
     float tot = 0.f;
     for (int w = 0; w < (blockDim.x + 31) / 32; ++w) tot += warp_sums[w];
-    slice_ss = tot;
+    const uint32_t a = map_to_cta(smem_u32(&slice_ss[rank]), static_cast<uint32_t>(tid));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(tot) : "memory");
   }
-  cluster_sync();  // every slice's sum is in its CTA's shared memory
-  if (tid == 0) {
-    float tot = 0.f;
-    const uint32_t a = smem_u32(&slice_ss);
-    for (uint32_t k = 0; k < CL; ++k) {
-      float v;
-      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(map_to_cta(a, k)) : "memory");
-      tot += v;
-    }
-    row_total = tot;
-  }
-  cluster_sync();  // peers have read this CTA's slice sum; row_total is visible
+  cluster_sync();  // all CL slice sums are in this CTA's shared memory; no remote access follows
   if (active) {
-    const float rstd = rsqrtf(row_total / static_cast<float>(p.H) + p.eps);
-    const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + h));
-    const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + h + 4));
+    float tot = 0.f;
+#pragma unroll
+    for (int k = 0; k < CL; ++k) tot += slice_ss[k];
+    const float rstd = rsqrtf(tot / static_cast<float>(p.H) + p.eps);
     const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
     float o[8];
 #pragma unroll
@@ -282,8 +286,9 @@ cudaError_t launch_add_rmsnorm(NormSource src, const NormParams& p, int grid_cap
       case NORM_SRC_BF16: return launch_cluster<NORM_SRC_BF16, 8, 1>(p, stream);
       case NORM_SRC_F32: return launch_cluster<NORM_SRC_F32, 8, 1>(p, stream);
       case NORM_SRC_SPLITK:
-        if (p.max_split <= 4) return launch_cluster<NORM_SRC_SPLITK, 8, 4>(p, stream);
-        if (p.max_split <= 8) return launch_cluster<NORM_SRC_SPLITK, 8, 8>(p, stream);
+        if (p.max_split + p.dyn_cpm <= 4) return launch_cluster<NORM_SRC_SPLITK, 8, 4>(p, stream);
+        if (p.max_split + p.dyn_cpm <= 8) return launch_cluster<NORM_SRC_SPLITK, 8, 8>(p, stream);
+        if (p.max_split + p.dyn_cpm <= 12) return launch_cluster<NORM_SRC_SPLITK, 8, 12>(p, stream);
         break;
     }
   }
@@ -291,9 +296,9 @@ cudaError_t launch_add_rmsnorm(NormSource src, const NormParams& p, int grid_cap
     case NORM_SRC_BF16: return launch_src<NORM_SRC_BF16, 1>(p, grid, stream);
     case NORM_SRC_F32: return launch_src<NORM_SRC_F32, 1>(p, grid, stream);
     case NORM_SRC_SPLITK:
-      if (p.max_split <= 4) return launch_src<NORM_SRC_SPLITK, 4>(p, grid, stream);
-      if (p.max_split <= 8) return launch_src<NORM_SRC_SPLITK, 8>(p, grid, stream);
-      if (p.max_split <= 16) return launch_src<NORM_SRC_SPLITK, 16>(p, grid, stream);
+      if (p.max_split + p.dyn_cpm <= 4) return launch_src<NORM_SRC_SPLITK, 4>(p, grid, stream);
+      if (p.max_split + p.dyn_cpm <= 8) return launch_src<NORM_SRC_SPLITK, 8>(p, grid, stream);
+      if (p.max_split + p.dyn_cpm <= 16) return launch_src<NORM_SRC_SPLITK, 16>(p, grid, stream);
       return cudaErrorInvalidValue;
   }
   return cudaErrorInvalidValue;

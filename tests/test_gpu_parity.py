@@ -73,6 +73,64 @@ def test_small_unfused_full_parity(wl, T):
     check_rows(rb, ob, d, wl, name=f"{wl.name} unfused T={T}")
 
 
+# K long enough (>= 256 K-blocks) that for <= 32 tokens the split-K GEMM hands
+# the last fifth of every m-tile's K-blocks out at run time
+DEEP = [
+    Workload("deep_k_ragged", T=64, K=16392, H=392, eps=1e-5, r_sigma=2.0, seed=11),
+    Workload("deep_k_gemma", T=64, K=28672, H=1024, norm_kind=1, eps=1e-6, gamma_mode="plain", seed=12),
+]
+
+
+@pytest.mark.parametrize("wl", DEEP, ids=lambda w: w.name)
+@pytest.mark.parametrize("T", [1, 9, 32, 64])
+def test_unfused_dynamic_chunks_full_parity(wl, T):
+    d = make_inputs(wl, T=T)
+    run = Run(d, wl.eps, wl.norm_kind)
+    rb, ob = run(UNFUSED)
+    check_rows(rb, ob, d, wl, name=f"{wl.name} unfused T={T}")
+    # the chunk counter returns to zero after every launch: repeats are bitwise equal
+    for _ in range(3):
+        rb2, ob2 = run(UNFUSED)
+        assert np.array_equal(rb, rb2) and np.array_equal(ob, ob2)
+
+
+def test_unfused_graph_replay_is_bitwise():
+    """The split-K path captured in a CUDA graph and replayed gives the eager
+    result on every replay (nothing of one launch is baked into the next)."""
+    import torch
+    from .gpu_util import dev_bf16, host_bits
+    wl = DEEP[0]
+    T = 16
+    d = make_inputs(wl, T=T)
+    x, W = dev_bf16(d["x"]), dev_bf16(d["W"])
+    gamma = torch.from_numpy(np.ascontiguousarray(d["gamma"], np.float32)).cuda()
+    r0 = dev_bf16(d["r0"])
+    fln.fln_set_plan(wl.K, wl.H, wl.norm_kind, UNFUSED)
+    try:
+        r = r0.clone()
+        out = torch.empty_like(r)
+        fln.fused_proj_add_rmsnorm(x, W, r, gamma, wl.eps, wl.norm_kind, 0, out)  # eager; sizes the workspace
+        fln.fln_device_status()
+        r_eager, o_eager = host_bits(r), host_bits(out)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        r.copy_(r0)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            fln.fused_proj_add_rmsnorm(x, W, r, gamma, wl.eps, wl.norm_kind, 0, out)
+        for _ in range(3):
+            r.copy_(r0)
+            out.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            fln.fln_device_status()
+            assert np.array_equal(host_bits(r), r_eager) and np.array_equal(host_bits(out), o_eager)
+    finally:
+        fln.fln_set_plan(wl.K, wl.H, wl.norm_kind, None)
+    check_rows(r_eager, o_eager, d, wl, name="graph replay")
+
+
 def test_chunk_invariance_is_bitwise():
     wl = Workload("chunks", T=700, K=256, H=512, eps=1e-5, r_sigma=2.0, seed=9)
     d = make_inputs(wl)

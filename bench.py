@@ -41,10 +41,15 @@ FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes per launch of the dominant kernel, from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, kernel,
-# tile width and the sha1 of the kernel sources the capture was taken on;
-# reported as null when the sources have changed since.
-NCU_TRAFFIC = {}
+# (dram__bytes_read.sum + dram__bytes_write.sum, one launch, -s 5 -c 1),
+# keyed by workload, tokens, kernel, plan tile width and the sha1 of the
+# kernel sources the capture was taken on; reported as null when the sources
+# have changed since.  Captures: profiles/ (same commands).
+NCU_TRAFFIC = {
+    ("llama3_8b_oproj", 4096, "gemm_fused", 256, "4d7d1fdc6e12"): 114142464 + 33394176,
+    ("llama70b_down_decode", 8, "gemm_splitk", 256, "4d7d1fdc6e12"): 471433472 + 3426304,
+    ("llama70b_oproj_decode", 8, "gemm_splitk", 256, "4d7d1fdc6e12"): 135539456 + 3152384,
+}
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -274,9 +279,10 @@ def run_gpu(args):
     for f in ("fln_gemm.cu", "fln_gemm2.cu", "fln_norm.cu", "fln_ptx.cuh"):
         h.update(open(os.path.join(ROOT, "decoder_layer_projection_gb300", "csrc", f), "rb").read())
     src_hash = h.hexdigest()[:12]
-    traffic = NCU_TRAFFIC.get((args.config, kname, plan["tile_n"], src_hash))
+    traffic = NCU_TRAFFIC.get((args.config, T, kname, plan["tile_n"], src_hash))
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kname,
+                "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
+                "kernel": kname,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback",
                 "kernel_ms_per_launch": round(avg_launch_ms, 5), "launches_per_step": launches_per_step,
                 "measured": "second timed pass of the same K steps with per-kernel CUDA events",

@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for y = x.W^T, r = r0 + y, out = RMSNorm(r).
+"""fp64 CPU oracle for y = x.W^T, r = r0 + y, out = RMSNorm(r), with bf16
+operands or FP8 (E4M3) operands and their dequantisation scales.
 
 TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
 CPU-baseline / reference leg may import this package; the library under
@@ -56,6 +57,12 @@ def _bind(path):
     lib.oracle_round_to_bf16.restype = None
     lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
     lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_double.restype = ctypes.c_double
+    lib.oracle_proj_add_rmsnorm_fp8.argtypes = [
+        p, p, ctypes.c_int, p, p, ctypes.c_int, p, p, ctypes.c_double, ctypes.c_int, L, L, L, p, L, p, p, p,
+        ctypes.c_int]
+    lib.oracle_proj_add_rmsnorm_fp8.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -128,6 +135,61 @@ def proj_add_rmsnorm(x, W, r0, gamma, eps, norm_kind, rows=None, nthreads=0):
     rc = lib.oracle_proj_add_rmsnorm(_ptr(x), _ptr(W), _ptr(r0), _ptr(gamma), float(eps),
                                      int(norm_kind), T, K, H, _ptr(rows_arr), n,
                                      _ptr(r), _ptr(o), _ptr(ms), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return r, o, ms
+
+
+def _u8(a, shape):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        raise TypeError("FP8 operands are passed as their uint8 E4M3 codes")
+    if a.shape != shape:
+        raise ValueError(f"expected shape {shape}, got {a.shape}")
+    return a
+
+
+def _scales(s, n, what):
+    s = np.ascontiguousarray(np.atleast_1d(s), dtype=np.float32)
+    if s.ndim != 1 or s.shape[0] not in (1, n):
+        raise ValueError(f"{what} must hold 1 or {n} values")
+    return s, int(s.shape[0] == n and n > 1)
+
+
+def e4m3_to_double(code: int) -> float:
+    """Value of one FP8 E4M3 code."""
+    return float(_load().oracle_e4m3_to_double(int(code) & 0xFF))
+
+
+def proj_add_rmsnorm_fp8(x, x_scale, W, w_scale, r0, gamma, eps, norm_kind, rows=None, nthreads=0):
+    """Return (r, o, ms) in float64 for FP8 operands.
+
+    x [T,K] and W [H,K] are E4M3 codes (uint8); x_scale holds 1 value (tensor)
+    or T (per token), w_scale 1 (tensor) or H (per output row of W), fp32;
+    r0 [T,H] bf16 bits; gamma [H] fp32.  y = sx * sw * sum_k x.W.
+    """
+    lib = _load()
+    T, K = np.shape(x)
+    H = np.shape(W)[0]
+    x = _u8(x, (T, K))
+    W = _u8(W, (H, K))
+    r0 = _u16(r0, (T, H))
+    sx, sx_row = _scales(x_scale, T, "x_scale")
+    sw, sw_row = _scales(w_scale, H, "w_scale")
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    if gamma.shape != (H,):
+        raise ValueError("gamma must be [H]")
+    rows_arr = None
+    n = T
+    if rows is not None:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n = rows_arr.shape[0]
+    r = np.empty((n, H), np.float64)
+    o = np.empty((n, H), np.float64)
+    ms = np.empty((n,), np.float64)
+    rc = lib.oracle_proj_add_rmsnorm_fp8(_ptr(x), _ptr(sx), sx_row, _ptr(W), _ptr(sw), sw_row, _ptr(r0),
+                                         _ptr(gamma), float(eps), int(norm_kind), T, K, H, _ptr(rows_arr), n,
+                                         _ptr(r), _ptr(o), _ptr(ms), int(nthreads))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return r, o, ms

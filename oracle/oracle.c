@@ -36,10 +36,21 @@
  * reordered beyond the definition above.  Rows are independent, so rows are
  * spread over OpenMP threads; that changes no result bit.
  *
- * Pins (tests/test_oracle.py): hand-worked 2x2, 4x4 and 1x3x2 cases, the
- * closed form of a constant row, the unit-RMS invariant, Gemma(0)==standard(1)
- * bit for bit, linearity of the residual add, eps=0 scale invariance, column
- * permutation of K, and the projection against numpy's float64 matmul.
+ * FP8 projection (the "TPSP Design" page, section 5 "To-do": "FP8 dense",
+ * quantized projections with scale handling across microchunks).  Reading:
+ * x and W hold FP8 E4M3 codes with fp32 dequantisation scales, one per tensor
+ * or one per token row of x and one per output row of W, so that
+ *   y[t,h] = sx[t] * sw[h] * sum_k e4m3(x[t,k]) * e4m3(W[h,k]);
+ * the residual add and the norm are unchanged.  A microchunk uses the scales
+ * of its own rows, so chunking changes no value.
+ *
+ * Pins (tests/test_oracle.py, tests/test_oracle_fp8.py): hand-worked 2x2, 4x4
+ * and 1x3x2 cases, the closed form of a constant row, the unit-RMS invariant,
+ * Gemma(0)==standard(1) bit for bit, linearity of the residual add, eps=0
+ * scale invariance, column permutation of K, the projection against numpy's
+ * float64 matmul; for FP8 the decoding of all 256 codes against PyTorch's
+ * float8_e4m3fn, a hand-worked scaled case, equality with the bf16 region on
+ * the same values at unit scales, and exact power-of-two scale laws.
  */
 #include <math.h>
 #include <stdint.h>
@@ -206,6 +217,78 @@ int oracle_add_rmsnorm(const uint16_t *y, const uint16_t *r0, const float *gamma
         double ms = rmsnorm_row(r, H, gamma, eps, norm_kind, o_out + t * H);
         if (ms_out)
             ms_out[t] = ms;
+    }
+    return 0;
+}
+
+/*
+ * FP8 E4M3 code -> double (the OCP 8-bit floating-point format in its "FN"
+ * form): 1 sign bit, 4 exponent bits with bias 7, 3 stored fraction bits.
+ * Exponent field 0 holds the subnormals f/8 * 2^-6; exponent field 15 with
+ * fraction 7 is the only NaN (no infinities), so the largest finite value is
+ * 1.75 * 2^8 = 448.  Every code is exact in double.
+ */
+double oracle_e4m3_to_double(uint8_t b)
+{
+    int sign = b >> 7;
+    int e = (b >> 3) & 0xF;
+    int f = b & 0x7;
+    double v;
+    if (e == 15 && f == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)f, -9);          /* (f / 8) * 2^-6 */
+    else
+        v = ldexp(8.0 + (double)f, e - 10); /* (1 + f / 8) * 2^(e - 7) */
+    return sign ? -v : v;
+}
+
+/*
+ * The region with FP8 operands.
+ *   x        [T, K] E4M3 codes, row-major
+ *   x_scale  [T] fp32 if x_per_row, else [1] (one scale for the tensor)
+ *   W        [H, K] E4M3 codes, row-major ([out, in])
+ *   w_scale  [H] fp32 if w_per_row, else [1]
+ *   the rest as in oracle_proj_add_rmsnorm.
+ * y[t,h] = sx * sw * (sum over k ascending of the exact products), in double.
+ */
+int oracle_proj_add_rmsnorm_fp8(const uint8_t *x, const float *x_scale, int x_per_row,
+                                const uint8_t *W, const float *w_scale, int w_per_row,
+                                const uint16_t *r0, const float *gamma, double eps, int norm_kind,
+                                long T, long K, long H, const long *rows, long nrows,
+                                double *r_out, double *o_out, double *ms_out, int nthreads)
+{
+    if (check_args(T, K, H, norm_kind, eps))
+        return -1;
+    if (!x_scale || !w_scale)
+        return -1;
+    long n = rows ? nrows : T;
+    for (long i = 0; rows && i < n; ++i)
+        if (rows[i] < 0 || rows[i] >= T)
+            return -1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long i = 0; i < n; ++i) {
+        long t = rows ? rows[i] : i;
+        const uint8_t *xt = x + t * K;
+        double sx = (double)x_scale[x_per_row ? t : 0];
+        double *r = r_out + i * H;
+        for (long h = 0; h < H; ++h) {
+            const uint8_t *wh = W + h * K;
+            double dot = 0.0;
+            for (long k = 0; k < K; ++k)
+                dot += oracle_e4m3_to_double(xt[k]) * oracle_e4m3_to_double(wh[k]);
+            double sw = (double)w_scale[w_per_row ? h : 0];
+            r[h] = bf16_bits_to_double(r0[t * H + h]) + sx * sw * dot;
+        }
+        double ms = rmsnorm_row(r, H, gamma, eps, norm_kind, o_out + i * H);
+        if (ms_out)
+            ms_out[i] = ms;
     }
     return 0;
 }

@@ -29,6 +29,12 @@ import numpy as np
 BLOCK = 1 << 20
 
 STREAM_X, STREAM_U, STREAM_W, STREAM_R, STREAM_GAMMA = 0, 1, 2, 3, 4
+STREAM_X8, STREAM_W8, STREAM_SX, STREAM_SW = 5, 6, 7, 8
+
+# FP8 operands are drawn as values of spread FP8_SPREAD and stored as E4M3
+# codes (see _fill_e4m3); the dequantisation scales bring them back to the
+# bf16 workloads' spreads.
+FP8_SPREAD = 16.0
 
 NORM_STANDARD = 0
 NORM_GEMMA = 1
@@ -62,10 +68,13 @@ class Workload:
     def flops(self) -> float:
         return 2.0 * self.T * self.K * self.H
 
-    def algorithmic_bytes(self) -> float:
-        """x read + W read once + residual read and written + out written + gamma."""
+    def algorithmic_bytes(self, operand_bytes: int = 2) -> float:
+        """x read + W read once + residual read and written + out written + gamma
+        (operand_bytes = 1 for FP8 x and W, whose scales add 4T + 4H at most)."""
         T, K, H = self.T, self.K, self.H
-        return 2.0 * T * K + 2.0 * H * K + 4.0 * T * H + 2.0 * T * H + 4.0 * H
+        b = float(operand_bytes)
+        extra = 4.0 * T + 4.0 * H if operand_bytes == 1 else 0.0
+        return b * T * K + b * H * K + 4.0 * T * H + 2.0 * T * H + 4.0 * H + extra
 
 
 CONFIGS = {
@@ -175,3 +184,72 @@ def make_inputs(wl: Workload, seed: int | None = None, T: int | None = None):
         raise ValueError(wl.gamma_mode)
     gamma = g.astype(np.float32)
     return {"x": x, "W": W, "r0": r0, "gamma": gamma}
+
+
+def _fill_e4m3(out: np.ndarray, seed: int, stream: int, spread: float):
+    """Codes of FP8 E4M3 values drawn as N(0, spread^2).
+
+    A drawn value v is stored by truncation toward zero to an E4M3 code: the
+    sign bit, the exponent field floor(log2|v|) + 7 (0 below 2^-6, where the
+    3-bit fraction counts units of 2^-9), and the top three fraction bits,
+    clamped below the largest finite code 0x7E; the NaN codes 0x7F/0xFF never
+    occur.
+    """
+    flat = out.reshape(-1)
+    n = flat.size
+    nb = (n + BLOCK - 1) // BLOCK
+    gens = _block_gens(seed, stream, nb)
+
+    def work(i):
+        s, e = i * BLOCK, min(n, (i + 1) * BLOCK)
+        v = gens[i].standard_normal(e - s) * spread
+        a = np.abs(v)
+        with np.errstate(divide="ignore"):
+            ex = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+        normal = (a >= 2.0 ** -6)
+        ef = np.clip(ex + 7, 1, 15)
+        frac_n = np.floor((a / np.exp2(ef - 7) - 1.0) * 8.0)
+        frac_s = np.floor(a / 2.0 ** -9)
+        frac = np.clip(np.where(normal, frac_n, frac_s), 0, 7)
+        efield = np.where(normal, ef, 0)
+        code = (efield.astype(np.int64) << 3) | frac.astype(np.int64)
+        code = np.minimum(code, 0x7E)
+        code |= (v < 0).astype(np.int64) << 7
+        flat[s:e] = code.astype(np.uint8)
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(work, range(nb)))
+
+
+def make_inputs_fp8(wl: Workload, seed: int | None = None, T: int | None = None,
+                    x_scale_per_token: bool = True, w_scale_per_channel: bool = True):
+    """FP8 operands for a workload: dict(x8=[T,K] u8, x_scale=[T] or [1] f32,
+    W8=[H,K] u8, w_scale=[H] or [1] f32, r0=[T,H] u16, gamma=[H] f32).
+
+    x8 and W8 are E4M3 codes of N(0, FP8_SPREAD^2) draws; the scales are
+    1/FP8_SPREAD (x) and 1/(FP8_SPREAD sqrt(K)) (W) times 2^u, u ~ U(-1/2, 1/2)
+    per token / per output row (per-tensor: u = 0), so the dequantised
+    operands have the bf16 workload's spreads.  r0 and gamma are the bf16
+    workload's tensors (same streams).
+    """
+    seed = wl.seed if seed is None else int(seed)
+    T = wl.T if T is None else int(T)
+    K, H = wl.K, wl.H
+    base = make_inputs(wl, seed=seed, T=T)
+    x8 = np.empty((T, K), np.uint8)
+    _fill_e4m3(x8, seed, STREAM_X8, FP8_SPREAD)
+    W8 = np.empty((H, K), np.uint8)
+    _fill_e4m3(W8, seed, STREAM_W8, FP8_SPREAD)
+    sx0 = 1.0 / FP8_SPREAD
+    sw0 = 1.0 / (FP8_SPREAD * math.sqrt(K))
+    if x_scale_per_token:
+        u = _block_gens(seed, STREAM_SX, 1)[0].uniform(-0.5, 0.5, T)
+        x_scale = (sx0 * np.exp2(u)).astype(np.float32)
+    else:
+        x_scale = np.array([sx0], np.float32)
+    if w_scale_per_channel:
+        u = _block_gens(seed, STREAM_SW, 1)[0].uniform(-0.5, 0.5, H)
+        w_scale = (sw0 * np.exp2(u)).astype(np.float32)
+    else:
+        w_scale = np.array([sw0], np.float32)
+    return {"x8": x8, "x_scale": x_scale, "W8": W8, "w_scale": w_scale, "r0": base["r0"], "gamma": base["gamma"]}

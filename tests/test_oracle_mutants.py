@@ -12,6 +12,7 @@ import pytest
 import oracle
 
 from . import test_oracle as pins
+from . import test_oracle_fp8 as fp8pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -35,6 +36,15 @@ MUTANTS = {
                          "r[h] = bf16_bits_to_double(r0[t * H + h]);"),
     "round_truncates": ("double qi = nearbyint(q);", "double qi = trunc(q);"),
     "round_ties_away": ("double qi = nearbyint(q);", "double qi = round(q);"),
+    "e4m3_bias_8": ("v = ldexp(8.0 + (double)f, e - 10);", "v = ldexp(8.0 + (double)f, e - 11);"),
+    "e4m3_subnormal_unit": ("v = ldexp((double)f, -9);", "v = ldexp((double)f, -10);"),
+    "e4m3_no_nan": ("    if (e == 15 && f == 7)\n        return NAN;\n", ""),
+    "e4m3_sign_dropped": ("return sign ? -v : v;", "return v;"),
+    "fp8_w_scale_by_token": ("double sw = (double)w_scale[w_per_row ? h : 0];",
+                             "double sw = (double)w_scale[w_per_row ? (t % H) : 0];"),
+    "fp8_x_scale_ignored": ("r[h] = bf16_bits_to_double(r0[t * H + h]) + sx * sw * dot;",
+                            "r[h] = bf16_bits_to_double(r0[t * H + h]) + sw * dot;"),
+    "fp8_x_scale_first_row": ("double sx = (double)x_scale[x_per_row ? t : 0];", "double sx = (double)x_scale[0];"),
 }
 
 
@@ -43,6 +53,14 @@ def _pin_calls():
     for name in dir(pins):
         if name.startswith("test_") and name != "test_hand_worked_cases":
             calls.append((name, getattr(pins, name)))
+    # FP8 pins (parametrized ones called with each of their parameters)
+    for code, value in [(0x38, 1.0), (0x7E, 448.0), (0x08, 2.0 ** -6), (0x01, 2.0 ** -9), (0xB8, -1.0)]:
+        calls.append((f"fp8.format_facts[{code:#x}]", lambda c=code, v=value: fp8pins.test_format_facts(c, v)))
+    for kind in (0, 1):
+        calls.append((f"fp8.unit_scales[{kind}]", lambda k=kind: fp8pins.test_unit_scales_equal_bf16_region(k)))
+    for name in dir(fp8pins):
+        if name.startswith("test_") and name not in ("test_format_facts", "test_unit_scales_equal_bf16_region"):
+            calls.append(("fp8." + name, getattr(fp8pins, name)))
     return calls
 
 

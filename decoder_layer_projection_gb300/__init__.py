@@ -31,13 +31,17 @@ PATH_FUSED = 1
 PATH_PIPELINED = 2
 PATH_UNFUSED = 3
 
+DTYPE_BF16 = 0
+DTYPE_E4M3 = 1
+
 KERNEL_NAMES = ("gemm_fused", "gemm_slot", "gemm_splitk", "norm_bf16", "norm_slot", "norm_splitk")
 
 EXPORTED_SYMBOLS = (
     "fused_proj_add_rmsnorm", "add_rmsnorm", "fln_autotune", "fln_set_overrides", "fln_set_plan",
     "fln_get_plan", "fln_device_status", "fln_last_error", "fln_release_workspace", "fln_launch_count",
     "fln_profile_enable", "fln_profile_read", "fln_version", "fused_proj_add_rmsnorm_noalloc",
-    "fln_debug_stall_next_call",
+    "fln_debug_stall_next_call", "fused_proj_add_rmsnorm_fp8", "fln_autotune_dtype", "fln_set_plan_dtype",
+    "fln_get_plan_dtype",
 )
 
 
@@ -110,6 +114,14 @@ def load(path: str | None = None):
         lib.fln_debug_stall_next_call.restype = i
         lib.fused_proj_add_rmsnorm_noalloc.argtypes = [vp, vp, vp, vp, f, i, i, i, i, vp, vp, vp]
         lib.fused_proj_add_rmsnorm_noalloc.restype = i
+        lib.fused_proj_add_rmsnorm_fp8.argtypes = [vp, vp, i, vp, vp, i, vp, vp, f, i, i, i, i, i, vp, vp]
+        lib.fused_proj_add_rmsnorm_fp8.restype = i
+        lib.fln_autotune_dtype.argtypes = [i, i, i, i, i, vp]
+        lib.fln_autotune_dtype.restype = i
+        lib.fln_set_plan_dtype.argtypes = [i, i, i, i, ctypes.POINTER(Plan)]
+        lib.fln_set_plan_dtype.restype = i
+        lib.fln_get_plan_dtype.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Plan)]
+        lib.fln_get_plan_dtype.restype = i
         _lib = lib
         return lib
 
@@ -178,6 +190,28 @@ def fused_proj_add_rmsnorm_noalloc_ptr(x_ptr, W_ptr, residual_ptr, gamma_ptr, ep
                                                  device_error_ptr, stream_ptr)
 
 
+def fused_proj_add_rmsnorm_fp8(x, x_scale, W, w_scale, residual, gamma, eps: float,
+                               norm_kind: int = NORM_STANDARD, microchunk_tokens: int = 0, out=None, stream=None):
+    """FP8 operands: residual += (x . W^T) * x_scale * w_scale; out = RMSNorm(residual).
+    x [T,K] and W [H,K] hold E4M3 codes (torch.uint8 or torch.float8_e4m3fn);
+    x_scale fp32 with T values (per token) or 1 (tensor); w_scale fp32 with H
+    values (per output row of W) or 1.  Returns out."""
+    T, K = x.shape
+    H = W.shape[0]
+    if out is None:
+        import torch
+        out = torch.empty((T, H), dtype=residual.dtype, device=residual.device)
+    x_per_token = 1 if (x_scale.numel() == T and T > 1) else 0
+    w_per_channel = 1 if (w_scale.numel() == H and H > 1) else 0
+    if x_scale.numel() not in (1, T) or w_scale.numel() not in (1, H):
+        raise ValueError("x_scale must hold 1 or T values and w_scale 1 or H values")
+    _check(load().fused_proj_add_rmsnorm_fp8(_ptr(x), _ptr(x_scale), x_per_token, _ptr(W), _ptr(w_scale),
+                                             w_per_channel, _ptr(residual), _ptr(gamma), float(eps),
+                                             int(norm_kind), int(T), int(K), int(H), int(microchunk_tokens),
+                                             _ptr(out), _stream_ptr(stream)))
+    return out
+
+
 def add_rmsnorm(y, residual, gamma, eps: float, norm_kind: int = NORM_STANDARD, out=None, stream=None):
     """residual += y; out = RMSNorm(residual).  y, residual, out [T,H] bf16; gamma [H] fp32."""
     T, H = y.shape
@@ -194,23 +228,27 @@ def add_rmsnorm_ptr(y_ptr, residual_ptr, gamma_ptr, eps, norm_kind, T, H, out_pt
                               out_ptr, stream_ptr)
 
 
-def fln_autotune(K: int, H: int, norm_kind: int, max_tokens: int, stream=None):
-    _check(load().fln_autotune(int(K), int(H), int(norm_kind), int(max_tokens), _stream_ptr(stream)))
+def fln_autotune(K: int, H: int, norm_kind: int, max_tokens: int, stream=None, dtype: int = DTYPE_BF16):
+    _check(load().fln_autotune_dtype(int(K), int(H), int(norm_kind), int(dtype), int(max_tokens),
+                                     _stream_ptr(stream)))
 
 
 def fln_set_overrides(microchunk_tokens: int = 0, threshold_tokens: int = 0):
     _check(load().fln_set_overrides(int(microchunk_tokens), int(threshold_tokens)))
 
 
-def fln_set_plan(K: int, H: int, norm_kind: int, plan: Plan | dict | None):
+def fln_set_plan(K: int, H: int, norm_kind: int, plan: Plan | dict | None, dtype: int = DTYPE_BF16):
     if isinstance(plan, dict):
         plan = Plan(**plan)
-    _check(load().fln_set_plan(int(K), int(H), int(norm_kind), ctypes.byref(plan) if plan is not None else None))
+    _check(load().fln_set_plan_dtype(int(K), int(H), int(norm_kind), int(dtype),
+                                     ctypes.byref(plan) if plan is not None else None))
 
 
-def fln_get_plan(K: int, H: int, norm_kind: int, T: int, microchunk_tokens: int = 0) -> dict:
+def fln_get_plan(K: int, H: int, norm_kind: int, T: int, microchunk_tokens: int = 0,
+                 dtype: int = DTYPE_BF16) -> dict:
     p = Plan()
-    _check(load().fln_get_plan(int(K), int(H), int(norm_kind), int(T), int(microchunk_tokens), ctypes.byref(p)))
+    _check(load().fln_get_plan_dtype(int(K), int(H), int(norm_kind), int(dtype), int(T), int(microchunk_tokens),
+                                     ctypes.byref(p)))
     return p.as_dict()
 
 

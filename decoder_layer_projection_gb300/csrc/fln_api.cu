@@ -26,6 +26,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "fln_internal.h"
@@ -85,16 +86,18 @@ struct Workspace {
   cudaEvent_t ev_free[3] = {};
   cudaEvent_t ev_join = nullptr;
   unsigned int gen = 0;
-  bool prepared[3][5] = {};
-  int pair_max[4] = {0, 0, 0, 0};  // resident CTA pairs of the fused pair kernel, tile 128 / 192 / 224 / 256
+  bool prepared[2][3][5] = {};     // [operand type][epilogue][tile]
+  int pair_max[2][4] = {};         // resident CTA pairs of the fused pair kernel, [operand type][tile 128/192/224/256]
 };
 
 std::mutex g_mu;
 std::map<int, Workspace*> g_ws;
 
 struct GroupKey {
-  int K, H, kind;
-  bool operator<(const GroupKey& o) const { return std::tie(K, H, kind) < std::tie(o.K, o.H, o.kind); }
+  int K, H, kind, dtype;
+  bool operator<(const GroupKey& o) const {
+    return std::tie(K, H, kind, dtype) < std::tie(o.K, o.H, o.kind, o.dtype);
+  }
 };
 std::map<GroupKey, fln_plan> g_plans;
 int g_override_chunk = 0;
@@ -178,28 +181,28 @@ int grow(T** p, size_t* cur, size_t need, bool zero, const char* what) {
   return FLN_OK;
 }
 
-int prepare_kernel(Workspace* ws, int bn, EpilogueKind epi) {
+int prepare_kernel(Workspace* ws, int bn, EpilogueKind epi, int f8) {
   const int bi = bn_index(bn);
   if (bi < 0) return fail(FLN_ERR_UNSUPPORTED, "tile width %d", bn);
-  if (!ws->prepared[epi][bi]) {
-    FLN_CUDA(gemm_prepare(bn, epi), "cudaFuncSetAttribute(max dynamic shared memory)");
-    ws->prepared[epi][bi] = true;
+  if (!ws->prepared[f8][epi][bi]) {
+    FLN_CUDA(gemm_prepare(bn, epi, f8), "cudaFuncSetAttribute(max dynamic shared memory)");
+    ws->prepared[f8][epi][bi] = true;
   }
   return FLN_OK;
 }
 
 int pair_index(int bn) { return bn == 128 ? 0 : bn == 192 ? 1 : bn == 224 ? 2 : bn == 256 ? 3 : -1; }
 
-int prepare_pair(Workspace* ws, int bn, int* max_pairs) {
+int prepare_pair(Workspace* ws, int bn, int f8, int* max_pairs) {
   const int i = pair_index(bn);
   if (i < 0) return fail(FLN_ERR_UNSUPPORTED, "fused tile width %d", bn);
-  if (ws->pair_max[i] == 0) {
+  if (ws->pair_max[f8][i] == 0) {
     int mp = 0;
-    FLN_CUDA(pair_gemm_prepare(bn, &mp), "pair kernel set-up (shared memory limit, resident clusters)");
+    FLN_CUDA(pair_gemm_prepare(bn, f8, &mp), "pair kernel set-up (shared memory limit, resident clusters)");
     if (mp < 1) return fail(FLN_ERR_UNSUPPORTED, "no CTA pair of the fused kernel fits on this device");
-    ws->pair_max[i] = mp;
+    ws->pair_max[f8][i] = mp;
   }
-  *max_pairs = ws->pair_max[i];
+  *max_pairs = ws->pair_max[f8][i];
   return FLN_OK;
 }
 
@@ -235,16 +238,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [rows, inner] (inner contiguous) read in boxes of
-// 64 x box_rows elements with 128-byte swizzle; out-of-range elements read 0.
-int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+// 2-D tensor [rows, inner] (inner contiguous) of bf16 (esize 2) or E4M3
+// codes (esize 1) read in boxes of 128 bytes x box_rows with 128-byte
+// swizzle; out-of-range elements read 0.
+int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows, int esize = 2) {
   auto enc = encode_fn();
   if (!enc) return fail(FLN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint64_t strides[1] = {inner * static_cast<uint64_t>(esize)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  const CUtensorMapDataType dt = esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FLN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
@@ -252,8 +257,8 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, ui
 }
 
 struct Call {
-  const __nv_bfloat16* x;
-  const __nv_bfloat16* W;
+  const void* x;  // [T, K] bf16, or E4M3 codes when f8
+  const void* W;  // [H, K] bf16, or E4M3 codes when f8
   __nv_bfloat16* residual;
   const float* gamma;
   float eps;
@@ -261,7 +266,21 @@ struct Call {
   int T, K, H;
   __nv_bfloat16* out;
   cudaStream_t stream;
+  int f8 = 0;                  // E4M3 operands with dequantisation scales
+  const float* x_scale = nullptr;
+  int x_scale_stride = 0;      // 1: per token, 0: per tensor
+  const float* w_scale = nullptr;
+  int w_scale_stride = 0;      // 1: per output row of W, 0: per tensor
+  int esize() const { return f8 ? 1 : 2; }
+  int k_blocks() const { return (K + kblock_elems(f8) - 1) / kblock_elems(f8); }
 };
+
+void set_scales(GemmParams& p, const Call& c) {
+  p.x_scale = c.x_scale;
+  p.x_scale_stride = c.x_scale_stride;
+  p.w_scale = c.w_scale;
+  p.w_scale_stride = c.w_scale_stride;
+}
 
 int round_bn_tokens(int T) {
   if (T <= 16) return 16;
@@ -274,11 +293,11 @@ int round_bn_tokens(int T) {
 // T <= 256: split-K GEMM with H on the MMA's M side, then reduce + add + norm.
 int run_unfused(Workspace* ws, const Call& c) {
   const int bn = round_bn_tokens(c.T);
-  int rc = prepare_kernel(ws, bn, EPI_SPLITK_SWAP);
+  int rc = prepare_kernel(ws, bn, EPI_SPLITK_SWAP, c.f8);
   if (rc) return rc;
   CUtensorMap tmA, tmB;
-  if ((rc = make_map(&tmA, c.W, c.K, c.H, 128))) return rc;
-  if ((rc = make_map(&tmB, c.x, c.K, c.T, bn))) return rc;
+  if ((rc = make_map(&tmA, c.W, c.K, c.H, 128, c.esize()))) return rc;
+  if ((rc = make_map(&tmB, c.x, c.K, c.T, bn, c.esize()))) return rc;
   GemmParams p{};
   p.M = c.H;
   p.N = c.T;
@@ -286,7 +305,7 @@ int run_unfused(Workspace* ws, const Call& c) {
   p.a_row0 = 0;
   p.num_m_tiles = (c.H + 127) / 128;
   p.num_n_tiles = 1;
-  p.num_k_blocks = (c.K + 63) / 64;
+  p.num_k_blocks = c.k_blocks();
   // Dynamic balancing: CTAs finish their static share at different times
   // (about +-10 % around the median), so about a fifth of each m-tile's
   // K-blocks (the last ones) is handed out at run time in chunks of >= 4
@@ -296,7 +315,7 @@ int run_unfused(Workspace* ws, const Call& c) {
   // 1-32 tokens, a loss at 64; no gain at K = 8192.
   const int KB = p.num_k_blocks;
   int kc = 0, cpm = 0;
-  if (c.T <= 32 && KB >= 256) {
+  if (c.T <= 32 && c.K >= 16384) {
     const double kd = 0.2 * KB;
     kc = std::max(4, static_cast<int>(std::ceil(kd / 8.0)));
     cpm = std::min(8, std::max(1, static_cast<int>(std::lround(kd / kc))));
@@ -336,7 +355,7 @@ int run_unfused(Workspace* ws, const Call& c) {
   p.err = ws->err_word;
   p.dyn_counter = ws->dyn_counter;
   rc = launch_counted(FLN_KERNEL_GEMM_SPLITK, c.stream,
-                      [&] { return launch_gemm(EPI_SPLITK_SWAP, bn, tmA, tmB, p, G, c.stream); },
+                      [&] { return launch_gemm(EPI_SPLITK_SWAP, bn, c.f8, tmA, tmB, p, G, c.stream); },
                       "split-K GEMM launch");
   if (rc) return rc;
   NormParams np{};
@@ -356,6 +375,12 @@ int run_unfused(Workspace* ws, const Call& c) {
   np.row0 = 0;
   np.H = c.H;
   np.pdl = g_prof ? 0 : 1;  // timing events between the two launches would break the overlap
+  if (c.f8) {
+    np.x_scale = c.x_scale;
+    np.x_scale_stride = c.x_scale_stride;
+    np.w_scale = c.w_scale;
+    np.w_scale_stride = c.w_scale_stride;
+  }
   return launch_counted(FLN_KERNEL_NORM_SPLITK, c.stream,
                         [&] { return launch_add_rmsnorm(NORM_SRC_SPLITK, np, 0, c.stream); },
                         "split-K add+norm launch");
@@ -370,11 +395,11 @@ int gemm_grid(Workspace* ws, const fln_plan& pl, long long tiles) {
 int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
   const int bn = pl.tile_n;
   int max_pairs = 0;
-  int rc = prepare_pair(ws, bn, &max_pairs);
+  int rc = prepare_pair(ws, bn, c.f8, &max_pairs);
   if (rc) return rc;
   CUtensorMap tmA, tmB;
-  if ((rc = make_map(&tmA, c.x, c.K, c.T, 128))) return rc;
-  if ((rc = make_map(&tmB, c.W, c.K, c.H, bn / 2))) return rc;
+  if ((rc = make_map(&tmA, c.x, c.K, c.T, 128, c.esize()))) return rc;
+  if ((rc = make_map(&tmB, c.W, c.K, c.H, bn / 2, c.esize()))) return rc;
   const int chunk = std::min(pl.microchunk_tokens, c.T);
   const int mt_alloc = 2 * ((chunk + 255) / 256);  // 128-row blocks, rounded up to whole pairs
   const int nt = (c.H + bn - 1) / bn;
@@ -398,7 +423,8 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     p.a_row0 = c0;
     p.num_m_tiles = (n + 127) / 128;
     p.num_n_tiles = nt;
-    p.num_k_blocks = (c.K + 63) / 64;
+    p.num_k_blocks = c.k_blocks();
+    set_scales(p, c);
     p.residual = c.residual;
     p.out = c.out;
     p.gamma = c.gamma;
@@ -418,7 +444,7 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     if (pl.gemm_ctas > 0) pairs = std::min(pairs, std::max(1, pl.gemm_ctas / 2));
     pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(pairs, tiles)));
     rc = launch_counted(FLN_KERNEL_GEMM_FUSED, c.stream,
-                        [&] { return launch_gemm_pair_fused(bn, tmA, tmB, tmR, tmRs, tmOs, p, pairs, c.stream); },
+                        [&] { return launch_gemm_pair_fused(bn, c.f8, tmA, tmB, tmR, tmRs, tmOs, p, pairs, c.stream); },
                         "fused pair GEMM launch");
     if (rc) return rc;
   }
@@ -429,11 +455,11 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
 // the library's second stream; three slots guarded by events.
 int run_pipelined(Workspace* ws, const Call& c, const fln_plan& pl) {
   const int bn = pl.tile_n;
-  int rc = prepare_kernel(ws, bn, EPI_STORE_F32);
+  int rc = prepare_kernel(ws, bn, EPI_STORE_F32, c.f8);
   if (rc) return rc;
   CUtensorMap tmA, tmB;
-  if ((rc = make_map(&tmA, c.x, c.K, c.T, 128))) return rc;
-  if ((rc = make_map(&tmB, c.W, c.K, c.H, bn))) return rc;
+  if ((rc = make_map(&tmA, c.x, c.K, c.T, 128, c.esize()))) return rc;
+  if ((rc = make_map(&tmB, c.W, c.K, c.H, bn, c.esize()))) return rc;
   const int chunk = std::min(pl.microchunk_tokens, c.T);
   const size_t slot_need = static_cast<size_t>(chunk) * c.H;
   if (slot_need > ws->slot_floats) {
@@ -460,13 +486,14 @@ int run_pipelined(Workspace* ws, const Call& c, const fln_plan& pl) {
     p.a_row0 = c0;
     p.num_m_tiles = (n + 127) / 128;
     p.num_n_tiles = nt;
-    p.num_k_blocks = (c.K + 63) / 64;
+    p.num_k_blocks = c.k_blocks();
+    set_scales(p, c);
     p.ld = c.H;
     p.yout = ws->slots[s];
     p.err = ws->err_word;
     const int G = gemm_grid(ws, pl, static_cast<long long>(p.num_m_tiles) * nt);
     rc = launch_counted(FLN_KERNEL_GEMM_SLOT, c.stream,
-                        [&] { return launch_gemm(EPI_STORE_F32, bn, tmA, tmB, p, G, c.stream); },
+                        [&] { return launch_gemm(EPI_STORE_F32, bn, c.f8, tmA, tmB, p, G, c.stream); },
                         "slot GEMM launch");
     if (rc) return rc;
     FLN_CUDA(cudaEventRecord(ws->ev_ready[s], c.stream), "cudaEventRecord(slot ready)");
@@ -552,8 +579,8 @@ int check_plan(const fln_plan& p) {
 
 // The plan for a call: group plan (or default), then global overrides, then
 // the call's own microchunk; below the threshold the UNFUSED path.
-int resolve_plan(int K, int H, int kind, int T, int chunk_arg, fln_plan* out) {
-  auto it = g_plans.find({K, H, kind});
+int resolve_plan(int K, int H, int kind, int dtype, int T, int chunk_arg, fln_plan* out) {
+  auto it = g_plans.find({K, H, kind, dtype});
   fln_plan p = it != g_plans.end() ? it->second : default_plan();
   if (g_override_chunk > 0) p.microchunk_tokens = g_override_chunk;
   if (g_override_threshold > 0) p.threshold_tokens = g_override_threshold;
@@ -601,6 +628,31 @@ int validate_fused(const fln_bf16* x, const fln_bf16* W, fln_bf16* residual, con
   return FLN_OK;
 }
 
+int validate_fp8(const uint8_t* x, const float* x_scale, int x_per_token, const uint8_t* W, const float* w_scale,
+                 int w_per_channel, fln_bf16* residual, const float* gamma, float eps, int kind, int T, int K, int H,
+                 int chunk, fln_bf16* out) {
+  int rc = check_common(eps, kind, T, H);
+  if (rc) return rc;
+  if (K < 16 || (K & 15)) return fail(FLN_ERR_INVALID_ARG, "K=%d must be a positive multiple of 16 for FP8", K);
+  if (K > kMaxK) return fail(FLN_ERR_UNSUPPORTED, "K=%d above the supported %d", K, kMaxK);
+  if (chunk < 0 || chunk > kMaxMicrochunk)
+    return fail(FLN_ERR_INVALID_ARG, "microchunk_tokens=%d outside 0..%d", chunk, kMaxMicrochunk);
+  if (T == 0) return FLN_OK;
+  if ((rc = check_ptr("x", x)) || (rc = check_ptr("W", W)) || (rc = check_ptr("x_scale", x_scale)) ||
+      (rc = check_ptr("w_scale", w_scale)) || (rc = check_ptr("residual", residual)) ||
+      (rc = check_ptr("gamma", gamma)) || (rc = check_ptr("out", out)))
+    return rc;
+  const size_t bx = size_t(T) * K, bw = size_t(H) * K, br = size_t(T) * H * 2, bg = size_t(H) * 4;
+  const size_t bsx = (x_per_token ? size_t(T) : 1) * 4, bsw = (w_per_channel ? size_t(H) : 1) * 4;
+  if (overlaps(out, br, x, bx) || overlaps(out, br, W, bw) || overlaps(out, br, residual, br) ||
+      overlaps(out, br, gamma, bg) || overlaps(out, br, x_scale, bsx) || overlaps(out, br, w_scale, bsw))
+    return fail(FLN_ERR_INVALID_ARG, "out overlaps an input");
+  if (overlaps(residual, br, x, bx) || overlaps(residual, br, W, bw) || overlaps(residual, br, gamma, bg) ||
+      overlaps(residual, br, x_scale, bsx) || overlaps(residual, br, w_scale, bsw))
+    return fail(FLN_ERR_INVALID_ARG, "residual overlaps x, W, gamma or a scale");
+  return FLN_OK;
+}
+
 // ------------------------------------------------------------------ tuner
 __global__ void fill_pseudo_normal(__nv_bfloat16* p, size_t n, uint32_t seed, float scale, float shift) {
   for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x) {
@@ -616,6 +668,23 @@ __global__ void fill_pseudo_normal(__nv_bfloat16* p, size_t n, uint32_t seed, fl
       s += static_cast<float>(h >> 8) * (1.0f / 16777216.0f);
     }
     p[i] = __float2bfloat16_rn((s - 2.0f) * 1.7320508f * scale + shift);
+  }
+}
+
+// E4M3 codes of the same pseudo-normal values (the tuner's FP8 inputs)
+__global__ void fill_pseudo_e4m3(uint8_t* p, size_t n, uint32_t seed, float scale) {
+  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x) {
+    float s = 0.f;
+    uint32_t h = static_cast<uint32_t>(i) * 0x9E3779B1u ^ seed ^ static_cast<uint32_t>(i >> 32) * 0x85EBCA77u;
+    for (int k = 0; k < 4; ++k) {
+      h ^= h >> 16;
+      h *= 0x7FEB352Du;
+      h ^= h >> 15;
+      h *= 0x846CA68Bu;
+      h ^= h >> 16;
+      s += static_cast<float>(h >> 8) * (1.0f / 16777216.0f);
+    }
+    p[i] = static_cast<uint8_t>(__nv_cvt_float_to_fp8((s - 2.0f) * 1.7320508f * scale, __NV_SATFINITE, __NV_E4M3));
   }
 }
 
@@ -719,7 +788,7 @@ int noalloc_setup(NoAllocDevice** out) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
-    FLN_CUDA(gemm_prepare(kNoAllocTile, EPI_FUSED_NORM), "cudaFuncSetAttribute(max dynamic shared memory)");
+    FLN_CUDA(gemm_prepare(kNoAllocTile, EPI_FUSED_NORM, 0), "cudaFuncSetAttribute(max dynamic shared memory)");
     d.scratch = static_cast<unsigned char*>(p);
     d.sms = sms;
     d.ready = true;
@@ -741,12 +810,35 @@ int fused_proj_add_rmsnorm(const fln_bf16* x, const fln_bf16* W, fln_bf16* resid
   if (rc) return rc;
   if (T == 0) return FLN_OK;
   fln_plan pl;
-  if ((rc = resolve_plan(K, H, norm_kind, T, microchunk_tokens, &pl))) return rc;
+  if ((rc = resolve_plan(K, H, norm_kind, FLN_DTYPE_BF16, T, microchunk_tokens, &pl))) return rc;
   Workspace* ws = nullptr;
   if ((rc = get_ws(&ws))) return rc;
   Call c{reinterpret_cast<const __nv_bfloat16*>(x), reinterpret_cast<const __nv_bfloat16*>(W),
          reinterpret_cast<__nv_bfloat16*>(residual), gamma, eps, norm_kind, T, K, H,
          reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<cudaStream_t>(stream)};
+  return run_plan(ws, c, pl);
+}
+
+int fused_proj_add_rmsnorm_fp8(const uint8_t* x, const float* x_scale, int x_scale_per_token, const uint8_t* W,
+                               const float* w_scale, int w_scale_per_channel, fln_bf16* residual,
+                               const float* gamma, float eps, int norm_kind, int T, int K, int H,
+                               int microchunk_tokens, fln_bf16* out, fln_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = validate_fp8(x, x_scale, x_scale_per_token, W, w_scale, w_scale_per_channel, residual, gamma, eps,
+                        norm_kind, T, K, H, microchunk_tokens, out);
+  if (rc) return rc;
+  if (T == 0) return FLN_OK;
+  fln_plan pl;
+  if ((rc = resolve_plan(K, H, norm_kind, FLN_DTYPE_E4M3, T, microchunk_tokens, &pl))) return rc;
+  Workspace* ws = nullptr;
+  if ((rc = get_ws(&ws))) return rc;
+  Call c{x, W, reinterpret_cast<__nv_bfloat16*>(residual), gamma, eps, norm_kind, T, K, H,
+         reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<cudaStream_t>(stream)};
+  c.f8 = 1;
+  c.x_scale = x_scale;
+  c.x_scale_stride = x_scale_per_token ? 1 : 0;
+  c.w_scale = w_scale;
+  c.w_scale_stride = w_scale_per_channel ? 1 : 0;
   return run_plan(ws, c, pl);
 }
 
@@ -792,33 +884,51 @@ int fln_set_overrides(int microchunk_tokens, int threshold_tokens) {
   return FLN_OK;
 }
 
-int fln_set_plan(int K, int H, int norm_kind, const fln_plan* plan) {
+int fln_set_plan_dtype(int K, int H, int norm_kind, int dtype, const fln_plan* plan) {
   std::lock_guard<std::mutex> lk(g_mu);
-  if (K < 8 || (K & 7) || H < 8 || (H & 7) || (norm_kind != 0 && norm_kind != 1))
-    return fail(FLN_ERR_INVALID_ARG, "bad group (K=%d, H=%d, kind=%d)", K, H, norm_kind);
+  if (K < 8 || (K & 7) || H < 8 || (H & 7) || (norm_kind != 0 && norm_kind != 1) ||
+      (dtype != FLN_DTYPE_BF16 && dtype != FLN_DTYPE_E4M3))
+    return fail(FLN_ERR_INVALID_ARG, "bad group (K=%d, H=%d, kind=%d, dtype=%d)", K, H, norm_kind, dtype);
   if (!plan) {
-    g_plans.erase({K, H, norm_kind});
+    g_plans.erase({K, H, norm_kind, dtype});
     return FLN_OK;
   }
   int rc = check_plan(*plan);
   if (rc) return rc;
-  g_plans[{K, H, norm_kind}] = *plan;
+  g_plans[{K, H, norm_kind, dtype}] = *plan;
   return FLN_OK;
 }
 
-int fln_get_plan(int K, int H, int norm_kind, int T, int microchunk_tokens, fln_plan* plan) {
+int fln_set_plan(int K, int H, int norm_kind, const fln_plan* plan) {
+  return fln_set_plan_dtype(K, H, norm_kind, FLN_DTYPE_BF16, plan);
+}
+
+int fln_get_plan_dtype(int K, int H, int norm_kind, int dtype, int T, int microchunk_tokens, fln_plan* plan) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!plan) return fail(FLN_ERR_INVALID_ARG, "plan is NULL");
+  if (dtype != FLN_DTYPE_BF16 && dtype != FLN_DTYPE_E4M3) return fail(FLN_ERR_INVALID_ARG, "dtype=%d", dtype);
   if (microchunk_tokens < 0 || microchunk_tokens > kMaxMicrochunk)
     return fail(FLN_ERR_INVALID_ARG, "microchunk_tokens=%d outside 0..%d", microchunk_tokens, kMaxMicrochunk);
-  return resolve_plan(K, H, norm_kind, T, microchunk_tokens, plan);
+  return resolve_plan(K, H, norm_kind, dtype, T, microchunk_tokens, plan);
+}
+
+int fln_get_plan(int K, int H, int norm_kind, int T, int microchunk_tokens, fln_plan* plan) {
+  return fln_get_plan_dtype(K, H, norm_kind, FLN_DTYPE_BF16, T, microchunk_tokens, plan);
 }
 
 int fln_autotune(int K, int H, int norm_kind, int max_tokens, fln_stream_t stream) {
+  return fln_autotune_dtype(K, H, norm_kind, FLN_DTYPE_BF16, max_tokens, stream);
+}
+
+int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, fln_stream_t stream) {
   std::lock_guard<std::mutex> lk(g_mu);
   int rc = check_common(1e-5f, norm_kind, max_tokens, H);
   if (rc) return rc;
-  if (K < 8 || (K & 7) || K > kMaxK) return fail(FLN_ERR_INVALID_ARG, "K=%d must be a multiple of 8 in [8, %d]", K, kMaxK);
+  if (dtype != FLN_DTYPE_BF16 && dtype != FLN_DTYPE_E4M3) return fail(FLN_ERR_INVALID_ARG, "dtype=%d", dtype);
+  const int f8 = dtype == FLN_DTYPE_E4M3 ? 1 : 0;
+  const int kalign = f8 ? 16 : 8;
+  if (K < kalign || K % kalign || K > kMaxK)
+    return fail(FLN_ERR_INVALID_ARG, "K=%d must be a multiple of %d in [%d, %d]", K, kalign, kalign, kMaxK);
   if (max_tokens < 1 || max_tokens > 65536) return fail(FLN_ERR_INVALID_ARG, "max_tokens must be in 1..65536");
   if (g_override_chunk > 0 && g_override_threshold > 0) return FLN_OK;  // both overrides: no scan, no check
   Workspace* ws = nullptr;
@@ -827,11 +937,12 @@ int fln_autotune(int K, int H, int norm_kind, int max_tokens, fln_stream_t strea
   FLN_CUDA(cudaStreamSynchronize(s), "tune: cudaStreamSynchronize");
   const int T = max_tokens;
   const int Tc = std::min(T, kMaxUnfusedTokens);  // rows used for the numerical check
-  DevBuf bx, bw, br0, br, bo, bg, bref_r, bref_o, bflush;
+  DevBuf bx, bw, br0, br, bo, bg, bref_r, bref_o, bflush, bscale;
   const size_t nx = size_t(T) * K, nw = size_t(H) * K, nr = size_t(T) * H;
   const size_t flush_bytes = size_t(256) << 20;
-  FLN_CUDA(cudaMalloc(&bx.p, nx * 2), "tune: cudaMalloc");
-  FLN_CUDA(cudaMalloc(&bw.p, nw * 2), "tune: cudaMalloc");
+  const size_t es = f8 ? 1 : 2;
+  FLN_CUDA(cudaMalloc(&bx.p, nx * es), "tune: cudaMalloc");
+  FLN_CUDA(cudaMalloc(&bw.p, nw * es), "tune: cudaMalloc");
   FLN_CUDA(cudaMalloc(&br0.p, nr * 2), "tune: cudaMalloc");
   FLN_CUDA(cudaMalloc(&br.p, nr * 2), "tune: cudaMalloc");
   FLN_CUDA(cudaMalloc(&bo.p, nr * 2), "tune: cudaMalloc");
@@ -839,19 +950,33 @@ int fln_autotune(int K, int H, int norm_kind, int max_tokens, fln_stream_t strea
   FLN_CUDA(cudaMalloc(&bref_r.p, size_t(Tc) * H * 2), "tune: cudaMalloc");
   FLN_CUDA(cudaMalloc(&bref_o.p, size_t(Tc) * H * 2), "tune: cudaMalloc");
   FLN_CUDA(cudaMalloc(&bflush.p, flush_bytes), "tune: cudaMalloc");
-  auto* x = static_cast<__nv_bfloat16*>(bx.p);
-  auto* w = static_cast<__nv_bfloat16*>(bw.p);
   auto* r0 = static_cast<__nv_bfloat16*>(br0.p);
-  fill_pseudo_normal<<<1024, 256, 0, s>>>(x, nx, 0x1234u, 1.0f, 0.0f);
-  fill_pseudo_normal<<<1024, 256, 0, s>>>(w, nw, 0x5678u, 1.0f / std::sqrt(float(K)), 0.0f);
+  // FP8 groups: E4M3 codes of N(0, 16^2) values, per-tensor scales 1/16 and
+  // 1/(16 sqrt K), so the dequantised operands match the bf16 tuning data
+  const float host_scales[4] = {1.0f / 16.0f, 1.0f / (16.0f * std::sqrt(float(K))), 0.f, 0.f};
+  if (f8) {
+    FLN_CUDA(cudaMalloc(&bscale.p, sizeof host_scales), "tune: cudaMalloc");
+    FLN_CUDA(cudaMemcpy(bscale.p, host_scales, sizeof host_scales, cudaMemcpyHostToDevice), "tune: scales");
+    fill_pseudo_e4m3<<<1024, 256, 0, s>>>(static_cast<uint8_t*>(bx.p), nx, 0x1234u, 16.0f);
+    fill_pseudo_e4m3<<<1024, 256, 0, s>>>(static_cast<uint8_t*>(bw.p), nw, 0x5678u, 16.0f);
+  } else {
+    fill_pseudo_normal<<<1024, 256, 0, s>>>(static_cast<__nv_bfloat16*>(bx.p), nx, 0x1234u, 1.0f, 0.0f);
+    fill_pseudo_normal<<<1024, 256, 0, s>>>(static_cast<__nv_bfloat16*>(bw.p), nw, 0x5678u,
+                                            1.0f / std::sqrt(float(K)), 0.0f);
+  }
   fill_pseudo_normal<<<1024, 256, 0, s>>>(r0, nr, 0x9ABCu, 2.0f, 0.0f);
   fill_gamma<<<64, 256, 0, s>>>(static_cast<float*>(bg.p), H, norm_kind);
   FLN_CUDA(cudaGetLastError(), "tune: fill launch");
 
   TuneCtx t{};
   t.ws = ws;
-  t.c = Call{x, w, static_cast<__nv_bfloat16*>(br.p), static_cast<float*>(bg.p), 1e-5f, norm_kind, T, K, H,
+  t.c = Call{bx.p, bw.p, static_cast<__nv_bfloat16*>(br.p), static_cast<float*>(bg.p), 1e-5f, norm_kind, T, K, H,
              static_cast<__nv_bfloat16*>(bo.p), s};
+  if (f8) {
+    t.c.f8 = 1;
+    t.c.x_scale = static_cast<const float*>(bscale.p);
+    t.c.w_scale = static_cast<const float*>(bscale.p) + 1;
+  }
   t.res0 = r0;
   t.flush = bflush.p;
   t.flush_bytes = flush_bytes;
@@ -937,7 +1062,9 @@ int fln_autotune(int K, int H, int norm_kind, int max_tokens, fln_stream_t strea
       }
     }
   }
-  if (!any) return fail(FLN_ERR_CUDA, "tune: no candidate passed the numerical check for (K=%d, H=%d)", K, H);
+  if (!any)
+    return fail(FLN_ERR_CUDA, "tune: no candidate passed the numerical check for (K=%d, H=%d, dtype=%d)", K, H,
+                dtype);
 
   // token-threshold search: UNFUSED vs the best prefill plan over a grid of T
   std::vector<int> grid;
@@ -961,7 +1088,7 @@ int fln_autotune(int K, int H, int norm_kind, int max_tokens, fln_stream_t strea
   if (i0 < grid.size()) threshold = grid[i0];
   best.threshold_tokens = threshold;
   best.tuned_max_tokens = T;
-  g_plans[{K, H, norm_kind}] = best;
+  g_plans[{K, H, norm_kind, dtype}] = best;
   FLN_CUDA(cudaStreamSynchronize(s), "tune: cudaStreamSynchronize");
   return FLN_OK;
 }
@@ -1108,7 +1235,7 @@ int fused_proj_add_rmsnorm_noalloc(const fln_bf16* x, const fln_bf16* W, fln_bf1
     p.gen = d->gen;
     p.err = err_word;
     const int G = std::max(1, std::min(d->sms, p.num_m_tiles * nt));
-    cudaError_t e = launch_gemm(EPI_FUSED_NORM, kNoAllocTile, tmA, tmB, p, G, s);
+    cudaError_t e = launch_gemm(EPI_FUSED_NORM, kNoAllocTile, 0, tmA, tmB, p, G, s);
     if (e != cudaSuccess) return cuda_fail(e, "no-allocation fused GEMM launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
   }

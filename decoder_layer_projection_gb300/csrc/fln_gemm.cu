@@ -17,9 +17,12 @@
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, one TMEM lane (= one
 //               result row) per thread
 //
-// Tiles: BM = 128 rows (MMA M), BN columns (MMA N), BK = 64 (one 128-byte
-// swizzle atom of bf16 per row).  Operands are K-major in shared memory with
-// 128-byte swizzle, exactly as TMA writes them.
+// Tiles: BM = 128 rows (MMA M), BN columns (MMA N), one 128-byte swizzle
+// atom of K per row and stage (64 bf16 or, with FP8 E4M3 operands and
+// kind::f8f6f4 MMAs, 128 elements).  Operands are K-major in shared memory
+// with 128-byte swizzle, exactly as TMA writes them.  With FP8 operands the
+// STORE_F32 epilogue applies the dequantisation scales; split-K partials stay
+// unscaled (the reducer scales their sum).
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -205,14 +208,15 @@ struct WorkSource {
   }
 };
 
-template <int BN, int EPI>
+template <int BN, int EPI, int F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fln_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
   constexpr int STAGES = stages_for(BN);
   constexpr int STAGE_BYTES = stage_bytes(BN);
   constexpr int TMEM_COLS = tmem_cols_for(BN);
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
+  constexpr int KBE = kblock_elems(F8);  // elements of K per 128-byte K-block
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -286,8 +290,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint8_t* sa = smem + stage * STAGE_BYTES;
         uint8_t* sb = sa + A_TILE_BYTES;
         mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
-        tma_load_2d(sa, &tmA, &full_bar[stage], kb * BK, a_row, pol_a);
-        tma_load_2d(sb, &tmB, &full_bar[stage], kb * BK, b_row, pol_b);
+        tma_load_2d(sa, &tmA, &full_bar[stage], kb * KBE, a_row, pol_a);
+        tma_load_2d(sb, &tmB, &full_bar[stage], kb * KBE, b_row, pol_b);
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
@@ -335,10 +339,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t adesc = sw128_kmajor_desc(sa);
         const uint64_t bdesc = sw128_kmajor_desc(sb);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          // advance 16 bf16 = 32 bytes along K inside the swizzle atom (encoded >> 4)
-          mma_bf16(d_tmem, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2), IDESC,
-                   (kb > w.kb_begin || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk) {
+          // advance 32 bytes along K inside the swizzle atom (encoded >> 4):
+          // 16 bf16 or 32 E4M3 elements per MMA
+          if (F8)
+            mma_e4m3(d_tmem, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2), IDESC,
+                     (kb > w.kb_begin || kk > 0) ? 1u : 0u);
+          else
+            mma_bf16(d_tmem, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2), IDESC,
+                     (kb > w.kb_begin || kk > 0) ? 1u : 0u);
         }
         issued_any = true;
         mma_commit(&empty_bar[stage]);  // frees the smem stage once these MMAs have read it
@@ -477,6 +486,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else if (EPI == EPI_STORE_F32) {
         const int n0 = w.n_tile * BN;
         float* yrow = p.yout + static_cast<size_t>(row) * static_cast<size_t>(p.ld);
+        // FP8: this row's token scale
+        const float sxr =
+            (F8 && vrow) ? __ldg(p.x_scale + static_cast<size_t>(p.a_row0 + row) * p.x_scale_stride) : 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           float v[16];
@@ -485,6 +497,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int col = n0 + c + 8 * h;
+              if (F8) {
+                float sw[8];
+                load_scale8(p.w_scale, p.w_scale_stride, col, col < p.N, sw);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[8 * h + j] *= sxr * sw[j];
+              }
               if (col < p.N) {
                 float4* d = reinterpret_cast<float4*>(yrow + col);
                 d[0] = make_float4(v[8 * h + 0], v[8 * h + 1], v[8 * h + 2], v[8 * h + 3]);
@@ -523,16 +541,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ---------------------------------------------------------------- host side
-template <int BN, int EPI>
+template <int BN, int EPI, int F8>
 static cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(fln_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(fln_gemm_kernel<BN, EPI, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               smem_bytes_for(BN));
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, int F8>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, int grid,
                               cudaStream_t stream) {
-  fln_gemm_kernel<BN, EPI><<<grid, NUM_THREADS, smem_bytes_for(BN), stream>>>(tmA, tmB, p);
+  fln_gemm_kernel<BN, EPI, F8><<<grid, NUM_THREADS, smem_bytes_for(BN), stream>>>(tmA, tmB, p);
   return cudaGetLastError();
 }
 
@@ -549,42 +567,57 @@ int gemm_smem_bytes(int bn) {
 
 int gemm_stages(int bn) { return stages_for(bn); }
 
-#define FLN_BN_SWITCH(bn, EPI, CALL)                \
+#define FLN_BN_SWITCH(bn, EPI, F8, CALL)            \
   switch (bn) {                                     \
-    case 16: return CALL<16, EPI>();                \
-    case 32: return CALL<32, EPI>();                \
-    case 64: return CALL<64, EPI>();                \
-    case 128: return CALL<128, EPI>();              \
-    case 256: return CALL<256, EPI>();              \
+    case 16: return CALL<16, EPI, F8>();            \
+    case 32: return CALL<32, EPI, F8>();            \
+    case 64: return CALL<64, EPI, F8>();            \
+    case 128: return CALL<128, EPI, F8>();          \
+    case 256: return CALL<256, EPI, F8>();          \
     default: return cudaErrorInvalidValue;          \
   }
 
-cudaError_t gemm_prepare(int bn, EpilogueKind epi) {
+// FP8 operands exist for the pipelined (STORE_F32) and split-K epilogues.
+cudaError_t gemm_prepare(int bn, EpilogueKind epi, int f8) {
+  if (f8) {
+    switch (epi) {
+      case EPI_STORE_F32: FLN_BN_SWITCH(bn, EPI_STORE_F32, 1, prepare_one)
+      case EPI_SPLITK_SWAP: FLN_BN_SWITCH(bn, EPI_SPLITK_SWAP, 1, prepare_one)
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (epi) {
-    case EPI_FUSED_NORM: FLN_BN_SWITCH(bn, EPI_FUSED_NORM, prepare_one)
-    case EPI_STORE_F32: FLN_BN_SWITCH(bn, EPI_STORE_F32, prepare_one)
-    case EPI_SPLITK_SWAP: FLN_BN_SWITCH(bn, EPI_SPLITK_SWAP, prepare_one)
+    case EPI_FUSED_NORM: FLN_BN_SWITCH(bn, EPI_FUSED_NORM, 0, prepare_one)
+    case EPI_STORE_F32: FLN_BN_SWITCH(bn, EPI_STORE_F32, 0, prepare_one)
+    case EPI_SPLITK_SWAP: FLN_BN_SWITCH(bn, EPI_SPLITK_SWAP, 0, prepare_one)
   }
   return cudaErrorInvalidValue;
 }
 
 #undef FLN_BN_SWITCH
-#define FLN_BN_LAUNCH(bn, EPI)                                            \
-  switch (bn) {                                                           \
-    case 16: return launch_one<16, EPI>(tmA, tmB, p, grid, stream);       \
-    case 32: return launch_one<32, EPI>(tmA, tmB, p, grid, stream);       \
-    case 64: return launch_one<64, EPI>(tmA, tmB, p, grid, stream);       \
-    case 128: return launch_one<128, EPI>(tmA, tmB, p, grid, stream);     \
-    case 256: return launch_one<256, EPI>(tmA, tmB, p, grid, stream);     \
-    default: return cudaErrorInvalidValue;                                \
+#define FLN_BN_LAUNCH(bn, EPI, F8)                                            \
+  switch (bn) {                                                               \
+    case 16: return launch_one<16, EPI, F8>(tmA, tmB, p, grid, stream);       \
+    case 32: return launch_one<32, EPI, F8>(tmA, tmB, p, grid, stream);       \
+    case 64: return launch_one<64, EPI, F8>(tmA, tmB, p, grid, stream);       \
+    case 128: return launch_one<128, EPI, F8>(tmA, tmB, p, grid, stream);     \
+    case 256: return launch_one<256, EPI, F8>(tmA, tmB, p, grid, stream);     \
+    default: return cudaErrorInvalidValue;                                    \
   }
 
-cudaError_t launch_gemm(EpilogueKind epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB,
+cudaError_t launch_gemm(EpilogueKind epi, int bn, int f8, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         const GemmParams& p, int grid, cudaStream_t stream) {
+  if (f8) {
+    switch (epi) {
+      case EPI_STORE_F32: FLN_BN_LAUNCH(bn, EPI_STORE_F32, 1)
+      case EPI_SPLITK_SWAP: FLN_BN_LAUNCH(bn, EPI_SPLITK_SWAP, 1)
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (epi) {
-    case EPI_FUSED_NORM: FLN_BN_LAUNCH(bn, EPI_FUSED_NORM)
-    case EPI_STORE_F32: FLN_BN_LAUNCH(bn, EPI_STORE_F32)
-    case EPI_SPLITK_SWAP: FLN_BN_LAUNCH(bn, EPI_SPLITK_SWAP)
+    case EPI_FUSED_NORM: FLN_BN_LAUNCH(bn, EPI_FUSED_NORM, 0)
+    case EPI_STORE_F32: FLN_BN_LAUNCH(bn, EPI_STORE_F32, 0)
+    case EPI_SPLITK_SWAP: FLN_BN_LAUNCH(bn, EPI_SPLITK_SWAP, 0)
   }
   return cudaErrorInvalidValue;
 }

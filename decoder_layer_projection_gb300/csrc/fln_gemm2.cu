@@ -19,11 +19,14 @@
 // holds 64 KiB of shared memory and the operand ring keeps 5 stages at
 // BN = 256.  Phase 1 forms r = r0 + acc in fp32
 // and the row's partial sum of squares; the row block's partial sums of all
-// N-tiles are exchanged through global memory (per-tile release flags,
-// acquire by the others, fixed summation order); phase 2 recomputes r, puts
-// bf16(r) and bf16(r * rstd * g) in shared memory and each warp writes its 32
-// rows back with coalesced 16-byte stores, rows past the chunk and columns
-// past H masked.
+// N-tiles are exchanged through global memory as 64-bit {launch generation,
+// value} words (fixed summation order); phase 2 reads r back from TMEM, stages
+// bf16(r * rstd * g) in shared memory and each warp writes its 32 rows back
+// with TMA stores, rows past the chunk and columns past H clipped.
+//
+// FP8 (E4M3) operands: the same kernel with kind::f8f6f4 MMAs over 128-byte
+// K-blocks of 128 elements; phase 1 scales the accumulator by the token's and
+// the column's dequantisation scales before the residual add.
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -66,14 +69,15 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <int BN>
+template <int BN, int F8>
 __global__ void __launch_bounds__(THREADS, 1)
     fln_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmRs,
                          const __grid_constant__ CUtensorMap tmOs, const GemmParams p) {
   using C = Cfg<BN>;
   constexpr int STAGES = C::STAGES;
-  constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN);
+  constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(2 * BM, BN) : idesc_bf16_f32(2 * BM, BN);
+  constexpr int KBE = kblock_elems(F8);  // elements of K per 128-byte K-block
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -154,8 +158,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint8_t* sb = sa + C::A_BYTES;
         const uint32_t fb = map_to_cta(smem_u32(&full_bar[stage]), 0);
         if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE);
-        tma_load_2d_pair(sa, &tmA, fb, kb * BK, a_row, pol);
-        tma_load_2d_pair(sb, &tmB, fb, kb * BK, b_row, pol);
+        tma_load_2d_pair(sa, &tmA, fb, kb * KBE, a_row, pol);
+        tma_load_2d_pair(sb, &tmB, fb, kb * KBE, b_row, pol);
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
@@ -229,10 +233,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t sa = smem_u32(ring + stage * C::STAGE);
         const uint64_t adesc = sw128_kmajor_desc(sa);
         const uint64_t bdesc = sw128_kmajor_desc(sa + C::A_BYTES);
+        // four MMAs of 32 bytes of K each (16 bf16 or 32 E4M3 elements)
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_bf16_pair(d_tmem, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2), IDESC,
-                        (kb > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk) {
+          if (F8)
+            mma_e4m3_pair(d_tmem, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2),
+                          IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+          else
+            mma_bf16_pair(d_tmem, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2),
+                          IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+        }
         issued_any = true;
         mma_commit_pair_mc(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
         if (++stage == STAGES) {
@@ -286,6 +296,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Rows past the chunk and columns past H read zeros: acc and r0 are 0.
       float ss = 0.f;
       int pending = -1;  // box whose TMA store may still be reading it (freed one box later)
+      // FP8: this row's token scale (rows past the chunk have a zero accumulator)
+      float sxr = 0.f;
+      if (F8 && wrow0 + lane < p.M)
+        sxr = __ldg(p.x_scale + static_cast<size_t>(p.a_row0 + wrow0 + lane) * p.x_scale_stride);
 #pragma unroll 1
       for (int g = 0; g < G; ++g, ++s) {
         const int halves = (BN - g * 64) >= 64 ? 2 : 1;  // 32-column halves of this box inside the tile
@@ -296,6 +310,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           float v[32];
           const uint32_t ta = tb + static_cast<uint32_t>(g * 64 + c2 * 32);
           tmem_ld32(ta, v);
+          if (F8) {
+            // dequantise: y = acc * (sx[token] * sw[column])
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int cc = n0 + g * 64 + c2 * 32 + 8 * h;
+              float sw[8];
+              load_scale8(p.w_scale, p.w_scale_stride, cc, cc < p.N, sw);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[8 * h + j] *= sxr * sw[j];
+            }
+          }
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             uint4* rp = reinterpret_cast<uint4*>(box + swz(rl, c2 * 4 + h));
@@ -469,7 +494,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
 }
 
-template <int BN>
+template <int BN, int F8>
 static cudaError_t launch_pair_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmR,
                                   const CUtensorMap& tmRs, const CUtensorMap& tmOs, const GemmParams& p, int pairs,
                                   cudaStream_t stream) {
@@ -485,12 +510,12 @@ static cudaError_t launch_pair_bn(const CUtensorMap& tmA, const CUtensorMap& tmB
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fln_gemm_pair_kernel<BN>, tmA, tmB, tmR, tmRs, tmOs, p);
+  return cudaLaunchKernelEx(&cfg, fln_gemm_pair_kernel<BN, F8>, tmA, tmB, tmR, tmRs, tmOs, p);
 }
 
-template <int BN>
+template <int BN, int F8>
 static cudaError_t prepare_pair_bn(int* max_pairs) {
-  cudaError_t e = cudaFuncSetAttribute(fln_gemm_pair_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(fln_gemm_pair_kernel<BN, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<BN>::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -504,29 +529,47 @@ static cudaError_t prepare_pair_bn(int* max_pairs) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(max_pairs, fln_gemm_pair_kernel<BN>, &cfg);
+  return cudaOccupancyMaxActiveClusters(max_pairs, fln_gemm_pair_kernel<BN, F8>, &cfg);
 }
 
 }  // namespace pair
 
-cudaError_t pair_gemm_prepare(int bn, int* max_pairs) {
+cudaError_t pair_gemm_prepare(int bn, int f8, int* max_pairs) {
+  if (f8) {
+    switch (bn) {
+      case 128: return pair::prepare_pair_bn<128, 1>(max_pairs);
+      case 192: return pair::prepare_pair_bn<192, 1>(max_pairs);
+      case 224: return pair::prepare_pair_bn<224, 1>(max_pairs);
+      case 256: return pair::prepare_pair_bn<256, 1>(max_pairs);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (bn) {
-    case 128: return pair::prepare_pair_bn<128>(max_pairs);
-    case 192: return pair::prepare_pair_bn<192>(max_pairs);
-    case 224: return pair::prepare_pair_bn<224>(max_pairs);
-    case 256: return pair::prepare_pair_bn<256>(max_pairs);
+    case 128: return pair::prepare_pair_bn<128, 0>(max_pairs);
+    case 192: return pair::prepare_pair_bn<192, 0>(max_pairs);
+    case 224: return pair::prepare_pair_bn<224, 0>(max_pairs);
+    case 256: return pair::prepare_pair_bn<256, 0>(max_pairs);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemm_pair_fused(int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmR,
-                                   const CUtensorMap& tmRs, const CUtensorMap& tmOs, const GemmParams& p, int pairs,
-                                   cudaStream_t stream) {
+cudaError_t launch_gemm_pair_fused(int bn, int f8, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                   const CUtensorMap& tmR, const CUtensorMap& tmRs, const CUtensorMap& tmOs,
+                                   const GemmParams& p, int pairs, cudaStream_t stream) {
+  if (f8) {
+    switch (bn) {
+      case 128: return pair::launch_pair_bn<128, 1>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
+      case 192: return pair::launch_pair_bn<192, 1>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
+      case 224: return pair::launch_pair_bn<224, 1>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
+      case 256: return pair::launch_pair_bn<256, 1>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (bn) {
-    case 128: return pair::launch_pair_bn<128>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
-    case 192: return pair::launch_pair_bn<192>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
-    case 224: return pair::launch_pair_bn<224>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
-    case 256: return pair::launch_pair_bn<256>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
+    case 128: return pair::launch_pair_bn<128, 0>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
+    case 192: return pair::launch_pair_bn<192, 0>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
+    case 224: return pair::launch_pair_bn<224, 0>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
+    case 256: return pair::launch_pair_bn<256, 0>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -58,6 +58,14 @@ struct GemmParams {
   int dyn_cpm;              // dynamic chunks per m-tile (0: none)
   int dyn_kc;               // K-blocks per dynamic chunk
   unsigned int* dyn_counter;  // chunk counter: zero before and after every launch
+  // FP8 (E4M3) operands: the accumulator of (token t, hidden h) is scaled by
+  // x_scale[t * x_scale_stride] * w_scale[h * w_scale_stride] (stride 0: one
+  // scale for the tensor); t is the global token row.  Unused for bf16.  The
+  // split-K epilogue stores unscaled partials (the reducer scales the sum).
+  const float* x_scale;
+  int x_scale_stride;
+  const float* w_scale;
+  int w_scale_stride;
   unsigned int* err;        // device error word
 };
 
@@ -81,14 +89,26 @@ struct NormParams {
   int row0;                     // global row of local row 0 (residual/out/y_bf16)
   int H;
   int pdl;                      // launched as a programmatic dependent of the preceding kernel
+  // FP8 split-K: scale the summed partials by x_scale[(row0 + t) * stride] *
+  // w_scale[h * stride] (null: no scaling)
+  const float* x_scale;
+  int x_scale_stride;
+  const float* w_scale;
+  int w_scale_stride;
 };
 
-// launchers (return cudaError_t of the launch)
-cudaError_t launch_gemm(EpilogueKind epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB,
+// Operand element type of a projection: bf16 (K-blocks of 64 elements) or
+// FP8 E4M3 (K-blocks of 128 elements); either way a K-block row is 128 bytes.
+enum OperandType : int { OPERAND_BF16 = 0, OPERAND_E4M3 = 1 };
+__host__ __device__ constexpr int kblock_elems(int f8) { return f8 ? 128 : 64; }
+
+// launchers (return cudaError_t of the launch).  f8: E4M3 operands (epilogues
+// STORE_F32 and SPLITK_SWAP only).
+cudaError_t launch_gemm(EpilogueKind epi, int bn, int f8, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         const GemmParams& p, int grid, cudaStream_t stream);
 int gemm_smem_bytes(int bn);
 int gemm_stages(int bn);
-cudaError_t gemm_prepare(int bn, EpilogueKind epi);  // sets max dynamic smem attributes
+cudaError_t gemm_prepare(int bn, EpilogueKind epi, int f8);  // sets max dynamic smem attributes
 
 // CTA-pair (cta_group::2) fused GEMM + add + RMSNorm for tile widths 128,
 // 192, 224, 256.  prepare sets the shared-memory limit and reports how many pairs
@@ -96,10 +116,10 @@ cudaError_t gemm_prepare(int bn, EpilogueKind epi);  // sets max dynamic smem at
 // row statistics).  tmR maps the chunk's residual rows (read in 128 x 64
 // boxes), tmRs / tmOs the chunk's residual and output rows in 32 x 64 boxes
 // (stores).
-cudaError_t pair_gemm_prepare(int bn, int* max_pairs);
-cudaError_t launch_gemm_pair_fused(int bn, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmR,
-                                   const CUtensorMap& tmRs, const CUtensorMap& tmOs, const GemmParams& p, int pairs,
-                                   cudaStream_t stream);
+cudaError_t pair_gemm_prepare(int bn, int f8, int* max_pairs);
+cudaError_t launch_gemm_pair_fused(int bn, int f8, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                   const CUtensorMap& tmR, const CUtensorMap& tmRs, const CUtensorMap& tmOs,
+                                   const GemmParams& p, int pairs, cudaStream_t stream);
 
 enum NormSource : int { NORM_SRC_BF16 = 0, NORM_SRC_F32 = 1, NORM_SRC_SPLITK = 2 };
 cudaError_t launch_add_rmsnorm(NormSource src, const NormParams& p, int grid_cap, cudaStream_t stream);

@@ -14,7 +14,8 @@
 //   BF16    a bf16 [T, H] tensor (the public add_rmsnorm call);
 //   F32     an fp32 pipeline slot written by the projection GEMM;
 //   SPLITK  the fp32 stream-K partials of the decode GEMM, summed here in a
-//           fixed order (deterministic).
+//           fixed order (deterministic); with FP8 operands the sum is scaled
+//           by the token's and the column's dequantisation scales.
 // Each thread keeps its VPT 8-element vectors of r in registers between the
 // statistics pass and the normalisation pass, so every byte is read once.  All
 // loads of a thread are independent and issued before their first use (the
@@ -61,6 +62,14 @@ __device__ __forceinline__ void load_splitk8(const NormParams& p, int t, int h, 
       y[0] += a[s].x; y[1] += a[s].y; y[2] += a[s].z; y[3] += a[s].w;
       y[4] += b[s].x; y[5] += b[s].y; y[6] += b[s].z; y[7] += b[s].w;
     }
+  }
+  if (p.w_scale) {
+    // FP8 operands: y = sum * (sx[token] * sw[column])
+    const float sx = __ldg(p.x_scale + static_cast<size_t>(p.row0 + t) * p.x_scale_stride);
+    float sw[8];
+    load_scale8(p.w_scale, p.w_scale_stride, h, true, sw);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) y[j] *= sx * sw[j];
   }
 }
 

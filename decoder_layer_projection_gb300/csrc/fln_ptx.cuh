@@ -169,6 +169,43 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Eight per-column scales starting at column c (stride 0: the tensor's one
+// scale); zeros for a chunk past the last column.  c is a multiple of 8 and a
+// per-column array is 16-byte aligned.
+__device__ __forceinline__ void load_scale8(const float* w, int stride, int c, bool valid, float (&s)[8]) {
+  if (!valid) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[j] = 0.f;
+  } else if (stride == 0) {
+    const float v = __ldg(w);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[j] = v;
+  } else {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(w + c));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(w + c + 4));
+    s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
+    s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
+  }
+}
+
+// Instruction descriptor, kind::f8f6f4 with E4M3 A and B (format code 0 in
+// bits 7-9 and 10-12), D fp32, both K-major; same M / N fields.  One MMA
+// consumes 32 bytes of K per row, like kind::f16, i.e. 32 FP8 elements.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with E4M3 operands, one CTA.
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, both K-major, one CTA.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -295,6 +332,17 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, 
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same on a CTA pair with E4M3 operands.
+__device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

@@ -115,6 +115,39 @@ int fused_proj_add_rmsnorm(const fln_bf16* x, const fln_bf16* W, fln_bf16* resid
                            float eps, int norm_kind, int T, int K, int H, int microchunk_tokens, fln_bf16* out,
                            fln_stream_t stream);
 
+/* Operand element types of a projection group. */
+typedef enum { FLN_DTYPE_BF16 = 0, FLN_DTYPE_E4M3 = 1 } fln_dtype;
+
+/*
+ * fused_proj_add_rmsnorm_fp8 -- the same region with FP8 operands ("TPSP
+ * Design", section 5 "To-do": FP8 dense, quantized projections and scale
+ * handling across microchunks):
+ *
+ *     y[t,h] = sx[t] * sw[h] * sum_k x[t,k] * W[h,k];  residual += y;  out = RMSNorm(residual)
+ *
+ *   x          [T, K] FP8 E4M3 codes (OCP "FN" form: bias 7, max 448, no
+ *              infinities), one byte per element, produced by the caller
+ *   x_scale    fp32 dequantisation scale(s) of x: [T] (x_scale_per_token != 0)
+ *              or [1] (one scale for the tensor)
+ *   W          [H, K] E4M3 codes, F.linear layout [out, in]
+ *   w_scale    fp32 scale(s) of W: [H] (w_scale_per_channel != 0, one per
+ *              output row) or [1]
+ *   K          multiple of 16 (16-byte rows), 16 <= K <= 2^20; H multiple of 8
+ *   the rest   as in fused_proj_add_rmsnorm (bf16 residual and out, fp32 gamma)
+ *
+ * The products are accumulated in fp32 by the tensor cores (tcgen05
+ * kind::f8f6f4) and scaled in fp32 before the residual add.  A microchunk
+ * uses its own tokens' scales, so the chunking changes no result bit.  Every
+ * path exists for FP8 (FUSED, PIPELINED, UNFUSED); plans, tuning and the
+ * threshold are kept per (K, H, norm_kind, FLN_DTYPE_E4M3) group.  The scale
+ * pointers must be device pointers, 16-byte aligned; the library does not
+ * quantise x (the producing operation supplies E4M3 codes and their scales).
+ */
+int fused_proj_add_rmsnorm_fp8(const uint8_t* x, const float* x_scale, int x_scale_per_token, const uint8_t* W,
+                               const float* w_scale, int w_scale_per_channel, fln_bf16* residual,
+                               const float* gamma, float eps, int norm_kind, int T, int K, int H,
+                               int microchunk_tokens, fln_bf16* out, fln_stream_t stream);
+
 /*
  * add_rmsnorm -- residual += y; out = RMSNorm(residual)   (the add/norm step alone)
  *
@@ -151,6 +184,13 @@ int fln_set_plan(int K, int H, int norm_kind, const fln_plan* plan);
 /* The plan a call with these arguments would use after overrides (path is
  * FLN_PATH_UNFUSED when T is below the threshold).  Writes *plan. */
 int fln_get_plan(int K, int H, int norm_kind, int T, int microchunk_tokens, fln_plan* plan);
+
+/* The three calls above for groups of a given operand type (fln_dtype); the
+ * calls without a dtype act on FLN_DTYPE_BF16 groups.  FP8 groups are tuned on
+ * synthetic E4M3 data with per-tensor scales. */
+int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, fln_stream_t stream);
+int fln_set_plan_dtype(int K, int H, int norm_kind, int dtype, const fln_plan* plan);
+int fln_get_plan_dtype(int K, int H, int norm_kind, int dtype, int T, int microchunk_tokens, fln_plan* plan);
 
 /* Synchronise `stream` and the internal stream, read and clear the device
  * error word.  FLN_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait. */

@@ -121,6 +121,37 @@ def test_fused_rejects_bad_arguments_before_any_launch(lib, kw, status):
     assert fln.fln_launch_count() == 0
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=24), fln.FLN_ERR_INVALID_ARG),        # FP8 rows must be 16 bytes: K multiple of 16
+    (dict(K=8), fln.FLN_ERR_INVALID_ARG),
+    (dict(norm_kind=5), fln.FLN_ERR_INVALID_ARG),
+    (dict(T=-3), fln.FLN_ERR_INVALID_ARG),
+    (dict(H=12), fln.FLN_ERR_INVALID_ARG),
+    (dict(microchunk_tokens=-1), fln.FLN_ERR_INVALID_ARG),
+])
+def test_fp8_rejects_bad_arguments_before_any_launch(lib, kw, status):
+    a = dict(eps=1e-5, norm_kind=0, T=16, K=256, H=256, microchunk_tokens=0)
+    a.update(kw)
+    rc = lib.fused_proj_add_rmsnorm_fp8(None, None, 1, None, None, 1, None, None, a["eps"], a["norm_kind"], a["T"],
+                                        a["K"], a["H"], a["microchunk_tokens"], None, None)
+    assert rc == status, fln.fln_last_error()
+    assert fln.fln_launch_count() == 0
+
+
+def test_dtype_plans_validation(lib):
+    p = fln.Plan(path=fln.PATH_FUSED, microchunk_tokens=512, tile_n=256, gemm_ctas=0, norm_ctas=0,
+                 threshold_tokens=1, tuned_max_tokens=0)
+    import ctypes
+    assert lib.fln_set_plan_dtype(1024, 768, 0, 7, ctypes.byref(p)) == fln.FLN_ERR_INVALID_ARG
+    fln.fln_set_plan(1024, 768, 0, p, dtype=fln.DTYPE_E4M3)
+    try:
+        assert fln.fln_get_plan(1024, 768, 0, 4096, dtype=fln.DTYPE_E4M3)["microchunk_tokens"] == 512
+        assert fln.fln_get_plan(1024, 768, 0, 4096)["microchunk_tokens"] == 4096   # bf16 group untouched
+    finally:
+        fln.fln_set_plan(1024, 768, 0, None, dtype=fln.DTYPE_E4M3)
+    assert fln.fln_get_plan(1024, 768, 0, 4096, dtype=fln.DTYPE_E4M3)["microchunk_tokens"] == 4096
+
+
 def test_empty_call_is_a_no_op(lib):
     assert fln.fused_proj_add_rmsnorm_ptr(None, None, None, None, 1e-5, 0, 0, 256, 256, 0, None, None) == 0
     assert fln.add_rmsnorm_ptr(None, None, None, 1e-5, 0, 0, 256, None, None) == 0

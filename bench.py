@@ -46,10 +46,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel sources the capture was taken on; reported as null when the sources
 # have changed since.  Captures: profiles/ (same commands).
 NCU_TRAFFIC = {
-    ("llama3_8b_oproj", 4096, "gemm_fused", 256, "4d7d1fdc6e12"): 114142464 + 33394176,
-    ("llama70b_down_decode", 8, "gemm_splitk", 256, "4d7d1fdc6e12"): 471433472 + 3426304,
-    ("llama70b_oproj_decode", 8, "gemm_splitk", 256, "4d7d1fdc6e12"): 135539456 + 3152384,
+    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "4d7d1fdc6e12"): 114142464 + 33394176,
+    ("llama70b_down_decode", 8, "bf16", "gemm_splitk", 256, "4d7d1fdc6e12"): 471433472 + 3426304,
+    ("llama70b_oproj_decode", 8, "bf16", "gemm_splitk", 256, "4d7d1fdc6e12"): 135539456 + 3152384,
 }
+# FP8 (E4M3) dense peak: the measured bf16 peak times NVIDIA's nominal dense
+# FP8 / BF16 ratio (4.5 / 2.25 PFLOP/s); no FP8 GEMM peak is measured
+FP8_OVER_BF16 = 2.0
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -167,7 +170,7 @@ def run_gpu(args):
     import torch.distributed as dist
 
     import decoder_layer_projection_gb300 as fln
-    from synth import make_inputs, workload
+    from synth import make_inputs, make_inputs_fp8, workload
 
     rank, world, local_rank = dist_env()
     torch.cuda.set_device(local_rank)
@@ -181,12 +184,25 @@ def run_gpu(args):
     if args.tokens:
         wl = wl.with_tokens(args.tokens)
     T, K, H = wl.T, wl.K, wl.H
-    d = make_inputs(wl, seed=rank_seed(wl.seed, rank))
+    f8 = args.dtype == "e4m3"
+    dt = fln.DTYPE_E4M3 if f8 else fln.DTYPE_BF16
+    if f8:
+        d = make_inputs_fp8(wl, seed=rank_seed(wl.seed, rank))
+    else:
+        d = make_inputs(wl, seed=rank_seed(wl.seed, rank))
 
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
 
-    x, W, r = up(d["x"]), up(d["W"]), up(d["r0"])
+    if f8:
+        x = torch.from_numpy(np.ascontiguousarray(d["x8"])).to(device)
+        W = torch.from_numpy(np.ascontiguousarray(d["W8"])).to(device)
+        sx = torch.from_numpy(d["x_scale"]).to(device)
+        sw = torch.from_numpy(d["w_scale"]).to(device)
+    else:
+        x, W = up(d["x"]), up(d["W"])
+        sx = sw = None
+    r = up(d["r0"])
     gamma = torch.from_numpy(d["gamma"]).to(device)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
@@ -195,19 +211,23 @@ def run_gpu(args):
     # profile the group on this device, as the pages' runtime does after the weights load
     t_tune = time.time()
     if args.plan == "auto":
-        fln.fln_autotune(K, H, wl.norm_kind, T, stream)
+        fln.fln_autotune(K, H, wl.norm_kind, T, stream, dtype=dt)
     else:
         f = args.plan.split(":")
         path = {"fused": fln.PATH_FUSED, "pipelined": fln.PATH_PIPELINED}[f[0]]
         fln.fln_set_plan(K, H, wl.norm_kind, dict(
             path=path, microchunk_tokens=int(f[1]), tile_n=int(f[2]), gemm_ctas=int(f[3]),
             norm_ctas=int(f[4]) if len(f) > 4 else 0, threshold_tokens=1 if T > 256 else 257,
-            tuned_max_tokens=0))
+            tuned_max_tokens=0), dtype=dt)
     t_tune = time.time() - t_tune
-    plan = fln.fln_get_plan(K, H, wl.norm_kind, T, args.microchunk)
+    plan = fln.fln_get_plan(K, H, wl.norm_kind, T, args.microchunk, dtype=dt)
 
     def step():
-        fln.fused_proj_add_rmsnorm(x, W, r, gamma, wl.eps, wl.norm_kind, args.microchunk, out, stream)
+        if f8:
+            fln.fused_proj_add_rmsnorm_fp8(x, sx, W, sw, r, gamma, wl.eps, wl.norm_kind, args.microchunk, out,
+                                           stream)
+        else:
+            fln.fused_proj_add_rmsnorm(x, W, r, gamma, wl.eps, wl.norm_kind, args.microchunk, out, stream)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -263,13 +283,15 @@ def run_gpu(args):
     avg_launch_ms = kp["total_ms"] / max(kp["launches"], 1)
     launches_per_step = kp["launches"] / args.steps
     tokens_per_launch = T / launches_per_step
+    ob = 1.0 if f8 else 2.0  # bytes per x / W element
+    tensor_peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if f8 else 1.0)
     if kname in ("gemm_fused", "gemm_slot"):
         # tensor bound: 2 * tokens * K * H per launch
         achieved = 2.0 * tokens_per_launch * K * H / (avg_launch_ms * 1e-3) / 1e12
-        bound, unit, peak = "tensor", "TFLOP/s", peaks["bf16_tflops"]
+        bound, unit, peak = "tensor", "TFLOP/s", tensor_peak
     elif kname == "gemm_splitk":
         # HBM bound: W read once plus x, per launch
-        achieved = (2.0 * H * K + 2.0 * tokens_per_launch * K) / (avg_launch_ms * 1e-3) / 1e9
+        achieved = (ob * H * K + ob * tokens_per_launch * K) / (avg_launch_ms * 1e-3) / 1e9
         bound, unit, peak = "hbm", "GB/s", peaks["hbm_gbs"]
     else:
         # add + norm: residual read and written, output written, gamma
@@ -279,27 +301,29 @@ def run_gpu(args):
     for f in ("fln_gemm.cu", "fln_gemm2.cu", "fln_norm.cu", "fln_ptx.cuh"):
         h.update(open(os.path.join(ROOT, "decoder_layer_projection_gb300", "csrc", f), "rb").read())
     src_hash = h.hexdigest()[:12]
-    traffic = NCU_TRAFFIC.get((args.config, T, kname, plan["tile_n"], src_hash))
+    traffic = NCU_TRAFFIC.get((args.config, T, args.dtype, kname, plan["tile_n"], src_hash))
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
                 "kernel": kname,
-                "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback",
+                "peak_source": (f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback")
+                + (" bf16 x 2, the nominal dense FP8/BF16 ratio" if f8 and bound == "tensor" else ""),
                 "kernel_ms_per_launch": round(avg_launch_ms, 5), "launches_per_step": launches_per_step,
                 "measured": "second timed pass of the same K steps with per-kernel CUDA events",
                 "profiled_ms_per_step": round(prof_s * 1e3 / args.steps, 5)}
     # full-step roofline: the slower of FLOPs at tensor peak and bytes at HBM bandwidth
-    t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), wl.algorithmic_bytes() / (peaks["hbm_gbs"] * 1e9))
+    t_roof = max(flops / (tensor_peak * 1e12), wl.algorithmic_bytes(1 if f8 else 2) / (peaks["hbm_gbs"] * 1e9))
     step_frac = t_roof / (ms_per_step * 1e-3)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
-    e2e = run_e2e(args, wl, d, W, gamma, device, stream, fln)
-    comparator = run_comparator(args, wl, x, W, d, gamma, device, stream, fln, flush)
+    e2e = run_e2e(args, wl, d, W, gamma, device, stream, fln, sw)
+    comparator = run_comparator(args, wl, x, W, d, gamma, device, stream, fln, flush, sx, sw)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "T": T, "K": K, "H": H, "norm": "gemma" if wl.norm_kind else "standard",
+        "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "T": T, "K": K, "H": H, "operands": args.dtype,
+                   "norm": "gemma" if wl.norm_kind else "standard",
                    "eps": wl.eps, "global_batch_tokens": T * world, "parallelism": f"dp{world} (replicas)",
                    "plan": plan, "plan_arg": args.plan, "microchunk_arg": args.microchunk,
                    "tune_s": round(t_tune, 2),
@@ -320,22 +344,34 @@ def run_gpu(args):
     return line if rank == 0 else None
 
 
-def run_e2e(args, wl, d, W, gamma, device, stream, fln):
+def run_e2e(args, wl, d, W, gamma, device, stream, fln, sw=None):
     import numpy as np
     import torch
     T, K, H = wl.T, wl.K, wl.H
-    hx = torch.from_numpy(np.ascontiguousarray(d["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    f8 = args.dtype == "e4m3"
+    if f8:
+        hx = torch.from_numpy(np.ascontiguousarray(d["x8"])).pin_memory()
+        hsx = torch.from_numpy(np.ascontiguousarray(d["x_scale"])).pin_memory()
+        dx = torch.empty((T, K), dtype=torch.uint8, device=device)
+        dsx = torch.empty_like(hsx, device=device)
+    else:
+        hx = torch.from_numpy(np.ascontiguousarray(d["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+        dx = torch.empty((T, K), dtype=torch.bfloat16, device=device)
     hr = torch.from_numpy(np.ascontiguousarray(d["r0"]).view(np.int16)).view(torch.bfloat16).pin_memory()
     ho = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     hr_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    dx = torch.empty((T, K), dtype=torch.bfloat16, device=device)
     dr = torch.empty((T, H), dtype=torch.bfloat16, device=device)
     do = torch.empty((T, H), dtype=torch.bfloat16, device=device)
 
     def step():
         dx.copy_(hx, non_blocking=True)
         dr.copy_(hr, non_blocking=True)
-        fln.fused_proj_add_rmsnorm(dx, W, dr, gamma, wl.eps, wl.norm_kind, args.microchunk, do, stream)
+        if f8:
+            dsx.copy_(hsx, non_blocking=True)
+            fln.fused_proj_add_rmsnorm_fp8(dx, dsx, W, sw, dr, gamma, wl.eps, wl.norm_kind, args.microchunk, do,
+                                           stream)
+        else:
+            fln.fused_proj_add_rmsnorm(dx, W, dr, gamma, wl.eps, wl.norm_kind, args.microchunk, do, stream)
         ho.copy_(do, non_blocking=True)
         hr_out.copy_(dr, non_blocking=True)
 
@@ -354,24 +390,38 @@ def run_e2e(args, wl, d, W, gamma, device, stream, fln):
     barrier(device)
     s = max_over_ranks(e0.elapsed_time(e1) / 1e3, device)
     _, world, _ = dist_env()
+    h2d = hx.numel() * hx.element_size() + hr.numel() * 2 + (hsx.numel() * 4 if f8 else 0)
     return {"value": round(whole_job_value(wl.flops() * n, world, s) / 1e12, 2), "unit": "TFLOP/s",
-            "h2d_bytes_per_step": 2 * T * K + 2 * T * H, "d2h_bytes_per_step": 4 * T * H, "steps": n,
-            "ms_per_step": round(s * 1e3 / n, 4), "weights": "W and gamma resident on the device"}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4 * T * H, "steps": n,
+            "ms_per_step": round(s * 1e3 / n, 4), "weights": "W, its scales and gamma resident on the device"}
 
 
-def run_comparator(args, wl, x, W, d, gamma, device, stream, fln, flush):
-    """Unfused sequence: cuBLAS bf16 GEMM (torch.matmul) then the library's add_rmsnorm."""
+def run_comparator(args, wl, x, W, d, gamma, device, stream, fln, flush, sx=None, sw=None):
+    """Unfused sequence: cuBLAS bf16 GEMM (torch.matmul) then the library's
+    add_rmsnorm (bf16 operands only)."""
     import numpy as np
     import torch
+    f8 = args.dtype == "e4m3"
     r = torch.from_numpy(np.ascontiguousarray(d["r0"]).view(np.int16)).view(torch.bfloat16).to(device)
     out = torch.empty_like(r)
+    T, H = r.shape
+    if f8:
+        # torch._scaled_mm with row-wise scales ended in an unspecified launch
+        # failure (Xid 43) on this GPU under PyTorch 2.9.1 (its kernel prints
+        # that it was built without sm_90+ TMA support); it is not run again
+        return {"unavailable": "torch._scaled_mm row-wise FP8 faulted on GB300 under PyTorch 2.9.1 "
+                               "(unspecified launch failure, Xid 43); not run"}
+    else:
+        def gemm():
+            return torch.matmul(x, W.t())
+        what = "torch.matmul (cuBLAS, bf16 out) then add_rmsnorm; y rounded to bf16 before the add"
     times = []
     for i in range(args.warmup + max(5, args.steps // 4)):
         flush.fill_(float(i))
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        y = torch.matmul(x, W.t())
+        y = gemm()
         fln.add_rmsnorm(y, r, gamma, wl.eps, wl.norm_kind, out, stream)
         e1.record(stream)
         times.append((e0, e1))
@@ -379,7 +429,7 @@ def run_comparator(args, wl, x, W, d, gamma, device, stream, fln, flush):
     ms = [a.elapsed_time(b) for a, b in times[args.warmup:]]
     m = sum(ms) / len(ms)
     return {"value": round(wl.flops() / (m * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(m, 5),
-            "what": "torch.matmul (cuBLAS, bf16 out) then add_rmsnorm; y rounded to bf16 before the add"}
+            "what": what}
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -387,8 +437,13 @@ def _oracle_rows_timed(wl, d, rows, nthreads=0):
     import numpy as np
     import oracle
     t = time.time()
-    oracle.proj_add_rmsnorm(d["x"], d["W"], d["r0"], d["gamma"], wl.eps, wl.norm_kind,
-                            rows=np.asarray(rows, np.int64), nthreads=nthreads)
+    rows = np.asarray(rows, np.int64)
+    if "x8" in d:
+        oracle.proj_add_rmsnorm_fp8(d["x8"], d["x_scale"], d["W8"], d["w_scale"], d["r0"], d["gamma"], wl.eps,
+                                    wl.norm_kind, rows=rows, nthreads=nthreads)
+    else:
+        oracle.proj_add_rmsnorm(d["x"], d["W"], d["r0"], d["gamma"], wl.eps, wl.norm_kind, rows=rows,
+                                nthreads=nthreads)
     return time.time() - t
 
 
@@ -408,7 +463,7 @@ def cpu_baseline(wl, d, seconds: float):
 def run_reference(args):
     """--impl reference: the oracle timed on host cores, same metric/unit/config."""
     import oracle
-    from synth import make_inputs, workload
+    from synth import make_inputs, make_inputs_fp8, workload
     rank, world, _ = dist_env()
     if rank != 0:
         return None
@@ -416,7 +471,7 @@ def run_reference(args):
     if args.tokens:
         wl = wl.with_tokens(args.tokens)
     oracle.build()
-    d = make_inputs(wl)
+    d = make_inputs_fp8(wl) if args.dtype == "e4m3" else make_inputs(wl)
     cores = oracle.max_threads()
     # rows per step sized so that warm-up + steps stay within about a minute
     probe = min(wl.T, max(1, cores))
@@ -430,11 +485,12 @@ def run_reference(args):
         total += _oracle_rows_timed(wl, d, [(i * rows + j) % wl.T for j in range(rows)])
     flops = 2.0 * rows * wl.K * wl.H * args.steps
     value = flops / total / 1e12
-    sample = f"{rows} of {wl.T} token rows per step of {wl.name} (fp64 oracle, OpenMP over rows)"
+    sample = f"{rows} of {wl.T} token rows per step of {wl.name} ({args.dtype} inputs, fp64 oracle, OpenMP over rows)"
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total * 1e3 / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "K": wl.K, "H": wl.H},
+            "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "K": wl.K, "H": wl.H,
+                                            "operands": args.dtype},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -454,6 +510,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the cpu_baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0, help="--impl reference: CPU work of the whole run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtype", choices=["bf16", "e4m3"], default="bf16",
+                    help="operand type of x and W (e4m3: FP8 with per-token / per-channel scales)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -218,7 +218,7 @@ def run_gpu(args):
         fln.fln_set_plan(K, H, wl.norm_kind, dict(
             path=path, microchunk_tokens=int(f[1]), tile_n=int(f[2]), gemm_ctas=int(f[3]),
             norm_ctas=int(f[4]) if len(f) > 4 else 0, threshold_tokens=1 if T > 256 else 257,
-            tuned_max_tokens=0), dtype=dt)
+            tuned_max_tokens=0, epi_warps=int(f[5]) if len(f) > 5 else 0), dtype=dt)
     t_tune = time.time() - t_tune
     plan = fln.fln_get_plan(K, H, wl.norm_kind, T, args.microchunk, dtype=dt)
 
@@ -506,7 +506,8 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=0, help="override T of the workload")
     ap.add_argument("--microchunk", type=int, default=0, help="0 = tuned plan")
     ap.add_argument("--plan", default="auto",
-                    help="auto (tune the group) or path:chunk:tile:gemm_ctas[:norm_ctas], path fused|pipelined")
+                    help="auto (tune the group) or path:chunk:tile:gemm_ctas[:norm_ctas[:epi_warps]], "
+                         "path fused|pipelined")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the cpu_baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0, help="--impl reference: CPU work of the whole run")
     ap.add_argument("--no-cpu-baseline", action="store_true")

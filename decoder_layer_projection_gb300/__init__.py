@@ -55,7 +55,7 @@ class FlnError(RuntimeError):
 class Plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("microchunk_tokens", ctypes.c_int), ("tile_n", ctypes.c_int),
                 ("gemm_ctas", ctypes.c_int), ("norm_ctas", ctypes.c_int), ("threshold_tokens", ctypes.c_int),
-                ("tuned_max_tokens", ctypes.c_int)]
+                ("tuned_max_tokens", ctypes.c_int), ("epi_warps", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

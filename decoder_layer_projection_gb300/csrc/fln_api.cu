@@ -87,7 +87,8 @@ struct Workspace {
   cudaEvent_t ev_join = nullptr;
   unsigned int gen = 0;
   bool prepared[2][3][5] = {};     // [operand type][epilogue][tile]
-  int pair_max[2][4] = {};         // resident CTA pairs of the fused pair kernel, [operand type][tile 128/192/224/256]
+  int pair_max[2][2][4] = {};      // resident CTA pairs of the fused pair kernel,
+                                   // [operand type][4 / 8 epilogue warps][tile 128/192/224/256]
 };
 
 std::mutex g_mu;
@@ -193,18 +194,20 @@ int prepare_kernel(Workspace* ws, int bn, EpilogueKind epi, int f8) {
 
 int pair_index(int bn) { return bn == 128 ? 0 : bn == 192 ? 1 : bn == 224 ? 2 : bn == 256 ? 3 : -1; }
 
-int prepare_pair(Workspace* ws, int bn, int f8, int* max_pairs) {
+int prepare_pair(Workspace* ws, int bn, int f8, int ew, int* max_pairs) {
   const int i = pair_index(bn);
   if (i < 0) return fail(FLN_ERR_UNSUPPORTED, "fused tile width %d", bn);
-  if (ws->pair_max[f8][i] == 0) {
+  const int e = ew == 8 ? 1 : 0;
+  if (ws->pair_max[f8][e][i] == 0) {
     int mp = 0;
-    FLN_CUDA(pair_gemm_prepare(bn, f8, &mp), "pair kernel set-up (shared memory limit, resident clusters)");
+    FLN_CUDA(pair_gemm_prepare(bn, f8, ew, &mp), "pair kernel set-up (shared memory limit, resident clusters)");
     if (mp < 1) return fail(FLN_ERR_UNSUPPORTED, "no CTA pair of the fused kernel fits on this device");
-    ws->pair_max[f8][i] = mp;
+    ws->pair_max[f8][e][i] = mp;
   }
-  *max_pairs = ws->pair_max[f8][i];
+  *max_pairs = ws->pair_max[f8][e][i];
   return FLN_OK;
 }
+
 
 // ------------------------------------------------------------------ launches
 template <typename F>
@@ -274,6 +277,14 @@ struct Call {
   int esize() const { return f8 ? 1 : 2; }
   int k_blocks() const { return (K + kblock_elems(f8) - 1) / kblock_elems(f8); }
 };
+
+// Epilogue warps of the fused kernel: the plan's choice, else eight for FP8
+// operands with short K loops (at most 48 K-blocks; there the epilogue, not
+// the mainloop, bounds a tile) on tiles 224 / 256, else four.
+int epi_warps_for(const fln_plan& pl, const Call& c) {
+  if (pl.epi_warps) return pl.epi_warps;
+  return (c.f8 && c.k_blocks() <= 48 && (pl.tile_n == 224 || pl.tile_n == 256)) ? 8 : 4;
+}
 
 void set_scales(GemmParams& p, const Call& c) {
   p.x_scale = c.x_scale;
@@ -395,7 +406,8 @@ int gemm_grid(Workspace* ws, const fln_plan& pl, long long tiles) {
 int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
   const int bn = pl.tile_n;
   int max_pairs = 0;
-  int rc = prepare_pair(ws, bn, c.f8, &max_pairs);
+  const int ew = epi_warps_for(pl, c);
+  int rc = prepare_pair(ws, bn, c.f8, ew, &max_pairs);
   if (rc) return rc;
   CUtensorMap tmA, tmB;
   if ((rc = make_map(&tmA, c.x, c.K, c.T, 128, c.esize()))) return rc;
@@ -403,9 +415,10 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
   const int chunk = std::min(pl.microchunk_tokens, c.T);
   const int mt_alloc = 2 * ((chunk + 255) / 256);  // 128-row blocks, rounded up to whole pairs
   const int nt = (c.H + bn - 1) / bn;
-  // row partial sums: one 64-bit {generation, value} word per row and N-tile,
-  // zeroed once at allocation (no launch uses generation 0)
-  if ((rc = grow(&ws->psum, &ws->psum_floats, 2 * static_cast<size_t>(mt_alloc) * nt * 128, true,
+  // row partial sums: one 64-bit {generation, value} word per row, N-tile and
+  // epilogue warp of the row (up to two), zeroed once at allocation (no launch
+  // uses generation 0)
+  if ((rc = grow(&ws->psum, &ws->psum_floats, 4 * static_cast<size_t>(mt_alloc) * nt * 128, true,
                  "cudaMalloc(row sums)")))
     return rc;
   for (int c0 = 0; c0 < c.T; c0 += chunk) {
@@ -444,7 +457,9 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     if (pl.gemm_ctas > 0) pairs = std::min(pairs, std::max(1, pl.gemm_ctas / 2));
     pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(pairs, tiles)));
     rc = launch_counted(FLN_KERNEL_GEMM_FUSED, c.stream,
-                        [&] { return launch_gemm_pair_fused(bn, c.f8, tmA, tmB, tmR, tmRs, tmOs, p, pairs, c.stream); },
+                        [&] {
+                          return launch_gemm_pair_fused(bn, c.f8, ew, tmA, tmB, tmR, tmRs, tmOs, p, pairs, c.stream);
+                        },
                         "fused pair GEMM launch");
     if (rc) return rc;
   }
@@ -558,6 +573,7 @@ fln_plan default_plan() {
   p.norm_ctas = 0;
   p.threshold_tokens = kDefaultThreshold;
   p.tuned_max_tokens = 0;
+  p.epi_warps = 0;
   return p;
 }
 
@@ -574,6 +590,10 @@ int check_plan(const fln_plan& p) {
   if (p.threshold_tokens < 1 || p.threshold_tokens > kDefaultThreshold)
     return fail(FLN_ERR_INVALID_ARG, "plan.threshold_tokens must be in 1..%d", kDefaultThreshold);
   if (p.tuned_max_tokens < 0) return fail(FLN_ERR_INVALID_ARG, "plan.tuned_max_tokens must be >= 0");
+  if (p.epi_warps != 0 && p.epi_warps != 4 && p.epi_warps != 8)
+    return fail(FLN_ERR_INVALID_ARG, "plan.epi_warps must be 0, 4 or 8");
+  if (p.epi_warps == 8 && (p.path != FLN_PATH_FUSED || (p.tile_n != 224 && p.tile_n != 256)))
+    return fail(FLN_ERR_INVALID_ARG, "plan.epi_warps 8 is available on the FUSED path with tile 224 or 256");
   return FLN_OK;
 }
 
@@ -1034,9 +1054,11 @@ int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, f
       for (int cch : chunks) {
         for (int g : ctas) {
           for (int nc : (path == FLN_PATH_PIPELINED ? std::vector<int>{0, ws->sms / 4} : std::vector<int>{0})) {
+           for (int ew : (path == FLN_PATH_FUSED && tile >= 224 ? std::vector<int>{4, 8} : std::vector<int>{4})) {
             fln_plan pl = default_plan();
             pl.path = path;
             pl.tile_n = tile;
+            pl.epi_warps = ew;
             pl.microchunk_tokens = cch;
             pl.gemm_ctas = g;
             pl.norm_ctas = nc;
@@ -1057,6 +1079,7 @@ int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, f
               best = pl;
               any = true;
             }
+           }
           }
         }
       }

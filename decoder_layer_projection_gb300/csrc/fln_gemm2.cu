@@ -13,16 +13,17 @@
 // halves, and each CTA's TMEM receives its own 128 rows.  Per SM this halves
 // the W traffic of a 128 x BN tile.
 //
-// Epilogue (warps 2-5 of each CTA, one TMEM lane = one row per thread): the
-// residual streams through a ring of three 128-byte-swizzled 128 x 64 TMA
-// boxes, once for each phase; with 16 KiB of output staging the epilogue
-// holds 64 KiB of shared memory and the operand ring keeps 5 stages at
-// BN = 256.  Phase 1 forms r = r0 + acc in fp32
-// and the row's partial sum of squares; the row block's partial sums of all
-// N-tiles are exchanged through global memory as 64-bit {launch generation,
-// value} words (fixed summation order); phase 2 reads r back from TMEM, stages
-// bf16(r * rstd * g) in shared memory and each warp writes its 32 rows back
-// with TMA stores, rows past the chunk and columns past H clipped.
+// Epilogue (eight warps per CTA: each quarter of the TMEM lanes, i.e. 32
+// rows, is shared by two warps that split every 64-column box into halves):
+// the residual streams through a ring of three 128-byte-swizzled 128 x 64 TMA
+// boxes; with 16 KiB of output staging the epilogue holds 64 KiB of shared
+// memory and the operand ring keeps 5 stages at BN = 256.  Phase 1 forms
+// r = r0 + acc in fp32 and each warp's part of the row's sum of squares; the
+// row block's partial sums of all N-tiles and halves are exchanged through
+// global memory as 64-bit {launch generation, value} words (fixed summation
+// order); phase 2 reads r back from TMEM, stages bf16(r * rstd * g) in shared
+// memory and one warp of each pair writes the 32 x 64 block with a TMA store,
+// rows past the chunk and columns past H clipped.
 //
 // FP8 (E4M3) operands: the same kernel with kind::f8f6f4 MMAs over 128-byte
 // K-blocks of 128 elements; phase 1 scales the accumulator by the token's and
@@ -41,7 +42,9 @@ namespace pair {
 
 constexpr int BM = 128;  // rows per CTA (256 per pair)
 constexpr int BK = 64;
-constexpr int THREADS = 224;  // warps: 0 producer, 1 MMA / TMEM, 2-5 epilogue, 6 residual loader
+// warps: 0 producer, 1 MMA / TMEM, 2-5 epilogue, 6 residual loader, and with
+// eight epilogue warps 7-10 as well
+__host__ __device__ constexpr int threads_for(int ew) { return ew == 8 ? 352 : 224; }
 constexpr int SMEM_LIMIT = 232448;  // 227 KiB opt-in per block
 constexpr int BAR_BYTES = 512;
 
@@ -69,8 +72,8 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <int BN, int F8>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int BN, int F8, int EW>
+__global__ void __launch_bounds__(threads_for(EW), 1)
     fln_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmRs,
                          const __grid_constant__ CUtensorMap tmOs, const GemmParams p) {
@@ -111,11 +114,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 8);  // 4 epilogue warps in each CTA of the pair
+      mbar_init(&acc_empty[b], 2 * EW);  // the epilogue warps of both CTAs of the pair
     }
     for (int e = 0; e < C::NBOX; ++e) {
       mbar_init(&e_full[e], 1);
-      mbar_init(&e_free[e], 4);  // one arrival per epilogue warp once it has read the box
+      mbar_init(&e_free[e], EW);  // one arrival per epilogue warp once it is done with the box
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -258,14 +261,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       volatile int no_abort = 0;
       mbar_wait(drain_bar, 0, &no_abort, p.err, FLN_DEVERR_TIMEOUT_DRAIN);
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else if (warp >= 2 && warp != 6) {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    const int q = warp & 3;        // TMEM lane quarter of this warp
+    // EW = 4: warps 2-5, one per quarter q = warp % 4 of the TMEM lanes (32
+    // rows), each covering all columns of a box.  EW = 8: the quarter is
+    // shared by warp hx = 0 (warps 2-5) and hx = 1 (warps 7-10); in every
+    // 64-column box warp hx takes the 32 columns [32 hx, 32 hx + 32), and the
+    // pair meets at named barrier 2 + q (64 threads) before hx = 0 issues the
+    // box's TMA store.  Two warps per SM sub-partition hide each other's
+    // TMEM, shared-memory and exchange latencies, which pays where the
+    // mainloop of a tile is short.
+    constexpr int NSPLIT = EW / 4;  // warps per lane quarter
+    const int q = warp & 3;         // TMEM lane quarter of this warp
+    const int hx = warp >= 7 ? 1 : 0;
     const int rl = q * 32 + lane;  // row within this CTA's 128 rows
+    const int pair_bar = 2 + q;
     const uint32_t acc_empty_leader = map_to_cta(smem_u32(&acc_empty[0]), 0);
     constexpr int G = C::GROUPS;
     constexpr int NB = C::NBOX;
-    uint8_t* ostage = sE + C::NBOX * C::BOX + q * (32 * 128);  // this warp's 32 output rows
+    uint8_t* ostage = sE + C::NBOX * C::BOX + q * (32 * 128);  // the quarter's 32 output rows
     unsigned long long* psum = reinterpret_cast<unsigned long long*>(p.psum);
     const unsigned long long tag = static_cast<unsigned long long>(p.gen) << 32;
     int s = 0;  // next residual box to consume
@@ -278,22 +292,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int nt = t % nN;
       const int n0 = nt * BN;
       const int col_end = min(p.N, n0 + BN);
-      const int wrow0 = mtile * BM + q * 32;  // this warp's first row in the chunk
-      // All 128 epilogue threads decide together whether to continue: a thread
-      // that leaves alone would strand the others at the named barrier.
+      const int wrow0 = mtile * BM + q * 32;  // this quarter's first row in the chunk
+      // All epilogue threads decide together whether to continue: a thread
+      // that leaves alone would strand the others at a named barrier.
       bool stop = failed;
       if (!stop && !mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) stop = true;
-      if (named_bar_any(1, 128, stop)) break;
+      if (named_bar_any(1, 32 * EW, stop)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
 
-      // phase 1: r = r0 + acc in fp32 and this tile's partial sum of squares.
-      // The fp32 r replaces the accumulator in TMEM (phase 2 reads it back) and
-      // bf16(r) replaces r0 in the residual box, from where each warp stores
-      // its 32 rows with one TMA store (rows past the chunk and columns past H
-      // are clipped by the tensor map).  A half-used last box (tile 224) is
-      // stored by the threads instead, so the next tile's columns stay intact.
-      // Rows past the chunk and columns past H read zeros: acc and r0 are 0.
+      // phase 1: r = r0 + acc in fp32 and this warp's part of the row's sum of
+      // squares.  The fp32 r replaces the accumulator in TMEM (phase 2 reads
+      // it back) and bf16(r) replaces r0 in the residual box, from where the
+      // quarter's 32 rows go out in one TMA store (rows past the chunk and
+      // columns past H are clipped by the tensor map).  A half-used last box
+      // (tile 224) is stored by the threads of warp hx = 0 instead, so the next
+      // tile's columns stay intact.  Rows past the chunk and columns past H
+      // read zeros: acc and r0 are 0.
       float ss = 0.f;
       int pending = -1;  // box whose TMA store may still be reading it (freed one box later)
       // FP8: this row's token scale (rows past the chunk have a zero accumulator)
@@ -306,7 +321,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_wait(&e_full[s % NB], static_cast<uint32_t>(s / NB) & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
         uint8_t* box = sE + (s % NB) * C::BOX;
 #pragma unroll 1
-        for (int c2 = 0; c2 < halves; ++c2) {
+        for (int c2 = (NSPLIT == 2 ? hx : 0); c2 < halves; c2 += NSPLIT) {
           float v[32];
           const uint32_t ta = tb + static_cast<uint32_t>(g * 64 + c2 * 32);
           tmem_ld32(ta, v);
@@ -337,58 +352,67 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_st32(ta, v);
         }
         if (halves == 2) {
-          fence_proxy_async_smem();  // the box rows are visible to the TMA store
+          fence_proxy_async_smem();  // this warp's rows of the box are visible to the TMA store
           __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmRs, box + q * (32 * 128), n0 + g * 64, wrow0);
-            bulk_commit_group();
-            if (pending >= 0) {
-              bulk_wait_group_read<1>();           // the previous box's store has read its rows
-              mbar_arrive(&e_free[pending % NB]);  // this warp is done with that box
+          if (NSPLIT == 2) named_bar_sync(pair_bar, 64);
+          if (hx == 0) {
+            if (lane == 0) {
+              tma_store_2d(&tmRs, box + q * (32 * 128), n0 + g * 64, wrow0);
+              bulk_commit_group();
+              if (pending >= 0) {
+                bulk_wait_group_read<1>();           // the previous box's store has read its rows
+                mbar_arrive(&e_free[pending % NB]);  // this warp is done with that box
+              }
             }
+            pending = s;
+            __syncwarp();
+          } else if (lane == 0) {
+            mbar_arrive(&e_free[s % NB]);  // the partner stores; this warp is done with box s
           }
-          pending = s;
-          __syncwarp();
         } else {
           __syncwarp();
+          if (hx == 0) {
 #pragma unroll 2
-          for (int it = 0; it < 8; ++it) {
-            const int rr = it * 4 + (lane >> 3);  // row within this warp's 32
-            const int ch = lane & 7;
-            const int lrow = wrow0 + rr;
-            const int col = n0 + g * 64 + ch * 8;
-            if (lrow < p.M && col < col_end) {
-              const size_t off = (static_cast<size_t>(p.a_row0) + lrow) * static_cast<size_t>(p.ld) + col;
-              *reinterpret_cast<uint4*>(p.residual + off) =
-                  *reinterpret_cast<const uint4*>(box + swz(q * 32 + rr, ch));
+            for (int it = 0; it < 8; ++it) {
+              const int rr = it * 4 + (lane >> 3);  // row within this quarter's 32
+              const int ch = lane & 7;
+              const int lrow = wrow0 + rr;
+              const int col = n0 + g * 64 + ch * 8;
+              if (lrow < p.M && col < col_end) {
+                const size_t off = (static_cast<size_t>(p.a_row0) + lrow) * static_cast<size_t>(p.ld) + col;
+                *reinterpret_cast<uint4*>(p.residual + off) =
+                    *reinterpret_cast<const uint4*>(box + swz(q * 32 + rr, ch));
+              }
             }
+            __syncwarp();
           }
-          __syncwarp();
           if (lane == 0) mbar_arrive(&e_free[s % NB]);  // this warp is done with box s
         }
       }
-      if (lane == 0 && pending >= 0) {
+      if (hx == 0 && lane == 0 && pending >= 0) {
         bulk_wait_group_read<0>();
         mbar_arrive(&e_free[pending % NB]);
       }
-      // Row statistics across the row block's N-tiles: each row's partial sum
-      // is published as one 64-bit word {generation of this launch, value}, so a
-      // reader that sees this launch's generation also sees its value; no fence
-      // or flag is needed.  The words are fetched eight at a time and added in
-      // N-tile order.
-      unsigned long long* prow = psum + static_cast<size_t>(mtile) * nN * BM + rl;
-      st_relaxed_gpu_u64(prow + static_cast<size_t>(nt) * BM, tag | __float_as_uint(ss));
+      // Row statistics across the row block's N-tiles: each warp publishes its
+      // rows' partial sums as 64-bit words {generation of this launch, value},
+      // one per (N-tile, half), so a reader that sees this launch's generation
+      // also sees its value; no fence or flag is needed.  Both warps of a
+      // quarter read the 2 nN words of their rows, eight at a time, and add
+      // them in (N-tile, half) order.
+      unsigned long long* prow = psum + static_cast<size_t>(mtile) * nN * NSPLIT * BM + rl;
+      st_relaxed_gpu_u64(prow + static_cast<size_t>(nt * NSPLIT + hx) * BM, tag | __float_as_uint(ss));
+      const int nw = NSPLIT * nN;
       float tot = 0.f;
       bool ok = true;
-      for (int j0 = 0; j0 < nN && ok; j0 += 8) {
+      for (int j0 = 0; j0 < nw && ok; j0 += 8) {
         unsigned long long v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          v[i] = (j0 + i < nN) ? ld_relaxed_gpu_u64(prow + static_cast<size_t>(j0 + i) * BM) : tag;
+          v[i] = (j0 + i < nw) ? ld_relaxed_gpu_u64(prow + static_cast<size_t>(j0 + i) * BM) : tag;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          if (j0 + i >= nN || !ok) continue;
-          // (the test switch makes slot 0 wait for a generation nobody publishes)
+          if (j0 + i >= nw || !ok) continue;
+          // (the test switch makes word 0 wait for a generation nobody publishes)
           const unsigned int want = (p.stall_rowstat && j0 + i == 0) ? p.gen + 1u : p.gen;
           if ((v[i] >> 32) != want) {
             const unsigned long long* f = prow + static_cast<size_t>(j0 + i) * BM;
@@ -406,28 +430,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) {
         if (!*abort_flag) atomicOr(p.err, FLN_DEVERR_TIMEOUT_ROWSTAT);
         *abort_flag = 1;
-        failed = true;  // this warp; the next top-of-loop barrier stops all four
+        failed = true;  // this warp; the next top-of-loop barrier stops all of them
       }
       const bool go = __all_sync(0xffffffffu, ok);
       const float rstd = rsqrtf(tot / static_cast<float>(p.ld) + p.eps);
 
-      // phase 2: out = r * rstd * g from the fp32 r in TMEM, staged in this
-      // warp's 32 output rows and written by one TMA store per warp and box
-      // (threads store a half-used last box themselves).
+      // phase 2: out = r * rstd * g from the fp32 r in TMEM.  Each warp puts
+      // its 32 columns of a box into the quarter's staging rows; once the pair
+      // has met, warp hx = 0 writes the 32 x 64 block with one TMA store (its
+      // threads store a half-used last box themselves).
       tmem_wait_st();
 #pragma unroll 1
       for (int g = 0; g < G; ++g) {
         const int halves = (BN - g * 64) >= 64 ? 2 : 1;
-        uint4 ob[8];  // this box's bf16 outputs, computed before waiting for the staging rows
+        uint4 ob[8];  // this warp's bf16 outputs of the box, computed before waiting for the staging rows
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
+        for (int k = 0; k < 2 / NSPLIT; ++k) {
+          const int c2 = NSPLIT == 2 ? hx : k;
           if (c2 < halves) {
             float v[32];
             tmem_ld32(tb + static_cast<uint32_t>(g * 64 + c2 * 32), v);
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-              const int chunk = c2 * 4 + h;
-              const int cc = n0 + g * 64 + chunk * 8;
+              const int cc = n0 + g * 64 + c2 * 32 + h * 8;
               float gw[8];
               if (cc < p.N) {
                 const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc));
@@ -444,24 +469,33 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const float gj = p.norm_kind ? 1.0f + gw[j] : gw[j];
                 o[j] = v[8 * h + j] * rstd * gj;
               }
-              ob[chunk] = f32x8_to_bf16(o);
+              ob[k * 4 + h] = f32x8_to_bf16(o);
             }
           }
         }
-        if (lane == 0) bulk_wait_group_read<0>();  // the previous box's store has read the staging rows
-        __syncwarp();
-#pragma unroll
-        for (int chunk = 0; chunk < 8; ++chunk)
-          if (chunk < halves * 4) *reinterpret_cast<uint4*>(ostage + swz(lane, chunk)) = ob[chunk];
         if (halves == 2) {
+          // the previous block's store has read the staging rows before they are overwritten
+          if (hx == 0 && lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+          if (NSPLIT == 2) named_bar_sync(pair_bar, 64);
+#pragma unroll
+          for (int k = 0; k < 2 / NSPLIT; ++k) {
+            const int c2 = NSPLIT == 2 ? hx : k;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) *reinterpret_cast<uint4*>(ostage + swz(lane, c2 * 4 + h)) = ob[k * 4 + h];
+          }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && go) {
+          if (NSPLIT == 2) named_bar_sync(pair_bar, 64);
+          if (hx == 0 && lane == 0 && go) {
             tma_store_2d(&tmOs, ostage, n0 + g * 64, wrow0);
             bulk_commit_group();
           }
+        } else if (hx == 0) {
+          if (lane == 0) bulk_wait_group_read<0>();
           __syncwarp();
-        } else {
+#pragma unroll
+          for (int h = 0; h < 4; ++h) *reinterpret_cast<uint4*>(ostage + swz(lane, h)) = ob[h];
           __syncwarp();
           if (go) {
 #pragma unroll 2
@@ -494,13 +528,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
 }
 
-template <int BN, int F8>
+template <int BN, int F8, int EW>
 static cudaError_t launch_pair_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmR,
                                   const CUtensorMap& tmRs, const CUtensorMap& tmOs, const GemmParams& p, int pairs,
                                   cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.blockDim = dim3(threads_for(EW), 1, 1);
   cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -510,17 +544,17 @@ static cudaError_t launch_pair_bn(const CUtensorMap& tmA, const CUtensorMap& tmB
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fln_gemm_pair_kernel<BN, F8>, tmA, tmB, tmR, tmRs, tmOs, p);
+  return cudaLaunchKernelEx(&cfg, fln_gemm_pair_kernel<BN, F8, EW>, tmA, tmB, tmR, tmRs, tmOs, p);
 }
 
-template <int BN, int F8>
+template <int BN, int F8, int EW>
 static cudaError_t prepare_pair_bn(int* max_pairs) {
-  cudaError_t e = cudaFuncSetAttribute(fln_gemm_pair_kernel<BN, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<BN>::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(fln_gemm_pair_kernel<BN, F8, EW>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.blockDim = dim3(threads_for(EW), 1, 1);
   cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -529,49 +563,57 @@ static cudaError_t prepare_pair_bn(int* max_pairs) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(max_pairs, fln_gemm_pair_kernel<BN, F8>, &cfg);
+  return cudaOccupancyMaxActiveClusters(max_pairs, fln_gemm_pair_kernel<BN, F8, EW>, &cfg);
+}
+
+// The instantiated variants: every tile width with four epilogue warps, tile
+// widths 224 and 256 also with eight.
+struct PairArgs {
+  const CUtensorMap *tmA, *tmB, *tmR, *tmRs, *tmOs;
+  const GemmParams* p;
+  int pairs;
+  cudaStream_t stream;
+  int* max_pairs;  // non-null: prepare instead of launch
+};
+
+template <int BN, int F8, int EW>
+static cudaError_t run_variant(const PairArgs& a) {
+  if (a.max_pairs) return prepare_pair_bn<BN, F8, EW>(a.max_pairs);
+  return launch_pair_bn<BN, F8, EW>(*a.tmA, *a.tmB, *a.tmR, *a.tmRs, *a.tmOs, *a.p, a.pairs, a.stream);
+}
+
+template <int F8>
+static cudaError_t dispatch_bn(int bn, int ew, const PairArgs& a) {
+  if (ew == 8) {
+    switch (bn) {
+      case 224: return run_variant<224, F8, 8>(a);
+      case 256: return run_variant<256, F8, 8>(a);
+    }
+    return cudaErrorInvalidValue;
+  }
+  if (ew != 4) return cudaErrorInvalidValue;
+  switch (bn) {
+    case 128: return run_variant<128, F8, 4>(a);
+    case 192: return run_variant<192, F8, 4>(a);
+    case 224: return run_variant<224, F8, 4>(a);
+    case 256: return run_variant<256, F8, 4>(a);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pair
 
-cudaError_t pair_gemm_prepare(int bn, int f8, int* max_pairs) {
-  if (f8) {
-    switch (bn) {
-      case 128: return pair::prepare_pair_bn<128, 1>(max_pairs);
-      case 192: return pair::prepare_pair_bn<192, 1>(max_pairs);
-      case 224: return pair::prepare_pair_bn<224, 1>(max_pairs);
-      case 256: return pair::prepare_pair_bn<256, 1>(max_pairs);
-    }
-    return cudaErrorInvalidValue;
-  }
-  switch (bn) {
-    case 128: return pair::prepare_pair_bn<128, 0>(max_pairs);
-    case 192: return pair::prepare_pair_bn<192, 0>(max_pairs);
-    case 224: return pair::prepare_pair_bn<224, 0>(max_pairs);
-    case 256: return pair::prepare_pair_bn<256, 0>(max_pairs);
-  }
-  return cudaErrorInvalidValue;
+cudaError_t pair_gemm_prepare(int bn, int f8, int ew, int* max_pairs) {
+  pair::PairArgs a{};
+  a.max_pairs = max_pairs;
+  return f8 ? pair::dispatch_bn<1>(bn, ew, a) : pair::dispatch_bn<0>(bn, ew, a);
 }
 
-cudaError_t launch_gemm_pair_fused(int bn, int f8, const CUtensorMap& tmA, const CUtensorMap& tmB,
+cudaError_t launch_gemm_pair_fused(int bn, int f8, int ew, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                    const CUtensorMap& tmR, const CUtensorMap& tmRs, const CUtensorMap& tmOs,
                                    const GemmParams& p, int pairs, cudaStream_t stream) {
-  if (f8) {
-    switch (bn) {
-      case 128: return pair::launch_pair_bn<128, 1>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
-      case 192: return pair::launch_pair_bn<192, 1>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
-      case 224: return pair::launch_pair_bn<224, 1>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
-      case 256: return pair::launch_pair_bn<256, 1>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
-    }
-    return cudaErrorInvalidValue;
-  }
-  switch (bn) {
-    case 128: return pair::launch_pair_bn<128, 0>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
-    case 192: return pair::launch_pair_bn<192, 0>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
-    case 224: return pair::launch_pair_bn<224, 0>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
-    case 256: return pair::launch_pair_bn<256, 0>(tmA, tmB, tmR, tmRs, tmOs, p, pairs, stream);
-  }
-  return cudaErrorInvalidValue;
+  pair::PairArgs a{&tmA, &tmB, &tmR, &tmRs, &tmOs, &p, pairs, stream, nullptr};
+  return f8 ? pair::dispatch_bn<1>(bn, ew, a) : pair::dispatch_bn<0>(bn, ew, a);
 }
 
 }  // namespace fln

@@ -111,13 +111,14 @@ int gemm_stages(int bn);
 cudaError_t gemm_prepare(int bn, EpilogueKind epi, int f8);  // sets max dynamic smem attributes
 
 // CTA-pair (cta_group::2) fused GEMM + add + RMSNorm for tile widths 128,
-// 192, 224, 256.  prepare sets the shared-memory limit and reports how many pairs
+// 192, 224, 256 with four epilogue warps per CTA, or 224, 256 with eight.  prepare sets the shared-memory limit and reports how many pairs
 // can be resident at once (the grid must not exceed it: the pairs exchange
 // row statistics).  tmR maps the chunk's residual rows (read in 128 x 64
 // boxes), tmRs / tmOs the chunk's residual and output rows in 32 x 64 boxes
 // (stores).
-cudaError_t pair_gemm_prepare(int bn, int f8, int* max_pairs);
-cudaError_t launch_gemm_pair_fused(int bn, int f8, const CUtensorMap& tmA, const CUtensorMap& tmB,
+// ew: epilogue warps per CTA, 4 (every tile width) or 8 (tile widths 224, 256).
+cudaError_t pair_gemm_prepare(int bn, int f8, int ew, int* max_pairs);
+cudaError_t launch_gemm_pair_fused(int bn, int f8, int ew, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                    const CUtensorMap& tmR, const CUtensorMap& tmRs, const CUtensorMap& tmOs,
                                    const GemmParams& p, int pairs, cudaStream_t stream);
 

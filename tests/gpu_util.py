@@ -21,9 +21,9 @@ def host_bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def plan(path, chunk=4096, tile_n=256, gemm_ctas=0, norm_ctas=0, threshold=1, tuned_max=0):
+def plan(path, chunk=4096, tile_n=256, gemm_ctas=0, norm_ctas=0, threshold=1, tuned_max=0, epi_warps=0):
     return dict(path=path, microchunk_tokens=chunk, tile_n=tile_n, gemm_ctas=gemm_ctas, norm_ctas=norm_ctas,
-                threshold_tokens=threshold, tuned_max_tokens=tuned_max)
+                threshold_tokens=threshold, tuned_max_tokens=tuned_max, epi_warps=epi_warps)
 
 
 UNFUSED = plan(fln.PATH_FUSED, threshold=257)  # every T <= 256 takes the UNFUSED path

@@ -170,3 +170,17 @@ def test_product_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
                 assert "liboracle" not in text and "oracle.c" not in text, f
+
+
+def test_epilogue_warps_plan_validation(lib):
+    base = dict(path=fln.PATH_FUSED, microchunk_tokens=512, tile_n=256, gemm_ctas=0, norm_ctas=0,
+                threshold_tokens=1, tuned_max_tokens=0)
+    for bad in (dict(epi_warps=5), dict(epi_warps=8, tile_n=128), dict(epi_warps=8, path=fln.PATH_PIPELINED)):
+        with pytest.raises(fln.FlnError) as e:
+            fln.fln_set_plan(1024, 768, 0, {**base, **bad})
+        assert e.value.status == fln.FLN_ERR_INVALID_ARG and "epi_warps" in e.value.message
+    fln.fln_set_plan(1024, 768, 0, {**base, "epi_warps": 8})
+    try:
+        assert fln.fln_get_plan(1024, 768, 0, 4096)["epi_warps"] == 8
+    finally:
+        fln.fln_set_plan(1024, 768, 0, None)

@@ -19,7 +19,8 @@ pytestmark = pytest.mark.gpu
 fln = pytest.importorskip("decoder_layer_projection_gb300")
 
 
-def test_bounded_wait_timeout_is_reported_and_the_context_survives():
+@pytest.mark.parametrize("epi_warps", [4, 8])
+def test_bounded_wait_timeout_is_reported_and_the_context_survives(epi_warps):
     fln.build()
     fln.load()
     wl = Workload("stall", T=300, K=256, H=512, eps=1e-5, r_sigma=2.0, seed=31)
@@ -28,12 +29,12 @@ def test_bounded_wait_timeout_is_reported_and_the_context_survives():
     fln.fln_device_status()  # nothing pending
     fln.fln_debug_stall_next_call(True)
     with pytest.raises(fln.FlnError) as e:
-        run(plan(fln.PATH_FUSED, chunk=4096, tile_n=256))
+        run(plan(fln.PATH_FUSED, chunk=4096, tile_n=256, epi_warps=epi_warps))
     assert e.value.status == fln.FLN_ERR_DEVICE_TIMEOUT
     assert "bounded wait" in str(e.value)
     # the error word was read and cleared; the context still computes correctly
     fln.fln_device_status()
-    rb, ob = run(plan(fln.PATH_FUSED, chunk=4096, tile_n=256))
+    rb, ob = run(plan(fln.PATH_FUSED, chunk=4096, tile_n=256, epi_warps=epi_warps))
     r, o, _ = oracle.proj_add_rmsnorm(d["x"], d["W"], d["r0"], d["gamma"], wl.eps, wl.norm_kind)
     compare(rb, r, "after timeout: residual")
     compare(ob, o, "after timeout: out")

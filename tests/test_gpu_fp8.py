@@ -112,6 +112,15 @@ def test_small_paths_full_parity(wl, path, tile):
     check(rb, ob, d, wl, name=f"{wl.name} fp8 path={path} tile={tile}")
 
 
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("tile,ew", [(256, 8), (224, 8), (256, 4)])
+def test_epilogue_warps_full_parity(wl, tile, ew):
+    d = make_inputs_fp8(wl)
+    run = Run8(d, wl.eps, wl.norm_kind)
+    rb, ob = run(plan(fln.PATH_FUSED, chunk=128, tile_n=tile, epi_warps=ew))
+    check(rb, ob, d, wl, name=f"{wl.name} fp8 tile={tile} epi_warps={ew}")
+
+
 @pytest.mark.parametrize("wl", SMALL[:3], ids=lambda w: w.name)
 @pytest.mark.parametrize("per_token,per_channel", [(False, False), (True, False), (False, True)])
 def test_scale_granularities(wl, per_token, per_channel):

@@ -64,6 +64,29 @@ def test_small_prefill_paths_full_parity(wl, path, tile):
     check_rows(rb, ob, d, wl, name=f"{wl.name} path={path} tile={tile}")
 
 
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("tile", [256, 224])
+def test_eight_epilogue_warps_full_parity(wl, tile):
+    d = make_inputs(wl)
+    run = Run(d, wl.eps, wl.norm_kind)
+    rb, ob = run(plan(1, chunk=128, tile_n=tile, epi_warps=8))
+    check_rows(rb, ob, d, wl, name=f"{wl.name} fused tile={tile} epi_warps=8")
+
+
+def test_epilogue_width_does_not_change_the_layout_of_work():
+    # four or eight epilogue warps: same tiles, same rows, results within the gate
+    wl = Workload("ew", T=700, K=320, H=1024, eps=1e-5, r_sigma=2.0, seed=21)
+    d = make_inputs(wl)
+    run = Run(d, wl.eps, wl.norm_kind)
+    for c in (128, 700):
+        a = run(plan(1, chunk=c, tile_n=256, epi_warps=4))
+        b = run(plan(1, chunk=c, tile_n=256, epi_warps=8))
+        check_rows(a[0], a[1], d, wl, name=f"ew4 chunk={c}")
+        check_rows(b[0], b[1], d, wl, name=f"ew8 chunk={c}")
+        # r is the same fp32 sum rounded once: bit-identical; out differs only through the row sum's order
+        assert np.array_equal(a[0], b[0])
+
+
 @pytest.mark.parametrize("wl", SMALL[:3], ids=lambda w: w.name)
 @pytest.mark.parametrize("T", [1, 7, 16, 33, 128, 256])
 def test_small_unfused_full_parity(wl, T):

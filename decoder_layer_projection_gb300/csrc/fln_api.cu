@@ -278,9 +278,10 @@ struct Call {
   int k_blocks() const { return (K + kblock_elems(f8) - 1) / kblock_elems(f8); }
 };
 
-// Epilogue warps of the fused kernel: the plan's choice, else eight for FP8
-// operands with short K loops (at most 48 K-blocks; there the epilogue, not
-// the mainloop, bounds a tile) on tiles 224 / 256, else four.
+// Epilogue warps of the fused kernel: the plan's choice, else eight (two
+// groups taking alternate tiles) for FP8 operands with short K loops (at most
+// 48 K-blocks; there the epilogue, not the mainloop, bounds a tile) on tiles
+// 224 / 256, else four.
 int epi_warps_for(const fln_plan& pl, const Call& c) {
   if (pl.epi_warps) return pl.epi_warps;
   return (c.f8 && c.k_blocks() <= 48 && (pl.tile_n == 224 || pl.tile_n == 256)) ? 8 : 4;
@@ -415,10 +416,9 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
   const int chunk = std::min(pl.microchunk_tokens, c.T);
   const int mt_alloc = 2 * ((chunk + 255) / 256);  // 128-row blocks, rounded up to whole pairs
   const int nt = (c.H + bn - 1) / bn;
-  // row partial sums: one 64-bit {generation, value} word per row, N-tile and
-  // epilogue warp of the row (up to two), zeroed once at allocation (no launch
-  // uses generation 0)
-  if ((rc = grow(&ws->psum, &ws->psum_floats, 4 * static_cast<size_t>(mt_alloc) * nt * 128, true,
+  // row partial sums: one 64-bit {generation, value} word per row and N-tile,
+  // zeroed once at allocation (no launch uses generation 0)
+  if ((rc = grow(&ws->psum, &ws->psum_floats, 2 * static_cast<size_t>(mt_alloc) * nt * 128, true,
                  "cudaMalloc(row sums)")))
     return rc;
   for (int c0 = 0; c0 < c.T; c0 += chunk) {

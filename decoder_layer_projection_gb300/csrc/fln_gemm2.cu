@@ -13,17 +13,16 @@
 // halves, and each CTA's TMEM receives its own 128 rows.  Per SM this halves
 // the W traffic of a 128 x BN tile.
 //
-// Epilogue (eight warps per CTA: each quarter of the TMEM lanes, i.e. 32
-// rows, is shared by two warps that split every 64-column box into halves):
-// the residual streams through a ring of three 128-byte-swizzled 128 x 64 TMA
-// boxes; with 16 KiB of output staging the epilogue holds 64 KiB of shared
-// memory and the operand ring keeps 5 stages at BN = 256.  Phase 1 forms
-// r = r0 + acc in fp32 and each warp's part of the row's sum of squares; the
-// row block's partial sums of all N-tiles and halves are exchanged through
-// global memory as 64-bit {launch generation, value} words (fixed summation
-// order); phase 2 reads r back from TMEM, stages bf16(r * rstd * g) in shared
-// memory and one warp of each pair writes the 32 x 64 block with a TMA store,
-// rows past the chunk and columns past H clipped.
+// Epilogue (four warps per CTA, one TMEM lane = one row per thread; or two
+// such groups taking alternate tiles): the residual streams through a ring of
+// three 128-byte-swizzled 128 x 64 TMA boxes; with 16 KiB of output staging
+// the epilogue holds 64 KiB of shared memory and the operand ring keeps 5
+// stages at BN = 256.  Phase 1 forms r = r0 + acc in fp32 and the row's
+// partial sum of squares; the row block's partial sums of all N-tiles are
+// exchanged through global memory as 64-bit {launch generation, value} words
+// (fixed summation order); phase 2 reads r back from TMEM, stages
+// bf16(r * rstd * g) in shared memory and each warp writes its 32 rows back
+// with TMA stores, rows past the chunk and columns past H clipped.
 //
 // FP8 (E4M3) operands: the same kernel with kind::f8f6f4 MMAs over 128-byte
 // K-blocks of 128 elements; phase 1 scales the accumulator by the token's and
@@ -93,7 +92,8 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
   uint64_t* e_full = acc_empty + 2;
   uint64_t* e_free = e_full + C::NBOX;
   uint64_t* drain_bar = e_free + C::NBOX;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint64_t* stg_done = drain_bar + 1;  // eight epilogue warps: per quarter, staging rows handed on
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(stg_done + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* epi_abort = abort_flag + 1;
 
@@ -114,13 +114,14 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 2 * EW);  // the epilogue warps of both CTAs of the pair
+      mbar_init(&acc_empty[b], 8);  // the buffer's four epilogue warps in each CTA of the pair
     }
     for (int e = 0; e < C::NBOX; ++e) {
       mbar_init(&e_full[e], 1);
-      mbar_init(&e_free[e], EW);  // one arrival per epilogue warp once it is done with the box
+      mbar_init(&e_free[e], 4);  // one arrival per warp of the consuming group once it is done with the box
     }
     mbar_init(drain_bar, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&stg_done[i], 1);
     *abort_flag = 0;
     *epi_abort = 0;
     fence_mbar_init();
@@ -263,52 +264,52 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
     }
   } else if (warp >= 2 && warp != 6) {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    // EW = 4: warps 2-5, one per quarter q = warp % 4 of the TMEM lanes (32
-    // rows), each covering all columns of a box.  EW = 8: the quarter is
-    // shared by warp hx = 0 (warps 2-5) and hx = 1 (warps 7-10); in every
-    // 64-column box warp hx takes the 32 columns [32 hx, 32 hx + 32), and the
-    // pair meets at named barrier 2 + q (64 threads) before hx = 0 issues the
-    // box's TMA store.  Two warps per SM sub-partition hide each other's
-    // TMEM, shared-memory and exchange latencies, which pays where the
-    // mainloop of a tile is short.
-    constexpr int NSPLIT = EW / 4;  // warps per lane quarter
-    const int q = warp & 3;         // TMEM lane quarter of this warp
-    const int hx = warp >= 7 ? 1 : 0;
+    // A group of four warps, one per quarter q = warp % 4 of the TMEM lanes
+    // (32 rows), each warp covering all columns of its rows.  EW = 4: warps
+    // 2-5 handle every tile of the pair.  EW = 8: warps 2-5 and 7-10 form two
+    // groups that take alternate tiles, so that one group's wait for the row
+    // statistics and its phase 2 overlap the other group's phase 1; the
+    // pair's k-th tile uses TMEM buffer k % 2, i.e. always its group's.  The
+    // groups share each quarter's output staging rows, passed on from tile to
+    // tile in order through one mbarrier per quarter.
+    constexpr int NG = EW / 4;    // epilogue groups
+    const int q = warp & 3;       // TMEM lane quarter of this warp
+    const int grp = warp >= 7 ? 1 : 0;
     const int rl = q * 32 + lane;  // row within this CTA's 128 rows
-    const int pair_bar = 2 + q;
     const uint32_t acc_empty_leader = map_to_cta(smem_u32(&acc_empty[0]), 0);
     constexpr int G = C::GROUPS;
     constexpr int NB = C::NBOX;
     uint8_t* ostage = sE + C::NBOX * C::BOX + q * (32 * 128);  // the quarter's 32 output rows
     unsigned long long* psum = reinterpret_cast<unsigned long long*>(p.psum);
     const unsigned long long tag = static_cast<unsigned long long>(p.gen) << 32;
-    int s = 0;  // next residual box to consume
-    int local = 0;
+    int local = 0;        // k: the pair's k-th tile
     bool failed = false;  // a row-statistics wait of this warp gave up
     for (int t = pair_id; t < total; t += num_pairs, ++local) {
+      if (NG == 2 && (local & 1) != grp) continue;  // the other group's tile
+      int s = local * G;  // this tile's first residual box
       const int b = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       const int mtile = (t / nN) * 2 + static_cast<int>(rank);  // 128-row block index in the launch
       const int nt = t % nN;
       const int n0 = nt * BN;
       const int col_end = min(p.N, n0 + BN);
-      const int wrow0 = mtile * BM + q * 32;  // this quarter's first row in the chunk
+      const int wrow0 = mtile * BM + q * 32;  // this warp's first row in the chunk
       // All epilogue threads decide together whether to continue: a thread
       // that leaves alone would strand the others at a named barrier.
       bool stop = failed;
       if (!stop && !mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) stop = true;
-      if (named_bar_any(1, 32 * EW, stop)) break;
+      if (named_bar_any(1 + grp, 128, stop)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
 
-      // phase 1: r = r0 + acc in fp32 and this warp's part of the row's sum of
-      // squares.  The fp32 r replaces the accumulator in TMEM (phase 2 reads
-      // it back) and bf16(r) replaces r0 in the residual box, from where the
-      // quarter's 32 rows go out in one TMA store (rows past the chunk and
+      // phase 1: r = r0 + acc in fp32 and the row's partial sum of squares
+      // over this tile.  The fp32 r replaces the accumulator in TMEM (phase 2
+      // reads it back) and bf16(r) replaces r0 in the residual box, from where
+      // each warp's 32 rows go out in one TMA store (rows past the chunk and
       // columns past H are clipped by the tensor map).  A half-used last box
-      // (tile 224) is stored by the threads of warp hx = 0 instead, so the next
-      // tile's columns stay intact.  Rows past the chunk and columns past H
-      // read zeros: acc and r0 are 0.
+      // (tile 224) is stored by the threads instead, so the next tile's
+      // columns stay intact.  Rows past the chunk and columns past H read
+      // zeros: acc and r0 are 0.
       float ss = 0.f;
       int pending = -1;  // box whose TMA store may still be reading it (freed one box later)
       // FP8: this row's token scale (rows past the chunk have a zero accumulator)
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
         mbar_wait(&e_full[s % NB], static_cast<uint32_t>(s / NB) & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC);
         uint8_t* box = sE + (s % NB) * C::BOX;
 #pragma unroll 1
-        for (int c2 = (NSPLIT == 2 ? hx : 0); c2 < halves; c2 += NSPLIT) {
+        for (int c2 = 0; c2 < halves; ++c2) {
           float v[32];
           const uint32_t ta = tb + static_cast<uint32_t>(g * 64 + c2 * 32);
           tmem_ld32(ta, v);
@@ -352,56 +353,48 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
           tmem_st32(ta, v);
         }
         if (halves == 2) {
-          fence_proxy_async_smem();  // this warp's rows of the box are visible to the TMA store
+          fence_proxy_async_smem();  // the box rows are visible to the TMA store
           __syncwarp();
-          if (NSPLIT == 2) named_bar_sync(pair_bar, 64);
-          if (hx == 0) {
-            if (lane == 0) {
-              tma_store_2d(&tmRs, box + q * (32 * 128), n0 + g * 64, wrow0);
-              bulk_commit_group();
-              if (pending >= 0) {
-                bulk_wait_group_read<1>();           // the previous box's store has read its rows
-                mbar_arrive(&e_free[pending % NB]);  // this warp is done with that box
-              }
+          if (lane == 0) {
+            tma_store_2d(&tmRs, box + q * (32 * 128), n0 + g * 64, wrow0);
+            bulk_commit_group();
+            if (pending >= 0) {
+              bulk_wait_group_read<1>();           // the previous box's store has read its rows
+              mbar_arrive(&e_free[pending % NB]);  // this warp is done with that box
             }
-            pending = s;
-            __syncwarp();
-          } else if (lane == 0) {
-            mbar_arrive(&e_free[s % NB]);  // the partner stores; this warp is done with box s
           }
+          pending = s;
+          __syncwarp();
         } else {
           __syncwarp();
-          if (hx == 0) {
 #pragma unroll 2
-            for (int it = 0; it < 8; ++it) {
-              const int rr = it * 4 + (lane >> 3);  // row within this quarter's 32
-              const int ch = lane & 7;
-              const int lrow = wrow0 + rr;
-              const int col = n0 + g * 64 + ch * 8;
-              if (lrow < p.M && col < col_end) {
-                const size_t off = (static_cast<size_t>(p.a_row0) + lrow) * static_cast<size_t>(p.ld) + col;
-                *reinterpret_cast<uint4*>(p.residual + off) =
-                    *reinterpret_cast<const uint4*>(box + swz(q * 32 + rr, ch));
-              }
+          for (int it = 0; it < 8; ++it) {
+            const int rr = it * 4 + (lane >> 3);  // row within this warp's 32
+            const int ch = lane & 7;
+            const int lrow = wrow0 + rr;
+            const int col = n0 + g * 64 + ch * 8;
+            if (lrow < p.M && col < col_end) {
+              const size_t off = (static_cast<size_t>(p.a_row0) + lrow) * static_cast<size_t>(p.ld) + col;
+              *reinterpret_cast<uint4*>(p.residual + off) =
+                  *reinterpret_cast<const uint4*>(box + swz(q * 32 + rr, ch));
             }
-            __syncwarp();
           }
+          __syncwarp();
           if (lane == 0) mbar_arrive(&e_free[s % NB]);  // this warp is done with box s
         }
       }
-      if (hx == 0 && lane == 0 && pending >= 0) {
+      if (lane == 0 && pending >= 0) {
         bulk_wait_group_read<0>();
         mbar_arrive(&e_free[pending % NB]);
       }
-      // Row statistics across the row block's N-tiles: each warp publishes its
-      // rows' partial sums as 64-bit words {generation of this launch, value},
-      // one per (N-tile, half), so a reader that sees this launch's generation
-      // also sees its value; no fence or flag is needed.  Both warps of a
-      // quarter read the 2 nN words of their rows, eight at a time, and add
-      // them in (N-tile, half) order.
-      unsigned long long* prow = psum + static_cast<size_t>(mtile) * nN * NSPLIT * BM + rl;
-      st_relaxed_gpu_u64(prow + static_cast<size_t>(nt * NSPLIT + hx) * BM, tag | __float_as_uint(ss));
-      const int nw = NSPLIT * nN;
+      // Row statistics across the row block's N-tiles: each row's partial sum
+      // is published as one 64-bit word {generation of this launch, value}, so a
+      // reader that sees this launch's generation also sees its value; no fence
+      // or flag is needed.  The words are fetched eight at a time and added in
+      // N-tile order.
+      unsigned long long* prow = psum + static_cast<size_t>(mtile) * nN * BM + rl;
+      st_relaxed_gpu_u64(prow + static_cast<size_t>(nt) * BM, tag | __float_as_uint(ss));
+      const int nw = nN;
       float tot = 0.f;
       bool ok = true;
       for (int j0 = 0; j0 < nw && ok; j0 += 8) {
@@ -432,27 +425,33 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
         *abort_flag = 1;
         failed = true;  // this warp; the next top-of-loop barrier stops all of them
       }
-      const bool go = __all_sync(0xffffffffu, ok);
+      bool go = __all_sync(0xffffffffu, ok);
       const float rstd = rsqrtf(tot / static_cast<float>(p.ld) + p.eps);
+      // two groups: the quarter's staging rows are free once the previous
+      // tile's phase 2 has handed them on
+      if (NG == 2 && local >= 1 &&
+          !mbar_wait(&stg_done[q], static_cast<uint32_t>(local - 1) & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) {
+        go = false;
+        failed = true;
+      }
 
-      // phase 2: out = r * rstd * g from the fp32 r in TMEM.  Each warp puts
-      // its 32 columns of a box into the quarter's staging rows; once the pair
-      // has met, warp hx = 0 writes the 32 x 64 block with one TMA store (its
-      // threads store a half-used last box themselves).
+      // phase 2: out = r * rstd * g from the fp32 r in TMEM, staged in this
+      // warp's 32 output rows and written by one TMA store per warp and box
+      // (threads store a half-used last box themselves).
       tmem_wait_st();
 #pragma unroll 1
       for (int g = 0; g < G; ++g) {
         const int halves = (BN - g * 64) >= 64 ? 2 : 1;
-        uint4 ob[8];  // this warp's bf16 outputs of the box, computed before waiting for the staging rows
+        uint4 ob[8];  // this box's bf16 outputs, computed before waiting for the staging rows
 #pragma unroll
-        for (int k = 0; k < 2 / NSPLIT; ++k) {
-          const int c2 = NSPLIT == 2 ? hx : k;
+        for (int c2 = 0; c2 < 2; ++c2) {
           if (c2 < halves) {
             float v[32];
             tmem_ld32(tb + static_cast<uint32_t>(g * 64 + c2 * 32), v);
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-              const int cc = n0 + g * 64 + c2 * 32 + h * 8;
+              const int chunk = c2 * 4 + h;
+              const int cc = n0 + g * 64 + chunk * 8;
               float gw[8];
               if (cc < p.N) {
                 const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc));
@@ -469,33 +468,24 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
                 const float gj = p.norm_kind ? 1.0f + gw[j] : gw[j];
                 o[j] = v[8 * h + j] * rstd * gj;
               }
-              ob[k * 4 + h] = f32x8_to_bf16(o);
+              ob[chunk] = f32x8_to_bf16(o);
             }
           }
         }
+        if (lane == 0) bulk_wait_group_read<0>();  // the previous box's store has read the staging rows
+        __syncwarp();
+#pragma unroll
+        for (int chunk = 0; chunk < 8; ++chunk)
+          if (chunk < halves * 4) *reinterpret_cast<uint4*>(ostage + swz(lane, chunk)) = ob[chunk];
         if (halves == 2) {
-          // the previous block's store has read the staging rows before they are overwritten
-          if (hx == 0 && lane == 0) bulk_wait_group_read<0>();
-          __syncwarp();
-          if (NSPLIT == 2) named_bar_sync(pair_bar, 64);
-#pragma unroll
-          for (int k = 0; k < 2 / NSPLIT; ++k) {
-            const int c2 = NSPLIT == 2 ? hx : k;
-#pragma unroll
-            for (int h = 0; h < 4; ++h) *reinterpret_cast<uint4*>(ostage + swz(lane, c2 * 4 + h)) = ob[k * 4 + h];
-          }
           fence_proxy_async_smem();
           __syncwarp();
-          if (NSPLIT == 2) named_bar_sync(pair_bar, 64);
-          if (hx == 0 && lane == 0 && go) {
+          if (lane == 0 && go) {
             tma_store_2d(&tmOs, ostage, n0 + g * 64, wrow0);
             bulk_commit_group();
           }
-        } else if (hx == 0) {
-          if (lane == 0) bulk_wait_group_read<0>();
           __syncwarp();
-#pragma unroll
-          for (int h = 0; h < 4; ++h) *reinterpret_cast<uint4*>(ostage + swz(lane, h)) = ob[h];
+        } else {
           __syncwarp();
           if (go) {
 #pragma unroll 2
@@ -512,6 +502,14 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
           }
           __syncwarp();
         }
+      }
+      if (NG == 2) {
+        // hand the staging rows on once this tile's last store has read them
+        if (lane == 0) {
+          bulk_wait_group_read<0>();
+          mbar_arrive(&stg_done[q]);
+        }
+        __syncwarp();
       }
       // TMEM reads of this tile are done: hand the accumulator back to the MMA issuer
       tc_fence_before();

@@ -116,7 +116,8 @@ cudaError_t gemm_prepare(int bn, EpilogueKind epi, int f8);  // sets max dynamic
 // row statistics).  tmR maps the chunk's residual rows (read in 128 x 64
 // boxes), tmRs / tmOs the chunk's residual and output rows in 32 x 64 boxes
 // (stores).
-// ew: epilogue warps per CTA, 4 (every tile width) or 8 (tile widths 224, 256).
+// ew: epilogue warps per CTA, 4 (every tile width) or 8 (two groups of four on
+// alternate tiles; tile widths 224, 256).
 cudaError_t pair_gemm_prepare(int bn, int f8, int ew, int* max_pairs);
 cudaError_t launch_gemm_pair_fused(int bn, int f8, int ew, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                    const CUtensorMap& tmR, const CUtensorMap& tmRs, const CUtensorMap& tmOs,

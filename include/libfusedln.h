@@ -90,8 +90,9 @@ typedef struct {
   int norm_ctas;         /* CTA cap of the second-stream add + norm (PIPELINED); 0 = no cap */
   int threshold_tokens;  /* T < threshold -> UNFUSED; 1..257 (UNFUSED handles T <= 256) */
   int tuned_max_tokens;  /* largest T the plan was profiled for; 0 = not profiled */
-  int epi_warps;         /* FUSED: epilogue warps per CTA, 4 or 8 (8: tile 224 or 256 only);
-                            0 = automatic (8 for FP8 operands with K <= 6144 on tiles 224 / 256, else 4) */
+  int epi_warps;         /* FUSED: epilogue warps per CTA, 4, or 8 = two groups of four taking
+                            alternate tiles (tile 224 or 256 only); 0 = automatic (8 for FP8
+                            operands with K <= 6144 on tiles 224 / 256, else 4) */
 } fln_plan;
 
 /*

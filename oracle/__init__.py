@@ -1,5 +1,6 @@
 """fp64 CPU oracle for y = x.W^T, r = r0 + y, out = RMSNorm(r), with bf16
-operands or FP8 (E4M3) operands and their dequantisation scales.
+operands, FP8 (E4M3) operands and their dequantisation scales, or NVFP4
+weights (E2M1 codes, E4M3 block scales, an fp32 tensor scale).
 
 TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
 CPU-baseline / reference leg may import this package; the library under
@@ -63,6 +64,11 @@ def _bind(path):
         p, p, ctypes.c_int, p, p, ctypes.c_int, p, p, ctypes.c_double, ctypes.c_int, L, L, L, p, L, p, p, p,
         ctypes.c_int]
     lib.oracle_proj_add_rmsnorm_fp8.restype = ctypes.c_int
+    lib.oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e2m1_to_double.restype = ctypes.c_double
+    lib.oracle_proj_add_rmsnorm_nvfp4.argtypes = [
+        p, p, p, ctypes.c_float, p, p, ctypes.c_double, ctypes.c_int, L, L, L, p, L, p, p, p, ctypes.c_int]
+    lib.oracle_proj_add_rmsnorm_nvfp4.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -190,6 +196,44 @@ def proj_add_rmsnorm_fp8(x, x_scale, W, w_scale, r0, gamma, eps, norm_kind, rows
     rc = lib.oracle_proj_add_rmsnorm_fp8(_ptr(x), _ptr(sx), sx_row, _ptr(W), _ptr(sw), sw_row, _ptr(r0),
                                          _ptr(gamma), float(eps), int(norm_kind), T, K, H, _ptr(rows_arr), n,
                                          _ptr(r), _ptr(o), _ptr(ms), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return r, o, ms
+
+
+def e2m1_to_double(code: int) -> float:
+    """Value of one FP4 E2M1 code (low four bits)."""
+    return float(_load().oracle_e2m1_to_double(int(code) & 0xF))
+
+
+def proj_add_rmsnorm_nvfp4(x, Wq, S, gs, r0, gamma, eps, norm_kind, rows=None, nthreads=0):
+    """Return (r, o, ms) in float64 for NVFP4 weights and bf16 activations.
+
+    x [T,K] bf16 bits; Wq [H,K/2] uint8 (E2M1 codes, element 2j in the low
+    nibble of byte j); S [H,ceil(K/16)] uint8 E4M3 block scales; gs the fp32
+    tensor scale; w = gs * S * e2m1(W).
+    """
+    lib = _load()
+    T, K = np.shape(x)
+    H = np.shape(Wq)[0]
+    x = _u16(x, (T, K))
+    Wq = _u8(Wq, (H, K // 2))
+    S = _u8(S, (H, (K + 15) // 16))
+    r0 = _u16(r0, (T, H))
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    if gamma.shape != (H,):
+        raise ValueError("gamma must be [H]")
+    rows_arr = None
+    n = T
+    if rows is not None:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n = rows_arr.shape[0]
+    r = np.empty((n, H), np.float64)
+    o = np.empty((n, H), np.float64)
+    ms = np.empty((n,), np.float64)
+    rc = lib.oracle_proj_add_rmsnorm_nvfp4(_ptr(x), _ptr(Wq), _ptr(S), float(gs), _ptr(r0), _ptr(gamma), float(eps),
+                                           int(norm_kind), T, K, H, _ptr(rows_arr), n, _ptr(r), _ptr(o), _ptr(ms),
+                                           int(nthreads))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return r, o, ms

@@ -44,7 +44,11 @@
  * the residual add and the norm are unchanged.  A microchunk uses the scales
  * of its own rows, so chunking changes no value.
  *
- * Pins (tests/test_oracle.py, tests/test_oracle_fp8.py): hand-worked 2x2, 4x4
+ * NVFP4 weights (the same page's "MXFP4 / NVFP4 dense" item, low-bit weight
+ * layouts and scaling): W holds E2M1 codes packed two per byte along K with
+ * one E4M3 scale per 16 elements and an fp32 tensor scale; x stays bf16.
+ *
+ * Pins (tests/test_oracle.py, tests/test_oracle_fp8.py, tests/test_oracle_fp4.py): hand-worked 2x2, 4x4
  * and 1x3x2 cases, the closed form of a constant row, the unit-RMS invariant,
  * Gemma(0)==standard(1) bit for bit, linearity of the residual add, eps=0
  * scale invariance, column permutation of K, the projection against numpy's
@@ -285,6 +289,76 @@ int oracle_proj_add_rmsnorm_fp8(const uint8_t *x, const float *x_scale, int x_pe
                 dot += oracle_e4m3_to_double(xt[k]) * oracle_e4m3_to_double(wh[k]);
             double sw = (double)w_scale[w_per_row ? h : 0];
             r[h] = bf16_bits_to_double(r0[t * H + h]) + sx * sw * dot;
+        }
+        double ms = rmsnorm_row(r, H, gamma, eps, norm_kind, o_out + i * H);
+        if (ms_out)
+            ms_out[i] = ms;
+    }
+    return 0;
+}
+
+/*
+ * FP4 E2M1 code (low 4 bits of b) -> double (the OCP 4-bit floating-point
+ * element): 1 sign bit, 2 exponent bits with bias 1, 1 fraction bit; exponent
+ * field 0 holds the subnormal 0.5 * f; no infinities or NaN.  Values
+ * 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives.
+ */
+double oracle_e2m1_to_double(uint8_t b)
+{
+    int sign = (b >> 3) & 1;
+    int e = (b >> 1) & 3;
+    int f = b & 1;
+    double v = e == 0 ? 0.5 * f : ldexp(1.0 + 0.5 * f, e - 1);
+    return (sign != 0) ? -v : v;
+}
+
+/*
+ * The region with NVFP4 weights ("TPSP Design", section 5 "To-do": MXFP4 /
+ * NVFP4 dense, low-bit weight layouts and their scaling).  Reading: W holds
+ * E2M1 codes, two per byte along K (element 2j in the low nibble of byte j,
+ * element 2j + 1 in the high nibble), each run of 16 elements of a row shares
+ * an E4M3 scale, and one fp32 scale applies to the whole tensor:
+ *   w[h,k] = gs * e4m3(S[h, k / 16]) * e2m1(W[h,k])
+ *   y[t,h] = sum_k x[t,k] * w[h,k]        (x bf16)
+ * then the unchanged add and norm.
+ *   x      [T, K] bf16 bits
+ *   Wq     [H, K / 2] bytes (K even)
+ *   S      [H, ceil(K / 16)] E4M3 codes
+ *   gs     the tensor's fp32 scale
+ */
+int oracle_proj_add_rmsnorm_nvfp4(const uint16_t *x, const uint8_t *Wq, const uint8_t *S, float gs,
+                                  const uint16_t *r0, const float *gamma, double eps, int norm_kind,
+                                  long T, long K, long H, const long *rows, long nrows,
+                                  double *r_out, double *o_out, double *ms_out, int nthreads)
+{
+    if (check_args(T, K, H, norm_kind, eps) || (K & 1))
+        return -1;
+    long nblk = (K + 15) / 16;
+    long n = rows ? nrows : T;
+    for (long i = 0; rows && i < n; ++i)
+        if (rows[i] < 0 || rows[i] >= T)
+            return -1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long i = 0; i < n; ++i) {
+        long t = rows ? rows[i] : i;
+        const uint16_t *xt = x + t * K;
+        double *r = r_out + i * H;
+        for (long h = 0; h < H; ++h) {
+            const uint8_t *wh = Wq + h * (K / 2);
+            const uint8_t *sh = S + h * nblk;
+            double acc = 0.0;
+            for (long k = 0; k < K; ++k) {
+                uint8_t code = (k & 1) ? (uint8_t)(wh[k / 2] >> 4) : (uint8_t)(wh[k / 2] & 0xF);
+                double w = (double)gs * oracle_e4m3_to_double(sh[k / 16]) * oracle_e2m1_to_double(code);
+                acc += bf16_bits_to_double(xt[k]) * w;
+            }
+            r[h] = bf16_bits_to_double(r0[t * H + h]) + acc;
         }
         double ms = rmsnorm_row(r, H, gamma, eps, norm_kind, o_out + i * H);
         if (ms_out)

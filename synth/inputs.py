@@ -30,6 +30,7 @@ BLOCK = 1 << 20
 
 STREAM_X, STREAM_U, STREAM_W, STREAM_R, STREAM_GAMMA = 0, 1, 2, 3, 4
 STREAM_X8, STREAM_W8, STREAM_SX, STREAM_SW = 5, 6, 7, 8
+STREAM_W4, STREAM_S4 = 9, 10
 
 # FP8 operands are drawn as values of spread FP8_SPREAD and stored as E4M3
 # codes (see _fill_e4m3); the dequantisation scales bring them back to the
@@ -253,3 +254,51 @@ def make_inputs_fp8(wl: Workload, seed: int | None = None, T: int | None = None,
     else:
         w_scale = np.array([sw0], np.float32)
     return {"x8": x8, "x_scale": x_scale, "W8": W8, "w_scale": w_scale, "r0": base["r0"], "gamma": base["gamma"]}
+
+
+def _fill_e2m1_packed(out: np.ndarray, seed: int, stream: int, spread: float):
+    """E2M1 codes of N(0, spread^2) draws, two per byte along a row (element
+    2j in the low nibble of byte j).  A draw is stored by truncation toward
+    zero onto the E2M1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (the code is the
+    index of the largest magnitude not above |v|), with its sign bit."""
+    flat = out.reshape(-1)
+    n = flat.size
+    nb = (n + BLOCK - 1) // BLOCK
+    gens = _block_gens(seed, stream, nb)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+    def work(i):
+        s0, e = i * BLOCK, min(n, (i + 1) * BLOCK)
+        v = gens[i].standard_normal(2 * (e - s0)) * spread
+        idx = np.searchsorted(grid, np.abs(v), side="right") - 1
+        code = idx.astype(np.int64) | ((v < 0).astype(np.int64) << 3)
+        flat[s0:e] = (code[0::2] | (code[1::2] << 4)).astype(np.uint8)
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(work, range(nb)))
+
+
+def make_inputs_nvfp4(wl: Workload, seed: int | None = None, T: int | None = None):
+    """NVFP4 weights for a workload: dict(x=[T,K] u16 bf16, Wq=[H,K/2] u8,
+    S=[H,ceil(K/16)] u8 E4M3 block scales, gs=float, r0, gamma).
+
+    W codes are E2M1 codes of N(0, 2^2) draws; each block scale is an E4M3
+    code 2^e * (1 + m/8) with e uniform in {-1, 0, 1} and m uniform in 0..7;
+    gs = 1 / (2 sqrt(K)), so the dequantised weights have about the bf16
+    workload's spread.  x, r0 and gamma are the bf16 workload's tensors.
+    """
+    seed = wl.seed if seed is None else int(seed)
+    T = wl.T if T is None else int(T)
+    K, H = wl.K, wl.H
+    if K % 2:
+        raise ValueError("NVFP4 rows pack two elements per byte: K must be even")
+    base = make_inputs(wl, seed=seed, T=T)
+    Wq = np.empty((H, K // 2), np.uint8)
+    _fill_e2m1_packed(Wq, seed, STREAM_W4, 2.0)
+    nblk = (K + 15) // 16
+    g = _block_gens(seed, STREAM_S4, 1)[0]
+    e = g.integers(-1, 2, size=(H, nblk))
+    m = g.integers(0, 8, size=(H, nblk))
+    S = (((e + 7) << 3) | m).astype(np.uint8)
+    gs = float(np.float32(1.0 / (2.0 * math.sqrt(K))))
+    return {"x": base["x"], "Wq": Wq, "S": S, "gs": gs, "r0": base["r0"], "gamma": base["gamma"]}

@@ -12,6 +12,7 @@ import pytest
 import oracle
 
 from . import test_oracle as pins
+from . import test_oracle_fp4 as fp4pins
 from . import test_oracle_fp8 as fp8pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -45,6 +46,15 @@ MUTANTS = {
     "fp8_x_scale_ignored": ("r[h] = bf16_bits_to_double(r0[t * H + h]) + sx * sw * dot;",
                             "r[h] = bf16_bits_to_double(r0[t * H + h]) + sw * dot;"),
     "fp8_x_scale_first_row": ("double sx = (double)x_scale[x_per_row ? t : 0];", "double sx = (double)x_scale[0];"),
+    "e2m1_bias_2": ("double v = e == 0 ? 0.5 * f : ldexp(1.0 + 0.5 * f, e - 1);",
+                    "double v = e == 0 ? 0.5 * f : ldexp(1.0 + 0.5 * f, e - 2);"),
+    "e2m1_subnormal_one": ("double v = e == 0 ? 0.5 * f : ldexp(1.0 + 0.5 * f, e - 1);",
+                           "double v = e == 0 ? 1.0 * f : ldexp(1.0 + 0.5 * f, e - 1);"),
+    "nvfp4_nibbles_swapped": ("uint8_t code = (k & 1) ? (uint8_t)(wh[k / 2] >> 4) : (uint8_t)(wh[k / 2] & 0xF);",
+                              "uint8_t code = (k & 1) ? (uint8_t)(wh[k / 2] & 0xF) : (uint8_t)(wh[k / 2] >> 4);"),
+    "nvfp4_block_32": ("oracle_e4m3_to_double(sh[k / 16])", "oracle_e4m3_to_double(sh[k / 32])"),
+    "nvfp4_tensor_scale_ignored": ("double w = (double)gs * oracle_e4m3_to_double(sh[k / 16])",
+                                   "double w = oracle_e4m3_to_double(sh[k / 16])"),
 }
 
 
@@ -61,6 +71,12 @@ def _pin_calls():
     for name in dir(fp8pins):
         if name.startswith("test_") and name not in ("test_format_facts", "test_unit_scales_equal_bf16_region"):
             calls.append(("fp8." + name, getattr(fp8pins, name)))
+    # NVFP4 pins
+    for kind in (0, 1):
+        calls.append((f"fp4.unit_scales[{kind}]", lambda k=kind: fp4pins.test_unit_scales_equal_bf16_region(k)))
+    for name in dir(fp4pins):
+        if name.startswith("test_") and name != "test_unit_scales_equal_bf16_region":
+            calls.append(("fp4." + name, getattr(fp4pins, name)))
     return calls
 
 

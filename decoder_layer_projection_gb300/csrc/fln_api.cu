@@ -81,6 +81,9 @@ struct Workspace {
   float* partial = nullptr;
   size_t partial_floats = 0;
   unsigned int* dyn_counter = nullptr;  // split-K dynamic chunk draws; each GEMM launch leaves it at zero
+  __nv_bfloat16* w4_bf16 = nullptr;    // NVFP4 weights converted to bf16 (paths with many tokens)
+  size_t w4_bf16_elems = 0;
+  bool prepared_w4[5] = {};
   cudaStream_t stream_b = nullptr;
   cudaEvent_t ev_ready[3] = {};
   cudaEvent_t ev_free[3] = {};
@@ -259,6 +262,23 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, ui
   return FLN_OK;
 }
 
+// 2-D byte tensor [rows, inner_bytes] read in unswizzled boxes of
+// box_bytes x box_rows (NVFP4 codes); out-of-range bytes read 0.
+int make_map_bytes(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_bytes,
+                   uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return fail(FLN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[2] = {inner_bytes, rows};
+  cuuint64_t strides[1] = {inner_bytes};
+  cuuint32_t box[2] = {box_bytes, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FLN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return FLN_OK;
+}
+
 struct Call {
   const void* x;  // [T, K] bf16, or E4M3 codes when f8
   const void* W;  // [H, K] bf16, or E4M3 codes when f8
@@ -274,6 +294,9 @@ struct Call {
   int x_scale_stride = 0;      // 1: per token, 0: per tensor
   const float* w_scale = nullptr;
   int w_scale_stride = 0;      // 1: per output row of W, 0: per tensor
+  int w4 = 0;                  // W holds packed NVFP4 codes (x bf16)
+  const uint8_t* w4_scales = nullptr;  // [H, K/16] E4M3 block scales
+  float y_scale = 1.0f;        // tensor scale of W, applied to the fp32 projection
   int esize() const { return f8 ? 1 : 2; }
   int k_blocks() const { return (K + kblock_elems(f8) - 1) / kblock_elems(f8); }
 };
@@ -305,10 +328,23 @@ int round_bn_tokens(int T) {
 // T <= 256: split-K GEMM with H on the MMA's M side, then reduce + add + norm.
 int run_unfused(Workspace* ws, const Call& c) {
   const int bn = round_bn_tokens(c.T);
-  int rc = prepare_kernel(ws, bn, EPI_SPLITK_SWAP, c.f8);
-  if (rc) return rc;
+  int rc = FLN_OK;
+  if (c.w4) {
+    const int bi = bn_index(bn);
+    if (!ws->prepared_w4[bi]) {
+      FLN_CUDA(w4_gemm_prepare(bn), "cudaFuncSetAttribute(max dynamic shared memory)");
+      ws->prepared_w4[bi] = true;
+    }
+  } else if ((rc = prepare_kernel(ws, bn, EPI_SPLITK_SWAP, c.f8))) {
+    return rc;
+  }
   CUtensorMap tmA, tmB;
-  if ((rc = make_map(&tmA, c.W, c.K, c.H, 128, c.esize()))) return rc;
+  if (c.w4) {
+    // packed codes: 32 bytes (64 codes) of 128 weight rows per K-block
+    if ((rc = make_map_bytes(&tmA, c.W, static_cast<uint64_t>(c.K) / 2, c.H, 32, 128))) return rc;
+  } else if ((rc = make_map(&tmA, c.W, c.K, c.H, 128, c.esize()))) {
+    return rc;
+  }
   if ((rc = make_map(&tmB, c.x, c.K, c.T, bn, c.esize()))) return rc;
   GemmParams p{};
   p.M = c.H;
@@ -327,7 +363,7 @@ int run_unfused(Workspace* ws, const Call& c) {
   // 1-32 tokens, a loss at 64; no gain at K = 8192.
   const int KB = p.num_k_blocks;
   int kc = 0, cpm = 0;
-  if (c.T <= 32 && c.K >= 16384) {
+  if (c.T <= 32 && c.K >= 16384 && !c.w4) {
     const double kd = 0.2 * KB;
     kc = std::max(4, static_cast<int>(std::ceil(kd / 8.0)));
     cpm = std::min(8, std::max(1, static_cast<int>(std::lround(kd / kc))));
@@ -364,10 +400,15 @@ int run_unfused(Workspace* ws, const Call& c) {
   const size_t need = static_cast<size_t>(p.num_m_tiles) * p.slot_stride * c.T * 128;
   if ((rc = grow(&ws->partial, &ws->partial_floats, need, false, "cudaMalloc(split-K partials)"))) return rc;
   p.partial = ws->partial;
+  p.w4_scales = c.w4_scales;
+  p.w4_nblk = c.K / 16;
   p.err = ws->err_word;
   p.dyn_counter = ws->dyn_counter;
   rc = launch_counted(FLN_KERNEL_GEMM_SPLITK, c.stream,
-                      [&] { return launch_gemm(EPI_SPLITK_SWAP, bn, c.f8, tmA, tmB, p, G, c.stream); },
+                      [&] {
+                        return c.w4 ? launch_w4_gemm_splitk(bn, tmA, tmB, p, G, c.stream)
+                                    : launch_gemm(EPI_SPLITK_SWAP, bn, c.f8, tmA, tmB, p, G, c.stream);
+                      },
                       "split-K GEMM launch");
   if (rc) return rc;
   NormParams np{};
@@ -387,6 +428,7 @@ int run_unfused(Workspace* ws, const Call& c) {
   np.row0 = 0;
   np.H = c.H;
   np.pdl = g_prof ? 0 : 1;  // timing events between the two launches would break the overlap
+  np.y_scale = c.y_scale;
   if (c.f8) {
     np.x_scale = c.x_scale;
     np.x_scale_stride = c.x_scale_stride;
@@ -438,6 +480,7 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     p.num_n_tiles = nt;
     p.num_k_blocks = c.k_blocks();
     set_scales(p, c);
+    p.y_scale = c.y_scale;
     p.residual = c.residual;
     p.out = c.out;
     p.gamma = c.gamma;
@@ -503,6 +546,7 @@ int run_pipelined(Workspace* ws, const Call& c, const fln_plan& pl) {
     p.num_n_tiles = nt;
     p.num_k_blocks = c.k_blocks();
     set_scales(p, c);
+    p.y_scale = c.y_scale;
     p.ld = c.H;
     p.yout = ws->slots[s];
     p.err = ws->err_word;
@@ -617,6 +661,23 @@ int resolve_plan(int K, int H, int kind, int dtype, int T, int chunk_arg, fln_pl
 
 int run_plan(Workspace* ws, const Call& c, const fln_plan& pl) {
   if (c.T == 0) return FLN_OK;
+  if (c.w4 && pl.path != FLN_PATH_UNFUSED) {
+    // many tokens: convert the whole weight to bf16 (exact), then the bf16 path
+    const size_t need = static_cast<size_t>(c.H) * c.K;
+    int rc = grow(&ws->w4_bf16, &ws->w4_bf16_elems, need, false, "cudaMalloc(bf16 weights)");
+    if (rc) return rc;
+    rc = launch_counted(FLN_KERNEL_W4_DEQUANT, c.stream,
+                        [&] {
+                          return launch_nvfp4_to_bf16(static_cast<const uint8_t*>(c.W), c.w4_scales, ws->w4_bf16,
+                                                      c.H, c.K, c.stream);
+                        },
+                        "NVFP4 weight conversion launch");
+    if (rc) return rc;
+    Call cb = c;
+    cb.w4 = 0;
+    cb.W = ws->w4_bf16;
+    return pl.path == FLN_PATH_FUSED ? run_fused(ws, cb, pl) : run_pipelined(ws, cb, pl);
+  }
   switch (pl.path) {
     case FLN_PATH_UNFUSED:
       if (c.T > kMaxUnfusedTokens) return fail(FLN_ERR_UNSUPPORTED, "UNFUSED path handles T <= %d", kMaxUnfusedTokens);
@@ -673,6 +734,30 @@ int validate_fp8(const uint8_t* x, const float* x_scale, int x_per_token, const 
   return FLN_OK;
 }
 
+int validate_w4(const fln_bf16* x, const uint8_t* W, const uint8_t* S, float gs, fln_bf16* residual,
+                const float* gamma, float eps, int kind, int T, int K, int H, int chunk, fln_bf16* out) {
+  int rc = check_common(eps, kind, T, H);
+  if (rc) return rc;
+  if (K < 64 || (K & 63)) return fail(FLN_ERR_INVALID_ARG, "K=%d must be a positive multiple of 64 for NVFP4", K);
+  if (K > kMaxK) return fail(FLN_ERR_UNSUPPORTED, "K=%d above the supported %d", K, kMaxK);
+  if (!std::isfinite(gs)) return fail(FLN_ERR_INVALID_ARG, "w_global_scale must be finite");
+  if (chunk < 0 || chunk > kMaxMicrochunk)
+    return fail(FLN_ERR_INVALID_ARG, "microchunk_tokens=%d outside 0..%d", chunk, kMaxMicrochunk);
+  if (T == 0) return FLN_OK;
+  if ((rc = check_ptr("x", x)) || (rc = check_ptr("W", W)) || (rc = check_ptr("W_scale", S)) ||
+      (rc = check_ptr("residual", residual)) || (rc = check_ptr("gamma", gamma)) || (rc = check_ptr("out", out)))
+    return rc;
+  const size_t bx = size_t(T) * K * 2, bw = size_t(H) * K / 2, bs = size_t(H) * K / 16, br = size_t(T) * H * 2,
+               bg = size_t(H) * 4;
+  if (overlaps(out, br, x, bx) || overlaps(out, br, W, bw) || overlaps(out, br, S, bs) ||
+      overlaps(out, br, residual, br) || overlaps(out, br, gamma, bg))
+    return fail(FLN_ERR_INVALID_ARG, "out overlaps an input");
+  if (overlaps(residual, br, x, bx) || overlaps(residual, br, W, bw) || overlaps(residual, br, S, bs) ||
+      overlaps(residual, br, gamma, bg))
+    return fail(FLN_ERR_INVALID_ARG, "residual overlaps x, W, W_scale or gamma");
+  return FLN_OK;
+}
+
 // ------------------------------------------------------------------ tuner
 __global__ void fill_pseudo_normal(__nv_bfloat16* p, size_t n, uint32_t seed, float scale, float shift) {
   for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x) {
@@ -688,6 +773,17 @@ __global__ void fill_pseudo_normal(__nv_bfloat16* p, size_t n, uint32_t seed, fl
       s += static_cast<float>(h >> 8) * (1.0f / 16777216.0f);
     }
     p[i] = __float2bfloat16_rn((s - 2.0f) * 1.7320508f * scale + shift);
+  }
+}
+
+// bytes (hash & mask) | base (the tuner's NVFP4 codes and block scales)
+__global__ void fill_bytes(uint8_t* p, size_t n, uint32_t seed, uint32_t mask, uint32_t base) {
+  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x) {
+    uint32_t h = static_cast<uint32_t>(i) * 0x9E3779B1u ^ seed ^ static_cast<uint32_t>(i >> 32) * 0x85EBCA77u;
+    h ^= h >> 16;
+    h *= 0x7FEB352Du;
+    h ^= h >> 15;
+    p[i] = static_cast<uint8_t>((h & mask) | base);
   }
 }
 
@@ -862,6 +958,27 @@ int fused_proj_add_rmsnorm_fp8(const uint8_t* x, const float* x_scale, int x_sca
   return run_plan(ws, c, pl);
 }
 
+int fused_proj_add_rmsnorm_nvfp4(const fln_bf16* x, const uint8_t* W, const uint8_t* W_scale,
+                                 float w_global_scale, fln_bf16* residual, const float* gamma, float eps,
+                                 int norm_kind, int T, int K, int H, int microchunk_tokens, fln_bf16* out,
+                                 fln_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = validate_w4(x, W, W_scale, w_global_scale, residual, gamma, eps, norm_kind, T, K, H, microchunk_tokens,
+                       out);
+  if (rc) return rc;
+  if (T == 0) return FLN_OK;
+  fln_plan pl;
+  if ((rc = resolve_plan(K, H, norm_kind, FLN_DTYPE_NVFP4, T, microchunk_tokens, &pl))) return rc;
+  Workspace* ws = nullptr;
+  if ((rc = get_ws(&ws))) return rc;
+  Call c{x, W, reinterpret_cast<__nv_bfloat16*>(residual), gamma, eps, norm_kind, T, K, H,
+         reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<cudaStream_t>(stream)};
+  c.w4 = 1;
+  c.w4_scales = W_scale;
+  c.y_scale = w_global_scale;
+  return run_plan(ws, c, pl);
+}
+
 int add_rmsnorm(const fln_bf16* y, fln_bf16* residual, const float* gamma, float eps, int norm_kind, int T, int H,
                 fln_bf16* out, fln_stream_t stream) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -907,7 +1024,7 @@ int fln_set_overrides(int microchunk_tokens, int threshold_tokens) {
 int fln_set_plan_dtype(int K, int H, int norm_kind, int dtype, const fln_plan* plan) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (K < 8 || (K & 7) || H < 8 || (H & 7) || (norm_kind != 0 && norm_kind != 1) ||
-      (dtype != FLN_DTYPE_BF16 && dtype != FLN_DTYPE_E4M3))
+      (dtype != FLN_DTYPE_BF16 && dtype != FLN_DTYPE_E4M3 && dtype != FLN_DTYPE_NVFP4))
     return fail(FLN_ERR_INVALID_ARG, "bad group (K=%d, H=%d, kind=%d, dtype=%d)", K, H, norm_kind, dtype);
   if (!plan) {
     g_plans.erase({K, H, norm_kind, dtype});
@@ -926,7 +1043,8 @@ int fln_set_plan(int K, int H, int norm_kind, const fln_plan* plan) {
 int fln_get_plan_dtype(int K, int H, int norm_kind, int dtype, int T, int microchunk_tokens, fln_plan* plan) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!plan) return fail(FLN_ERR_INVALID_ARG, "plan is NULL");
-  if (dtype != FLN_DTYPE_BF16 && dtype != FLN_DTYPE_E4M3) return fail(FLN_ERR_INVALID_ARG, "dtype=%d", dtype);
+  if (dtype != FLN_DTYPE_BF16 && dtype != FLN_DTYPE_E4M3 && dtype != FLN_DTYPE_NVFP4)
+    return fail(FLN_ERR_INVALID_ARG, "dtype=%d", dtype);
   if (microchunk_tokens < 0 || microchunk_tokens > kMaxMicrochunk)
     return fail(FLN_ERR_INVALID_ARG, "microchunk_tokens=%d outside 0..%d", microchunk_tokens, kMaxMicrochunk);
   return resolve_plan(K, H, norm_kind, dtype, T, microchunk_tokens, plan);
@@ -944,9 +1062,11 @@ int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, f
   std::lock_guard<std::mutex> lk(g_mu);
   int rc = check_common(1e-5f, norm_kind, max_tokens, H);
   if (rc) return rc;
-  if (dtype != FLN_DTYPE_BF16 && dtype != FLN_DTYPE_E4M3) return fail(FLN_ERR_INVALID_ARG, "dtype=%d", dtype);
+  if (dtype != FLN_DTYPE_BF16 && dtype != FLN_DTYPE_E4M3 && dtype != FLN_DTYPE_NVFP4)
+    return fail(FLN_ERR_INVALID_ARG, "dtype=%d", dtype);
   const int f8 = dtype == FLN_DTYPE_E4M3 ? 1 : 0;
-  const int kalign = f8 ? 16 : 8;
+  const int w4 = dtype == FLN_DTYPE_NVFP4 ? 1 : 0;
+  const int kalign = w4 ? 64 : f8 ? 16 : 8;
   if (K < kalign || K % kalign || K > kMaxK)
     return fail(FLN_ERR_INVALID_ARG, "K=%d must be a multiple of %d in [%d, %d]", K, kalign, kalign, kMaxK);
   if (max_tokens < 1 || max_tokens > 65536) return fail(FLN_ERR_INVALID_ARG, "max_tokens must be in 1..65536");
@@ -957,12 +1077,12 @@ int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, f
   FLN_CUDA(cudaStreamSynchronize(s), "tune: cudaStreamSynchronize");
   const int T = max_tokens;
   const int Tc = std::min(T, kMaxUnfusedTokens);  // rows used for the numerical check
-  DevBuf bx, bw, br0, br, bo, bg, bref_r, bref_o, bflush, bscale;
+  DevBuf bx, bw, br0, br, bo, bg, bref_r, bref_o, bflush, bscale, bw4s;
   const size_t nx = size_t(T) * K, nw = size_t(H) * K, nr = size_t(T) * H;
   const size_t flush_bytes = size_t(256) << 20;
   const size_t es = f8 ? 1 : 2;
   FLN_CUDA(cudaMalloc(&bx.p, nx * es), "tune: cudaMalloc");
-  FLN_CUDA(cudaMalloc(&bw.p, nw * es), "tune: cudaMalloc");
+  FLN_CUDA(cudaMalloc(&bw.p, w4 ? nw / 2 : nw * es), "tune: cudaMalloc");
   FLN_CUDA(cudaMalloc(&br0.p, nr * 2), "tune: cudaMalloc");
   FLN_CUDA(cudaMalloc(&br.p, nr * 2), "tune: cudaMalloc");
   FLN_CUDA(cudaMalloc(&bo.p, nr * 2), "tune: cudaMalloc");
@@ -974,7 +1094,14 @@ int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, f
   // FP8 groups: E4M3 codes of N(0, 16^2) values, per-tensor scales 1/16 and
   // 1/(16 sqrt K), so the dequantised operands match the bf16 tuning data
   const float host_scales[4] = {1.0f / 16.0f, 1.0f / (16.0f * std::sqrt(float(K))), 0.f, 0.f};
-  if (f8) {
+  if (w4) {
+    // NVFP4: random code bytes (every byte is two valid codes), block scales
+    // 0.5 .. 1.875 (E4M3 codes 0x30 .. 0x3F), tensor scale 1/(2 sqrt K)
+    FLN_CUDA(cudaMalloc(&bw4s.p, nw / 16), "tune: cudaMalloc");
+    fill_bytes<<<1024, 256, 0, s>>>(static_cast<uint8_t*>(bw.p), nw / 2, 0x5678u, 0xFFu, 0u);
+    fill_bytes<<<1024, 256, 0, s>>>(static_cast<uint8_t*>(bw4s.p), nw / 16, 0x4321u, 0x0Fu, 0x30u);
+    fill_pseudo_normal<<<1024, 256, 0, s>>>(static_cast<__nv_bfloat16*>(bx.p), nx, 0x1234u, 1.0f, 0.0f);
+  } else if (f8) {
     FLN_CUDA(cudaMalloc(&bscale.p, sizeof host_scales), "tune: cudaMalloc");
     FLN_CUDA(cudaMemcpy(bscale.p, host_scales, sizeof host_scales, cudaMemcpyHostToDevice), "tune: scales");
     fill_pseudo_e4m3<<<1024, 256, 0, s>>>(static_cast<uint8_t*>(bx.p), nx, 0x1234u, 16.0f);
@@ -996,6 +1123,11 @@ int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, f
     t.c.f8 = 1;
     t.c.x_scale = static_cast<const float*>(bscale.p);
     t.c.w_scale = static_cast<const float*>(bscale.p) + 1;
+  }
+  if (w4) {
+    t.c.w4 = 1;
+    t.c.w4_scales = static_cast<const uint8_t*>(bw4s.p);
+    t.c.y_scale = 1.0f / (2.0f * std::sqrt(float(K)));
   }
   t.res0 = r0;
   t.flush = bflush.p;
@@ -1148,6 +1280,7 @@ void fln_release_workspace(void) {
     for (int i = 0; i < 3; ++i) cudaFree(ws->slots[i]);
     cudaFree(ws->partial);
     cudaFree(ws->dyn_counter);
+    cudaFree(ws->w4_bf16);
     for (int i = 0; i < 3; ++i) {
       cudaEventDestroy(ws->ev_ready[i]);
       cudaEventDestroy(ws->ev_free[i]);

@@ -502,6 +502,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 load_scale8(p.w_scale, p.w_scale_stride, col, col < p.N, sw);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[8 * h + j] *= sxr * sw[j];
+              } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[8 * h + j] *= p.y_scale;  // NVFP4 tensor scale, else 1
               }
               if (col < p.N) {
                 float4* d = reinterpret_cast<float4*>(yrow + col);

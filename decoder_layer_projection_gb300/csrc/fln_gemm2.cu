@@ -336,6 +336,10 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
 #pragma unroll
               for (int j = 0; j < 8; ++j) v[8 * h + j] *= sxr * sw[j];
             }
+          } else {
+            // a tensor scale of the weights (NVFP4 dequantised to bf16); 1 otherwise
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= p.y_scale;
           }
 #pragma unroll
           for (int h = 0; h < 4; ++h) {

@@ -63,6 +63,8 @@ __device__ __forceinline__ void load_splitk8(const NormParams& p, int t, int h, 
       y[4] += b[s].x; y[5] += b[s].y; y[6] += b[s].z; y[7] += b[s].w;
     }
   }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) y[j] *= p.y_scale;  // NVFP4 tensor scale, else 1
   if (p.w_scale) {
     // FP8 operands: y = sum * (sx[token] * sw[column])
     const float sx = __ldg(p.x_scale + static_cast<size_t>(p.row0 + t) * p.x_scale_stride);

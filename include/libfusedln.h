@@ -119,7 +119,7 @@ int fused_proj_add_rmsnorm(const fln_bf16* x, const fln_bf16* W, fln_bf16* resid
                            fln_stream_t stream);
 
 /* Operand element types of a projection group. */
-typedef enum { FLN_DTYPE_BF16 = 0, FLN_DTYPE_E4M3 = 1 } fln_dtype;
+typedef enum { FLN_DTYPE_BF16 = 0, FLN_DTYPE_E4M3 = 1, FLN_DTYPE_NVFP4 = 2 } fln_dtype;
 
 /*
  * fused_proj_add_rmsnorm_fp8 -- the same region with FP8 operands ("TPSP
@@ -150,6 +150,36 @@ int fused_proj_add_rmsnorm_fp8(const uint8_t* x, const float* x_scale, int x_sca
                                const float* w_scale, int w_scale_per_channel, fln_bf16* residual,
                                const float* gamma, float eps, int norm_kind, int T, int K, int H,
                                int microchunk_tokens, fln_bf16* out, fln_stream_t stream);
+
+/*
+ * fused_proj_add_rmsnorm_nvfp4 -- the region with NVFP4 weights and bf16
+ * activations ("TPSP Design", section 5 "To-do": MXFP4 / NVFP4 dense, low-bit
+ * weight layouts and their scaling):
+ *
+ *     w[h,k] = w_global_scale * e4m3(W_scale[h, k/16]) * e2m1(W[h,k])
+ *     residual += x . w^T;  out = RMSNorm(residual)
+ *
+ *   x           [T, K] bf16
+ *   W           [H, K/2] bytes: E2M1 codes, element 2j of a row in the low
+ *               nibble of byte j, element 2j + 1 in the high nibble
+ *   W_scale     [H, K/16] E4M3 codes, one per 16 consecutive elements of a
+ *               row (finite)
+ *   w_global_scale  the fp32 tensor scale
+ *   K           multiple of 64; the rest as in fused_proj_add_rmsnorm
+ *
+ * e2m1 * e4m3 is exact in bf16, so the tensor cores multiply bf16 x by exact
+ * bf16 weights with fp32 accumulation, and the tensor scale multiplies the
+ * fp32 result.  Below the threshold (few tokens) the split-K GEMM reads W
+ * packed (0.5625 bytes per weight) and dequantises it in shared memory; at
+ * and above it the call first converts the whole weight to bf16 in the
+ * workspace (H * K * 2 bytes) and runs the bf16 FUSED or PIPELINED path.
+ * Plans, tuning and the threshold are kept per (K, H, norm_kind,
+ * FLN_DTYPE_NVFP4) group.
+ */
+int fused_proj_add_rmsnorm_nvfp4(const fln_bf16* x, const uint8_t* W, const uint8_t* W_scale,
+                                 float w_global_scale, fln_bf16* residual, const float* gamma, float eps,
+                                 int norm_kind, int T, int K, int H, int microchunk_tokens, fln_bf16* out,
+                                 fln_stream_t stream);
 
 /*
  * add_rmsnorm -- residual += y; out = RMSNorm(residual)   (the add/norm step alone)
@@ -217,7 +247,8 @@ enum {
   FLN_KERNEL_NORM_BF16 = 3,    /* add_rmsnorm */
   FLN_KERNEL_NORM_SLOT = 4,    /* pipeline second stage */
   FLN_KERNEL_NORM_SPLITK = 5,  /* split-K reduce + add + norm */
-  FLN_KERNEL_KINDS = 6
+  FLN_KERNEL_W4_DEQUANT = 6,   /* NVFP4 weights to bf16 (paths with many tokens) */
+  FLN_KERNEL_KINDS = 7
 };
 typedef struct {
   uint64_t launches[FLN_KERNEL_KINDS];

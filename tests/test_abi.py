@@ -184,3 +184,19 @@ def test_epilogue_warps_plan_validation(lib):
         assert fln.fln_get_plan(1024, 768, 0, 4096)["epi_warps"] == 8
     finally:
         fln.fln_set_plan(1024, 768, 0, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=96), fln.FLN_ERR_INVALID_ARG),        # NVFP4 K-blocks: K multiple of 64
+    (dict(K=32), fln.FLN_ERR_INVALID_ARG),
+    (dict(norm_kind=4), fln.FLN_ERR_INVALID_ARG),
+    (dict(T=-1), fln.FLN_ERR_INVALID_ARG),
+    (dict(gs=float("nan")), fln.FLN_ERR_INVALID_ARG),
+])
+def test_nvfp4_rejects_bad_arguments_before_any_launch(lib, kw, status):
+    a = dict(eps=1e-5, norm_kind=0, T=16, K=256, H=256, microchunk_tokens=0, gs=0.5)
+    a.update(kw)
+    rc = lib.fused_proj_add_rmsnorm_nvfp4(None, None, None, a["gs"], None, None, a["eps"], a["norm_kind"], a["T"],
+                                          a["K"], a["H"], a["microchunk_tokens"], None, None)
+    assert rc == status, fln.fln_last_error()
+    assert fln.fln_launch_count() == 0

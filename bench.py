@@ -170,7 +170,7 @@ def run_gpu(args):
     import torch.distributed as dist
 
     import decoder_layer_projection_gb300 as fln
-    from synth import make_inputs, make_inputs_fp8, workload
+    from synth import make_inputs, make_inputs_fp8, make_inputs_nvfp4, workload
 
     rank, world, local_rank = dist_env()
     torch.cuda.set_device(local_rank)
@@ -185,9 +185,12 @@ def run_gpu(args):
         wl = wl.with_tokens(args.tokens)
     T, K, H = wl.T, wl.K, wl.H
     f8 = args.dtype == "e4m3"
-    dt = fln.DTYPE_E4M3 if f8 else fln.DTYPE_BF16
+    w4 = args.dtype == "nvfp4"
+    dt = fln.DTYPE_E4M3 if f8 else fln.DTYPE_NVFP4 if w4 else fln.DTYPE_BF16
     if f8:
         d = make_inputs_fp8(wl, seed=rank_seed(wl.seed, rank))
+    elif w4:
+        d = make_inputs_nvfp4(wl, seed=rank_seed(wl.seed, rank))
     else:
         d = make_inputs(wl, seed=rank_seed(wl.seed, rank))
 
@@ -199,6 +202,11 @@ def run_gpu(args):
         W = torch.from_numpy(np.ascontiguousarray(d["W8"])).to(device)
         sx = torch.from_numpy(d["x_scale"]).to(device)
         sw = torch.from_numpy(d["w_scale"]).to(device)
+    elif w4:
+        x = up(d["x"])
+        W = torch.from_numpy(np.ascontiguousarray(d["Wq"])).to(device)
+        sw = torch.from_numpy(np.ascontiguousarray(d["S"])).to(device)  # block scales
+        sx = None
     else:
         x, W = up(d["x"]), up(d["W"])
         sx = sw = None
@@ -226,6 +234,9 @@ def run_gpu(args):
         if f8:
             fln.fused_proj_add_rmsnorm_fp8(x, sx, W, sw, r, gamma, wl.eps, wl.norm_kind, args.microchunk, out,
                                            stream)
+        elif w4:
+            fln.fused_proj_add_rmsnorm_nvfp4(x, W, sw, d["gs"], r, gamma, wl.eps, wl.norm_kind, args.microchunk,
+                                             out, stream)
         else:
             fln.fused_proj_add_rmsnorm(x, W, r, gamma, wl.eps, wl.norm_kind, args.microchunk, out, stream)
 
@@ -283,7 +294,8 @@ def run_gpu(args):
     avg_launch_ms = kp["total_ms"] / max(kp["launches"], 1)
     launches_per_step = kp["launches"] / args.steps
     tokens_per_launch = T / launches_per_step
-    ob = 1.0 if f8 else 2.0  # bytes per x / W element
+    ob = 1.0 if f8 else 2.0  # bytes per x element (and per W element, except NVFP4)
+    wb = 0.5 + 1.0 / 16.0 if w4 else ob  # bytes per W element
     tensor_peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if f8 else 1.0)
     if kname in ("gemm_fused", "gemm_slot"):
         # tensor bound: 2 * tokens * K * H per launch
@@ -291,7 +303,7 @@ def run_gpu(args):
         bound, unit, peak = "tensor", "TFLOP/s", tensor_peak
     elif kname == "gemm_splitk":
         # HBM bound: W read once plus x, per launch
-        achieved = (ob * H * K + ob * tokens_per_launch * K) / (avg_launch_ms * 1e-3) / 1e9
+        achieved = (wb * H * K + ob * tokens_per_launch * K) / (avg_launch_ms * 1e-3) / 1e9
         bound, unit, peak = "hbm", "GB/s", peaks["hbm_gbs"]
     else:
         # add + norm: residual read and written, output written, gamma
@@ -311,7 +323,8 @@ def run_gpu(args):
                 "measured": "second timed pass of the same K steps with per-kernel CUDA events",
                 "profiled_ms_per_step": round(prof_s * 1e3 / args.steps, 5)}
     # full-step roofline: the slower of FLOPs at tensor peak and bytes at HBM bandwidth
-    t_roof = max(flops / (tensor_peak * 1e12), wl.algorithmic_bytes(1 if f8 else 2) / (peaks["hbm_gbs"] * 1e9))
+    t_roof = max(flops / (tensor_peak * 1e12),
+                 wl.algorithmic_bytes(1 if f8 else 0 if w4 else 2) / (peaks["hbm_gbs"] * 1e9))
     step_frac = t_roof / (ms_per_step * 1e-3)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
@@ -370,6 +383,9 @@ def run_e2e(args, wl, d, W, gamma, device, stream, fln, sw=None):
             dsx.copy_(hsx, non_blocking=True)
             fln.fused_proj_add_rmsnorm_fp8(dx, dsx, W, sw, dr, gamma, wl.eps, wl.norm_kind, args.microchunk, do,
                                            stream)
+        elif args.dtype == "nvfp4":
+            fln.fused_proj_add_rmsnorm_nvfp4(dx, W, sw, d["gs"], dr, gamma, wl.eps, wl.norm_kind, args.microchunk,
+                                             do, stream)
         else:
             fln.fused_proj_add_rmsnorm(dx, W, dr, gamma, wl.eps, wl.norm_kind, args.microchunk, do, stream)
         ho.copy_(do, non_blocking=True)
@@ -405,6 +421,8 @@ def run_comparator(args, wl, x, W, d, gamma, device, stream, fln, flush, sx=None
     r = torch.from_numpy(np.ascontiguousarray(d["r0"]).view(np.int16)).view(torch.bfloat16).to(device)
     out = torch.empty_like(r)
     T, H = r.shape
+    if args.dtype == "nvfp4":
+        return {"unavailable": "no library GEMM takes NVFP4 weights with bf16 activations here"}
     if f8:
         # torch._scaled_mm with row-wise scales ended in an unspecified launch
         # failure (Xid 43) on this GPU under PyTorch 2.9.1 (its kernel prints
@@ -441,6 +459,9 @@ def _oracle_rows_timed(wl, d, rows, nthreads=0):
     if "x8" in d:
         oracle.proj_add_rmsnorm_fp8(d["x8"], d["x_scale"], d["W8"], d["w_scale"], d["r0"], d["gamma"], wl.eps,
                                     wl.norm_kind, rows=rows, nthreads=nthreads)
+    elif "Wq" in d:
+        oracle.proj_add_rmsnorm_nvfp4(d["x"], d["Wq"], d["S"], d["gs"], d["r0"], d["gamma"], wl.eps, wl.norm_kind,
+                                      rows=rows, nthreads=nthreads)
     else:
         oracle.proj_add_rmsnorm(d["x"], d["W"], d["r0"], d["gamma"], wl.eps, wl.norm_kind, rows=rows,
                                 nthreads=nthreads)
@@ -463,7 +484,7 @@ def cpu_baseline(wl, d, seconds: float):
 def run_reference(args):
     """--impl reference: the oracle timed on host cores, same metric/unit/config."""
     import oracle
-    from synth import make_inputs, make_inputs_fp8, workload
+    from synth import make_inputs, make_inputs_fp8, make_inputs_nvfp4, workload
     rank, world, _ = dist_env()
     if rank != 0:
         return None
@@ -471,7 +492,8 @@ def run_reference(args):
     if args.tokens:
         wl = wl.with_tokens(args.tokens)
     oracle.build()
-    d = make_inputs_fp8(wl) if args.dtype == "e4m3" else make_inputs(wl)
+    d = (make_inputs_fp8(wl) if args.dtype == "e4m3" else make_inputs_nvfp4(wl) if args.dtype == "nvfp4"
+         else make_inputs(wl))
     cores = oracle.max_threads()
     # rows per step sized so that warm-up + steps stay within about a minute
     probe = min(wl.T, max(1, cores))
@@ -511,8 +533,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the cpu_baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0, help="--impl reference: CPU work of the whole run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--dtype", choices=["bf16", "e4m3"], default="bf16",
-                    help="operand type of x and W (e4m3: FP8 with per-token / per-channel scales)")
+    ap.add_argument("--dtype", choices=["bf16", "e4m3", "nvfp4"], default="bf16",
+                    help="operand types: bf16; e4m3 (FP8 x and W with per-token / per-channel scales); "
+                         "nvfp4 (NVFP4 weights, bf16 x)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

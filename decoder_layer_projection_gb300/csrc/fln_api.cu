@@ -262,18 +262,17 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, ui
   return FLN_OK;
 }
 
-// 2-D byte tensor [rows, inner_bytes] read in unswizzled boxes of
-// box_bytes x box_rows (NVFP4 codes); out-of-range bytes read 0.
-int make_map_bytes(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_bytes,
-                   uint32_t box_rows) {
+// 2-D byte tensor [rows, inner_bytes] read in boxes of 128 bytes x box_rows
+// with 128-byte swizzle (NVFP4 codes); out-of-range bytes read 0.
+int make_map_bytes(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint32_t box_rows) {
   auto enc = encode_fn();
   if (!enc) return fail(FLN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   cuuint64_t dims[2] = {inner_bytes, rows};
   cuuint64_t strides[1] = {inner_bytes};
-  cuuint32_t box[2] = {box_bytes, box_rows};
+  cuuint32_t box[2] = {128, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FLN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
   return FLN_OK;
@@ -340,8 +339,8 @@ int run_unfused(Workspace* ws, const Call& c) {
   }
   CUtensorMap tmA, tmB;
   if (c.w4) {
-    // packed codes: 32 bytes (64 codes) of 128 weight rows per K-block
-    if ((rc = make_map_bytes(&tmA, c.W, static_cast<uint64_t>(c.K) / 2, c.H, 32, 128))) return rc;
+    // packed codes: 128 bytes (four K-blocks of 64 codes) of 128 weight rows per entry
+    if ((rc = make_map_bytes(&tmA, c.W, static_cast<uint64_t>(c.K) / 2, c.H, 128))) return rc;
   } else if ((rc = make_map(&tmA, c.W, c.K, c.H, 128, c.esize()))) {
     return rc;
   }
@@ -428,7 +427,8 @@ int run_unfused(Workspace* ws, const Call& c) {
   np.row0 = 0;
   np.H = c.H;
   np.pdl = g_prof ? 0 : 1;  // timing events between the two launches would break the overlap
-  np.y_scale = c.y_scale;
+  // the NVFP4 split-K kernel's partials are y * 2^-8 (its dequantised weights carry that factor)
+  np.y_scale = c.w4 ? c.y_scale * 256.0f : c.y_scale;
   if (c.f8) {
     np.x_scale = c.x_scale;
     np.x_scale_stride = c.x_scale_stride;
@@ -740,7 +740,8 @@ int validate_w4(const fln_bf16* x, const uint8_t* W, const uint8_t* S, float gs,
   if (rc) return rc;
   if (K < 64 || (K & 63)) return fail(FLN_ERR_INVALID_ARG, "K=%d must be a positive multiple of 64 for NVFP4", K);
   if (K > kMaxK) return fail(FLN_ERR_UNSUPPORTED, "K=%d above the supported %d", K, kMaxK);
-  if (!std::isfinite(gs)) return fail(FLN_ERR_INVALID_ARG, "w_global_scale must be finite");
+  if (!std::isfinite(gs) || std::fabs(gs) > 0x1p100f)
+    return fail(FLN_ERR_INVALID_ARG, "w_global_scale must be finite with magnitude at most 2^100");
   if (chunk < 0 || chunk > kMaxMicrochunk)
     return fail(FLN_ERR_INVALID_ARG, "microchunk_tokens=%d outside 0..%d", chunk, kMaxMicrochunk);
   if (T == 0) return FLN_OK;

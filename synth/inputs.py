@@ -71,11 +71,16 @@ class Workload:
 
     def algorithmic_bytes(self, operand_bytes: int = 2) -> float:
         """x read + W read once + residual read and written + out written + gamma
-        (operand_bytes = 1 for FP8 x and W, whose scales add 4T + 4H at most)."""
+        (operand_bytes = 1 for FP8 x and W, whose scales add 4T + 4H at most;
+        operand_bytes = 0 for NVFP4 weights: bf16 x, W at half a byte per
+        weight plus one scale byte per 16)."""
         T, K, H = self.T, self.K, self.H
+        rest = 4.0 * T * H + 2.0 * T * H + 4.0 * H
+        if operand_bytes == 0:
+            return 2.0 * T * K + 0.5 * H * K + H * K / 16.0 + rest
         b = float(operand_bytes)
         extra = 4.0 * T + 4.0 * H if operand_bytes == 1 else 0.0
-        return b * T * K + b * H * K + 4.0 * T * H + 2.0 * T * H + 4.0 * H + extra
+        return b * T * K + b * H * K + rest + extra
 
 
 CONFIGS = {

@@ -429,25 +429,34 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(C::A_COL0 + s * A_COLS);
-        const int g1 = min(kb1, g0 + KG);
-        for (int kb = g0; kb < g1; ++kb) {
-          const int jx = (kb - g0) % C::XK;  // K-block within the x stage
-          if (jx == 0 && !mbar_wait(&x_full[xs], xph, abort_flag, p.err, FLN_DEVERR_TIMEOUT_FULL)) {
-            ok = false;
-            break;
-          }
-          const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sX + xs * C::XSTAGE + jx * C::X_BYTES));
-          const uint32_t ak = a_tmem + static_cast<uint32_t>(32 * (kb - g0));
+        // straight-line issue of the entry's (up to) 4 x 4 MMAs: j = K-block, kk = K-step
+        const int nk = min(kb1 - g0, KG);
+        const bool first = g0 == kb0;  // the item's first entry starts every accumulator afresh
+        uint64_t bdesc0 = 0;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // 16 elements of K = 8 TMEM columns of A, 32 bytes of B's rows
-            mma_bf16_ts(d_tmem + static_cast<uint32_t>((kk % NSUB) * BN), ak + static_cast<uint32_t>(kk * 8),
-                        bdesc + static_cast<uint64_t>(kk * 2), IDESC, (kb > kb0 || kk >= NSUB) ? 1u : 0u);
-          issued_any = true;
-          if (jx == C::XK - 1 || kb == g1 - 1) {
-            mma_commit(&x_empty[xs]);  // the x stage is free once these MMAs have read it
-            if (++xs == XS) {
-              xs = 0;
-              xph ^= 1u;
+        for (int j = 0; j < KG; ++j) {
+          if (j < nk) {
+            constexpr int XK = C::XK;
+            if (j % XK == 0) {
+              if (!mbar_wait(&x_full[xs], xph, abort_flag, p.err, FLN_DEVERR_TIMEOUT_FULL)) {
+                ok = false;
+                break;
+              }
+              bdesc0 = sw128_kmajor_desc(smem_u32(sX + xs * C::XSTAGE));
+            }
+            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((j % XK) * (C::X_BYTES >> 4));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // 16 elements of K = 8 TMEM columns of A, 32 bytes of B's rows
+              mma_bf16_ts(d_tmem + static_cast<uint32_t>((kk % NSUB) * BN),
+                          a_tmem + static_cast<uint32_t>(32 * j + 8 * kk), bdesc + static_cast<uint64_t>(kk * 2),
+                          IDESC, (first && j == 0 && kk < NSUB) ? 0u : 1u);
+            issued_any = true;
+            if (j % XK == XK - 1 || j == nk - 1) {
+              mma_commit(&x_empty[xs]);  // the x stage is free once these MMAs have read it
+              if (++xs == XS) {
+                xs = 0;
+                xph ^= 1u;
+              }
             }
           }
         }

@@ -46,7 +46,7 @@ constexpr int S_BYTES = BM * 4 * KG;         // block scales of a W entry: 128 r
 constexpr int TMEM_COLS = 512;
 constexpr int A_COLS = 32 * KG;              // one dequantised W entry in TMEM: 4 x 64 bf16 per lane
 constexpr int SMEM_LIMIT = 232448;
-constexpr int BAR_BYTES = 1024;
+constexpr int BAR_BYTES = 2048;            // barriers, then (from byte 1024) the scale table
 
 // Shared memory: packed W entries with their scales (the HBM stream: as many
 // bytes in flight as fit) and the x ring (XK K-blocks a stage).  TMEM: NACC tiles of NSUB fp32
@@ -210,6 +210,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* drain_bar = acc_empty + NACC;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  // E4M3 code -> its value times 2^118 as bf16, in both halves (the dequantisation's block-scale operand)
+  uint32_t* scale_lut = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(w_full) + 1024);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -239,6 +241,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_proxy_async_smem();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+  }
+  if (threadIdx.x < 256) {
+    const uint32_t b = e4m3_to_bf16_bits_x2p118(threadIdx.x);
+    scale_lut[threadIdx.x] = b | (b << 16);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, TMEM_COLS);
@@ -346,6 +352,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int half = (warp - 6) >> 2;
     const uint32_t a_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                             static_cast<uint32_t>(C::A_COL0 + 16 * half);
+    uint32_t coff[KG];  // this thread's 16-byte chunk of K-block j in a swizzled entry: chunk 2 j + half
+#pragma unroll
+    for (int j = 0; j < KG; ++j) coff[j] = swz(row, 2 * j + half);
     Items it(p);
     int m_tile, kb0, kb1, split;
     int rw = 0, s = 0;
@@ -369,11 +378,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int j = 0; j < KG; ++j) {
           if (j < nk) {
             // 16-byte chunk 2 j + half of this row in the swizzled entry
-            const uint4 cq = *reinterpret_cast<const uint4*>(went + swz(row, 2 * j + half));
+            const uint4 cq = *reinterpret_cast<const uint4*>(went + coff[j]);
             const uint32_t sc = vrow ? (scw[j] >> (16 * half)) : 0u;
             // values w * 2^-8 (block scale times 2^118 on codes times 2^-126); the reducer multiplies by 2^8
-            const uint32_t s0 = e4m3_to_bf16_bits_x2p118(sc & 0xFFu), s1 = e4m3_to_bf16_bits_x2p118((sc >> 8) & 0xFFu);
-            const uint32_t s20 = s0 | (s0 << 16), s21 = s1 | (s1 << 16);
+            const uint32_t s20 = scale_lut[sc & 0xFFu], s21 = scale_lut[(sc >> 8) & 0xFFu];
             const uint4 v0 = e2m1x8_to_bf16_biased(cq.x, s20), v1 = e2m1x8_to_bf16_biased(cq.y, s20);
             const uint4 v2 = e2m1x8_to_bf16_biased(cq.z, s21), v3 = e2m1x8_to_bf16_biased(cq.w, s21);
             v[j][0] = v0.x, v[j][1] = v0.y, v[j][2] = v0.z, v[j][3] = v0.w;

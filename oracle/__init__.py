@@ -69,6 +69,11 @@ def _bind(path):
     lib.oracle_proj_add_rmsnorm_nvfp4.argtypes = [
         p, p, p, ctypes.c_float, p, p, ctypes.c_double, ctypes.c_int, L, L, L, p, L, p, p, p, ctypes.c_int]
     lib.oracle_proj_add_rmsnorm_nvfp4.restype = ctypes.c_int
+    lib.oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e8m0_to_double.restype = ctypes.c_double
+    lib.oracle_proj_add_rmsnorm_mxfp4.argtypes = [
+        p, p, p, p, p, ctypes.c_double, ctypes.c_int, L, L, L, p, L, p, p, p, ctypes.c_int]
+    lib.oracle_proj_add_rmsnorm_mxfp4.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -232,6 +237,43 @@ def proj_add_rmsnorm_nvfp4(x, Wq, S, gs, r0, gamma, eps, norm_kind, rows=None, n
     o = np.empty((n, H), np.float64)
     ms = np.empty((n,), np.float64)
     rc = lib.oracle_proj_add_rmsnorm_nvfp4(_ptr(x), _ptr(Wq), _ptr(S), float(gs), _ptr(r0), _ptr(gamma), float(eps),
+                                           int(norm_kind), T, K, H, _ptr(rows_arr), n, _ptr(r), _ptr(o), _ptr(ms),
+                                           int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return r, o, ms
+
+
+def e8m0_to_double(E):
+    """Value of an OCP E8M0 scale code (2^(E-127); NaN for 255)."""
+    return _load().oracle_e8m0_to_double(int(E) & 0xFF)
+
+
+def proj_add_rmsnorm_mxfp4(x, Wq, S, r0, gamma, eps, norm_kind, rows=None, nthreads=0):
+    """Return (r, o, ms) in float64 for MXFP4 weights and bf16 activations.
+
+    x [T,K] bf16 bits; Wq [H,K/2] uint8 (E2M1 codes, element 2j in the low
+    nibble of byte j); S [H,ceil(K/32)] uint8 E8M0 block scales; w = S * e2m1(W).
+    """
+    lib = _load()
+    T, K = np.shape(x)
+    H = np.shape(Wq)[0]
+    x = _u16(x, (T, K))
+    Wq = _u8(Wq, (H, K // 2))
+    S = _u8(S, (H, (K + 31) // 32))
+    r0 = _u16(r0, (T, H))
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    if gamma.shape != (H,):
+        raise ValueError("gamma must be [H]")
+    rows_arr = None
+    n = T
+    if rows is not None:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n = rows_arr.shape[0]
+    r = np.empty((n, H), np.float64)
+    o = np.empty((n, H), np.float64)
+    ms = np.empty((n,), np.float64)
+    rc = lib.oracle_proj_add_rmsnorm_mxfp4(_ptr(x), _ptr(Wq), _ptr(S), _ptr(r0), _ptr(gamma), float(eps),
                                            int(norm_kind), T, K, H, _ptr(rows_arr), n, _ptr(r), _ptr(o), _ptr(ms),
                                            int(nthreads))
     if rc != 0:

@@ -47,8 +47,11 @@
  * NVFP4 weights (the same page's "MXFP4 / NVFP4 dense" item, low-bit weight
  * layouts and scaling): W holds E2M1 codes packed two per byte along K with
  * one E4M3 scale per 16 elements and an fp32 tensor scale; x stays bf16.
+ * MXFP4 weights: the same codes with one E8M0 (power-of-two) scale per 32
+ * elements and no tensor scale.
  *
- * Pins (tests/test_oracle.py, tests/test_oracle_fp8.py, tests/test_oracle_fp4.py): hand-worked 2x2, 4x4
+ * Pins (tests/test_oracle.py, tests/test_oracle_fp8.py, tests/test_oracle_fp4.py,
+ * tests/test_oracle_mx.py): hand-worked 2x2, 4x4
  * and 1x3x2 cases, the closed form of a constant row, the unit-RMS invariant,
  * Gemma(0)==standard(1) bit for bit, linearity of the residual add, eps=0
  * scale invariance, column permutation of K, the projection against numpy's
@@ -359,6 +362,69 @@ int oracle_proj_add_rmsnorm_nvfp4(const uint16_t *x, const uint8_t *Wq, const ui
                 acc += bf16_bits_to_double(xt[k]) * w;
             }
             r[h] = bf16_bits_to_double(r0[t * H + h]) + acc;
+        }
+        double ms = rmsnorm_row(r, H, gamma, eps, norm_kind, o_out + i * H);
+        if (ms_out)
+            ms_out[i] = ms;
+    }
+    return 0;
+}
+
+/*
+ * OCP microscaling E8M0 scale code -> double: a bare biased exponent, the
+ * value 2^(E - 127) for E = 0 .. 254; the code 255 is NaN.
+ */
+double oracle_e8m0_to_double(uint8_t E)
+{
+    if (E == 255)
+        return NAN;
+    return ldexp(1.0, (int)E - 127);
+}
+
+/*
+ * The region with MXFP4 weights (the same "MXFP4 / NVFP4 dense" item).
+ * Reading: the OCP MX layout for FP4 -- E2M1 codes packed two per byte along
+ * K exactly as for NVFP4, one E8M0 scale shared by each run of 32 elements
+ * of a row, no tensor scale:
+ *   w[h,k] = e8m0(S[h, k / 32]) * e2m1(W[h,k])
+ *   y[t,h] = sum_k x[t,k] * w[h,k]        (x bf16)
+ * then the unchanged add and norm.
+ *   S      [H, ceil(K / 32)] E8M0 codes
+ */
+int oracle_proj_add_rmsnorm_mxfp4(const uint16_t *x, const uint8_t *Wq, const uint8_t *S,
+                                  const uint16_t *r0, const float *gamma, double eps, int norm_kind,
+                                  long T, long K, long H, const long *rows, long nrows,
+                                  double *r_out, double *o_out, double *ms_out, int nthreads)
+{
+    if (check_args(T, K, H, norm_kind, eps) || (K % 2) != 0)
+        return -1;
+    long scales_per_row = (K + 31) / 32;
+    long nout = rows ? nrows : T;
+    for (long i = 0; rows && i < nout; ++i)
+        if (rows[i] < 0 || rows[i] >= T)
+            return -1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long i = 0; i < nout; ++i) {
+        long tok = rows ? rows[i] : i;
+        const uint16_t *xrow = x + tok * K;
+        double *r = r_out + i * H;
+        for (long h = 0; h < H; ++h) {
+            const uint8_t *codes = Wq + h * (K / 2);
+            const uint8_t *scales = S + h * scales_per_row;
+            double sum = 0.0;
+            for (long k = 0; k < K; ++k) {
+                uint8_t byte = codes[k / 2];
+                uint8_t nib = (k % 2 == 0) ? (uint8_t)(byte & 0x0F) : (uint8_t)(byte >> 4);
+                double wv = oracle_e8m0_to_double(scales[k / 32]) * oracle_e2m1_to_double(nib);
+                sum += bf16_bits_to_double(xrow[k]) * wv;
+            }
+            r[h] = bf16_bits_to_double(r0[tok * H + h]) + sum;
         }
         double ms = rmsnorm_row(r, H, gamma, eps, norm_kind, o_out + i * H);
         if (ms_out)

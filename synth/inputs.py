@@ -31,6 +31,7 @@ BLOCK = 1 << 20
 STREAM_X, STREAM_U, STREAM_W, STREAM_R, STREAM_GAMMA = 0, 1, 2, 3, 4
 STREAM_X8, STREAM_W8, STREAM_SX, STREAM_SW = 5, 6, 7, 8
 STREAM_W4, STREAM_S4 = 9, 10
+STREAM_S5 = 11
 
 # FP8 operands are drawn as values of spread FP8_SPREAD and stored as E4M3
 # codes (see _fill_e4m3); the dequantisation scales bring them back to the
@@ -73,11 +74,14 @@ class Workload:
         """x read + W read once + residual read and written + out written + gamma
         (operand_bytes = 1 for FP8 x and W, whose scales add 4T + 4H at most;
         operand_bytes = 0 for NVFP4 weights: bf16 x, W at half a byte per
-        weight plus one scale byte per 16)."""
+        weight plus one scale byte per 16; operand_bytes = -1 for MXFP4
+        weights: one scale byte per 32)."""
         T, K, H = self.T, self.K, self.H
         rest = 4.0 * T * H + 2.0 * T * H + 4.0 * H
         if operand_bytes == 0:
             return 2.0 * T * K + 0.5 * H * K + H * K / 16.0 + rest
+        if operand_bytes == -1:
+            return 2.0 * T * K + 0.5 * H * K + H * K / 32.0 + rest
         b = float(operand_bytes)
         extra = 4.0 * T + 4.0 * H if operand_bytes == 1 else 0.0
         return b * T * K + b * H * K + rest + extra
@@ -307,3 +311,27 @@ def make_inputs_nvfp4(wl: Workload, seed: int | None = None, T: int | None = Non
     S = (((e + 7) << 3) | m).astype(np.uint8)
     gs = float(np.float32(1.0 / (2.0 * math.sqrt(K))))
     return {"x": base["x"], "Wq": Wq, "S": S, "gs": gs, "r0": base["r0"], "gamma": base["gamma"]}
+
+
+def make_inputs_mxfp4(wl: Workload, seed: int | None = None, T: int | None = None):
+    """MXFP4 weights for a workload: dict(x=[T,K] u16 bf16, Wq=[H,K/2] u8,
+    S=[H,ceil(K/32)] u8 E8M0 block scales, r0, gamma).
+
+    W codes are those of make_inputs_nvfp4 (E2M1 codes of N(0, 2^2) draws);
+    each block scale is the E8M0 code of 2^(e0 + u), u uniform in {-1, 0, 1},
+    e0 = round(log2(1 / (2 sqrt(K)))), so the dequantised weights have about
+    the bf16 workload's spread.  x, r0 and gamma are the bf16 workload's tensors.
+    """
+    seed = wl.seed if seed is None else int(seed)
+    T = wl.T if T is None else int(T)
+    K, H = wl.K, wl.H
+    if K % 2:
+        raise ValueError("MXFP4 rows pack two elements per byte: K must be even")
+    base = make_inputs(wl, seed=seed, T=T)
+    Wq = np.empty((H, K // 2), np.uint8)
+    _fill_e2m1_packed(Wq, seed, STREAM_W4, 2.0)
+    nblk = (K + 31) // 32
+    e0 = int(round(math.log2(1.0 / (2.0 * math.sqrt(K)))))
+    u = _block_gens(seed, STREAM_S5, 1)[0].integers(-1, 2, size=(H, nblk))
+    S = (127 + e0 + u).astype(np.uint8)
+    return {"x": base["x"], "Wq": Wq, "S": S, "r0": base["r0"], "gamma": base["gamma"]}

@@ -14,6 +14,7 @@ import oracle
 from . import test_oracle as pins
 from . import test_oracle_fp4 as fp4pins
 from . import test_oracle_fp8 as fp8pins
+from . import test_oracle_mx as mxpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -55,6 +56,11 @@ MUTANTS = {
     "nvfp4_block_32": ("oracle_e4m3_to_double(sh[k / 16])", "oracle_e4m3_to_double(sh[k / 32])"),
     "nvfp4_tensor_scale_ignored": ("double w = (double)gs * oracle_e4m3_to_double(sh[k / 16])",
                                    "double w = oracle_e4m3_to_double(sh[k / 16])"),
+    "e8m0_bias_128": ("return ldexp(1.0, (int)E - 127);", "return ldexp(1.0, (int)E - 128);"),
+    "e8m0_nan_dropped": ("    if (E == 255)\n        return NAN;\n", ""),
+    "mxfp4_block_16": ("oracle_e8m0_to_double(scales[k / 32])", "oracle_e8m0_to_double(scales[k / 16])"),
+    "mxfp4_nibbles_swapped": ("(k % 2 == 0) ? (uint8_t)(byte & 0x0F) : (uint8_t)(byte >> 4);",
+                              "(k % 2 == 0) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0x0F);"),
 }
 
 
@@ -77,6 +83,12 @@ def _pin_calls():
     for name in dir(fp4pins):
         if name.startswith("test_") and name != "test_unit_scales_equal_bf16_region":
             calls.append(("fp4." + name, getattr(fp4pins, name)))
+    # MXFP4 pins
+    for kind in (0, 1):
+        calls.append((f"mx.unit_scales[{kind}]", lambda k=kind: mxpins.test_unit_scales_equal_bf16_region(k)))
+    for name in dir(mxpins):
+        if name.startswith("test_") and name != "test_unit_scales_equal_bf16_region":
+            calls.append(("mx." + name, getattr(mxpins, name)))
     return calls
 
 

@@ -170,7 +170,7 @@ def run_gpu(args):
     import torch.distributed as dist
 
     import decoder_layer_projection_gb300 as fln
-    from synth import make_inputs, make_inputs_fp8, make_inputs_nvfp4, workload
+    from synth import make_inputs, make_inputs_fp8, make_inputs_mxfp4, make_inputs_nvfp4, workload
 
     rank, world, local_rank = dist_env()
     torch.cuda.set_device(local_rank)
@@ -185,12 +185,13 @@ def run_gpu(args):
         wl = wl.with_tokens(args.tokens)
     T, K, H = wl.T, wl.K, wl.H
     f8 = args.dtype == "e4m3"
-    w4 = args.dtype == "nvfp4"
-    dt = fln.DTYPE_E4M3 if f8 else fln.DTYPE_NVFP4 if w4 else fln.DTYPE_BF16
+    w4 = args.dtype in ("nvfp4", "mxfp4")
+    mx = args.dtype == "mxfp4"
+    dt = (fln.DTYPE_E4M3 if f8 else fln.DTYPE_MXFP4 if mx else fln.DTYPE_NVFP4 if w4 else fln.DTYPE_BF16)
     if f8:
         d = make_inputs_fp8(wl, seed=rank_seed(wl.seed, rank))
     elif w4:
-        d = make_inputs_nvfp4(wl, seed=rank_seed(wl.seed, rank))
+        d = (make_inputs_mxfp4 if mx else make_inputs_nvfp4)(wl, seed=rank_seed(wl.seed, rank))
     else:
         d = make_inputs(wl, seed=rank_seed(wl.seed, rank))
 
@@ -234,6 +235,8 @@ def run_gpu(args):
         if f8:
             fln.fused_proj_add_rmsnorm_fp8(x, sx, W, sw, r, gamma, wl.eps, wl.norm_kind, args.microchunk, out,
                                            stream)
+        elif mx:
+            fln.fused_proj_add_rmsnorm_mxfp4(x, W, sw, r, gamma, wl.eps, wl.norm_kind, args.microchunk, out, stream)
         elif w4:
             fln.fused_proj_add_rmsnorm_nvfp4(x, W, sw, d["gs"], r, gamma, wl.eps, wl.norm_kind, args.microchunk,
                                              out, stream)
@@ -295,7 +298,7 @@ def run_gpu(args):
     launches_per_step = kp["launches"] / args.steps
     tokens_per_launch = T / launches_per_step
     ob = 1.0 if f8 else 2.0  # bytes per x element (and per W element, except NVFP4)
-    wb = 0.5 + 1.0 / 16.0 if w4 else ob  # bytes per W element
+    wb = 0.5 + (1.0 / 32.0 if mx else 1.0 / 16.0) if w4 else ob  # bytes per W element
     tensor_peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if f8 else 1.0)
     if kname in ("gemm_fused", "gemm_slot"):
         # tensor bound: 2 * tokens * K * H per launch
@@ -324,7 +327,7 @@ def run_gpu(args):
                 "profiled_ms_per_step": round(prof_s * 1e3 / args.steps, 5)}
     # full-step roofline: the slower of FLOPs at tensor peak and bytes at HBM bandwidth
     t_roof = max(flops / (tensor_peak * 1e12),
-                 wl.algorithmic_bytes(1 if f8 else 0 if w4 else 2) / (peaks["hbm_gbs"] * 1e9))
+                 wl.algorithmic_bytes(1 if f8 else -1 if mx else 0 if w4 else 2) / (peaks["hbm_gbs"] * 1e9))
     step_frac = t_roof / (ms_per_step * 1e-3)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
@@ -386,6 +389,8 @@ def run_e2e(args, wl, d, W, gamma, device, stream, fln, sw=None):
         elif args.dtype == "nvfp4":
             fln.fused_proj_add_rmsnorm_nvfp4(dx, W, sw, d["gs"], dr, gamma, wl.eps, wl.norm_kind, args.microchunk,
                                              do, stream)
+        elif args.dtype == "mxfp4":
+            fln.fused_proj_add_rmsnorm_mxfp4(dx, W, sw, dr, gamma, wl.eps, wl.norm_kind, args.microchunk, do, stream)
         else:
             fln.fused_proj_add_rmsnorm(dx, W, dr, gamma, wl.eps, wl.norm_kind, args.microchunk, do, stream)
         ho.copy_(do, non_blocking=True)
@@ -421,8 +426,8 @@ def run_comparator(args, wl, x, W, d, gamma, device, stream, fln, flush, sx=None
     r = torch.from_numpy(np.ascontiguousarray(d["r0"]).view(np.int16)).view(torch.bfloat16).to(device)
     out = torch.empty_like(r)
     T, H = r.shape
-    if args.dtype == "nvfp4":
-        return {"unavailable": "no library GEMM takes NVFP4 weights with bf16 activations here"}
+    if args.dtype in ("nvfp4", "mxfp4"):
+        return {"unavailable": "no library GEMM takes FP4 weights with bf16 activations here"}
     if f8:
         # torch._scaled_mm with row-wise scales ended in an unspecified launch
         # failure (Xid 43) on this GPU under PyTorch 2.9.1 (its kernel prints
@@ -459,6 +464,9 @@ def _oracle_rows_timed(wl, d, rows, nthreads=0):
     if "x8" in d:
         oracle.proj_add_rmsnorm_fp8(d["x8"], d["x_scale"], d["W8"], d["w_scale"], d["r0"], d["gamma"], wl.eps,
                                     wl.norm_kind, rows=rows, nthreads=nthreads)
+    elif "Wq" in d and "gs" not in d:
+        oracle.proj_add_rmsnorm_mxfp4(d["x"], d["Wq"], d["S"], d["r0"], d["gamma"], wl.eps, wl.norm_kind, rows=rows,
+                                      nthreads=nthreads)
     elif "Wq" in d:
         oracle.proj_add_rmsnorm_nvfp4(d["x"], d["Wq"], d["S"], d["gs"], d["r0"], d["gamma"], wl.eps, wl.norm_kind,
                                       rows=rows, nthreads=nthreads)
@@ -484,7 +492,7 @@ def cpu_baseline(wl, d, seconds: float):
 def run_reference(args):
     """--impl reference: the oracle timed on host cores, same metric/unit/config."""
     import oracle
-    from synth import make_inputs, make_inputs_fp8, make_inputs_nvfp4, workload
+    from synth import make_inputs, make_inputs_fp8, make_inputs_mxfp4, make_inputs_nvfp4, workload
     rank, world, _ = dist_env()
     if rank != 0:
         return None
@@ -493,7 +501,7 @@ def run_reference(args):
         wl = wl.with_tokens(args.tokens)
     oracle.build()
     d = (make_inputs_fp8(wl) if args.dtype == "e4m3" else make_inputs_nvfp4(wl) if args.dtype == "nvfp4"
-         else make_inputs(wl))
+         else make_inputs_mxfp4(wl) if args.dtype == "mxfp4" else make_inputs(wl))
     cores = oracle.max_threads()
     # rows per step sized so that warm-up + steps stay within about a minute
     probe = min(wl.T, max(1, cores))
@@ -533,9 +541,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the cpu_baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0, help="--impl reference: CPU work of the whole run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--dtype", choices=["bf16", "e4m3", "nvfp4"], default="bf16",
+    ap.add_argument("--dtype", choices=["bf16", "e4m3", "nvfp4", "mxfp4"], default="bf16",
                     help="operand types: bf16; e4m3 (FP8 x and W with per-token / per-channel scales); "
-                         "nvfp4 (NVFP4 weights, bf16 x)")
+                         "nvfp4 (NVFP4 weights, bf16 x); mxfp4 (MXFP4 weights, bf16 x)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

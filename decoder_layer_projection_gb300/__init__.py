@@ -34,6 +34,7 @@ PATH_UNFUSED = 3
 DTYPE_BF16 = 0
 DTYPE_E4M3 = 1
 DTYPE_NVFP4 = 2
+DTYPE_MXFP4 = 3
 
 KERNEL_NAMES = ("gemm_fused", "gemm_slot", "gemm_splitk", "norm_bf16", "norm_slot", "norm_splitk", "w4_dequant")
 
@@ -42,7 +43,7 @@ EXPORTED_SYMBOLS = (
     "fln_get_plan", "fln_device_status", "fln_last_error", "fln_release_workspace", "fln_launch_count",
     "fln_profile_enable", "fln_profile_read", "fln_version", "fused_proj_add_rmsnorm_noalloc",
     "fln_debug_stall_next_call", "fused_proj_add_rmsnorm_fp8", "fln_autotune_dtype", "fln_set_plan_dtype",
-    "fln_get_plan_dtype", "fused_proj_add_rmsnorm_nvfp4",
+    "fln_get_plan_dtype", "fused_proj_add_rmsnorm_nvfp4", "fused_proj_add_rmsnorm_mxfp4",
 )
 
 
@@ -119,6 +120,8 @@ def load(path: str | None = None):
         lib.fused_proj_add_rmsnorm_fp8.restype = i
         lib.fused_proj_add_rmsnorm_nvfp4.argtypes = [vp, vp, vp, f, vp, vp, f, i, i, i, i, i, vp, vp]
         lib.fused_proj_add_rmsnorm_nvfp4.restype = i
+        lib.fused_proj_add_rmsnorm_mxfp4.argtypes = [vp, vp, vp, vp, vp, f, i, i, i, i, i, vp, vp]
+        lib.fused_proj_add_rmsnorm_mxfp4.restype = i
         lib.fln_autotune_dtype.argtypes = [i, i, i, i, i, vp]
         lib.fln_autotune_dtype.restype = i
         lib.fln_set_plan_dtype.argtypes = [i, i, i, i, ctypes.POINTER(Plan)]
@@ -231,6 +234,22 @@ def fused_proj_add_rmsnorm_nvfp4(x, W, W_scale, w_global_scale: float, residual,
                                                _stream_ptr(stream)))
     return out
 
+
+
+def fused_proj_add_rmsnorm_mxfp4(x, W, W_scale, residual, gamma, eps: float, norm_kind: int = NORM_STANDARD,
+                                 microchunk_tokens: int = 0, out=None, stream=None):
+    """MXFP4 weights, bf16 activations: w = 2^(W_scale[h, k/32] - 127) * e2m1(W[h, k]);
+    residual += x . w^T; out = RMSNorm(residual).  x [T,K] bf16; W [H,K/2] uint8 (element 2j in
+    the low nibble of byte j); W_scale [H,K/32] uint8 E8M0 codes.  Returns out."""
+    T, K = x.shape
+    H = W.shape[0]
+    if out is None:
+        import torch
+        out = torch.empty((T, H), dtype=residual.dtype, device=residual.device)
+    _check(load().fused_proj_add_rmsnorm_mxfp4(_ptr(x), _ptr(W), _ptr(W_scale), _ptr(residual), _ptr(gamma),
+                                               float(eps), int(norm_kind), int(T), int(K), int(H),
+                                               int(microchunk_tokens), _ptr(out), _stream_ptr(stream)))
+    return out
 
 def add_rmsnorm(y, residual, gamma, eps: float, norm_kind: int = NORM_STANDARD, out=None, stream=None):
     """residual += y; out = RMSNorm(residual).  y, residual, out [T,H] bf16; gamma [H] fp32."""

@@ -83,7 +83,7 @@ struct Workspace {
   unsigned int* dyn_counter = nullptr;  // split-K dynamic chunk draws; each GEMM launch leaves it at zero
   __nv_bfloat16* w4_bf16 = nullptr;    // NVFP4 weights converted to bf16 (paths with many tokens)
   size_t w4_bf16_elems = 0;
-  bool prepared_w4[5] = {};
+  bool prepared_w4[2][5] = {};          // [fmt][tile]
   cudaStream_t stream_b = nullptr;
   cudaEvent_t ev_ready[3] = {};
   cudaEvent_t ev_free[3] = {};
@@ -293,8 +293,9 @@ struct Call {
   int x_scale_stride = 0;      // 1: per token, 0: per tensor
   const float* w_scale = nullptr;
   int w_scale_stride = 0;      // 1: per output row of W, 0: per tensor
-  int w4 = 0;                  // W holds packed NVFP4 codes (x bf16)
-  const uint8_t* w4_scales = nullptr;  // [H, K/16] E4M3 block scales
+  int w4 = 0;                  // W holds packed FP4 codes (x bf16)
+  int w4_fmt = 0;              // 0 NVFP4: [H, K/16] E4M3 block scales; 1 MXFP4: [H, K/32] E8M0
+  const uint8_t* w4_scales = nullptr;
   float y_scale = 1.0f;        // tensor scale of W, applied to the fp32 projection
   int esize() const { return f8 ? 1 : 2; }
   int k_blocks() const { return (K + kblock_elems(f8) - 1) / kblock_elems(f8); }
@@ -330,9 +331,9 @@ int run_unfused(Workspace* ws, const Call& c) {
   int rc = FLN_OK;
   if (c.w4) {
     const int bi = bn_index(bn);
-    if (!ws->prepared_w4[bi]) {
-      FLN_CUDA(w4_gemm_prepare(bn), "cudaFuncSetAttribute(max dynamic shared memory)");
-      ws->prepared_w4[bi] = true;
+    if (!ws->prepared_w4[c.w4_fmt][bi]) {
+      FLN_CUDA(w4_gemm_prepare(bn, c.w4_fmt), "cudaFuncSetAttribute(max dynamic shared memory)");
+      ws->prepared_w4[c.w4_fmt][bi] = true;
     }
   } else if ((rc = prepare_kernel(ws, bn, EPI_SPLITK_SWAP, c.f8))) {
     return rc;
@@ -400,12 +401,12 @@ int run_unfused(Workspace* ws, const Call& c) {
   if ((rc = grow(&ws->partial, &ws->partial_floats, need, false, "cudaMalloc(split-K partials)"))) return rc;
   p.partial = ws->partial;
   p.w4_scales = c.w4_scales;
-  p.w4_nblk = c.K / 16;
+  p.w4_nblk = c.w4_fmt ? c.K / 32 : c.K / 16;  // scale bytes per row
   p.err = ws->err_word;
   p.dyn_counter = ws->dyn_counter;
   rc = launch_counted(FLN_KERNEL_GEMM_SPLITK, c.stream,
                       [&] {
-                        return c.w4 ? launch_w4_gemm_splitk(bn, tmA, tmB, p, G, c.stream)
+                        return c.w4 ? launch_w4_gemm_splitk(bn, c.w4_fmt, tmA, tmB, p, G, c.stream)
                                     : launch_gemm(EPI_SPLITK_SWAP, bn, c.f8, tmA, tmB, p, G, c.stream);
                       },
                       "split-K GEMM launch");
@@ -428,7 +429,7 @@ int run_unfused(Workspace* ws, const Call& c) {
   np.H = c.H;
   np.pdl = g_prof ? 0 : 1;  // timing events between the two launches would break the overlap
   // the NVFP4 split-K kernel's partials are y * 2^-8 (its dequantised weights carry that factor)
-  np.y_scale = c.w4 ? c.y_scale * 256.0f : c.y_scale;
+  np.y_scale = c.w4 && c.w4_fmt == 0 ? c.y_scale * 256.0f : c.y_scale;
   if (c.f8) {
     np.x_scale = c.x_scale;
     np.x_scale_stride = c.x_scale_stride;
@@ -668,10 +669,10 @@ int run_plan(Workspace* ws, const Call& c, const fln_plan& pl) {
     if (rc) return rc;
     rc = launch_counted(FLN_KERNEL_W4_DEQUANT, c.stream,
                         [&] {
-                          return launch_nvfp4_to_bf16(static_cast<const uint8_t*>(c.W), c.w4_scales, ws->w4_bf16,
-                                                      c.H, c.K, c.stream);
+                          return launch_fp4_to_bf16(c.w4_fmt, static_cast<const uint8_t*>(c.W), c.w4_scales,
+                                                    ws->w4_bf16, c.H, c.K, c.stream);
                         },
-                        "NVFP4 weight conversion launch");
+                        "FP4 weight conversion launch");
     if (rc) return rc;
     Call cb = c;
     cb.w4 = 0;
@@ -734,11 +735,13 @@ int validate_fp8(const uint8_t* x, const float* x_scale, int x_per_token, const 
   return FLN_OK;
 }
 
-int validate_w4(const fln_bf16* x, const uint8_t* W, const uint8_t* S, float gs, fln_bf16* residual,
+int validate_w4(int fmt, const fln_bf16* x, const uint8_t* W, const uint8_t* S, float gs, fln_bf16* residual,
                 const float* gamma, float eps, int kind, int T, int K, int H, int chunk, fln_bf16* out) {
   int rc = check_common(eps, kind, T, H);
   if (rc) return rc;
-  if (K < 64 || (K & 63)) return fail(FLN_ERR_INVALID_ARG, "K=%d must be a positive multiple of 64 for NVFP4", K);
+  const int kal = fmt ? 128 : 64;  // MXFP4: rows of K/32 scale bytes are whole 4-byte words
+  if (K < kal || K % kal)
+    return fail(FLN_ERR_INVALID_ARG, "K=%d must be a positive multiple of %d for %s", K, kal, fmt ? "MXFP4" : "NVFP4");
   if (K > kMaxK) return fail(FLN_ERR_UNSUPPORTED, "K=%d above the supported %d", K, kMaxK);
   if (!std::isfinite(gs) || std::fabs(gs) > 0x1p100f)
     return fail(FLN_ERR_INVALID_ARG, "w_global_scale must be finite with magnitude at most 2^100");
@@ -748,7 +751,8 @@ int validate_w4(const fln_bf16* x, const uint8_t* W, const uint8_t* S, float gs,
   if ((rc = check_ptr("x", x)) || (rc = check_ptr("W", W)) || (rc = check_ptr("W_scale", S)) ||
       (rc = check_ptr("residual", residual)) || (rc = check_ptr("gamma", gamma)) || (rc = check_ptr("out", out)))
     return rc;
-  const size_t bx = size_t(T) * K * 2, bw = size_t(H) * K / 2, bs = size_t(H) * K / 16, br = size_t(T) * H * 2,
+  const size_t bx = size_t(T) * K * 2, bw = size_t(H) * K / 2, bs = size_t(H) * K / (fmt ? 32 : 16),
+               br = size_t(T) * H * 2,
                bg = size_t(H) * 4;
   if (overlaps(out, br, x, bx) || overlaps(out, br, W, bw) || overlaps(out, br, S, bs) ||
       overlaps(out, br, residual, br) || overlaps(out, br, gamma, bg))
@@ -964,8 +968,8 @@ int fused_proj_add_rmsnorm_nvfp4(const fln_bf16* x, const uint8_t* W, const uint
                                  int norm_kind, int T, int K, int H, int microchunk_tokens, fln_bf16* out,
                                  fln_stream_t stream) {
   std::lock_guard<std::mutex> lk(g_mu);
-  int rc = validate_w4(x, W, W_scale, w_global_scale, residual, gamma, eps, norm_kind, T, K, H, microchunk_tokens,
-                       out);
+  int rc = validate_w4(0, x, W, W_scale, w_global_scale, residual, gamma, eps, norm_kind, T, K, H,
+                       microchunk_tokens, out);
   if (rc) return rc;
   if (T == 0) return FLN_OK;
   fln_plan pl;
@@ -977,6 +981,25 @@ int fused_proj_add_rmsnorm_nvfp4(const fln_bf16* x, const uint8_t* W, const uint
   c.w4 = 1;
   c.w4_scales = W_scale;
   c.y_scale = w_global_scale;
+  return run_plan(ws, c, pl);
+}
+
+int fused_proj_add_rmsnorm_mxfp4(const fln_bf16* x, const uint8_t* W, const uint8_t* W_scale, fln_bf16* residual,
+                                 const float* gamma, float eps, int norm_kind, int T, int K, int H,
+                                 int microchunk_tokens, fln_bf16* out, fln_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = validate_w4(1, x, W, W_scale, 1.0f, residual, gamma, eps, norm_kind, T, K, H, microchunk_tokens, out);
+  if (rc) return rc;
+  if (T == 0) return FLN_OK;
+  fln_plan pl;
+  if ((rc = resolve_plan(K, H, norm_kind, FLN_DTYPE_MXFP4, T, microchunk_tokens, &pl))) return rc;
+  Workspace* ws = nullptr;
+  if ((rc = get_ws(&ws))) return rc;
+  Call c{x, W, reinterpret_cast<__nv_bfloat16*>(residual), gamma, eps, norm_kind, T, K, H,
+         reinterpret_cast<__nv_bfloat16*>(out), reinterpret_cast<cudaStream_t>(stream)};
+  c.w4 = 1;
+  c.w4_fmt = 1;
+  c.w4_scales = W_scale;
   return run_plan(ws, c, pl);
 }
 
@@ -1025,7 +1048,7 @@ int fln_set_overrides(int microchunk_tokens, int threshold_tokens) {
 int fln_set_plan_dtype(int K, int H, int norm_kind, int dtype, const fln_plan* plan) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (K < 8 || (K & 7) || H < 8 || (H & 7) || (norm_kind != 0 && norm_kind != 1) ||
-      (dtype != FLN_DTYPE_BF16 && dtype != FLN_DTYPE_E4M3 && dtype != FLN_DTYPE_NVFP4))
+      dtype < FLN_DTYPE_BF16 || dtype > FLN_DTYPE_MXFP4)
     return fail(FLN_ERR_INVALID_ARG, "bad group (K=%d, H=%d, kind=%d, dtype=%d)", K, H, norm_kind, dtype);
   if (!plan) {
     g_plans.erase({K, H, norm_kind, dtype});
@@ -1044,8 +1067,7 @@ int fln_set_plan(int K, int H, int norm_kind, const fln_plan* plan) {
 int fln_get_plan_dtype(int K, int H, int norm_kind, int dtype, int T, int microchunk_tokens, fln_plan* plan) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!plan) return fail(FLN_ERR_INVALID_ARG, "plan is NULL");
-  if (dtype != FLN_DTYPE_BF16 && dtype != FLN_DTYPE_E4M3 && dtype != FLN_DTYPE_NVFP4)
-    return fail(FLN_ERR_INVALID_ARG, "dtype=%d", dtype);
+  if (dtype < FLN_DTYPE_BF16 || dtype > FLN_DTYPE_MXFP4) return fail(FLN_ERR_INVALID_ARG, "dtype=%d", dtype);
   if (microchunk_tokens < 0 || microchunk_tokens > kMaxMicrochunk)
     return fail(FLN_ERR_INVALID_ARG, "microchunk_tokens=%d outside 0..%d", microchunk_tokens, kMaxMicrochunk);
   return resolve_plan(K, H, norm_kind, dtype, T, microchunk_tokens, plan);
@@ -1063,11 +1085,11 @@ int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, f
   std::lock_guard<std::mutex> lk(g_mu);
   int rc = check_common(1e-5f, norm_kind, max_tokens, H);
   if (rc) return rc;
-  if (dtype != FLN_DTYPE_BF16 && dtype != FLN_DTYPE_E4M3 && dtype != FLN_DTYPE_NVFP4)
-    return fail(FLN_ERR_INVALID_ARG, "dtype=%d", dtype);
+  if (dtype < FLN_DTYPE_BF16 || dtype > FLN_DTYPE_MXFP4) return fail(FLN_ERR_INVALID_ARG, "dtype=%d", dtype);
   const int f8 = dtype == FLN_DTYPE_E4M3 ? 1 : 0;
-  const int w4 = dtype == FLN_DTYPE_NVFP4 ? 1 : 0;
-  const int kalign = w4 ? 64 : f8 ? 16 : 8;
+  const int w4 = dtype == FLN_DTYPE_NVFP4 || dtype == FLN_DTYPE_MXFP4 ? 1 : 0;
+  const int w4_fmt = dtype == FLN_DTYPE_MXFP4 ? 1 : 0;
+  const int kalign = w4_fmt ? 128 : w4 ? 64 : f8 ? 16 : 8;
   if (K < kalign || K % kalign || K > kMaxK)
     return fail(FLN_ERR_INVALID_ARG, "K=%d must be a multiple of %d in [%d, %d]", K, kalign, kalign, kMaxK);
   if (max_tokens < 1 || max_tokens > 65536) return fail(FLN_ERR_INVALID_ARG, "max_tokens must be in 1..65536");
@@ -1097,10 +1119,13 @@ int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, f
   const float host_scales[4] = {1.0f / 16.0f, 1.0f / (16.0f * std::sqrt(float(K))), 0.f, 0.f};
   if (w4) {
     // NVFP4: random code bytes (every byte is two valid codes), block scales
-    // 0.5 .. 1.875 (E4M3 codes 0x30 .. 0x3F), tensor scale 1/(2 sqrt K)
-    FLN_CUDA(cudaMalloc(&bw4s.p, nw / 16), "tune: cudaMalloc");
+    // 0.5 .. 1.875 (E4M3 codes 0x30 .. 0x3F), tensor scale 1/(2 sqrt K);
+    // MXFP4: the same codes, block scales 2^-3 .. 1 (E8M0 codes 124 .. 127)
+    const size_t ns = nw / (w4_fmt ? 32 : 16);
+    FLN_CUDA(cudaMalloc(&bw4s.p, ns), "tune: cudaMalloc");
     fill_bytes<<<1024, 256, 0, s>>>(static_cast<uint8_t*>(bw.p), nw / 2, 0x5678u, 0xFFu, 0u);
-    fill_bytes<<<1024, 256, 0, s>>>(static_cast<uint8_t*>(bw4s.p), nw / 16, 0x4321u, 0x0Fu, 0x30u);
+    fill_bytes<<<1024, 256, 0, s>>>(static_cast<uint8_t*>(bw4s.p), ns, 0x4321u, w4_fmt ? 0x03u : 0x0Fu,
+                                    w4_fmt ? 0x7Cu : 0x30u);
     fill_pseudo_normal<<<1024, 256, 0, s>>>(static_cast<__nv_bfloat16*>(bx.p), nx, 0x1234u, 1.0f, 0.0f);
   } else if (f8) {
     FLN_CUDA(cudaMalloc(&bscale.p, sizeof host_scales), "tune: cudaMalloc");
@@ -1127,8 +1152,9 @@ int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, f
   }
   if (w4) {
     t.c.w4 = 1;
+    t.c.w4_fmt = w4_fmt;
     t.c.w4_scales = static_cast<const uint8_t*>(bw4s.p);
-    t.c.y_scale = 1.0f / (2.0f * std::sqrt(float(K)));
+    t.c.y_scale = w4_fmt ? 1.0f : 1.0f / (2.0f * std::sqrt(float(K)));
   }
   t.res0 = r0;
   t.flush = bflush.p;

@@ -1,10 +1,11 @@
-// fln_gemm_w4.cu -- split-K projection GEMM for few tokens with NVFP4 weights
+// fln_gemm_w4.cu -- split-K projection GEMM for few tokens with NVFP4 or MXFP4 weights
 // (the UNFUSED path of the "TPSP Design" page, section 3, for the page's
 // section 5 to-do item "MXFP4 / NVFP4 dense": low-bit weight layouts and
 // their scaling).
 //
 // W holds E2M1 codes packed two per byte along K (element 2j in the low
-// nibble of byte j) with one E4M3 scale per 16 elements of a row; x is bf16.
+// nibble of byte j) with one E4M3 scale per 16 elements of a row (NVFP4) or
+// one E8M0 scale per 32 (MXFP4, the OCP microscaling layout); x is bf16.
 // Four K-blocks of 64 elements of 128 weight rows arrive packed (16 KiB,
 // 128-byte swizzled) in one TMA load, their block scales by cp.async on the
 // same barrier; eight dequantisation warps turn each row's 64 codes of a
@@ -139,9 +140,16 @@ __device__ __forceinline__ uint32_t e4m3_to_bf16_bits_x2p118(uint32_t code) {
   return (b & 0x7FFFu) ? b + (118u << 7) : 0u;
 }
 
+// bf16 bits of the E8M0 scale code E: 2^(E - 127) (the code 0 is the bf16
+// subnormal 2^-127), NaN for 255
+__device__ __forceinline__ uint32_t e8m0_to_bf16_bits(uint32_t E) {
+  return E == 255u ? 0x7FC0u : E == 0u ? 0x0040u : (E << 7);
+}
+
 // Eight E2M1 codes (code i in bits 4i..4i+3 of w) -> four bf16 pairs, codes
 // 2j and 2j + 1 in the low and high half of word j, each e2m1 * 2^-126 times
-// the bf16 in both halves of s2.  A code's three magnitude bits become the two
+// the bf16 in both halves of s2 (with UNBIAS, first times 2^126: then e2m1
+// times s2, exact for any power-of-two scale whose product stays finite).  A code's three magnitude bits become the two
 // lowest exponent bits and the top fraction bit of a bf16 and its sign the
 // sign: that bf16 is e2m1 * 2^-126 exactly (the zero exponent, a subnormal,
 // gives the code of 0.5 its value).  Byte j of ev / od holds code 2j / 2j + 1
@@ -150,14 +158,18 @@ __device__ __forceinline__ uint32_t e4m3_to_bf16_bits_x2p118(uint32_t code) {
 // makes the shifted copies (magnitude at bit 6, sign at bit 15 of each half,
 // no carries: the copies do not overlap) and a mask keeps those bits.  The
 // product with s2 is exact when s2 holds a block scale times 2^118.
+template <bool UNBIAS>
 __device__ __forceinline__ uint4 e2m1x8_to_bf16_biased(uint32_t w, uint32_t s2) {
   const uint32_t ev = w & 0x0F0F0F0Fu, od = (w >> 4) & 0x0F0F0F0Fu;
   const __nv_bfloat162 sc = *reinterpret_cast<const __nv_bfloat162*>(&s2);
+  constexpr uint32_t P126 = 0x7E807E80u;  // 2^126 in both halves
   uint32_t o[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t b = (prmt(ev, od, 0xC480u + 0x1111u * static_cast<uint32_t>(j)) * 4160u) & 0x81C081C0u;
-    const __nv_bfloat162 t = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b), sc);
+    __nv_bfloat162 t = *reinterpret_cast<const __nv_bfloat162*>(&b);
+    if (UNBIAS) t = __hmul2(t, *reinterpret_cast<const __nv_bfloat162*>(&P126));
+    t = __hmul2(t, sc);
     o[j] = *reinterpret_cast<const uint32_t*>(&t);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
@@ -186,12 +198,15 @@ struct Items {
   }
 };
 
-template <int BN>
+// FMT 0: NVFP4 (E4M3 scale per 16 elements, w carries 2^-8 for the reducer
+// to undo); FMT 1: MXFP4 (E8M0 scale per 32 elements, w exact)
+template <int BN, int FMT>
 __global__ void __launch_bounds__(THREADS, 1)
     fln_gemm_w4_splitk_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                               const GemmParams p) {
   using C = Cfg<BN>;
   constexpr int RW = C::RW, XS = C::XS, NACC = C::NACC, AS = C::AS, NSUB = C::NSUB;
+  constexpr int SPK = FMT ? 2 : 4;  // scale bytes per K-block of a row
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -210,7 +225,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* drain_bar = acc_empty + NACC;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  // E4M3 code -> its value times 2^118 as bf16, in both halves (the dequantisation's block-scale operand)
+  // scale code -> the dequantisation's block-scale operand as bf16, in both halves: an E4M3 value
+  // times 2^118 (NVFP4) or an E8M0 value (MXFP4)
   uint32_t* scale_lut = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(w_full) + 1024);
 
   const int warp = threadIdx.x >> 5;
@@ -243,7 +259,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmX);
   }
   if (threadIdx.x < 256) {
-    const uint32_t b = e4m3_to_bf16_bits_x2p118(threadIdx.x);
+    const uint32_t b = FMT ? e8m0_to_bf16_bits(threadIdx.x) : e4m3_to_bf16_bits_x2p118(threadIdx.x);
     scale_lut[threadIdx.x] = b | (b << 16);
   }
   if (warp == 1) {
@@ -282,15 +298,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           w_mask |= 1u << rw;
           w_par = (w_par & ~(1u << rw)) | (wph << rw);
         }
-        // scales of K-blocks [g0, g1): row r's 4 bytes of K-block kb land at r * 16 + 4 (kb - g0)
+        // scales of K-blocks [g0, g1), SPK bytes a K-block: the 4-byte words covering them land
+        // at r * 16 + 4 i (rows hold a multiple of 4 scale bytes, so no word crosses a row's end)
+        const int b0 = (SPK * g0) & ~3, nw = ((SPK * g1 + 3) & ~3) - b0;
         const uint32_t sdst = smem_u32(sS + rw * S_BYTES);
 #pragma unroll
         for (int i = 0; i < BM / 32; ++i) {
           const int r = lane + 32 * i;
           const int h = m_tile * BM + r;
           if (h < p.M) {
-            const uint8_t* src = p.w4_scales + static_cast<size_t>(h) * static_cast<size_t>(p.w4_nblk) + 4 * g0;
-            for (int j = 0; j < g1 - g0; ++j) cp_async4(sdst + static_cast<uint32_t>(r * 16 + 4 * j), src + 4 * j);
+            const uint8_t* src = p.w4_scales + static_cast<size_t>(h) * static_cast<size_t>(p.w4_nblk) + b0;
+            for (int o = 0; o < nw; o += 4) cp_async4(sdst + static_cast<uint32_t>(r * 16 + o), src + o);
           }
         }
         cp_async_mbar_arrive_noinc(&w_full[rw]);
@@ -369,9 +387,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           ok = false;
           break;
         }
-        // this row's scales of the entry: word j = K-block g0 + j, this thread's two in bytes 2 half, 2 half + 1
+        // this row's scale bytes of the entry (first byte at (SPK g0) % 4): NVFP4 K-block j's two for
+        // this thread in word j, bytes 2 half and 2 half + 1; MXFP4 K-block j's one at byte 2 j + half
         const uint4 sc4 = *reinterpret_cast<const uint4*>(sS + rw * S_BYTES + row * 16);
         const uint32_t scw[KG] = {sc4.x, sc4.y, sc4.z, sc4.w};
+        const int mx0 = ((SPK * g0) & 3) + half;  // MXFP4: byte of K-block 0
         const uint8_t* went = sW + rw * W_BYTES;
         uint32_t v[KG][16];
 #pragma unroll
@@ -379,11 +399,21 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (j < nk) {
             // 16-byte chunk 2 j + half of this row in the swizzled entry
             const uint4 cq = *reinterpret_cast<const uint4*>(went + coff[j]);
-            const uint32_t sc = vrow ? (scw[j] >> (16 * half)) : 0u;
-            // values w * 2^-8 (block scale times 2^118 on codes times 2^-126); the reducer multiplies by 2^8
-            const uint32_t s20 = scale_lut[sc & 0xFFu], s21 = scale_lut[(sc >> 8) & 0xFFu];
-            const uint4 v0 = e2m1x8_to_bf16_biased(cq.x, s20), v1 = e2m1x8_to_bf16_biased(cq.y, s20);
-            const uint4 v2 = e2m1x8_to_bf16_biased(cq.z, s21), v3 = e2m1x8_to_bf16_biased(cq.w, s21);
+            uint32_t s20, s21;
+            if (FMT == 0) {
+              // values w * 2^-8 (block scale times 2^118 on codes times 2^-126); the reducer multiplies by 2^8
+              const uint32_t sc = vrow ? (scw[j] >> (16 * half)) : 0u;
+              s20 = scale_lut[sc & 0xFFu];
+              s21 = scale_lut[(sc >> 8) & 0xFFu];
+            } else {
+              const int bi = mx0 + 2 * j;
+              const uint32_t wd = bi < 4 ? scw[0] : bi < 8 ? scw[1] : scw[2];
+              s20 = s21 = vrow ? scale_lut[(wd >> (8 * (bi & 3))) & 0xFFu] : 0u;
+            }
+            const uint4 v0 = e2m1x8_to_bf16_biased<FMT == 1>(cq.x, s20);
+            const uint4 v1 = e2m1x8_to_bf16_biased<FMT == 1>(cq.y, s20);
+            const uint4 v2 = e2m1x8_to_bf16_biased<FMT == 1>(cq.z, s21);
+            const uint4 v3 = e2m1x8_to_bf16_biased<FMT == 1>(cq.w, s21);
             v[j][0] = v0.x, v[j][1] = v0.y, v[j][2] = v0.z, v[j][3] = v0.w;
             v[j][4] = v1.x, v[j][5] = v1.y, v[j][6] = v1.z, v[j][7] = v1.w;
             v[j][8] = v2.x, v[j][9] = v2.y, v[j][10] = v2.z, v[j][11] = v2.w;
@@ -532,62 +562,74 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
-template <int BN>
+template <int BN, int FMT>
 static cudaError_t run_bn(const CUtensorMap* tmW, const CUtensorMap* tmX, const GemmParams* p, int grid,
                           cudaStream_t stream) {
   if (!tmW) {
-    return cudaFuncSetAttribute(fln_gemm_w4_splitk_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(fln_gemm_w4_splitk_kernel<BN, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Cfg<BN>::SMEM);
   }
-  fln_gemm_w4_splitk_kernel<BN><<<grid, THREADS, Cfg<BN>::SMEM, stream>>>(*tmW, *tmX, *p);
+  fln_gemm_w4_splitk_kernel<BN, FMT><<<grid, THREADS, Cfg<BN>::SMEM, stream>>>(*tmW, *tmX, *p);
   return cudaGetLastError();
 }
 
-static cudaError_t dispatch(int bn, const CUtensorMap* tmW, const CUtensorMap* tmX, const GemmParams* p, int grid,
-                            cudaStream_t stream) {
+template <int FMT>
+static cudaError_t dispatch_fmt(int bn, const CUtensorMap* tmW, const CUtensorMap* tmX, const GemmParams* p,
+                                int grid, cudaStream_t stream) {
   switch (bn) {
-    case 16: return run_bn<16>(tmW, tmX, p, grid, stream);
-    case 32: return run_bn<32>(tmW, tmX, p, grid, stream);
-    case 64: return run_bn<64>(tmW, tmX, p, grid, stream);
-    case 128: return run_bn<128>(tmW, tmX, p, grid, stream);
-    case 256: return run_bn<256>(tmW, tmX, p, grid, stream);
+    case 16: return run_bn<16, FMT>(tmW, tmX, p, grid, stream);
+    case 32: return run_bn<32, FMT>(tmW, tmX, p, grid, stream);
+    case 64: return run_bn<64, FMT>(tmW, tmX, p, grid, stream);
+    case 128: return run_bn<128, FMT>(tmW, tmX, p, grid, stream);
+    case 256: return run_bn<256, FMT>(tmW, tmX, p, grid, stream);
   }
   return cudaErrorInvalidValue;
 }
 
+static cudaError_t dispatch(int bn, int fmt, const CUtensorMap* tmW, const CUtensorMap* tmX, const GemmParams* p,
+                            int grid, cudaStream_t stream) {
+  return fmt ? dispatch_fmt<1>(bn, tmW, tmX, p, grid, stream) : dispatch_fmt<0>(bn, tmW, tmX, p, grid, stream);
+}
+
 // Whole weight to bf16 for the paths with many tokens: one thread per eight
 // elements (one 32-bit word of codes), w = e2m1 * block scale (exact); the
-// tensor scale stays with the GEMM.  K % 64 == 0.
-__global__ void nvfp4_to_bf16_kernel(const uint32_t* __restrict__ Wq, const uint8_t* __restrict__ S,
-                                     uint4* __restrict__ out, int H, int K) {
+// NVFP4 tensor scale stays with the GEMM.  K % 64 == 0.
+template <int FMT>
+__global__ void fp4_to_bf16_kernel(const uint32_t* __restrict__ Wq, const uint8_t* __restrict__ S,
+                                   uint4* __restrict__ out, int H, int K) {
   const size_t words = static_cast<size_t>(H) * (K / 8);
-  const int wpr = K / 8;      // words per row
-  const int nblk = K / 16;
+  const int wpr = K / 8;                       // words per row
+  const int nblk = FMT ? K / 32 : K / 16;      // scales per row
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < words;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const size_t h = i / wpr;
     const int c = static_cast<int>(i - h * wpr);   // elements 8c .. 8c + 7 of the row
-    const uint32_t sb = e4m3_to_bf16_bits(S[h * nblk + (c >> 1)]);
+    const uint32_t code = S[h * nblk + (FMT ? (c >> 2) : (c >> 1))];
+    const uint32_t sb = FMT ? e8m0_to_bf16_bits(code) : e4m3_to_bf16_bits(code);
     out[i] = e2m1x8_to_bf16(__ldg(Wq + i), sb | (sb << 16));
   }
 }
 
 }  // namespace w4
 
-cudaError_t launch_nvfp4_to_bf16(const uint8_t* Wq, const uint8_t* S, __nv_bfloat16* out, int H, int K,
-                                 cudaStream_t stream) {
+cudaError_t launch_fp4_to_bf16(int fmt, const uint8_t* Wq, const uint8_t* S, __nv_bfloat16* out, int H, int K,
+                               cudaStream_t stream) {
   const size_t words = static_cast<size_t>(H) * (K / 8);
   const int grid = static_cast<int>(std::min<size_t>((words + 255) / 256, 152 * 16));
-  w4::nvfp4_to_bf16_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint32_t*>(Wq), S,
-                                                     reinterpret_cast<uint4*>(out), H, K);
+  if (fmt)
+    w4::fp4_to_bf16_kernel<1><<<grid, 256, 0, stream>>>(reinterpret_cast<const uint32_t*>(Wq), S,
+                                                        reinterpret_cast<uint4*>(out), H, K);
+  else
+    w4::fp4_to_bf16_kernel<0><<<grid, 256, 0, stream>>>(reinterpret_cast<const uint32_t*>(Wq), S,
+                                                        reinterpret_cast<uint4*>(out), H, K);
   return cudaGetLastError();
 }
 
-cudaError_t w4_gemm_prepare(int bn) { return w4::dispatch(bn, nullptr, nullptr, nullptr, 0, nullptr); }
+cudaError_t w4_gemm_prepare(int bn, int fmt) { return w4::dispatch(bn, fmt, nullptr, nullptr, nullptr, 0, nullptr); }
 
-cudaError_t launch_w4_gemm_splitk(int bn, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p,
-                                  int grid, cudaStream_t stream) {
-  return w4::dispatch(bn, &tmW, &tmX, &p, grid, stream);
+cudaError_t launch_w4_gemm_splitk(int bn, int fmt, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                                  const GemmParams& p, int grid, cudaStream_t stream) {
+  return w4::dispatch(bn, fmt, &tmW, &tmX, &p, grid, stream);
 }
 
 }  // namespace fln

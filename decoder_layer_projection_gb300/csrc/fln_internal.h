@@ -66,8 +66,8 @@ struct GemmParams {
   int x_scale_stride;
   const float* w_scale;
   int w_scale_stride;
-  // NVFP4 weights (split-K kernel of fln_gemm_w4.cu): E4M3 block scales
-  // [M rows, w4_nblk], one per 16 elements of a row
+  // FP4 weights (split-K kernel of fln_gemm_w4.cu): block scales [M rows,
+  // w4_nblk bytes], one per 16 (NVFP4) or 32 (MXFP4) elements of a row
   const uint8_t* w4_scales;
   int w4_nblk;
   // every path: the accumulator is multiplied by y_scale before anything
@@ -131,15 +131,16 @@ cudaError_t launch_gemm_pair_fused(int bn, int f8, int ew, const CUtensorMap& tm
                                    const CUtensorMap& tmR, const CUtensorMap& tmRs, const CUtensorMap& tmOs,
                                    const GemmParams& p, int pairs, cudaStream_t stream);
 
-// NVFP4 weights: the split-K GEMM that dequantises W in shared memory
-// (fln_gemm_w4.cu; tokens on N: bn 16..256), and the conversion of a whole
-// weight to bf16 (w = e2m1 * block scale, exact) for the paths with many
-// tokens.  prepare sets the shared-memory limit.
-cudaError_t w4_gemm_prepare(int bn);
-cudaError_t launch_w4_gemm_splitk(int bn, const CUtensorMap& tmW, const CUtensorMap& tmX, const GemmParams& p,
-                                  int grid, cudaStream_t stream);
-cudaError_t launch_nvfp4_to_bf16(const uint8_t* Wq, const uint8_t* S, __nv_bfloat16* out, int H, int K,
-                                 cudaStream_t stream);
+// FP4 weights (fmt 0 NVFP4: E4M3 scale per 16 elements; fmt 1 MXFP4: E8M0
+// scale per 32): the split-K GEMM that dequantises W on the SM into tensor
+// memory (fln_gemm_w4.cu; tokens on N: bn 16..256), and the conversion of a
+// whole weight to bf16 (w = e2m1 * block scale, exact) for the paths with
+// many tokens.  prepare sets the shared-memory limit.
+cudaError_t w4_gemm_prepare(int bn, int fmt);
+cudaError_t launch_w4_gemm_splitk(int bn, int fmt, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                                  const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fp4_to_bf16(int fmt, const uint8_t* Wq, const uint8_t* S, __nv_bfloat16* out, int H, int K,
+                               cudaStream_t stream);
 
 enum NormSource : int { NORM_SRC_BF16 = 0, NORM_SRC_F32 = 1, NORM_SRC_SPLITK = 2 };
 cudaError_t launch_add_rmsnorm(NormSource src, const NormParams& p, int grid_cap, cudaStream_t stream);

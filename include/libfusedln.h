@@ -119,7 +119,7 @@ int fused_proj_add_rmsnorm(const fln_bf16* x, const fln_bf16* W, fln_bf16* resid
                            fln_stream_t stream);
 
 /* Operand element types of a projection group. */
-typedef enum { FLN_DTYPE_BF16 = 0, FLN_DTYPE_E4M3 = 1, FLN_DTYPE_NVFP4 = 2 } fln_dtype;
+typedef enum { FLN_DTYPE_BF16 = 0, FLN_DTYPE_E4M3 = 1, FLN_DTYPE_NVFP4 = 2, FLN_DTYPE_MXFP4 = 3 } fln_dtype;
 
 /*
  * fused_proj_add_rmsnorm_fp8 -- the same region with FP8 operands ("TPSP
@@ -170,16 +170,40 @@ int fused_proj_add_rmsnorm_fp8(const uint8_t* x, const float* x_scale, int x_sca
  * e2m1 * e4m3 is exact in bf16, so the tensor cores multiply bf16 x by exact
  * bf16 weights with fp32 accumulation, and the tensor scale multiplies the
  * fp32 result.  Below the threshold (few tokens) the split-K GEMM reads W
- * packed (0.5625 bytes per weight) and dequantises it in shared memory; at
- * and above it the call first converts the whole weight to bf16 in the
+ * packed (0.5625 bytes per weight) and dequantises it on the SM; at and
+ * above it the call first converts the whole weight to bf16 in the
  * workspace (H * K * 2 bytes) and runs the bf16 FUSED or PIPELINED path.
  * Plans, tuning and the threshold are kept per (K, H, norm_kind,
- * FLN_DTYPE_NVFP4) group.
+ * FLN_DTYPE_NVFP4) group.  |w_global_scale| must not exceed 2^100
+ * (FLN_ERR_INVALID_ARG otherwise).
  */
 int fused_proj_add_rmsnorm_nvfp4(const fln_bf16* x, const uint8_t* W, const uint8_t* W_scale,
                                  float w_global_scale, fln_bf16* residual, const float* gamma, float eps,
                                  int norm_kind, int T, int K, int H, int microchunk_tokens, fln_bf16* out,
                                  fln_stream_t stream);
+
+/*
+ * fused_proj_add_rmsnorm_mxfp4 -- the region with MXFP4 weights (the OCP
+ * microscaling FP4 layout) and bf16 activations (the same "MXFP4 / NVFP4
+ * dense" to-do item):
+ *
+ *     w[h,k] = e8m0(W_scale[h, k/32]) * e2m1(W[h,k]),  e8m0(E) = 2^(E - 127)
+ *     residual += x . w^T;  out = RMSNorm(residual)
+ *
+ *   x           [T, K] bf16
+ *   W           [H, K/2] bytes, packed as for fused_proj_add_rmsnorm_nvfp4
+ *   W_scale     [H, K/32] E8M0 codes, one per 32 consecutive elements of a
+ *               row; the code 255 (NaN) makes its row's outputs NaN
+ *   K           multiple of 128; the rest as in fused_proj_add_rmsnorm
+ *
+ * Every w is a bf16 value as long as |w| stays below the bf16 maximum
+ * (E <= 252 always does): the tensor cores multiply bf16 x by exact bf16
+ * weights with fp32 accumulation.  Paths, workspace and plans as for NVFP4,
+ * per (K, H, norm_kind, FLN_DTYPE_MXFP4) group.
+ */
+int fused_proj_add_rmsnorm_mxfp4(const fln_bf16* x, const uint8_t* W, const uint8_t* W_scale, fln_bf16* residual,
+                                 const float* gamma, float eps, int norm_kind, int T, int K, int H,
+                                 int microchunk_tokens, fln_bf16* out, fln_stream_t stream);
 
 /*
  * add_rmsnorm -- residual += y; out = RMSNorm(residual)   (the add/norm step alone)

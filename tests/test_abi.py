@@ -192,6 +192,7 @@ def test_epilogue_warps_plan_validation(lib):
     (dict(norm_kind=4), fln.FLN_ERR_INVALID_ARG),
     (dict(T=-1), fln.FLN_ERR_INVALID_ARG),
     (dict(gs=float("nan")), fln.FLN_ERR_INVALID_ARG),
+    (dict(gs=2.0 ** 101), fln.FLN_ERR_INVALID_ARG),  # the reducer scales the split-K sum by gs * 2^8
 ])
 def test_nvfp4_rejects_bad_arguments_before_any_launch(lib, kw, status):
     a = dict(eps=1e-5, norm_kind=0, T=16, K=256, H=256, microchunk_tokens=0, gs=0.5)
@@ -200,3 +201,26 @@ def test_nvfp4_rejects_bad_arguments_before_any_launch(lib, kw, status):
                                           a["K"], a["H"], a["microchunk_tokens"], None, None)
     assert rc == status, fln.fln_last_error()
     assert fln.fln_launch_count() == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=192), fln.FLN_ERR_INVALID_ARG),       # MXFP4: K multiple of 128 (whole 4-byte words of scales)
+    (dict(K=64), fln.FLN_ERR_INVALID_ARG),
+    (dict(norm_kind=2), fln.FLN_ERR_INVALID_ARG),
+    (dict(H=0), fln.FLN_ERR_INVALID_ARG),
+    (dict(microchunk_tokens=5000), fln.FLN_ERR_INVALID_ARG),
+])
+def test_mxfp4_rejects_bad_arguments_before_any_launch(lib, kw, status):
+    a = dict(eps=1e-5, norm_kind=0, T=16, K=256, H=256, microchunk_tokens=0)
+    a.update(kw)
+    rc = lib.fused_proj_add_rmsnorm_mxfp4(None, None, None, None, None, a["eps"], a["norm_kind"], a["T"], a["K"],
+                                          a["H"], a["microchunk_tokens"], None, None)
+    assert rc == status, fln.fln_last_error()
+    assert fln.fln_launch_count() == 0
+
+
+def test_mxfp4_plan_group_is_its_own(lib):
+    import ctypes
+    p = fln.Plan()
+    assert lib.fln_get_plan_dtype(1024, 768, 0, fln.DTYPE_MXFP4, 64, 0, ctypes.byref(p)) == fln.FLN_OK
+    assert lib.fln_get_plan_dtype(1024, 768, 0, 4, 64, 0, ctypes.byref(p)) == fln.FLN_ERR_INVALID_ARG

@@ -1,7 +1,7 @@
 """GPU parity of the NVFP4-weight region against the fp64 oracle, through the C ABI.
 
 Same bar as the bf16 paths (tests/parity.py): the split-K path that reads W
-packed and dequantises it in shared memory (1 to 256 tokens, several tile
+packed and dequantises it on the SM (1 to 256 tokens, several tile
 widths of the token side), the FUSED and PIPELINED paths after the whole
 weight is converted to bf16, ragged T and H, chunk invariance bit for bit,
 the tuner, full-size workloads on sampled rows, guard rows after T untouched.

@@ -45,10 +45,25 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # keyed by workload, tokens, kernel, plan tile width and the sha1 of the
 # kernel sources the capture was taken on; reported as null when the sources
 # have changed since.  Captures: profiles/ (same commands).
+def kernel_sources_hash(dtype):
+    """sha1 (12 hex digits) of the kernel sources a dtype's timed kernels are built from."""
+    h = hashlib.sha1()
+    files = ["fln_gemm.cu", "fln_gemm2.cu", "fln_norm.cu", "fln_ptx.cuh"]
+    if dtype in ("nvfp4", "mxfp4"):
+        files.append("fln_gemm_w4.cu")
+    for f in files:
+        h.update(open(os.path.join(ROOT, "decoder_layer_projection_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:12]
+
+
 NCU_TRAFFIC = {
-    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "4d7d1fdc6e12"): 114142464 + 33394176,
-    ("llama70b_down_decode", 8, "bf16", "gemm_splitk", 256, "4d7d1fdc6e12"): 471433472 + 3426304,
-    ("llama70b_oproj_decode", 8, "bf16", "gemm_splitk", 256, "4d7d1fdc6e12"): 135539456 + 3152384,
+    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "5ab7fd5e2d00"): 116271872 + 33481984,
+    ("llama70b_down_decode", 8, "bf16", "gemm_splitk", 256, "5ab7fd5e2d00"): 471424256 + 3233792,
+    ("llama70b_oproj_decode", 8, "bf16", "gemm_splitk", 256, "5ab7fd5e2d00"): 135537920 + 2888192,
+    ("llama70b_down_decode", 8, "nvfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 135886080 + 2963712,
+    ("llama70b_oproj_decode", 8, "nvfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 37937152 + 0,
+    ("llama70b_down_decode", 8, "mxfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 128547072 + 2881536,
+    ("llama70b_oproj_decode", 8, "mxfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 35841280 + 0,
 }
 # FP8 (E4M3) dense peak: the measured bf16 peak times NVIDIA's nominal dense
 # FP8 / BF16 ratio (4.5 / 2.25 PFLOP/s); no FP8 GEMM peak is measured
@@ -312,10 +327,7 @@ def run_gpu(args):
         # add + norm: residual read and written, output written, gamma
         achieved = (tokens_per_launch * H * 6.0 + 4.0 * H) / (avg_launch_ms * 1e-3) / 1e9
         bound, unit, peak = "hbm", "GB/s", peaks["hbm_gbs"]
-    h = hashlib.sha1()
-    for f in ("fln_gemm.cu", "fln_gemm2.cu", "fln_norm.cu", "fln_ptx.cuh"):
-        h.update(open(os.path.join(ROOT, "decoder_layer_projection_gb300", "csrc", f), "rb").read())
-    src_hash = h.hexdigest()[:12]
+    src_hash = kernel_sources_hash(args.dtype)
     traffic = NCU_TRAFFIC.get((args.config, T, args.dtype, kname, plan["tile_n"], src_hash))
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",

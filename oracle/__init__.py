@@ -74,6 +74,13 @@ def _bind(path):
     lib.oracle_proj_add_rmsnorm_mxfp4.argtypes = [
         p, p, p, p, p, ctypes.c_double, ctypes.c_int, L, L, L, p, L, p, p, p, ctypes.c_int]
     lib.oracle_proj_add_rmsnorm_mxfp4.restype = ctypes.c_int
+    lib.oracle_moe_route.argtypes = [p, L, L, L, p, p]
+    lib.oracle_moe_route.restype = ctypes.c_int
+    lib.oracle_moe_permute.argtypes = [p, L, L, L, p, p, p, p]
+    lib.oracle_moe_permute.restype = ctypes.c_int
+    lib.oracle_moe_down_region.argtypes = [
+        p, p, p, p, p, p, p, ctypes.c_double, ctypes.c_int, L, L, L, L, L, p, p, p, ctypes.c_int]
+    lib.oracle_moe_down_region.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -276,6 +283,63 @@ def proj_add_rmsnorm_mxfp4(x, Wq, S, r0, gamma, eps, norm_kind, rows=None, nthre
     rc = lib.oracle_proj_add_rmsnorm_mxfp4(_ptr(x), _ptr(Wq), _ptr(S), _ptr(r0), _ptr(gamma), float(eps),
                                            int(norm_kind), T, K, H, _ptr(rows_arr), n, _ptr(r), _ptr(o), _ptr(ms),
                                            int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return r, o, ms
+
+
+def moe_route(logits, k):
+    """Top-k experts per token (larger logit first, equal logits: smaller index first) and
+    their softmax weights over the chosen logits.  logits [T,E] float32 -> (ids [T,k] int32,
+    w [T,k] float64)."""
+    lib = _load()
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = logits.shape
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    if lib.oracle_moe_route(_ptr(logits), T, E, int(k), _ptr(ids), _ptr(w)) != 0:
+        raise ValueError("oracle rejected its arguments")
+    return ids, w
+
+
+def moe_permute(ids, E):
+    """Rows grouped by expert (tokens ascending within an expert).  ids [T,k] int32 ->
+    (offsets [E+1], row_token [T*k], row_slot [T*k], row_of [T,k]) int32."""
+    lib = _load()
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    T, k = ids.shape
+    offsets = np.empty(E + 1, np.int32)
+    row_token = np.empty(T * k, np.int32)
+    row_slot = np.empty(T * k, np.int32)
+    row_of = np.empty((T, k), np.int32)
+    if lib.oracle_moe_permute(_ptr(ids), T, int(E), k, _ptr(offsets), _ptr(row_token), _ptr(row_slot),
+                              _ptr(row_of)) != 0:
+        raise ValueError("oracle rejected its arguments")
+    return offsets, row_token, row_slot, row_of
+
+
+def moe_down_region(hg, offsets, row_of, wt, We, r0, gamma, eps, norm_kind, nthreads=0):
+    """Return (r, o, ms) in float64: grouped down projection of hg [T*k,K] (bf16 bits, grouped by
+    expert per offsets) by We [E,H,K] (bf16 bits), unpermuted through row_of [T,k] with gate
+    weights wt [T,k] (float32), added to r0 [T,H] and normalised."""
+    lib = _load()
+    row_of = np.ascontiguousarray(row_of, dtype=np.int32)
+    T, k = row_of.shape
+    E, H, K = np.shape(We)
+    hg = _u16(hg, (T * k, K))
+    We = _u16(We, (E, H, K))
+    offsets = np.ascontiguousarray(offsets, dtype=np.int32)
+    wt = np.ascontiguousarray(wt, dtype=np.float32)
+    r0 = _u16(r0, (T, H))
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    if offsets.shape != (E + 1,) or wt.shape != (T, k) or gamma.shape != (H,):
+        raise ValueError("shape mismatch")
+    r = np.empty((T, H), np.float64)
+    o = np.empty((T, H), np.float64)
+    ms = np.empty((T,), np.float64)
+    rc = lib.oracle_moe_down_region(_ptr(hg), _ptr(offsets), _ptr(row_of), _ptr(wt), _ptr(We), _ptr(r0),
+                                    _ptr(gamma), float(eps), int(norm_kind), T, K, H, E, k, _ptr(r), _ptr(o),
+                                    _ptr(ms), int(nthreads))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return r, o, ms

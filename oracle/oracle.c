@@ -51,7 +51,7 @@
  * elements and no tensor scale.
  *
  * Pins (tests/test_oracle.py, tests/test_oracle_fp8.py, tests/test_oracle_fp4.py,
- * tests/test_oracle_mx.py): hand-worked 2x2, 4x4
+ * tests/test_oracle_mx.py, tests/test_oracle_moe.py): hand-worked 2x2, 4x4
  * and 1x3x2 cases, the closed form of a constant row, the unit-RMS invariant,
  * Gemma(0)==standard(1) bit for bit, linearity of the residual add, eps=0
  * scale invariance, column permutation of K, the projection against numpy's
@@ -429,6 +429,139 @@ int oracle_proj_add_rmsnorm_mxfp4(const uint16_t *x, const uint8_t *Wq, const ui
         double ms = rmsnorm_row(r, H, gamma, eps, norm_kind, o_out + i * H);
         if (ms_out)
             ms_out[i] = ms;
+    }
+    return 0;
+}
+
+/*
+ * The MoE region ("TPSP Design", section 3 "Fusion regions": the MoE design
+ * extends the dense regions to routing and expert reordering -- routing and
+ * permute before the grouped GEMM, grouped GEMM then unpermute and the
+ * add / next norm; section 5 "To-do": MoE).  The pages give the order of the
+ * steps, not their arithmetic; readings:
+ *
+ * routing: logits [T, E] fp32 from the router; each token takes the k
+ * experts of largest logit (equal logits: the smaller expert index first),
+ * listed in that order, with weights softmax over the k chosen logits
+ *   w[t,j] = exp(l[t,e_j] - l[t,e_0]) / sum_i exp(l[t,e_i] - l[t,e_0]).
+ */
+int oracle_moe_route(const float *logits, long T, long E, long k, int32_t *ids, double *w)
+{
+    if (T < 0 || E <= 0 || k <= 0 || k > E)
+        return -1;
+    for (long t = 0; t < T; ++t) {
+        const float *lt = logits + t * E;
+        int32_t *it = ids + t * k;
+        for (long j = 0; j < k; ++j) {
+            long best = -1;
+            for (long e = 0; e < E; ++e) {
+                int taken = 0;
+                for (long i = 0; i < j; ++i)
+                    if (it[i] == e)
+                        taken = 1;
+                if (taken)
+                    continue;
+                if (best < 0 || (double)lt[e] > (double)lt[best])
+                    best = e;
+            }
+            it[j] = (int32_t)best;
+        }
+        double top = (double)lt[it[0]], denom = 0.0;
+        for (long j = 0; j < k; ++j)
+            denom += exp((double)lt[it[j]] - top);
+        for (long j = 0; j < k; ++j)
+            w[t * k + j] = exp((double)lt[it[j]] - top) / denom;
+    }
+    return 0;
+}
+
+/*
+ * permute: the T * k (token, slot) pairs grouped by expert, experts in
+ * ascending order and, within an expert, tokens ascending (a token lists an
+ * expert at most once).  offsets [E + 1]: expert e owns rows
+ * [offsets[e], offsets[e + 1]); row_token / row_slot [T * k]: the pair of each
+ * row; row_of [T * k]: the row of pair (t, j) (the unpermute index).
+ */
+int oracle_moe_permute(const int32_t *ids, long T, long E, long k, int32_t *offsets, int32_t *row_token,
+                       int32_t *row_slot, int32_t *row_of)
+{
+    if (T < 0 || E <= 0 || k <= 0 || k > E)
+        return -1;
+    for (long i = 0; i < T * k; ++i)
+        if (ids[i] < 0 || ids[i] >= E)
+            return -1;
+    long next = 0;
+    for (long e = 0; e < E; ++e) {
+        offsets[e] = (int32_t)next;
+        for (long t = 0; t < T; ++t)
+            for (long j = 0; j < k; ++j)
+                if (ids[t * k + j] == e) {
+                    row_token[next] = (int32_t)t;
+                    row_slot[next] = (int32_t)j;
+                    row_of[t * k + j] = (int32_t)next;
+                    ++next;
+                }
+    }
+    offsets[E] = (int32_t)next;
+    return 0;
+}
+
+/*
+ * grouped GEMM, unpermute, add and norm: row r of the grouped activations
+ * hg [T * k, K] (bf16, expert e's rows at [offsets[e], offsets[e + 1])) is
+ * projected by its expert's down weight We [E, H, K] (bf16),
+ *   y[r, h] = sum_c hg[r, c] * We[e(r), h, c];
+ * each token gathers its k rows in slot order, weighted by its fp32 gate
+ * weights wt [T, k]:  z[t, h] = sum_j wt[t, j] * y[row_of[t, j], h];
+ * then r = r0 + z and out = RMSNorm(r) as in the dense region.
+ */
+int oracle_moe_down_region(const uint16_t *hg, const int32_t *offsets, const int32_t *row_of, const float *wt,
+                           const uint16_t *We, const uint16_t *r0, const float *gamma, double eps, int norm_kind,
+                           long T, long K, long H, long E, long k, double *r_out, double *o_out, double *ms_out,
+                           int nthreads)
+{
+    if (check_args(T, K, H, norm_kind, eps) || E <= 0 || k <= 0 || k > E)
+        return -1;
+    long R = T * k;
+    if (offsets[0] != 0 || offsets[E] != R)
+        return -1;
+    for (long e = 0; e < E; ++e)
+        if (offsets[e + 1] < offsets[e])
+            return -1;
+    for (long i = 0; i < R; ++i)
+        if (row_of[i] < 0 || row_of[i] >= R)
+            return -1;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long t = 0; t < T; ++t) {
+        double *r = r_out + t * H;
+        for (long h = 0; h < H; ++h)
+            r[h] = 0.0;
+        for (long j = 0; j < k; ++j) {
+            long row = row_of[t * k + j];
+            long e = 0;
+            while (!(row >= offsets[e] && row < offsets[e + 1]))
+                ++e;
+            const uint16_t *a = hg + row * K;
+            double gate = (double)wt[t * k + j];
+            for (long h = 0; h < H; ++h) {
+                const uint16_t *wrow = We + (e * H + h) * K;
+                double dot = 0.0;
+                for (long c = 0; c < K; ++c)
+                    dot += bf16_bits_to_double(a[c]) * bf16_bits_to_double(wrow[c]);
+                r[h] += gate * dot;
+            }
+        }
+        for (long h = 0; h < H; ++h)
+            r[h] += bf16_bits_to_double(r0[t * H + h]);
+        double ms = rmsnorm_row(r, H, gamma, eps, norm_kind, o_out + t * H);
+        if (ms_out)
+            ms_out[t] = ms;
     }
     return 0;
 }

@@ -32,6 +32,7 @@ STREAM_X, STREAM_U, STREAM_W, STREAM_R, STREAM_GAMMA = 0, 1, 2, 3, 4
 STREAM_X8, STREAM_W8, STREAM_SX, STREAM_SW = 5, 6, 7, 8
 STREAM_W4, STREAM_S4 = 9, 10
 STREAM_S5 = 11
+STREAM_LOGITS, STREAM_IDS, STREAM_GATE, STREAM_HG, STREAM_WE = 12, 13, 14, 15, 16
 
 # FP8 operands are drawn as values of spread FP8_SPREAD and stored as E4M3
 # codes (see _fill_e4m3); the dequantisation scales bring them back to the
@@ -102,6 +103,15 @@ CONFIGS = {
                                       eps=1e-5, r_sigma=2.0),
     "llama70b_down_decode": Workload("llama70b_down_decode", T=256, K=28672, H=8192,
                                      eps=1e-5, r_sigma=2.0),
+}
+
+
+# MoE down-projection regions: (workload with K = expert width, H = hidden; experts E; top-k)
+MOE_CONFIGS = {
+    "moe_tiny": (Workload("moe_tiny", T=24, K=256, H=256, eps=1e-6, r_sigma=1.0), 4, 2),
+    "mixtral_8x7b_down": (Workload("mixtral_8x7b_down", T=4096, K=14336, H=4096, eps=1e-5, r_sigma=2.0), 8, 2),
+    "mixtral_8x7b_down_decode": (Workload("mixtral_8x7b_down_decode", T=8, K=14336, H=4096, eps=1e-5,
+                                          r_sigma=2.0), 8, 2),
 }
 
 
@@ -335,3 +345,32 @@ def make_inputs_mxfp4(wl: Workload, seed: int | None = None, T: int | None = Non
     u = _block_gens(seed, STREAM_S5, 1)[0].integers(-1, 2, size=(H, nblk))
     S = (127 + e0 + u).astype(np.uint8)
     return {"x": base["x"], "Wq": Wq, "S": S, "r0": base["r0"], "gamma": base["gamma"]}
+
+
+def make_inputs_moe(wl: Workload, E: int, k: int, seed: int | None = None, T: int | None = None):
+    """MoE down-projection region inputs for a workload (K = expert width, H = hidden):
+    dict(logits=[T,E] f32, ids=[T,k] i32, wt=[T,k] f32, hg=[T*k,K] u16 bf16, We=[E,H,K] u16 bf16,
+    r0, gamma).
+
+    logits are N(0, 1) draws (router output); ids are k distinct experts per token drawn
+    uniformly (an assignment given to the down region directly, not a routing of the logits);
+    wt are U(0.05, 1) gate weights; hg holds the expert activations, one N(0, x_sigma^2) row
+    per (token, slot) pair in the grouped order; We[e] is an [H, K] bf16 weight with the
+    workload's W spread.  r0 and gamma are the bf16 workload's tensors.
+    """
+    seed = wl.seed if seed is None else int(seed)
+    T = wl.T if T is None else int(T)
+    K, H = wl.K, wl.H
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    base = make_inputs(wl, seed=seed, T=T)
+    logits = _block_gens(seed, STREAM_LOGITS, 1)[0].standard_normal((T, E)).astype(np.float32)
+    g = _block_gens(seed, STREAM_IDS, 1)[0]
+    ids = np.stack([g.permutation(E)[:k] for _ in range(T)]).astype(np.int32) if T else np.zeros((0, k), np.int32)
+    wt = _block_gens(seed, STREAM_GATE, 1)[0].uniform(0.05, 1.0, (T, k)).astype(np.float32)
+    hg = np.empty((T * k, K), np.uint16)
+    _fill_bf16(hg, seed, STREAM_HG, wl.x_sigma)
+    We = np.empty((E, H, K), np.uint16)
+    _fill_bf16(We.reshape(E * H, K), seed, STREAM_WE, wl.w_sigma)
+    return {"logits": logits, "ids": ids, "wt": wt, "hg": hg, "We": We, "r0": base["r0"], "gamma": base["gamma"]}
+

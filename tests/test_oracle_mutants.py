@@ -14,6 +14,7 @@ import oracle
 from . import test_oracle as pins
 from . import test_oracle_fp4 as fp4pins
 from . import test_oracle_fp8 as fp8pins
+from . import test_oracle_moe as moepins
 from . import test_oracle_mx as mxpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -59,6 +60,14 @@ MUTANTS = {
     "e8m0_bias_128": ("return ldexp(1.0, (int)E - 127);", "return ldexp(1.0, (int)E - 128);"),
     "e8m0_nan_dropped": ("    if (E == 255)\n        return NAN;\n", ""),
     "mxfp4_block_16": ("oracle_e8m0_to_double(scales[k / 32])", "oracle_e8m0_to_double(scales[k / 16])"),
+    "moe_ties_to_larger_index": ("if (best < 0 || (double)lt[e] > (double)lt[best])",
+                                 "if (best < 0 || (double)lt[e] >= (double)lt[best])"),
+    "moe_softmax_over_all_experts": ("for (long j = 0; j < k; ++j)\n            denom += exp((double)lt[it[j]] - top);",
+                                     "for (long j = 0; j < E; ++j)\n            denom += exp((double)lt[j] - top);"),
+    "moe_permute_slot_major": ("        for (long t = 0; t < T; ++t)\n            for (long j = 0; j < k; ++j)\n                if (ids[t * k + j] == e) {",
+                               "        for (long j = 0; j < k; ++j)\n            for (long t = 0; t < T; ++t)\n                if (ids[t * k + j] == e) {"),
+    "moe_gate_dropped": ("                r[h] += gate * dot;", "                r[h] += dot;"),
+    "moe_wrong_expert": ("while (!(row >= offsets[e] && row < offsets[e + 1]))", "while (!(row >= offsets[e] && row <= offsets[e + 1]))"),
     "mxfp4_nibbles_swapped": ("(k % 2 == 0) ? (uint8_t)(byte & 0x0F) : (uint8_t)(byte >> 4);",
                               "(k % 2 == 0) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0x0F);"),
 }
@@ -83,6 +92,10 @@ def _pin_calls():
     for name in dir(fp4pins):
         if name.startswith("test_") and name != "test_unit_scales_equal_bf16_region":
             calls.append(("fp4." + name, getattr(fp4pins, name)))
+    # MoE pins
+    for name in dir(moepins):
+        if name.startswith("test_"):
+            calls.append(("moe." + name, getattr(moepins, name)))
     # MXFP4 pins
     for kind in (0, 1):
         calls.append((f"mx.unit_scales[{kind}]", lambda k=kind: mxpins.test_unit_scales_equal_bf16_region(k)))

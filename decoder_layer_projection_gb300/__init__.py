@@ -36,14 +36,16 @@ DTYPE_E4M3 = 1
 DTYPE_NVFP4 = 2
 DTYPE_MXFP4 = 3
 
-KERNEL_NAMES = ("gemm_fused", "gemm_slot", "gemm_splitk", "norm_bf16", "norm_slot", "norm_splitk", "w4_dequant")
+KERNEL_NAMES = ("gemm_fused", "gemm_slot", "gemm_splitk", "norm_bf16", "norm_slot", "norm_splitk", "w4_dequant",
+                "moe_route", "moe_gemm", "moe_norm")
 
 EXPORTED_SYMBOLS = (
     "fused_proj_add_rmsnorm", "add_rmsnorm", "fln_autotune", "fln_set_overrides", "fln_set_plan",
     "fln_get_plan", "fln_device_status", "fln_last_error", "fln_release_workspace", "fln_launch_count",
     "fln_profile_enable", "fln_profile_read", "fln_version", "fused_proj_add_rmsnorm_noalloc",
     "fln_debug_stall_next_call", "fused_proj_add_rmsnorm_fp8", "fln_autotune_dtype", "fln_set_plan_dtype",
-    "fln_get_plan_dtype", "fused_proj_add_rmsnorm_nvfp4", "fused_proj_add_rmsnorm_mxfp4",
+    "fln_get_plan_dtype", "fused_proj_add_rmsnorm_nvfp4", "fused_proj_add_rmsnorm_mxfp4", "fln_moe_route",
+    "fused_moe_down_add_rmsnorm",
 )
 
 
@@ -64,7 +66,7 @@ class Plan(ctypes.Structure):
 
 
 class ProfileStats(ctypes.Structure):
-    _fields_ = [("launches", ctypes.c_uint64 * 7), ("total_ms", ctypes.c_double * 7)]
+    _fields_ = [("launches", ctypes.c_uint64 * len(KERNEL_NAMES)), ("total_ms", ctypes.c_double * len(KERNEL_NAMES))]
 
 
 _lock = threading.Lock()
@@ -122,6 +124,10 @@ def load(path: str | None = None):
         lib.fused_proj_add_rmsnorm_nvfp4.restype = i
         lib.fused_proj_add_rmsnorm_mxfp4.argtypes = [vp, vp, vp, vp, vp, f, i, i, i, i, i, vp, vp]
         lib.fused_proj_add_rmsnorm_mxfp4.restype = i
+        lib.fln_moe_route.argtypes = [vp, i, i, i, vp, vp, vp, vp, vp, vp, vp]
+        lib.fln_moe_route.restype = i
+        lib.fused_moe_down_add_rmsnorm.argtypes = [vp, vp, vp, vp, vp, vp, vp, f, i, i, i, i, i, i, vp, vp]
+        lib.fused_moe_down_add_rmsnorm.restype = i
         lib.fln_autotune_dtype.argtypes = [i, i, i, i, i, vp]
         lib.fln_autotune_dtype.restype = i
         lib.fln_set_plan_dtype.argtypes = [i, i, i, i, ctypes.POINTER(Plan)]
@@ -330,3 +336,39 @@ def fln_version() -> int:
 def build(force: bool = False) -> str:
     from . import _build
     return _build.build(force=force)
+
+
+def fln_moe_route(logits, k: int, stream=None):
+    """MoE routing and grouping on the device: logits [T,E] float32 CUDA tensor -> dict of int32 /
+    float32 CUDA tensors ids [T,k], gates [T,k], offsets [E+1], row_token [T*k], row_slot [T*k],
+    row_of [T,k] (expert e owns grouped rows offsets[e]..offsets[e+1]-1, tokens ascending)."""
+    import torch
+    T, E = logits.shape
+    dev = logits.device
+    res = {"ids": torch.empty((T, k), dtype=torch.int32, device=dev),
+           "gates": torch.empty((T, k), dtype=torch.float32, device=dev),
+           "offsets": torch.empty((E + 1,), dtype=torch.int32, device=dev),
+           "row_token": torch.empty((T * k,), dtype=torch.int32, device=dev),
+           "row_slot": torch.empty((T * k,), dtype=torch.int32, device=dev),
+           "row_of": torch.empty((T, k), dtype=torch.int32, device=dev)}
+    _check(load().fln_moe_route(_ptr(logits), int(T), int(E), int(k), _ptr(res["ids"]), _ptr(res["gates"]),
+                                _ptr(res["offsets"]), _ptr(res["row_token"]), _ptr(res["row_slot"]),
+                                _ptr(res["row_of"]), _stream_ptr(stream)))
+    return res
+
+
+def fused_moe_down_add_rmsnorm(hg, offsets, row_of, gates, We, residual, gamma, eps: float,
+                               norm_kind: int = NORM_STANDARD, out=None, stream=None):
+    """MoE region after the experts: y = hg . We[e(row)]^T per grouped row; residual += sum_j gates[t,j] *
+    y[row_of[t,j]]; out = RMSNorm(residual).  hg [T*k,K] bf16; offsets [E+1], row_of [T,k] int32;
+    gates [T,k] float32; We [E,H,K] bf16.  Returns out."""
+    T, k = row_of.shape
+    E, H, K = We.shape
+    if out is None:
+        import torch
+        out = torch.empty((T, H), dtype=residual.dtype, device=residual.device)
+    _check(load().fused_moe_down_add_rmsnorm(_ptr(hg), _ptr(offsets), _ptr(row_of), _ptr(gates), _ptr(We),
+                                             _ptr(residual), _ptr(gamma), float(eps), int(norm_kind), int(T), int(K),
+                                             int(H), int(E), int(k), _ptr(out), _stream_ptr(stream)))
+    return out
+

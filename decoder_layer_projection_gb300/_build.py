@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfusedln.so")
-SOURCES = ["fln_api.cu", "fln_gemm.cu", "fln_gemm2.cu", "fln_gemm_w4.cu", "fln_norm.cu"]
+SOURCES = ["fln_api.cu", "fln_gemm.cu", "fln_gemm2.cu", "fln_gemm_w4.cu", "fln_moe.cu", "fln_norm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

@@ -84,6 +84,9 @@ struct Workspace {
   __nv_bfloat16* w4_bf16 = nullptr;    // NVFP4 weights converted to bf16 (paths with many tokens)
   size_t w4_bf16_elems = 0;
   bool prepared_w4[2][5] = {};          // [fmt][tile]
+  float* moe_y = nullptr;               // MoE grouped GEMM output [T * k, H] fp32
+  size_t moe_y_floats = 0;
+  bool prepared_moe = false;
   cudaStream_t stream_b = nullptr;
   cudaEvent_t ev_ready[3] = {};
   cudaEvent_t ev_free[3] = {};
@@ -984,6 +987,82 @@ int fused_proj_add_rmsnorm_nvfp4(const fln_bf16* x, const uint8_t* W, const uint
   return run_plan(ws, c, pl);
 }
 
+namespace {
+constexpr int kMoeMaxE = 256, kMoeMaxK = 8, kMoeMaxH = 16384;
+
+int check_moe_shape(int T, int E, int k) {
+  if (T < 0 || T > kMaxT) return fail(FLN_ERR_INVALID_ARG, "T=%d outside [0, %d]", T, kMaxT);
+  if (E < 1 || E > kMoeMaxE) return fail(FLN_ERR_INVALID_ARG, "E=%d outside [1, %d]", E, kMoeMaxE);
+  if (k < 1 || k > kMoeMaxK || k > E) return fail(FLN_ERR_INVALID_ARG, "k=%d outside [1, min(%d, E)]", k, kMoeMaxK);
+  if (static_cast<long long>(T) * k >= (1ll << 31)) return fail(FLN_ERR_INVALID_ARG, "T * k too large");
+  return FLN_OK;
+}
+}  // namespace
+
+int fln_moe_route(const float* logits, int T, int E, int k, int* ids, float* gates, int* offsets, int* row_token,
+                  int* row_slot, int* row_of, fln_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = check_moe_shape(T, E, k);
+  if (rc) return rc;
+  if ((rc = check_ptr("offsets", offsets))) return rc;
+  if (T > 0 && ((rc = check_ptr("logits", logits)) || (rc = check_ptr("ids", ids)) || (rc = check_ptr("gates", gates)) ||
+                (rc = check_ptr("row_token", row_token)) || (rc = check_ptr("row_slot", row_slot)) ||
+                (rc = check_ptr("row_of", row_of))))
+    return rc;
+  Workspace* ws = nullptr;
+  if ((rc = get_ws(&ws))) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return launch_counted(FLN_KERNEL_MOE_ROUTE, s,
+                        [&] { return launch_moe_route(logits, T, E, k, ids, gates, offsets, row_token, row_slot,
+                                                      row_of, s); },
+                        "MoE routing launch");
+}
+
+int fused_moe_down_add_rmsnorm(const fln_bf16* hg, const int* offsets, const int* row_of, const float* gates,
+                               const fln_bf16* We, fln_bf16* residual, const float* gamma, float eps, int norm_kind,
+                               int T, int K, int H, int E, int k, fln_bf16* out, fln_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = check_common(eps, norm_kind, T, H);
+  if (rc) return rc;
+  if ((rc = check_moe_shape(T, E, k))) return rc;
+  if (H > kMoeMaxH) return fail(FLN_ERR_UNSUPPORTED, "H=%d above the supported %d for MoE", H, kMoeMaxH);
+  if (K < 8 || (K & 7) || K > kMaxK) return fail(FLN_ERR_INVALID_ARG, "K=%d must be a positive multiple of 8", K);
+  if (T == 0) return FLN_OK;
+  if ((rc = check_ptr("hg", hg)) || (rc = check_ptr("offsets", offsets)) || (rc = check_ptr("row_of", row_of)) ||
+      (rc = check_ptr("gates", gates)) || (rc = check_ptr("We", We)) || (rc = check_ptr("residual", residual)) ||
+      (rc = check_ptr("gamma", gamma)) || (rc = check_ptr("out", out)))
+    return rc;
+  const size_t R = static_cast<size_t>(T) * k;
+  const size_t br = size_t(T) * H * 2, bh = R * K * 2, bw = size_t(E) * H * K * 2;
+  if (overlaps(out, br, residual, br) || overlaps(out, br, hg, bh) || overlaps(out, br, We, bw) ||
+      overlaps(residual, br, hg, bh) || overlaps(residual, br, We, bw))
+    return fail(FLN_ERR_INVALID_ARG, "out or residual overlaps an input");
+  Workspace* ws = nullptr;
+  if ((rc = get_ws(&ws))) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = grow(&ws->moe_y, &ws->moe_y_floats, R * H, false, "cudaMalloc(MoE rows)"))) return rc;
+  if (!ws->prepared_moe) {
+    FLN_CUDA(moe_gemm_prepare(), "cudaFuncSetAttribute(max dynamic shared memory)");
+    ws->prepared_moe = true;
+  }
+  CUtensorMap tmA, tmB;
+  if ((rc = make_map(&tmA, hg, K, R, 128))) return rc;
+  if ((rc = make_map(&tmB, We, K, static_cast<uint64_t>(E) * H, 256))) return rc;
+  rc = launch_counted(FLN_KERNEL_MOE_GEMM, s,
+                      [&] { return launch_moe_grouped_gemm(tmA, tmB, offsets, E, H, K, ws->moe_y, ws->err_word,
+                                                           ws->sms, s); },
+                      "MoE grouped GEMM launch");
+  if (rc) return rc;
+  return launch_counted(FLN_KERNEL_MOE_NORM, s,
+                        [&] {
+                          return launch_moe_combine_norm(ws->moe_y, row_of, gates,
+                                                         reinterpret_cast<__nv_bfloat16*>(residual), gamma, eps,
+                                                         norm_kind, T, H, k, reinterpret_cast<__nv_bfloat16*>(out),
+                                                         s);
+                        },
+                        "MoE combine + add + norm launch");
+}
+
 int fused_proj_add_rmsnorm_mxfp4(const fln_bf16* x, const uint8_t* W, const uint8_t* W_scale, fln_bf16* residual,
                                  const float* gamma, float eps, int norm_kind, int T, int K, int H,
                                  int microchunk_tokens, fln_bf16* out, fln_stream_t stream) {
@@ -1308,6 +1387,7 @@ void fln_release_workspace(void) {
     cudaFree(ws->partial);
     cudaFree(ws->dyn_counter);
     cudaFree(ws->w4_bf16);
+    cudaFree(ws->moe_y);
     for (int i = 0; i < 3; ++i) {
       cudaEventDestroy(ws->ev_ready[i]);
       cudaEventDestroy(ws->ev_free[i]);

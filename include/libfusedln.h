@@ -206,6 +206,53 @@ int fused_proj_add_rmsnorm_mxfp4(const fln_bf16* x, const uint8_t* W, const uint
                                  int microchunk_tokens, fln_bf16* out, fln_stream_t stream);
 
 /*
+ * fln_moe_route -- routing and expert grouping of the MoE region ("TPSP
+ * Design", section 3 "Fusion regions": routing and permute before the
+ * grouped GEMM; section 5 "To-do": MoE).
+ *
+ *   logits     [T, E] fp32 router outputs (finite), device
+ *   ids        [T, k] int32 out: the k experts of largest logit per token,
+ *              largest first, equal logits: smaller expert index first
+ *   gates      [T, k] fp32 out: softmax over the token's k chosen logits
+ *   offsets    [E + 1] int32 out: expert e owns grouped rows
+ *              [offsets[e], offsets[e + 1]); offsets[E] = T * k
+ *   row_token  [T * k] int32 out: the token of each grouped row
+ *   row_slot   [T * k] int32 out: its slot j (ids[token, j] is the row's expert)
+ *   row_of     [T, k] int32 out: the grouped row of pair (t, j)
+ *   1 <= E <= 256, 1 <= k <= min(8, E), T * k < 2^31.
+ *
+ * Rows of an expert are ordered by token.  All arrays are caller-owned device
+ * memory, 16-byte aligned; nothing is allocated.  The up-projection of the
+ * MoE layer (gather by row_token, expert MLP) is the caller's; its grouped
+ * output feeds fused_moe_down_add_rmsnorm.
+ */
+int fln_moe_route(const float* logits, int T, int E, int k, int* ids, float* gates, int* offsets, int* row_token,
+                  int* row_slot, int* row_of, fln_stream_t stream);
+
+/*
+ * fused_moe_down_add_rmsnorm -- the MoE region after the experts: grouped
+ * down projection, unpermute, residual add and RMSNorm ("TPSP Design",
+ * section 3: grouped GEMM -> unpermute -> add / next norm):
+ *
+ *   y[r, :]  = hg[r, :] . We[e(r)]^T          (e(r): the expert owning row r)
+ *   residual[t, :] += sum_j gates[t, j] * y[row_of[t, j], :]   (slot order, fp32)
+ *   out[t, :] = RMSNorm(residual[t, :])
+ *
+ *   hg         [T * k, K] bf16 grouped expert activations (rows as offsets)
+ *   offsets    [E + 1], row_of [T, k], gates [T, k]: as fln_moe_route writes
+ *   We         [E, H, K] bf16 down-projection weights (F.linear layout)
+ *   residual, gamma, eps, norm_kind, out: as in fused_proj_add_rmsnorm
+ *   K % 8 == 0; H % 8 == 0, H <= 16384; E, k as in fln_moe_route.
+ *
+ * y is kept in fp32 in the library workspace ([T * k, H]); the grouped GEMM
+ * is a persistent tcgen05 kernel over (expert, 128-row tile, 256-column tile)
+ * items read from the device offsets, so no host synchronisation is needed.
+ */
+int fused_moe_down_add_rmsnorm(const fln_bf16* hg, const int* offsets, const int* row_of, const float* gates,
+                               const fln_bf16* We, fln_bf16* residual, const float* gamma, float eps, int norm_kind,
+                               int T, int K, int H, int E, int k, fln_bf16* out, fln_stream_t stream);
+
+/*
  * add_rmsnorm -- residual += y; out = RMSNorm(residual)   (the add/norm step alone)
  *
  *   y [T, H] bf16 addend; residual [T, H] bf16 in/out; gamma [H] fp32;
@@ -271,8 +318,11 @@ enum {
   FLN_KERNEL_NORM_BF16 = 3,    /* add_rmsnorm */
   FLN_KERNEL_NORM_SLOT = 4,    /* pipeline second stage */
   FLN_KERNEL_NORM_SPLITK = 5,  /* split-K reduce + add + norm */
-  FLN_KERNEL_W4_DEQUANT = 6,   /* NVFP4 weights to bf16 (paths with many tokens) */
-  FLN_KERNEL_KINDS = 7
+  FLN_KERNEL_W4_DEQUANT = 6,   /* FP4 weights to bf16 (paths with many tokens) */
+  FLN_KERNEL_MOE_ROUTE = 7,    /* MoE routing + grouping */
+  FLN_KERNEL_MOE_GEMM = 8,     /* MoE grouped down projection */
+  FLN_KERNEL_MOE_NORM = 9,     /* MoE unpermute + add + norm */
+  FLN_KERNEL_KINDS = 10
 };
 typedef struct {
   uint64_t launches[FLN_KERNEL_KINDS];

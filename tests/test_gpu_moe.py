@@ -1,0 +1,176 @@
+"""GPU parity of the MoE region against the fp64 oracle, through the C ABI.
+
+* routing: expert ids and the grouping (offsets, row_token, row_slot, row_of)
+  bit for bit, gates within fp32 rounding, with planted equal logits;
+* the grouped down projection + unpermute + add + norm on ragged shapes
+  (K and H tails, experts without rows, one expert, k = 1..4), the same bar
+  as the dense paths (tests/parity.py), guard rows after T untouched;
+* routing then the region chained on the device;
+* the Mixtral-8x7B down shape at decode and at 512 tokens on sampled rows;
+* argument checks.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from synth import MOE_CONFIGS, Workload, make_inputs_moe
+
+from .gpu_util import dev_bf16, host_bits
+from .parity import compare
+
+pytestmark = pytest.mark.gpu
+
+fln = pytest.importorskip("decoder_layer_projection_gb300")
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fln.build()
+    fln.load()
+    yield
+
+
+def _logits(T, E, seed):
+    g = np.random.default_rng(seed)
+    lg = g.standard_normal((T, E)).astype(np.float32)
+    if T > 3:
+        lg[1, :] = 0.5                      # every logit equal
+        lg[2, E // 2] = lg[2, 0] = 7.0      # a tie for the top
+        lg[3, ::2] = -1.25                  # ties lower down
+    return lg
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 4, 1), (7, 8, 2), (300, 8, 2), (129, 64, 4), (1024, 256, 8), (33, 5, 5)])
+def test_routing_matches_oracle(T, E, k):
+    lg = _logits(T, E, seed=T + E + k)
+    res = fln.fln_moe_route(torch.from_numpy(lg).cuda(), k)
+    fln.fln_device_status()
+    ids, w = oracle.moe_route(lg, k)
+    np.testing.assert_array_equal(res["ids"].cpu().numpy(), ids)
+    np.testing.assert_allclose(res["gates"].cpu().numpy(), w, rtol=2e-6, atol=1e-7)
+    offsets, row_token, row_slot, row_of = oracle.moe_permute(ids, E)
+    np.testing.assert_array_equal(res["offsets"].cpu().numpy(), offsets)
+    np.testing.assert_array_equal(res["row_token"].cpu().numpy(), row_token)
+    np.testing.assert_array_equal(res["row_slot"].cpu().numpy(), row_slot)
+    np.testing.assert_array_equal(res["row_of"].cpu().numpy(), row_of)
+
+
+class RunMoe:
+    GUARD = 3
+
+    def __init__(self, d, E, eps, kind):
+        self.d, self.E, self.eps, self.kind = d, E, eps, kind
+        self.T, self.k = d["ids"].shape
+        self.offsets, _, _, self.row_of = oracle.moe_permute(d["ids"], E)
+        self.hg = dev_bf16(d["hg"])
+        self.We = torch.from_numpy(np.ascontiguousarray(d["We"]).view(np.int16)).view(torch.bfloat16).cuda()
+        self.gamma = torch.from_numpy(np.ascontiguousarray(d["gamma"], np.float32)).cuda()
+
+    def __call__(self):
+        d = self.d
+        H = d["We"].shape[1]
+        r = dev_bf16(d["r0"], extra_rows=self.GUARD)
+        out = dev_bf16(np.zeros((self.T, H), np.uint16), extra_rows=self.GUARD, fill_bits=0x7FC2)
+        offs = torch.from_numpy(self.offsets).cuda()
+        row_of = torch.from_numpy(self.row_of).cuda()
+        gates = torch.from_numpy(d["wt"]).cuda()
+        fln.fused_moe_down_add_rmsnorm(self.hg, offs, row_of, gates, self.We, r[:self.T], self.gamma, self.eps,
+                                       self.kind, out=out[:self.T])
+        fln.fln_device_status()
+        rb, ob = host_bits(r), host_bits(out)
+        assert np.all(rb[self.T:] == 0x7FC1), "residual guard rows were written"
+        assert np.all(ob[self.T:] == 0x7FC2), "output guard rows were written"
+        return rb[:self.T], ob[:self.T]
+
+    def check(self, rb, ob, name, rows=None):
+        d = self.d
+        r, o, _ = oracle.moe_down_region(d["hg"], self.offsets, self.row_of, d["wt"], d["We"], d["r0"], d["gamma"],
+                                         self.eps, self.kind)
+        if rows is not None:
+            r, o, rb, ob = r[rows], o[rows], rb[rows], ob[rows]
+        compare(rb, r, name + " residual")
+        compare(ob, o, name + " out")
+
+
+SMALL = [
+    (Workload("moe_a", T=24, K=256, H=256, eps=1e-6, r_sigma=1.0, seed=1), 4, 2),
+    (Workload("moe_ragged", T=61, K=200, H=264, eps=1e-5, r_sigma=2.0, seed=2), 6, 3),
+    (Workload("moe_one", T=5, K=136, H=520, eps=1e-5, r_sigma=2.0, seed=3), 1, 1),
+    (Workload("moe_gemma", T=200, K=384, H=1032, norm_kind=1, eps=1e-6, gamma_mode="plain", seed=4), 8, 4),
+    (Workload("moe_long_k", T=9, K=4104, H=512, eps=1e-5, r_sigma=2.0, seed=5), 8, 2),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: c[0].name)
+def test_down_region_parity(case):
+    wl, E, k = case
+    d = make_inputs_moe(wl, E, k)
+    run = RunMoe(d, E, wl.eps, wl.norm_kind)
+    rb, ob = run()
+    run.check(rb, ob, wl.name)
+    rb2, ob2 = run()
+    assert np.array_equal(rb, rb2) and np.array_equal(ob, ob2)
+
+
+def test_expert_without_rows():
+    wl = Workload("moe_empty", T=40, K=256, H=384, eps=1e-5, r_sigma=2.0, seed=6)
+    d = dict(make_inputs_moe(wl, 8, 2))
+    g = np.random.default_rng(6)
+    d["ids"] = np.stack([g.choice([0, 1, 2, 4, 5, 6, 7], 2, replace=False) for _ in range(wl.T)]).astype(np.int32)
+    run = RunMoe(d, 8, wl.eps, wl.norm_kind)
+    assert run.offsets[3] == run.offsets[4]
+    rb, ob = run()
+    run.check(rb, ob, "expert without rows")
+
+
+def test_route_then_region_on_device():
+    wl, E, k = MOE_CONFIGS["moe_tiny"]
+    d = make_inputs_moe(wl, E, k)
+    lg = torch.from_numpy(d["logits"]).cuda()
+    res = fln.fln_moe_route(lg, k)
+    ids, w = oracle.moe_route(d["logits"], k)
+    offsets, _, _, row_of = oracle.moe_permute(ids, E)
+    # the grouped activations follow the device grouping (identical to the oracle's, checked above)
+    r = dev_bf16(d["r0"])
+    out = torch.empty_like(r)
+    We = torch.from_numpy(np.ascontiguousarray(d["We"]).view(np.int16)).view(torch.bfloat16).cuda()
+    gamma = torch.from_numpy(d["gamma"]).cuda()
+    fln.fused_moe_down_add_rmsnorm(dev_bf16(d["hg"]), res["offsets"], res["row_of"], res["gates"], We, r, gamma,
+                                   wl.eps, wl.norm_kind, out=out)
+    fln.fln_device_status()
+    ro, oo, _ = oracle.moe_down_region(d["hg"], offsets, row_of, w.astype(np.float32), d["We"], d["r0"], d["gamma"],
+                                       wl.eps, wl.norm_kind)
+    compare(host_bits(r), ro, "chained residual")
+    compare(host_bits(out), oo, "chained out")
+
+
+@pytest.mark.parametrize("name,T", [("mixtral_8x7b_down_decode", 8), ("mixtral_8x7b_down", 512)])
+def test_full_size_sampled_rows(name, T):
+    wl, E, k = MOE_CONFIGS[name]
+    d = make_inputs_moe(wl, E, k, T=T)
+    run = RunMoe(d, E, wl.eps, wl.norm_kind)
+    rb, ob = run()
+    rows = sorted({0, 1, T // 2, T - 1} | set(np.random.default_rng(T).choice(T, size=min(4, T), replace=False).tolist()))
+    sel = np.array(rows, np.int64)
+    # the oracle on the sampled tokens alone: their (token, slot) rows regrouped; each token's result
+    # depends only on its own rows, gates and residual
+    ids_s = d["ids"][sel]
+    off_s, tok_s, slot_s, row_of_s = oracle.moe_permute(ids_s, E)
+    hg_s = d["hg"][run.row_of[sel[tok_s], slot_s]]
+    r, o, _ = oracle.moe_down_region(hg_s, off_s, row_of_s, d["wt"][sel], d["We"], d["r0"][sel], d["gamma"], wl.eps,
+                                     wl.norm_kind)
+    compare(rb[sel], r, f"{name} T={T} residual")
+    compare(ob[sel], o, f"{name} T={T} out")
+
+
+def test_rejects_bad_arguments():
+    lib = fln.load()
+    assert lib.fln_moe_route(None, 4, 300, 2, None, None, None, None, None, None, None) == fln.FLN_ERR_INVALID_ARG
+    assert lib.fln_moe_route(None, 4, 8, 9, None, None, None, None, None, None, None) == fln.FLN_ERR_INVALID_ARG
+    assert lib.fln_moe_route(None, 4, 4, 5, None, None, None, None, None, None, None) == fln.FLN_ERR_INVALID_ARG
+    rc = lib.fused_moe_down_add_rmsnorm(None, None, None, None, None, None, None, 1e-5, 0, 4, 100, 256, 8, 2, None, None)
+    assert rc == fln.FLN_ERR_INVALID_ARG and "K=" in fln.fln_last_error()
+    rc = lib.fused_moe_down_add_rmsnorm(None, None, None, None, None, None, None, 1e-5, 0, 4, 128, 20000, 8, 2, None,
+                                        None)
+    assert rc == fln.FLN_ERR_UNSUPPORTED

@@ -372,6 +372,224 @@ def run_gpu(args):
     return line if rank == 0 else None
 
 
+def _moe_sample(d, E, sel):
+    """The MoE region restricted to tokens sel, regrouped (a token's result depends only on its own rows)."""
+    import oracle
+    ids_s = d["ids"][sel]
+    _, _, _, row_of = oracle.moe_permute(d["ids"], E)
+    off_s, tok_s, slot_s, row_of_s = oracle.moe_permute(ids_s, E)
+    return d["hg"][row_of[sel[tok_s], slot_s]], off_s, row_of_s, d["wt"][sel], d["r0"][sel]
+
+
+def moe_cpu_baseline(wl, E, k, d, seconds):
+    """The fp64 oracle's MoE region on a sample of token rows, on the host cores."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+
+    def timed(n):
+        hg, off, row_of, wt, r0 = _moe_sample(d, E, np.arange(n))
+        t = time.time()
+        oracle.moe_down_region(hg, off, row_of, wt, d["We"], r0, d["gamma"], wl.eps, wl.norm_kind)
+        return time.time() - t
+
+    probe = min(wl.T, max(1, cores))
+    t = timed(probe)
+    n = int(min(wl.T, max(probe, probe * seconds / max(t, 1e-6))))
+    t = timed(n) if n > probe else t
+    flops = 2.0 * n * k * wl.K * wl.H
+    return {"value": round(flops / t / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {wl.T} tokens of {wl.name} (E={E}, k={k}; fp64, OpenMP over tokens), "
+                      f"{t:.1f} s"}
+
+
+def run_gpu_moe(args):
+    """The MoE region (routing + grouping, grouped down projection, unpermute + add + norm) as one step."""
+    import numpy as np
+    import torch
+
+    import decoder_layer_projection_gb300 as fln
+    from synth import MOE_CONFIGS, make_inputs_moe
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    fln.build()
+    fln.load()
+    wl, E, k = MOE_CONFIGS[args.config]
+    if args.tokens:
+        wl = wl.with_tokens(args.tokens)
+    T, K, H = wl.T, wl.K, wl.H
+    d = make_inputs_moe(wl, E, k, seed=rank_seed(wl.seed, rank))
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    logits = torch.from_numpy(d["logits"]).to(device)
+    hg, We, r = up(d["hg"]), up(d["We"]), up(d["r0"])
+    gamma = torch.from_numpy(d["gamma"]).to(device)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        g = fln.fln_moe_route(logits, k, stream)
+        fln.fused_moe_down_add_rmsnorm(hg, g["offsets"], g["row_of"], g["gates"], We, r, gamma, wl.eps,
+                                       wl.norm_kind, out, stream)
+        return g
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        g = step()
+    fln.fln_device_status(stream)
+    used = int(np.unique(g["ids"].cpu().numpy()).size)
+
+    def timed_pass(profile):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        if profile:
+            fln.fln_profile_enable(True)
+        launches0 = fln.fln_launch_count()
+        barrier(device)
+        torch.cuda.synchronize(device)
+        if sampler is not None:
+            sampler.mark_begin()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(device)
+        barrier(device)
+        if sampler is not None:
+            sampler.mark_end()
+        nl = fln.fln_launch_count() - launches0
+        prof = None
+        if profile:
+            prof = fln.fln_profile_read()
+            fln.fln_profile_enable(False)
+        fln.fln_device_status(stream)
+        return sum(st.elapsed_time(en) for st, en in zip(starts, ends)) / 1e3, nl, prof
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    local_s, launches, _ = timed_pass(False)
+    clocks = sampler.stop()
+    sampler = None
+    prof_s, _, prof = timed_pass(True)
+    max_s = max_over_ranks(local_s, device)
+    ms_per_step = max_s * 1e3 / args.steps
+    R = T * k
+    flops = 2.0 * R * K * H
+    value = whole_job_value(flops * args.steps, world, max_s) / 1e12
+    peaks, peak_src = load_peaks()
+    kp = prof["moe_gemm"]
+    avg_ms = kp["total_ms"] / max(kp["launches"], 1)
+    w_bytes = used * H * K * 2.0
+    if R <= 256:
+        achieved = (w_bytes + 2.0 * R * K) / (avg_ms * 1e-3) / 1e9
+        bound, unit, peak = "hbm", "GB/s", peaks["hbm_gbs"]
+    else:
+        achieved = flops / (avg_ms * 1e-3) / 1e12
+        bound, unit, peak = "tensor", "TFLOP/s", peaks["bf16_tflops"]
+    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": None, "traffic_unit": "bytes per launch (ncu)",
+                "kernel": "moe_gemm",
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback",
+                "kernel_ms_per_launch": round(avg_ms, 5), "launches_per_step": kp["launches"] / args.steps,
+                "experts_used": used,
+                "measured": "second timed pass of the same K steps with per-kernel CUDA events",
+                "profiled_ms_per_step": round(prof_s * 1e3 / args.steps, 5)}
+    alg_bytes = w_bytes + 2.0 * R * K + 6.0 * T * H + 4.0 * H + 4.0 * T * E
+    t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), alg_bytes / (peaks["hbm_gbs"] * 1e9))
+
+    # end to end: logits, grouped activations and residual up, output and residual down, every step
+    h_lg = torch.from_numpy(d["logits"]).pin_memory()
+    h_hg = torch.from_numpy(np.ascontiguousarray(d["hg"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_r = torch.from_numpy(np.ascontiguousarray(d["r0"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_o = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    h_ro = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        logits.copy_(h_lg, non_blocking=True)
+        hg.copy_(h_hg, non_blocking=True)
+        r.copy_(h_r, non_blocking=True)
+        step()
+        h_o.copy_(out, non_blocking=True)
+        h_ro.copy_(r, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    n = max(5, args.steps // 4)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    es = max_over_ranks(e0.elapsed_time(e1) / 1e3, device)
+    e2e = {"value": round(whole_job_value(flops * n, world, es) / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(4 * T * E + 2 * R * K + 2 * T * H), "d2h_bytes_per_step": int(4 * T * H),
+           "steps": n, "ms_per_step": round(es * 1e3 / n, 4), "weights": "We and gamma resident on the device"}
+
+    # conventional sequence: one cuBLAS GEMM per expert, gated scatter-add, then add_rmsnorm
+    offs = g["offsets"].cpu().numpy()
+    row_token = g["row_token"].long()
+    gate_row = g["gates"].reshape(-1)[g["row_token"].long() * k + g["row_slot"].long()]
+    r2 = up(d["r0"])
+    out2 = torch.empty_like(out)
+    times = []
+    for i in range(args.warmup + max(5, args.steps // 4)):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        y = torch.empty((R, H), dtype=torch.bfloat16, device=device)
+        for e in range(E):
+            if offs[e + 1] > offs[e]:
+                torch.matmul(hg[offs[e]:offs[e + 1]], We[e].t(), out=y[offs[e]:offs[e + 1]])
+        z = torch.zeros((T, H), dtype=torch.float32, device=device)
+        z.index_add_(0, row_token, y.float() * gate_row[:, None])
+        fln.add_rmsnorm(z.to(torch.bfloat16), r2, gamma, wl.eps, wl.norm_kind, out2, stream)
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize(device)
+    cms = [a.elapsed_time(b) for a, b in times[args.warmup:]]
+    cm = sum(cms) / len(cms)
+    comparator = {"value": round(flops / (cm * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(cm, 5),
+                  "what": "per-expert torch.matmul (cuBLAS, bf16 out), gated index_add in fp32, then add_rmsnorm"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "T": T, "K": K, "H": H, "experts": E, "top_k": k,
+                   "region": "MoE: routing + grouping, grouped down projection, unpermute + add + RMSNorm",
+                   "norm": "gemma" if wl.norm_kind else "standard", "eps": wl.eps,
+                   "global_batch_tokens": T * world, "parallelism": f"dp{world} (replicas)",
+                   "l2": "flushed between timed steps (512 MiB write)"},
+        "tokens_per_s": round(whole_job_value(T * args.steps, world, max_s), 1),
+        "step_roofline_frac": round(t_roof / (ms_per_step * 1e-3), 4),
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "kernel_time_ms": {kk: round(v["total_ms"] / args.steps, 5) for kk, v in prof.items() if v["launches"]},
+        "comparator_unfused_cublas": comparator,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = moe_cpu_baseline(wl, E, k, d, args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
 def run_e2e(args, wl, d, W, gamma, device, stream, fln, sw=None):
     import numpy as np
     import torch
@@ -538,6 +756,47 @@ def run_reference(args):
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_reference_moe(args):
+    """--impl reference for a MoE workload: the fp64 oracle's region on host cores, sampled tokens per step."""
+    import numpy as np
+    import oracle
+    from synth import MOE_CONFIGS, make_inputs_moe
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    wl, E, k = MOE_CONFIGS[args.config]
+    if args.tokens:
+        wl = wl.with_tokens(args.tokens)
+    oracle.build()
+    d = make_inputs_moe(wl, E, k)
+    cores = oracle.max_threads()
+
+    def timed(sel):
+        hg, off, row_of, wt, r0 = _moe_sample(d, E, np.asarray(sel, np.int64))
+        t = time.time()
+        oracle.moe_route(d["logits"][sel], k)
+        oracle.moe_down_region(hg, off, row_of, wt, d["We"], r0, d["gamma"], wl.eps, wl.norm_kind)
+        return time.time() - t
+
+    probe = min(wl.T, max(1, cores))
+    t = timed(list(range(probe)))
+    per_step = float(args.ref_seconds) / max(1, args.steps + args.warmup)
+    rows = int(min(wl.T, max(1, probe * per_step / max(t, 1e-6))))
+    for i in range(args.warmup):
+        timed([(i * rows + j) % wl.T for j in range(rows)])
+    total = sum(timed([(i * rows + j) % wl.T for j in range(rows)]) for i in range(args.steps))
+    value = 2.0 * rows * k * wl.K * wl.H * args.steps / total / 1e12
+    sample = f"{rows} of {wl.T} tokens per step of {wl.name} (E={E}, k={k}; fp64 oracle, OpenMP over tokens)"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "K": wl.K, "H": wl.H, "experts": E,
+                                            "top_k": k},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -559,7 +818,14 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    from synth import MOE_CONFIGS
+    if args.config in MOE_CONFIGS:
+        if args.impl == "reference":
+            line = run_reference_moe(args)
+        else:
+            line = run_gpu_moe(args)
+    else:
+        line = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

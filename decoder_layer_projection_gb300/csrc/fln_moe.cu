@@ -354,8 +354,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 // (fp32), sum r^2 over H, out = r * rsqrt(ms + eps) * g; residual and out
 // written as bf16.
 constexpr int CN_THREADS = 256;
-constexpr int CN_MAX_GROUPS = 8;  // H <= 256 * 8 * 8 = 16384
 
+// GROUPS 8-column groups a thread: H <= 256 * 8 * GROUPS (2: 4096, 4: 8192, 8: 16384); fewer groups keep
+// fewer values in registers, so more CTAs share an SM
+template <int GROUPS>
 __global__ void __launch_bounds__(CN_THREADS)
     combine_norm_kernel(const float* __restrict__ y, const int* __restrict__ row_of, const float* __restrict__ gates,
                         __nv_bfloat16* __restrict__ residual, const float* __restrict__ gamma, float eps,
@@ -371,10 +373,10 @@ __global__ void __launch_bounds__(CN_THREADS)
     rows[j] = j < k ? row_of[static_cast<size_t>(t) * k + j] : 0;
     gw[j] = j < k ? gates[static_cast<size_t>(t) * k + j] : 0.f;
   }
-  float r[CN_MAX_GROUPS][8];
+  float r[GROUPS][8];
   float ss = 0.f;
 #pragma unroll
-  for (int i = 0; i < CN_MAX_GROUPS; ++i) {
+  for (int i = 0; i < GROUPS; ++i) {
     const int g = threadIdx.x + i * CN_THREADS;
     if (g < G) {
       float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -408,7 +410,7 @@ __global__ void __launch_bounds__(CN_THREADS)
   __syncthreads();
   const float inv = rsqrtf(total / static_cast<float>(H) + eps);
 #pragma unroll
-  for (int i = 0; i < CN_MAX_GROUPS; ++i) {
+  for (int i = 0; i < GROUPS; ++i) {
     const int g = threadIdx.x + i * CN_THREADS;
     if (g < G) {
       float o[8];
@@ -449,8 +451,16 @@ cudaError_t launch_moe_grouped_gemm(const CUtensorMap& tmA, const CUtensorMap& t
 cudaError_t launch_moe_combine_norm(const float* y, const int* row_of, const float* gates, __nv_bfloat16* residual,
                                     const float* gamma, float eps, int norm_kind, int T, int H, int k,
                                     __nv_bfloat16* out, cudaStream_t stream) {
-  moe::combine_norm_kernel<<<T, moe::CN_THREADS, 0, stream>>>(y, row_of, gates, residual, gamma, eps, norm_kind, H, k,
-                                                              out);
+  const int groups = (H / 8 + moe::CN_THREADS - 1) / moe::CN_THREADS;
+  if (groups <= 2)
+    moe::combine_norm_kernel<2><<<T, moe::CN_THREADS, 0, stream>>>(y, row_of, gates, residual, gamma, eps, norm_kind,
+                                                                   H, k, out);
+  else if (groups <= 4)
+    moe::combine_norm_kernel<4><<<T, moe::CN_THREADS, 0, stream>>>(y, row_of, gates, residual, gamma, eps, norm_kind,
+                                                                   H, k, out);
+  else
+    moe::combine_norm_kernel<8><<<T, moe::CN_THREADS, 0, stream>>>(y, row_of, gates, residual, gamma, eps, norm_kind,
+                                                                   H, k, out);
   return cudaGetLastError();
 }
 

@@ -51,6 +51,8 @@ def kernel_sources_hash(dtype):
     files = ["fln_gemm.cu", "fln_gemm2.cu", "fln_norm.cu", "fln_ptx.cuh"]
     if dtype in ("nvfp4", "mxfp4"):
         files.append("fln_gemm_w4.cu")
+    if dtype == "moe":
+        files = ["fln_moe.cu", "fln_ptx.cuh"]
     for f in files:
         h.update(open(os.path.join(ROOT, "decoder_layer_projection_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:12]
@@ -64,6 +66,8 @@ NCU_TRAFFIC = {
     ("llama70b_oproj_decode", 8, "nvfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 37937152 + 0,
     ("llama70b_down_decode", 8, "mxfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 128547072 + 2881536,
     ("llama70b_oproj_decode", 8, "mxfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 35841280 + 0,
+    ("mixtral_8x7b_down_decode", 8, "moe", "moe_gemm", 256, "b18246ddda96"): 822594816 + 2957568,
+    ("mixtral_8x7b_down", 4096, "moe", "moe_gemm", 256, "b18246ddda96"): 3157513216 + 100808704,
 }
 # FP8 (E4M3) dense peak: the measured bf16 peak times NVIDIA's nominal dense
 # FP8 / BF16 ratio (4.5 / 2.25 PFLOP/s); no FP8 GEMM peak is measured
@@ -496,8 +500,9 @@ def run_gpu_moe(args):
     else:
         achieved = flops / (avg_ms * 1e-3) / 1e12
         bound, unit, peak = "tensor", "TFLOP/s", peaks["bf16_tflops"]
+    traffic = NCU_TRAFFIC.get((args.config, T, "moe", "moe_gemm", 256, kernel_sources_hash("moe")))
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": None, "traffic_unit": "bytes per launch (ncu)",
+                "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
                 "kernel": "moe_gemm",
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback",
                 "kernel_ms_per_launch": round(avg_ms, 5), "launches_per_step": kp["launches"] / args.steps,

@@ -31,11 +31,9 @@ constexpr int MAX_K = 8;
 // One warp per token.  Lane l holds the logits of experts l, l + 32, ...; for
 // each of the k picks every lane proposes its best unchosen expert (larger
 // logit, then smaller index) and a butterfly reduction agrees on the winner.
-__global__ void route_kernel(const float* __restrict__ logits, int T, int E, int k, int* __restrict__ ids,
-                             float* __restrict__ gates) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (t >= T) return;
+__device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int k,
+                                            int* __restrict__ ids, float* __restrict__ gates) {
+  const int lane = threadIdx.x & 31;
   const float* lt = logits + static_cast<size_t>(t) * E;
   float v[MAX_E / 32];
   unsigned taken = 0;
@@ -84,15 +82,21 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
     if (j < k && lane == j) gates[static_cast<size_t>(t) * k + j] = __expf(sel[j] - sel[0]) / denom;
 }
 
+__global__ void route_kernel(const float* __restrict__ logits, int T, int E, int k, int* __restrict__ ids,
+                             float* __restrict__ gates) {
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t < T) route_token(logits, t, E, k, ids, gates);
+}
+
 // ------------------------------------------------------------------ permute
 // One CTA of 1024 threads.  Pass 1 counts the pairs of each expert; the scan
 // gives offsets; pass 2 walks the pairs in (token, slot) order in chunks of
 // 1024: a pair's row is its expert's running cursor plus the number of
 // earlier pairs of the same expert in the chunk (lanes of the same expert in
 // its warp by __match_any_sync, earlier warps by their per-expert counts).
-__global__ void __launch_bounds__(1024, 1)
-    permute_kernel(const int* __restrict__ ids, int T, int E, int k, int* __restrict__ offsets,
-                   int* __restrict__ row_token, int* __restrict__ row_slot, int* __restrict__ row_of) {
+__device__ __forceinline__ void permute_block(const int* __restrict__ ids, int T, int E, int k,
+                                              int* __restrict__ offsets, int* __restrict__ row_token,
+                                              int* __restrict__ row_slot, int* __restrict__ row_of) {
   __shared__ int cnt[MAX_E];
   __shared__ int cursor[MAX_E];
   __shared__ int wcnt[32][MAX_E];
@@ -138,6 +142,23 @@ __global__ void __launch_bounds__(1024, 1)
     }
     __syncthreads();
   }
+}
+
+__global__ void __launch_bounds__(1024, 1)
+    permute_kernel(const int* __restrict__ ids, int T, int E, int k, int* __restrict__ offsets,
+                   int* __restrict__ row_token, int* __restrict__ row_slot, int* __restrict__ row_of) {
+  permute_block(ids, T, E, k, offsets, row_token, row_slot, row_of);
+}
+
+// T <= 32: both steps in one CTA (warp w routes token w), one launch instead of two
+__global__ void __launch_bounds__(1024, 1)
+    route_permute_kernel(const float* __restrict__ logits, int T, int E, int k, int* __restrict__ ids,
+                         float* __restrict__ gates, int* __restrict__ offsets, int* __restrict__ row_token,
+                         int* __restrict__ row_slot, int* __restrict__ row_of) {
+  const int w = threadIdx.x >> 5;
+  if (w < T) route_token(logits, w, E, k, ids, gates);
+  __syncthreads();  // the block's global writes of ids are visible to the block after the barrier
+  permute_block(ids, T, E, k, offsets, row_token, row_slot, row_of);
 }
 
 // ------------------------------------------------------------------ grouped GEMM
@@ -429,6 +450,11 @@ __global__ void __launch_bounds__(CN_THREADS)
 
 cudaError_t launch_moe_route(const float* logits, int T, int E, int k, int* ids, float* gates, int* offsets,
                              int* row_token, int* row_slot, int* row_of, cudaStream_t stream) {
+  if (T > 0 && T <= 32) {
+    moe::route_permute_kernel<<<1, 1024, 0, stream>>>(logits, T, E, k, ids, gates, offsets, row_token, row_slot,
+                                                       row_of);
+    return cudaGetLastError();
+  }
   if (T > 0) {
     moe::route_kernel<<<(T + 7) / 8, 256, 0, stream>>>(logits, T, E, k, ids, gates);
     cudaError_t e = cudaGetLastError();

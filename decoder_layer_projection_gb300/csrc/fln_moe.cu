@@ -162,8 +162,9 @@ __global__ void __launch_bounds__(1024, 1)
 }
 
 // ------------------------------------------------------------------ grouped GEMM
-// Persistent, one CTA per SM.  Items are (expert, 128-row tile of its rows,
-// 256-column tile of H), expert-major; CTA c takes items c, c + G, ...  A =
+// Persistent, one CTA per SM.  Items are (expert, 256-column tile of H,
+// 128-row tile of its rows), expert-major, row tiles fastest; CTA c takes
+// items c, c + G, ...  A =
 // 128 grouped rows of hg (rows past the expert's last belong to other experts
 // or lie past the end and are never stored), B = 256 rows of We[e] viewed as
 // [E * H, K] (rows past H are never stored).  Warps: 0 TMA producer, 1 TMEM
@@ -190,8 +191,9 @@ struct Sched {
     }
     e = lo;
     const int local = item - tb[e];
-    const int m = local / NT;
-    n = local - m * NT;
+    const int mt = (off[e + 1] - off[e] + BM - 1) / BM;  // row tiles of the expert, fastest: the CTAs of a
+    n = local / mt;                                        // wave share the W tiles they stream
+    const int m = local - n * mt;
     row0 = off[e] + m * BM;
     rows = min(BM, off[e + 1] - row0);
   }
@@ -258,13 +260,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_a = l2_policy_evict_last();
-    const uint64_t pol_b = l2_policy_evict_first();
+    // W tiles are read again by the expert's other row tiles when it has more than one
+    const uint64_t pol_b_once = l2_policy_evict_first(), pol_b_again = l2_policy_evict_normal();
     int s = 0;
     uint32_t ph = 0, mask = 0, par = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
       int e, row0, rows, n;
       sch.decode(item, e, row0, rows, n);
+      const uint64_t pol_b = s_off[e + 1] - s_off[e] > BM ? pol_b_again : pol_b_once;
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, err, FLN_DEVERR_TIMEOUT_EMPTY)) {
           ok = false;

@@ -37,7 +37,7 @@ DTYPE_NVFP4 = 2
 DTYPE_MXFP4 = 3
 
 KERNEL_NAMES = ("gemm_fused", "gemm_slot", "gemm_splitk", "norm_bf16", "norm_slot", "norm_splitk", "w4_dequant",
-                "moe_route", "moe_gemm", "moe_norm")
+                "moe_route", "moe_gemm", "moe_norm", "moe_gather")
 
 EXPORTED_SYMBOLS = (
     "fused_proj_add_rmsnorm", "add_rmsnorm", "fln_autotune", "fln_set_overrides", "fln_set_plan",
@@ -45,7 +45,7 @@ EXPORTED_SYMBOLS = (
     "fln_profile_enable", "fln_profile_read", "fln_version", "fused_proj_add_rmsnorm_noalloc",
     "fln_debug_stall_next_call", "fused_proj_add_rmsnorm_fp8", "fln_autotune_dtype", "fln_set_plan_dtype",
     "fln_get_plan_dtype", "fused_proj_add_rmsnorm_nvfp4", "fused_proj_add_rmsnorm_mxfp4", "fln_moe_route",
-    "fused_moe_down_add_rmsnorm",
+    "fused_moe_down_add_rmsnorm", "fln_moe_gather",
 )
 
 
@@ -128,6 +128,8 @@ def load(path: str | None = None):
         lib.fln_moe_route.restype = i
         lib.fused_moe_down_add_rmsnorm.argtypes = [vp, vp, vp, vp, vp, vp, vp, f, i, i, i, i, i, i, vp, vp]
         lib.fused_moe_down_add_rmsnorm.restype = i
+        lib.fln_moe_gather.argtypes = [vp, vp, i, i, i, vp, vp]
+        lib.fln_moe_gather.restype = i
         lib.fln_autotune_dtype.argtypes = [i, i, i, i, i, vp]
         lib.fln_autotune_dtype.restype = i
         lib.fln_set_plan_dtype.argtypes = [i, i, i, i, ctypes.POINTER(Plan)]
@@ -370,5 +372,15 @@ def fused_moe_down_add_rmsnorm(hg, offsets, row_of, gates, We, residual, gamma, 
     _check(load().fused_moe_down_add_rmsnorm(_ptr(hg), _ptr(offsets), _ptr(row_of), _ptr(gates), _ptr(We),
                                              _ptr(residual), _ptr(gamma), float(eps), int(norm_kind), int(T), int(K),
                                              int(H), int(E), int(k), _ptr(out), _stream_ptr(stream)))
+    return out
+
+
+def fln_moe_gather(x, row_token, k: int, out=None, stream=None):
+    """Grouped copy of the hidden states: out[r] = x[row_token[r]] (x [T,H] bf16, row_token [T*k] int32)."""
+    T, H = x.shape
+    if out is None:
+        import torch
+        out = torch.empty((T * k, H), dtype=x.dtype, device=x.device)
+    _check(load().fln_moe_gather(_ptr(x), _ptr(row_token), int(T), int(k), int(H), _ptr(out), _stream_ptr(stream)))
     return out
 

@@ -160,8 +160,9 @@ int get_ws(Workspace** out) {
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ws->ev_free[i], cudaEventDisableTiming);
   }
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ws->ev_join, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaMalloc(&ws->err_word, sizeof(unsigned int));
-  if (e == cudaSuccess) e = cudaMemset(ws->err_word, 0, sizeof(unsigned int));
+  // word 0: the device error bits; word 1: the MoE GEMM's verdict on its offsets, read by the combine kernel
+  if (e == cudaSuccess) e = cudaMalloc(&ws->err_word, 2 * sizeof(unsigned int));
+  if (e == cudaSuccess) e = cudaMemset(ws->err_word, 0, 2 * sizeof(unsigned int));
   if (e == cudaSuccess) e = cudaMalloc(&ws->dyn_counter, sizeof(unsigned int));
   if (e == cudaSuccess) e = cudaMemset(ws->dyn_counter, 0, sizeof(unsigned int));
   if (e != cudaSuccess) {
@@ -1018,6 +1019,25 @@ int fln_moe_route(const float* logits, int T, int E, int k, int* ids, float* gat
                         "MoE routing launch");
 }
 
+int fln_moe_gather(const fln_bf16* x, const int* row_token, int T, int k, int H, fln_bf16* xg, fln_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = check_moe_shape(T, k, k);
+  if (rc) return rc;
+  if (H < 8 || (H & 7) || H > kMaxH) return fail(FLN_ERR_INVALID_ARG, "H=%d must be a multiple of 8 in [8, %d]", H, kMaxH);
+  if (T == 0) return FLN_OK;
+  if ((rc = check_ptr("x", x)) || (rc = check_ptr("row_token", row_token)) || (rc = check_ptr("xg", xg))) return rc;
+  if (overlaps(xg, size_t(T) * k * H * 2, x, size_t(T) * H * 2)) return fail(FLN_ERR_INVALID_ARG, "xg overlaps x");
+  Workspace* ws = nullptr;
+  if ((rc = get_ws(&ws))) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return launch_counted(FLN_KERNEL_MOE_GATHER, s,
+                        [&] {
+                          return launch_moe_gather(reinterpret_cast<const __nv_bfloat16*>(x), row_token, T, k, H,
+                                                   reinterpret_cast<__nv_bfloat16*>(xg), ws->err_word, ws->sms, s);
+                        },
+                        "MoE gather launch");
+}
+
 int fused_moe_down_add_rmsnorm(const fln_bf16* hg, const int* offsets, const int* row_of, const float* gates,
                                const fln_bf16* We, fln_bf16* residual, const float* gamma, float eps, int norm_kind,
                                int T, int K, int H, int E, int k, fln_bf16* out, fln_stream_t stream) {
@@ -1049,8 +1069,10 @@ int fused_moe_down_add_rmsnorm(const fln_bf16* hg, const int* offsets, const int
   if ((rc = make_map(&tmA, hg, K, R, 128))) return rc;
   if ((rc = make_map(&tmB, We, K, static_cast<uint64_t>(E) * H, 256))) return rc;
   rc = launch_counted(FLN_KERNEL_MOE_GEMM, s,
-                      [&] { return launch_moe_grouped_gemm(tmA, tmB, offsets, E, H, K, ws->moe_y, ws->err_word,
-                                                           ws->sms, s); },
+                      [&] {
+                        return launch_moe_grouped_gemm(tmA, tmB, offsets, E, static_cast<int>(R), H, K, ws->moe_y,
+                                                       ws->err_word, ws->err_word + 1, ws->sms, s);
+                      },
                       "MoE grouped GEMM launch");
   if (rc) return rc;
   return launch_counted(FLN_KERNEL_MOE_NORM, s,
@@ -1058,7 +1080,7 @@ int fused_moe_down_add_rmsnorm(const fln_bf16* hg, const int* offsets, const int
                           return launch_moe_combine_norm(ws->moe_y, row_of, gates,
                                                          reinterpret_cast<__nv_bfloat16*>(residual), gamma, eps,
                                                          norm_kind, T, H, k, reinterpret_cast<__nv_bfloat16*>(out),
-                                                         s);
+                                                         ws->err_word, ws->err_word + 1, s);
                         },
                         "MoE combine + add + norm launch");
 }
@@ -1365,6 +1387,8 @@ int fln_device_status(fln_stream_t stream) {
   FLN_CUDA(cudaMemcpy(&word, ws->err_word, sizeof word, cudaMemcpyDeviceToHost), "read device error word");
   if (word) {
     FLN_CUDA(cudaMemset(ws->err_word, 0, sizeof word), "clear device error word");
+    if (word & FLN_DEVERR_BAD_INDEX)
+      return fail(FLN_ERR_INVALID_ARG, "a kernel met a device index out of range (device error bits 0x%x)", word);
     return fail(FLN_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (device error bits 0x%x)", word);
   }
   return FLN_OK;

@@ -133,14 +133,21 @@ cudaError_t launch_gemm_pair_fused(int bn, int f8, int ew, const CUtensorMap& tm
 
 // MoE region (fln_moe.cu): routing + grouping (two kernels), the grouped
 // down projection into fp32 rows y [T * k, H], and the unpermute + add + norm.
+// device error word bit for a device-resident MoE index (offsets, row_of, row_token) out of range; the
+// bounded-wait bits sit beside the wait helpers
+#define FLN_DEVERR_BAD_INDEX 0x20u
 cudaError_t launch_moe_route(const float* logits, int T, int E, int k, int* ids, float* gates, int* offsets,
                              int* row_token, int* row_slot, int* row_of, cudaStream_t stream);
+cudaError_t launch_moe_gather(const __nv_bfloat16* x, const int* row_token, int T, int k, int H, __nv_bfloat16* xg,
+                              unsigned int* err, int sms, cudaStream_t stream);
 cudaError_t moe_gemm_prepare();
-cudaError_t launch_moe_grouped_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const int* offsets, int E, int H,
-                                    int K, float* y, unsigned int* err, int grid, cudaStream_t stream);
+cudaError_t launch_moe_grouped_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const int* offsets, int E, int R,
+                                    int H, int K, float* y, unsigned int* err, unsigned int* bad_offsets, int grid,
+                                    cudaStream_t stream);
 cudaError_t launch_moe_combine_norm(const float* y, const int* row_of, const float* gates, __nv_bfloat16* residual,
                                     const float* gamma, float eps, int norm_kind, int T, int H, int k,
-                                    __nv_bfloat16* out, cudaStream_t stream);
+                                    __nv_bfloat16* out, unsigned int* err, const unsigned int* bad_offsets,
+                                    cudaStream_t stream);
 
 // FP4 weights (fmt 0 NVFP4: E4M3 scale per 16 elements; fmt 1 MXFP4: E8M0
 // scale per 32): the split-K GEMM that dequantises W on the SM into tensor

@@ -12,6 +12,7 @@
 //              (tcgen05, bf16 operands, fp32 accumulate in TMEM);
 //   combine + add + norm   r[t] += sum_j gate[t, j] * y[row_of[t, j]] (slot
 //              order, fp32), out[t] = RMSNorm(r[t]).
+#include <algorithm>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -161,6 +162,26 @@ __global__ void __launch_bounds__(1024, 1)
   permute_block(ids, T, E, k, offsets, row_token, row_slot, row_of);
 }
 
+// ------------------------------------------------------------------ gather (permute)
+// Grouped row r of xg is token row_token[r] of x: one 16-byte word (eight
+// bf16) a thread, grid-stride over R * H / 8 words (H % 8 == 0).  A token
+// index outside [0, T) leaves its row unwritten and raises the bad-index bit.
+__global__ void gather_kernel(const uint4* __restrict__ x, const int* __restrict__ row_token, int T, int R, int W8,
+                              uint4* __restrict__ xg, unsigned int* err) {
+  const size_t n = static_cast<size_t>(R) * W8;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t r = i / W8;
+    const int c = static_cast<int>(i - r * W8);
+    const int t = row_token[r];
+    if (static_cast<unsigned>(t) >= static_cast<unsigned>(T)) {
+      if (c == 0) atomicOr(err, FLN_DEVERR_BAD_INDEX);
+      continue;
+    }
+    xg[i] = x[static_cast<size_t>(t) * W8 + c];
+  }
+}
+
 // ------------------------------------------------------------------ grouped GEMM
 // Persistent, one CTA per SM.  Items are (expert, 256-column tile of H,
 // 128-row tile of its rows), expert-major, row tiles fastest; CTA c takes
@@ -201,8 +222,8 @@ struct Sched {
 
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const int* __restrict__ offsets, int E, int H, int K, float* __restrict__ y,
-                        unsigned int* err) {
+                        const int* __restrict__ offsets, int E, int R, int H, int K, float* __restrict__ y,
+                        unsigned int* err, unsigned int* bad_offsets) {
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -222,6 +243,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int NT = (H + BN - 1) / BN;
   const int KB = (K + 63) / 64;
   for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = offsets[e];
+  __syncthreads();
+  // the offsets must describe a grouping of the R rows: 0 = off[0] <= off[1] <= ... <= off[E] = R; else no row
+  // is written (every CTA leaves before it allocates TMEM or arms a barrier) and the verdict tells the combine
+  // kernel that follows on the stream to write nothing either
+  bool ok = threadIdx.x != 0 || (s_off[0] == 0 && s_off[E] == R);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) ok = ok && s_off[e] <= s_off[e + 1];
+  ok = __syncthreads_and(ok);
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    *bad_offsets = ok ? 0u : 1u;
+    if (!ok) atomicOr(err, FLN_DEVERR_BAD_INDEX);
+  }
+  if (!ok) return;
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1);
@@ -386,17 +419,27 @@ template <int GROUPS>
 __global__ void __launch_bounds__(CN_THREADS)
     combine_norm_kernel(const float* __restrict__ y, const int* __restrict__ row_of, const float* __restrict__ gates,
                         __nv_bfloat16* __restrict__ residual, const float* __restrict__ gamma, float eps,
-                        int norm_kind, int H, int k, __nv_bfloat16* __restrict__ out) {
+                        int norm_kind, int H, int k, __nv_bfloat16* __restrict__ out, unsigned int* err,
+                        const unsigned int* __restrict__ bad_offsets) {
+  if (*bad_offsets) return;  // the grouped GEMM refused the offsets and left y unwritten
   const int t = blockIdx.x;
   const int G = H / 8;
+  const unsigned R = static_cast<unsigned>(gridDim.x) * k;
   __shared__ float red[CN_THREADS / 32];
   __shared__ float total;
   int rows[MAX_K];
   float gw[MAX_K];
+  bool bad = false;
 #pragma unroll
   for (int j = 0; j < MAX_K; ++j) {
     rows[j] = j < k ? row_of[static_cast<size_t>(t) * k + j] : 0;
     gw[j] = j < k ? gates[static_cast<size_t>(t) * k + j] : 0.f;
+    bad = bad || static_cast<unsigned>(rows[j]) >= R;
+  }
+  // the token's rows are the same for every thread of the block, so the whole block leaves together
+  if (bad) {
+    if (threadIdx.x == 0) atomicOr(err, FLN_DEVERR_BAD_INDEX);
+    return;
   }
   float r[GROUPS][8];
   float ss = 0.f;
@@ -468,29 +511,43 @@ cudaError_t launch_moe_route(const float* logits, int T, int E, int k, int* ids,
   return cudaGetLastError();
 }
 
+cudaError_t launch_moe_gather(const __nv_bfloat16* x, const int* row_token, int T, int k, int H, __nv_bfloat16* xg,
+                              unsigned int* err, int sms, cudaStream_t stream) {
+  const int R = T * k;
+  const size_t words = static_cast<size_t>(R) * (H / 8);
+  const int grid = static_cast<int>(std::min<size_t>((words + 255) / 256, static_cast<size_t>(sms) * 8));
+  if (grid > 0)
+    moe::gather_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), row_token, T, R, H / 8,
+                                                  reinterpret_cast<uint4*>(xg), err);
+  return cudaGetLastError();
+}
+
 cudaError_t moe_gemm_prepare() {
   return cudaFuncSetAttribute(moe::grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, moe::SMEM);
 }
 
-cudaError_t launch_moe_grouped_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const int* offsets, int E, int H,
-                                    int K, float* y, unsigned int* err, int grid, cudaStream_t stream) {
-  moe::grouped_gemm_kernel<<<grid, moe::THREADS, moe::SMEM, stream>>>(tmA, tmB, offsets, E, H, K, y, err);
+cudaError_t launch_moe_grouped_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const int* offsets, int E, int R,
+                                    int H, int K, float* y, unsigned int* err, unsigned int* bad_offsets, int grid,
+                                    cudaStream_t stream) {
+  moe::grouped_gemm_kernel<<<grid, moe::THREADS, moe::SMEM, stream>>>(tmA, tmB, offsets, E, R, H, K, y, err,
+                                                                       bad_offsets);
   return cudaGetLastError();
 }
 
 cudaError_t launch_moe_combine_norm(const float* y, const int* row_of, const float* gates, __nv_bfloat16* residual,
                                     const float* gamma, float eps, int norm_kind, int T, int H, int k,
-                                    __nv_bfloat16* out, cudaStream_t stream) {
+                                    __nv_bfloat16* out, unsigned int* err, const unsigned int* bad_offsets,
+                                    cudaStream_t stream) {
   const int groups = (H / 8 + moe::CN_THREADS - 1) / moe::CN_THREADS;
   if (groups <= 2)
     moe::combine_norm_kernel<2><<<T, moe::CN_THREADS, 0, stream>>>(y, row_of, gates, residual, gamma, eps, norm_kind,
-                                                                   H, k, out);
+                                                                   H, k, out, err, bad_offsets);
   else if (groups <= 4)
     moe::combine_norm_kernel<4><<<T, moe::CN_THREADS, 0, stream>>>(y, row_of, gates, residual, gamma, eps, norm_kind,
-                                                                   H, k, out);
+                                                                   H, k, out, err, bad_offsets);
   else
     moe::combine_norm_kernel<8><<<T, moe::CN_THREADS, 0, stream>>>(y, row_of, gates, residual, gamma, eps, norm_kind,
-                                                                   H, k, out);
+                                                                   H, k, out, err, bad_offsets);
   return cudaGetLastError();
 }
 

@@ -230,6 +230,22 @@ int fln_moe_route(const float* logits, int T, int E, int k, int* ids, float* gat
                   int* row_slot, int* row_of, fln_stream_t stream);
 
 /*
+ * fln_moe_gather -- the permute step of the MoE region's input side: gathers
+ * the (normalised) hidden states into the grouped order fln_moe_route wrote,
+ *
+ *   xg[r, :] = x[row_token[r], :]      r < T * k
+ *
+ *   x          [T, H] bf16; row_token [T * k] int32 (fln_moe_route's, every
+ *              entry in [0, T)); xg [T * k, H] bf16 out, must not overlap x
+ *   H % 8 == 0; 1 <= k <= 8.  Bit-exact copy; device memory, 16-byte aligned.
+ *   A row_token entry outside [0, T) leaves its row of xg unwritten and makes
+ *   fln_device_status return FLN_ERR_INVALID_ARG.
+ * The expert MLP (the caller's) turns xg into the grouped activations hg of
+ * fused_moe_down_add_rmsnorm.
+ */
+int fln_moe_gather(const fln_bf16* x, const int* row_token, int T, int k, int H, fln_bf16* xg, fln_stream_t stream);
+
+/*
  * fused_moe_down_add_rmsnorm -- the MoE region after the experts: grouped
  * down projection, unpermute, residual add and RMSNorm ("TPSP Design",
  * section 3: grouped GEMM -> unpermute -> add / next norm):
@@ -247,6 +263,10 @@ int fln_moe_route(const float* logits, int T, int E, int k, int* ids, float* gat
  * y is kept in fp32 in the library workspace ([T * k, H]); the grouped GEMM
  * is a persistent tcgen05 kernel over (expert, 128-row tile, 256-column tile)
  * items read from the device offsets, so no host synchronisation is needed.
+ * Offsets that are not a grouping of the T * k rows (0 first, T * k last,
+ * non-decreasing) make the call write nothing, a row_of entry outside
+ * [0, T * k) leaves that token's residual and out rows untouched; either
+ * makes fln_device_status return FLN_ERR_INVALID_ARG.
  */
 int fused_moe_down_add_rmsnorm(const fln_bf16* hg, const int* offsets, const int* row_of, const float* gates,
                                const fln_bf16* We, fln_bf16* residual, const float* gamma, float eps, int norm_kind,
@@ -297,7 +317,11 @@ int fln_set_plan_dtype(int K, int H, int norm_kind, int dtype, const fln_plan* p
 int fln_get_plan_dtype(int K, int H, int norm_kind, int dtype, int T, int microchunk_tokens, fln_plan* plan);
 
 /* Synchronise `stream` and the internal stream, read and clear the device
- * error word.  FLN_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait. */
+ * error word.  FLN_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait;
+ * FLN_ERR_INVALID_ARG if an MoE kernel met a device-resident index out of
+ * range (offsets that are not a grouping of the T * k rows, a row_of entry
+ * outside [0, T * k), a row_token entry outside [0, T)): the kernel then
+ * wrote none of the rows that index touches. */
 int fln_device_status(fln_stream_t stream);
 
 /* Message for the last error on the calling thread ("" if none). */
@@ -322,7 +346,8 @@ enum {
   FLN_KERNEL_MOE_ROUTE = 7,    /* MoE routing + grouping */
   FLN_KERNEL_MOE_GEMM = 8,     /* MoE grouped down projection */
   FLN_KERNEL_MOE_NORM = 9,     /* MoE unpermute + add + norm */
-  FLN_KERNEL_KINDS = 10
+  FLN_KERNEL_MOE_GATHER = 10,  /* MoE gather of hidden states into grouped order */
+  FLN_KERNEL_KINDS = 11
 };
 typedef struct {
   uint64_t launches[FLN_KERNEL_KINDS];

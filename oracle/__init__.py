@@ -318,6 +318,19 @@ def moe_permute(ids, E):
     return offsets, row_token, row_slot, row_of
 
 
+def moe_gather(x, row_token):
+    """The permute step of the MoE region's input side: grouped row r is token row_token[r] of x
+    ([T,H] bf16 bits) -> [T*k,H] bf16 bits."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    row_token = np.ascontiguousarray(row_token, dtype=np.int64)
+    if row_token.size and (row_token.min() < 0 or row_token.max() >= x.shape[0]):
+        raise ValueError("row_token out of range")
+    out = np.empty((row_token.size, x.shape[1]), np.uint16)
+    for r in range(row_token.size):
+        out[r] = x[row_token[r]]
+    return out
+
+
 def moe_down_region(hg, offsets, row_of, wt, We, r0, gamma, eps, norm_kind, nthreads=0):
     """Return (r, o, ms) in float64: grouped down projection of hg [T*k,K] (bf16 bits, grouped by
     expert per offsets) by We [E,H,K] (bf16 bits), unpermuted through row_of [T,k] with gate

@@ -174,3 +174,133 @@ def test_rejects_bad_arguments():
     rc = lib.fused_moe_down_add_rmsnorm(None, None, None, None, None, None, None, 1e-5, 0, 4, 128, 20000, 8, 2, None,
                                         None)
     assert rc == fln.FLN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("T,E,k,H", [(1, 4, 1, 8), (300, 8, 2, 264), (129, 64, 4, 4096), (33, 5, 5, 1032)])
+def test_gather_matches_oracle(T, E, k, H):
+    lg = _logits(T, E, seed=3 * T + H)
+    res = fln.fln_moe_route(torch.from_numpy(lg).cuda(), k)
+    x = np.random.default_rng(T + H).integers(0, 1 << 16, size=(T, H), dtype=np.uint16)
+    xg = fln.fln_moe_gather(dev_bf16(x), res["row_token"], k)
+    fln.fln_device_status()
+    ids, _ = oracle.moe_route(lg, k)
+    _, row_token, _, _ = oracle.moe_permute(ids, E)
+    assert np.array_equal(host_bits(xg), oracle.moe_gather(x, row_token))
+
+
+def test_gather_argument_checks():
+    lib = fln.load()
+    assert lib.fln_moe_gather(None, None, 4, 2, 12, None, None) == fln.FLN_ERR_INVALID_ARG
+    assert lib.fln_moe_gather(None, None, 4, 9, 16, None, None) == fln.FLN_ERR_INVALID_ARG
+    assert lib.fln_moe_gather(None, None, 0, 2, 16, None, None) == fln.FLN_OK
+    buf = torch.zeros((24, 16), dtype=torch.bfloat16, device="cuda")
+    tok = torch.zeros((16,), dtype=torch.int32, device="cuda")
+    with pytest.raises(fln.FlnError, match="overlaps"):
+        fln.fln_moe_gather(buf[:8], tok, 2, out=buf[4:20])   # xg [16, 16] starts inside x [8, 16]
+
+
+def _expect_bad_index():
+    with pytest.raises(fln.FlnError) as ei:
+        fln.fln_device_status()
+    assert ei.value.status == fln.FLN_ERR_INVALID_ARG and "index out of range" in ei.value.message
+
+
+def test_bad_device_indices_are_reported_and_skipped():
+    """Indices that live in device memory (row_token, offsets, row_of) are checked by the kernels: the rows
+    they touch are left unwritten, the status call reports it, and the next call runs normally."""
+    wl, E, k = MOE_CONFIGS["moe_tiny"]
+    d = make_inputs_moe(wl, E, k)
+    T, H = d["r0"].shape
+    # gather: two bad token indices
+    x = np.random.default_rng(1).integers(0, 1 << 15, size=(T, H), dtype=np.uint16)
+    _, row_token, _, _ = oracle.moe_permute(d["ids"], E)
+    bad_tok = row_token.copy()
+    bad_tok[1], bad_tok[4] = T, -1
+    xg = dev_bf16(np.full((T * k, H), 0x7FC3, np.uint16))
+    fln.fln_moe_gather(dev_bf16(x), torch.from_numpy(bad_tok).cuda(), k, out=xg)
+    _expect_bad_index()
+    got, want = host_bits(xg), oracle.moe_gather(x, row_token)
+    assert np.all(got[[1, 4]] == 0x7FC3)
+    keep = np.setdiff1d(np.arange(T * k), [1, 4])
+    assert np.array_equal(got[keep], want[keep])
+    # region: offsets that do not end at T * k -> nothing written, residual and out untouched
+    run = RunMoe(d, E, wl.eps, wl.norm_kind)
+    good = run.offsets
+    bad_end = good.copy()
+    bad_end[E] += 128
+    r = dev_bf16(d["r0"])
+    out = dev_bf16(np.full((T, H), 0x7FC2, np.uint16))
+    fln.fused_moe_down_add_rmsnorm(run.hg, torch.from_numpy(bad_end).cuda(), torch.from_numpy(run.row_of).cuda(),
+                                   torch.from_numpy(d["wt"]).cuda(), run.We, r, run.gamma, wl.eps, wl.norm_kind,
+                                   out=out)
+    _expect_bad_index()
+    assert np.array_equal(host_bits(r), d["r0"]) and np.all(host_bits(out) == 0x7FC2)
+    fln.fln_device_status()         # the error word was cleared by the report
+    # region: offsets out of order
+    run.offsets = good.copy()
+    run.offsets[1], run.offsets[2] = good[2], good[1]
+    assert run.offsets[1] != run.offsets[2]
+    with pytest.raises(fln.FlnError, match="index out of range"):
+        run()
+    # region: one bad row_of entry -> that token's rows untouched, the others exact
+    run.offsets = good
+    bad_row = run.row_of.copy()
+    bad_row[3, k - 1] = T * k
+    r = dev_bf16(d["r0"])
+    out = dev_bf16(np.full((T, H), 0x7FC2, np.uint16))
+    fln.fused_moe_down_add_rmsnorm(run.hg, torch.from_numpy(good).cuda(), torch.from_numpy(bad_row).cuda(),
+                                   torch.from_numpy(d["wt"]).cuda(), run.We, r, run.gamma, wl.eps, wl.norm_kind,
+                                   out=out)
+    _expect_bad_index()
+    rb, ob = host_bits(r), host_bits(out)
+    assert np.array_equal(rb[3], d["r0"][3]) and np.all(ob[3] == 0x7FC2)
+    rb_ok, ob_ok = run()
+    others = np.setdiff1d(np.arange(T), [3])
+    assert np.array_equal(rb[others], rb_ok[others]) and np.array_equal(ob[others], ob_ok[others])
+    run.check(rb_ok, ob_ok, "after bad indices")
+
+
+def test_moe_path_graph_replay_is_bitwise():
+    """Routing, gather and the down region captured in one CUDA graph: every replay gives the eager result
+    (nothing is read back on the host between the steps, so the whole path captures), and that result is the
+    oracle's with the gathered rows standing in for the expert activations."""
+    wl, E, k = MOE_CONFIGS["moe_tiny"]
+    d = make_inputs_moe(wl, E, k)
+    T, K = d["hg"].shape[0] // k, d["We"].shape[2]
+    x_np = np.random.default_rng(11).integers(0, 1 << 15, size=(T, K), dtype=np.uint16) & 0xBF7F  # finite
+    x, lg = dev_bf16(x_np), torch.from_numpy(d["logits"]).cuda()
+    We = torch.from_numpy(np.ascontiguousarray(d["We"]).view(np.int16)).view(torch.bfloat16).cuda()
+    gamma = torch.from_numpy(d["gamma"]).cuda()
+    r0 = dev_bf16(d["r0"])
+    r, out = r0.clone(), torch.empty_like(r0)
+
+    def step():
+        res = fln.fln_moe_route(lg, k)
+        xg = fln.fln_moe_gather(x, res["row_token"], k)
+        fln.fused_moe_down_add_rmsnorm(xg, res["offsets"], res["row_of"], res["gates"], We, r, gamma, wl.eps,
+                                       wl.norm_kind, out=out)
+        return res
+
+    step()                                   # eager; sizes the workspace
+    fln.fln_device_status()
+    r_eager, o_eager = host_bits(r), host_bits(out)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    r.copy_(r0)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for _ in range(3):
+        r.copy_(r0)
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        fln.fln_device_status()
+        assert np.array_equal(host_bits(r), r_eager) and np.array_equal(host_bits(out), o_eager)
+    ids, w = oracle.moe_route(d["logits"], k)
+    offsets, row_token, _, row_of = oracle.moe_permute(ids, E)
+    ro, oo, _ = oracle.moe_down_region(oracle.moe_gather(x_np, row_token), offsets, row_of, w.astype(np.float32),
+                                       d["We"], d["r0"], d["gamma"], wl.eps, wl.norm_kind)
+    compare(r_eager, ro, "graph path residual")
+    compare(o_eager, oo, "graph path out")

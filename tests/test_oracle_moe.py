@@ -149,3 +149,17 @@ def test_hand_worked_case():
     r, o, ms = oracle.moe_down_region(hg, offsets, row_of, wt, We, r0, g, 0.0, 0)
     np.testing.assert_array_equal(r, [[10.5, 5.0]])
     np.testing.assert_allclose(ms, [(10.5 ** 2 + 25) / 2], rtol=1e-15)
+
+
+def test_gather_inverts_the_grouping():
+    g = np.random.default_rng(8)
+    T, E, k, H = 30, 6, 3, 16
+    ids = np.stack([g.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    _, row_token, row_slot, row_of = oracle.moe_permute(ids, E)
+    x = g.integers(0, 1 << 16, size=(T, H), dtype=np.uint16)
+    xg = oracle.moe_gather(x, row_token)
+    for t in range(T):
+        for j in range(k):
+            assert np.array_equal(xg[row_of[t, j]], x[t])
+    assert np.array_equal(np.sort(row_token), np.repeat(np.arange(T), k))
+

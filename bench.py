@@ -66,8 +66,8 @@ NCU_TRAFFIC = {
     ("llama70b_oproj_decode", 8, "nvfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 37937152 + 0,
     ("llama70b_down_decode", 8, "mxfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 128547072 + 2881536,
     ("llama70b_oproj_decode", 8, "mxfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 35841280 + 0,
-    ("mixtral_8x7b_down_decode", 8, "moe", "moe_gemm", 256, "1bba0200a6b9"): 822610944 + 3069952,
-    ("mixtral_8x7b_down", 4096, "moe", "moe_gemm", 256, "1bba0200a6b9"): 1323656960 + 135161600,
+    ("mixtral_8x7b_down_decode", 8, "moe", "moe_gemm", 256, "ea0f5d1ffc77"): 822708224 + 2672640,
+    ("mixtral_8x7b_down", 4096, "moe", "moe_gemm", 256, "ea0f5d1ffc77"): 1323357952 + 135113472,
 }
 # FP8 (E4M3) dense peak: the measured bf16 peak times NVIDIA's nominal dense
 # FP8 / BF16 ratio (4.5 / 2.25 PFLOP/s); no FP8 GEMM peak is measured

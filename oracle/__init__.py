@@ -1,6 +1,9 @@
 """fp64 CPU oracle for y = x.W^T, r = r0 + y, out = RMSNorm(r), with bf16
-operands, FP8 (E4M3) operands and their dequantisation scales, or NVFP4
-weights (E2M1 codes, E4M3 block scales, an fp32 tensor scale).
+operands, FP8 (E4M3) operands and their dequantisation scales, or FP4
+weights (E2M1 codes with E4M3 block scales and an fp32 tensor scale, or
+E8M0 block scales); and for the MoE region: top-k routing, grouping of the
+(token, slot) pairs by expert, the gather into grouped order, the grouped
+down projection, the gated unpermute, add and norm.
 
 TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
 CPU-baseline / reference leg may import this package; the library under

@@ -45,27 +45,29 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # keyed by workload, tokens, kernel, plan tile width and the sha1 of the
 # kernel sources the capture was taken on; reported as null when the sources
 # have changed since.  Captures: profiles/ (same commands).
-def kernel_sources_hash(dtype):
-    """sha1 (12 hex digits) of the kernel sources a dtype's timed kernels are built from."""
+def kernel_sources_hash(dtype, kernel):
+    """sha1 (12 hex digits) of the sources the dominant kernel (by its profile name) is built from."""
     h = hashlib.sha1()
-    files = ["fln_gemm.cu", "fln_gemm2.cu", "fln_norm.cu", "fln_ptx.cuh"]
-    if dtype in ("nvfp4", "mxfp4"):
-        files.append("fln_gemm_w4.cu")
     if dtype == "moe":
         files = ["fln_moe.cu", "fln_ptx.cuh"]
+    elif kernel == "gemm_fused":
+        files = ["fln_gemm2.cu", "fln_ptx.cuh"]
+    elif kernel == "gemm_splitk" and dtype in ("nvfp4", "mxfp4"):
+        files = ["fln_gemm_w4.cu", "fln_ptx.cuh"]
+    else:
+        files = ["fln_gemm.cu", "fln_ptx.cuh"]
     for f in files:
         h.update(open(os.path.join(ROOT, "decoder_layer_projection_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:12]
 
 
 NCU_TRAFFIC = {
-    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "5ab7fd5e2d00"): 116271872 + 33481984,
-    ("llama70b_down_decode", 8, "bf16", "gemm_splitk", 256, "5ab7fd5e2d00"): 471424256 + 3233792,
-    ("llama70b_oproj_decode", 8, "bf16", "gemm_splitk", 256, "5ab7fd5e2d00"): 135537920 + 2888192,
-    ("llama70b_down_decode", 8, "nvfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 135886080 + 2963712,
-    ("llama70b_oproj_decode", 8, "nvfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 37937152 + 0,
-    ("llama70b_down_decode", 8, "mxfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 128547072 + 2881536,
-    ("llama70b_oproj_decode", 8, "mxfp4", "gemm_splitk", 256, "4b1b0566d3f6"): 35841280 + 0,
+    ("llama70b_down_decode", 8, "bf16", "gemm_splitk", 256, "9658cd6e0d51"): 471424256 + 3233792,
+    ("llama70b_oproj_decode", 8, "bf16", "gemm_splitk", 256, "9658cd6e0d51"): 135537920 + 2888192,
+    ("llama70b_down_decode", 8, "nvfp4", "gemm_splitk", 256, "75d05af169d4"): 135886080 + 2963712,
+    ("llama70b_oproj_decode", 8, "nvfp4", "gemm_splitk", 256, "75d05af169d4"): 37937152 + 0,
+    ("llama70b_down_decode", 8, "mxfp4", "gemm_splitk", 256, "75d05af169d4"): 128547072 + 2881536,
+    ("llama70b_oproj_decode", 8, "mxfp4", "gemm_splitk", 256, "75d05af169d4"): 35841280 + 0,
     ("mixtral_8x7b_down_decode", 8, "moe", "moe_gemm", 256, "ea0f5d1ffc77"): 822708224 + 2672640,
     ("mixtral_8x7b_down", 4096, "moe", "moe_gemm", 256, "ea0f5d1ffc77"): 1323357952 + 135113472,
 }
@@ -331,7 +333,7 @@ def run_gpu(args):
         # add + norm: residual read and written, output written, gamma
         achieved = (tokens_per_launch * H * 6.0 + 4.0 * H) / (avg_launch_ms * 1e-3) / 1e9
         bound, unit, peak = "hbm", "GB/s", peaks["hbm_gbs"]
-    src_hash = kernel_sources_hash(args.dtype)
+    src_hash = kernel_sources_hash(args.dtype, kname)
     traffic = NCU_TRAFFIC.get((args.config, T, args.dtype, kname, plan["tile_n"], src_hash))
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
@@ -500,7 +502,7 @@ def run_gpu_moe(args):
     else:
         achieved = flops / (avg_ms * 1e-3) / 1e12
         bound, unit, peak = "tensor", "TFLOP/s", peaks["bf16_tflops"]
-    traffic = NCU_TRAFFIC.get((args.config, T, "moe", "moe_gemm", 256, kernel_sources_hash("moe")))
+    traffic = NCU_TRAFFIC.get((args.config, T, "moe", "moe_gemm", 256, kernel_sources_hash("moe", "moe_gemm")))
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
                 "kernel": "moe_gemm",

@@ -38,6 +38,7 @@ using namespace fln;
 namespace {
 
 constexpr int kMaxMicrochunk = 4096;   // per-call chunk cap ("TPSP Design", section 4)
+constexpr int kSplitMinKBlocks = 128;   // fused pair kernel: K-blocks from which a last round is split
 constexpr int kMaxUnfusedTokens = 256; // the split-K path puts T on the MMA's N side (N <= 256)
 constexpr int kMaxH = 32768;
 constexpr int kMaxK = 1 << 20;
@@ -74,6 +75,10 @@ struct Workspace {
   unsigned int* err_word = nullptr;
   float* psum = nullptr;
   size_t psum_floats = 0;
+  float* split_buf = nullptr;           // second K-halves of split tiles (fused pair kernel)
+  size_t split_floats = 0;
+  unsigned long long* split_flags = nullptr;
+  size_t split_flag_words = 0;
   unsigned int* flags = nullptr;
   size_t flags_count = 0;
   float* slots[3] = {nullptr, nullptr, nullptr};
@@ -450,6 +455,8 @@ int gemm_grid(Workspace* ws, const fln_plan& pl, long long tiles) {
   return static_cast<int>(std::max<long long>(1, std::min<long long>(g, tiles)));
 }
 
+int run_pipelined(Workspace* ws, const Call& c, const fln_plan& pl);
+
 // Per microchunk: one persistent CTA-pair GEMM whose epilogue does add + norm.
 int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
   const int bn = pl.tile_n;
@@ -468,6 +475,33 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
   if ((rc = grow(&ws->psum, &ws->psum_floats, 2 * static_cast<size_t>(mt_alloc) * nt * 128, true,
                  "cudaMalloc(row sums)")))
     return rc;
+  int cap = max_pairs;
+  if (pl.gemm_ctas > 0) cap = std::min(cap, std::max(1, pl.gemm_ctas / 2));
+  // Each pair's epilogue finishes a tile (norm included) before it starts its
+  // next one, and a tile's norm waits for every N-tile of its row block: the
+  // N-tiles of a row block must fall on distinct pairs.  Wider rows take the
+  // PIPELINED path (separate norm pass).
+  if (nt > cap) {
+    fln_plan pp = pl;
+    pp.path = FLN_PATH_PIPELINED;
+    if (pp.tile_n != 128 && pp.tile_n != 256) pp.tile_n = 256;
+    pp.epi_warps = 0;
+    return run_pipelined(ws, c, pp);
+  }
+  // A split pays when half a tile's K-loop outlasts what the helper pair
+  // still has to finish first (its previous tile's epilogue, about a 55
+  // K-block mainloop's time at BN = 256) plus the hand-off; measured on
+  // 4096-token chunks at 152 CTAs: K = 4096 (64 K-blocks) 108 -> 116 us,
+  // K = 14336 (224 K-blocks) 636 -> 582 us.
+  const bool may_split = ew == 4 && c.k_blocks() >= kSplitMinKBlocks;
+  if (may_split) {
+    // split halves of at most cap / 2 tiles: fp32 128 x bn per CTA, four flag words per CTA
+    if ((rc = grow(&ws->split_buf, &ws->split_floats, static_cast<size_t>(cap) * 128 * bn, false,
+                   "cudaMalloc(split tiles)")) ||
+        (rc = grow(&ws->split_flags, &ws->split_flag_words, static_cast<size_t>(cap) * 4, true,
+                   "cudaMalloc(split flags)")))
+      return rc;
+  }
   for (int c0 = 0; c0 < c.T; c0 += chunk) {
     const int n = std::min(chunk, c.T - c0);
     // the chunk's residual and output rows: rows past the chunk read as zeros
@@ -501,9 +535,18 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     // every pair of the grid must be resident at once (they exchange row
     // statistics), so the grid never exceeds the resident-pair count
     const long long tiles = static_cast<long long>((p.num_m_tiles + 1) / 2) * nt;
-    int pairs = max_pairs;
-    if (pl.gemm_ctas > 0) pairs = std::min(pairs, std::max(1, pl.gemm_ctas / 2));
-    pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(pairs, tiles)));
+    // The last round of tiles, when it leaves at least half of the pairs idle:
+    // each of its tiles is split into two K-halves on two pairs.  The pairs of
+    // that round must hold no whole tile of a row block that has split tiles
+    // (their norm would wait for a split tile whose helper is stuck behind
+    // it): the x whole tiles of the row block the split starts in sit on the
+    // last x pairs of the round before.
+    const long long rem = tiles % cap;
+    const long long x = (tiles - rem) % nt;
+    p.split_tiles = (may_split && rem > 0 && 2 * rem + x <= cap) ? static_cast<int>(rem) : 0;
+    p.split_buf = ws->split_buf;
+    p.split_flags = ws->split_flags;
+    const int pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, tiles + p.split_tiles)));
     rc = launch_counted(FLN_KERNEL_GEMM_FUSED, c.stream,
                         [&] {
                           return launch_gemm_pair_fused(bn, c.f8, ew, tmA, tmB, tmR, tmRs, tmOs, p, pairs, c.stream);
@@ -1406,6 +1449,8 @@ void fln_release_workspace(void) {
     cudaDeviceSynchronize();
     cudaFree(ws->err_word);
     cudaFree(ws->psum);
+    cudaFree(ws->split_buf);
+    cudaFree(ws->split_flags);
     cudaFree(ws->flags);
     for (int i = 0; i < 3; ++i) cudaFree(ws->slots[i]);
     cudaFree(ws->partial);

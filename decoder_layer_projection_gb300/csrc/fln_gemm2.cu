@@ -24,6 +24,14 @@
 // bf16(r * rstd * g) in shared memory and each warp writes its 32 rows back
 // with TMA stores, rows past the chunk and columns past H clipped.
 //
+// Work units: the launch's tiles in row-block-major order, pair p taking
+// units p, p + pairs, ...  When the last round of tiles would leave at least
+// half of the pairs idle, each of its tiles becomes two units, one per half
+// of the K-blocks: the first half's pair owns the tile (residual, norm,
+// stores), the second half's pair writes its fp32 accumulator to global
+// memory (L2) and announces it with a {launch generation, 1} word per lane
+// quarter; the owner adds it to its own accumulator before the residual.
+//
 // FP8 (E4M3) operands: the same kernel with kind::f8f6f4 MMAs over 128-byte
 // K-blocks of 128 elements; phase 1 scales the accumulator by the token's and
 // the column's dequantisation scales before the residual add.
@@ -66,6 +74,58 @@ struct Cfg {
   static_assert(SMEM <= SMEM_LIMIT, "shared memory");
 };
 
+enum UnitRole { UNIT_WHOLE = 0, UNIT_OWNER = 1, UNIT_HELPER = 2 };
+
+struct Unit {
+  int t;         // tile: row block t / nN, N-tile t % nN
+  int kb0, kb1;  // K-blocks [kb0, kb1)
+  int role;
+  int j;         // split tiles: index among them
+};
+
+// unit u of a launch with `total` tiles whose last S are split (units: total + S)
+__device__ __forceinline__ Unit unit_at(int u, int total, int S, int KB) {
+  Unit w;
+  const int D = total - S;
+  if (u < D) {
+    w.t = u;
+    w.kb0 = 0;
+    w.kb1 = KB;
+    w.role = UNIT_WHOLE;
+    w.j = 0;
+  } else {
+    const int v = u - D;
+    const int h = v & 1;
+    w.j = v >> 1;
+    w.t = D + w.j;
+    w.kb0 = h ? KB / 2 : 0;
+    w.kb1 = h ? KB : KB / 2;
+    w.role = h ? UNIT_HELPER : UNIT_OWNER;
+  }
+  return w;
+}
+
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// wait (bounded) until the word at f carries generation gen
+__device__ __forceinline__ bool wait_gen_word(const unsigned long long* f, unsigned int gen,
+                                              volatile int* abort_flag) {
+  if (static_cast<unsigned int>(ld_acquire_gpu_u64(f) >> 32) == gen) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (static_cast<unsigned int>(ld_acquire_gpu_u64(f) >> 32) != gen) {
+    if (*abort_flag || globaltimer_ns() - t0 > FLN_WAIT_TIMEOUT_NS) return false;
+  }
+  return true;
+}
+
 // byte offset of the 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled box
 __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
@@ -106,6 +166,11 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
   const int nN = p.num_n_tiles;
   const int num_pm = (p.num_m_tiles + 1) / 2;
   const int total = num_pm * nN;
+  // split tiles only with one epilogue group (the two groups' staging hand-off
+  // assumes every unit stores)
+  const int S = EW == 4 ? p.split_tiles : 0;
+  const int units = total + S;
+  const int KB = p.num_k_blocks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -149,11 +214,12 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = true;
-    for (int t = pair_id; ok && t < total; t += num_pairs) {
-      const int pm = t / nN, nt = t % nN;
+    for (int u = pair_id; ok && u < units; u += num_pairs) {
+      const Unit w = unit_at(u, total, S, KB);
+      const int pm = w.t / nN, nt = w.t % nN;
       const int a_row = p.a_row0 + pm * 2 * BM + static_cast<int>(rank) * BM;
       const int b_row = nt * BN + static_cast<int>(rank) * (BN / 2);
-      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
         if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_EMPTY)) {
           ok = false;
           break;
@@ -184,27 +250,27 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
     // ------------------------------------------------------------ residual loader (both CTAs)
     // (a warp of its own: a lane spinning on a barrier would steal issue
     // slots from a producer or MMA lane of the same warp)
-    // Box s of this CTA's sequence: local tile s / G, group s % G, buffer s % NBOX.
+    // Box s of this CTA's sequence (buffer s % NBOX): the G boxes of each
+    // unit that reads the residual, in unit order (a helper half reads none).
     constexpr int G = C::GROUPS;
-    constexpr int BOXES = G;
     constexpr int NB = C::NBOX;
     const uint64_t pol_r = l2_policy_evict_normal();
     int s = 0;
     bool ok = true;
-    for (;; ++s) {
-      const int k = s / BOXES;
-      const int t = pair_id + k * num_pairs;
-      if (t >= total) break;
-      if (s >= NB && !mbar_wait(&e_free[s % NB], static_cast<uint32_t>(s / NB - 1) & 1u, abort_flag, p.err,
-                                FLN_DEVERR_TIMEOUT_EMPTY)) {
-        ok = false;
-        break;
+    for (int u = pair_id; ok && u < units; u += num_pairs) {
+      const Unit w = unit_at(u, total, S, KB);
+      if (w.role == UNIT_HELPER) continue;
+      const int m0 = ((w.t / nN) * 2 + static_cast<int>(rank)) * BM;
+      for (int g = 0; g < G; ++g, ++s) {
+        if (s >= NB && !mbar_wait(&e_free[s % NB], static_cast<uint32_t>(s / NB - 1) & 1u, abort_flag, p.err,
+                                  FLN_DEVERR_TIMEOUT_EMPTY)) {
+          ok = false;
+          break;
+        }
+        const int n0 = (w.t % nN) * BN + g * 64;
+        mbar_arrive_expect_tx(&e_full[s % NB], C::BOX);
+        tma_load_2d(sE + (s % NB) * C::BOX, &tmR, &e_full[s % NB], n0, m0, pol_r);
       }
-      const int g = s % BOXES;
-      const int m0 = ((t / nN) * 2 + static_cast<int>(rank)) * BM;
-      const int n0 = (t % nN) * BN + g * 64;
-      mbar_arrive_expect_tx(&e_full[s % NB], C::BOX);
-      tma_load_2d(sE + (s % NB) * C::BOX, &tmR, &e_full[s % NB], n0, m0, pol_r);
     }
     // let the last boxes land before the CTA can exit (they may be unconsumed after an abort)
     for (int k = 1; k <= NB && s - k >= 0; ++k) {
@@ -219,7 +285,8 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
     uint32_t phase = 0;
     int local = 0;
     bool ok = true, issued_any = false;
-    for (int t = pair_id; ok && t < total; t += num_pairs, ++local) {
+    for (int u = pair_id; ok && u < units; u += num_pairs, ++local) {
+      const Unit w = unit_at(u, total, S, KB);
       const int b = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(&acc_empty[b], (use & 1u) ^ 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) {
@@ -228,7 +295,7 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
         if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.err, FLN_DEVERR_TIMEOUT_FULL)) {
           ok = false;
           break;
@@ -242,10 +309,10 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
         for (int kk = 0; kk < 4; ++kk) {
           if (F8)
             mma_e4m3_pair(d_tmem, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2),
-                          IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+                          IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
           else
             mma_bf16_pair(d_tmem, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2),
-                          IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+                          IDESC, (kb > w.kb0 || kk > 0) ? 1u : 0u);
         }
         issued_any = true;
         mma_commit_pair_mc(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
@@ -282,11 +349,15 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
     uint8_t* ostage = sE + C::NBOX * C::BOX + q * (32 * 128);  // the quarter's 32 output rows
     unsigned long long* psum = reinterpret_cast<unsigned long long*>(p.psum);
     const unsigned long long tag = static_cast<unsigned long long>(p.gen) << 32;
-    int local = 0;        // k: the pair's k-th tile
-    bool failed = false;  // a row-statistics wait of this warp gave up
-    for (int t = pair_id; t < total; t += num_pairs, ++local) {
+    int local = 0;        // k: the pair's k-th unit
+    bool failed = false;  // a row-statistics or split wait of this warp gave up
+    int sbox = 0;         // first residual box of the next unit that reads the residual
+    for (int u = pair_id; u < units; u += num_pairs, ++local) {
+      const Unit w = unit_at(u, total, S, KB);
+      const int t = w.t;
+      int s = sbox;  // this unit's first residual box
+      if (w.role != UNIT_HELPER) sbox += G;
       if (NG == 2 && (local & 1) != grp) continue;  // the other group's tile
-      int s = local * G;  // this tile's first residual box
       const int b = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       const int mtile = (t / nN) * 2 + static_cast<int>(rank);  // 128-row block index in the launch
@@ -298,9 +369,39 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
       // that leaves alone would strand the others at a named barrier.
       bool stop = failed;
       if (!stop && !mbar_wait(&acc_full[b], use & 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_ACC)) stop = true;
+      // a split tile's owner: the other K-half of these 32 rows must have arrived
+      const size_t split_slot = static_cast<size_t>(w.j) * 2 + rank;
+      if (!stop && w.role == UNIT_OWNER && !wait_gen_word(p.split_flags + split_slot * 4 + q, p.gen, abort_flag)) {
+        if (!*abort_flag) atomicOr(p.err, FLN_DEVERR_TIMEOUT_SPLIT);
+        *abort_flag = 1;
+        failed = true;
+        stop = true;
+      }
       if (named_bar_any(1 + grp, 128, stop)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
+      // fp32 halves of split tiles: [chunk of 32 columns][quad i of 4 columns][row of this CTA][4], so
+      // that each 16-byte access of a warp covers 512 contiguous bytes
+      float* const half = p.split_buf + split_slot * (static_cast<size_t>(BN) * BM);
+      if (w.role == UNIT_HELPER) {
+        // second K-half: the raw accumulator goes to the owner (scales and the residual are the owner's)
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tb + static_cast<uint32_t>(c * 32), v);
+          float4* d4 = reinterpret_cast<float4*>(half) + static_cast<size_t>(c) * 8 * BM + rl;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            __stcg(d4 + i * BM, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_leader + static_cast<uint32_t>(b * 8));
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu_u64(p.split_flags + split_slot * 4 + q, tag | 1ull);
+        continue;
+      }
 
       // phase 1: r = r0 + acc in fp32 and the row's partial sum of squares
       // over this tile.  The fp32 r replaces the accumulator in TMEM (phase 2
@@ -326,6 +427,18 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
           float v[32];
           const uint32_t ta = tb + static_cast<uint32_t>(g * 64 + c2 * 32);
           tmem_ld32(ta, v);
+          if (w.role == UNIT_OWNER) {
+            // the other K-half of the accumulator (fixed order: this half + that half)
+            const float4* h4 = reinterpret_cast<const float4*>(half) + static_cast<size_t>(g * 2 + c2) * 8 * BM + rl;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 a = __ldcg(h4 + i * BM);
+              v[4 * i] += a.x;
+              v[4 * i + 1] += a.y;
+              v[4 * i + 2] += a.z;
+              v[4 * i + 3] += a.w;
+            }
+          }
           if (F8) {
             // dequantise: y = acc * (sx[token] * sw[column])
 #pragma unroll

@@ -74,6 +74,13 @@ struct GemmParams {
   // else (the NVFP4 tensor scale; 1 otherwise, an exact identity)
   float y_scale = 1.0f;
   unsigned int* err;        // device error word
+  // pair kernel: the last split_tiles tiles of the launch are each computed
+  // as two halves of their K-blocks on two pairs; the second half's fp32
+  // accumulator goes through split_buf ([split_tiles, 2 CTAs, BN / 32, 8,
+  // 128, 4]) and is announced by a {gen, 1} word per (tile, CTA, lane quarter)
+  int split_tiles;
+  float* split_buf;
+  unsigned long long* split_flags;
 };
 
 struct NormParams {
@@ -136,6 +143,8 @@ cudaError_t launch_gemm_pair_fused(int bn, int f8, int ew, const CUtensorMap& tm
 // device error word bit for a device-resident MoE index (offsets, row_of, row_token) out of range; the
 // bounded-wait bits sit beside the wait helpers
 #define FLN_DEVERR_BAD_INDEX 0x20u
+// device error word bit: the second K-half of a split tile never arrived at its owner (pair kernel)
+#define FLN_DEVERR_TIMEOUT_SPLIT 0x40u
 cudaError_t launch_moe_route(const float* logits, int T, int E, int k, int* ids, float* gates, int* offsets,
                              int* row_token, int* row_slot, int* row_of, cudaStream_t stream);
 cudaError_t launch_moe_gather(const __nv_bfloat16* x, const int* row_token, int T, int k, int H, __nv_bfloat16* xg,

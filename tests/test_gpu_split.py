@@ -1,0 +1,138 @@
+"""GPU parity of the fused pair kernel's split last round, through the C ABI.
+
+When the last round of a launch's tiles would leave at least half of the
+CTA pairs idle and K spans at least 128 K-blocks, each of its tiles is
+computed as two halves of its K-blocks on two pairs; the second half's fp32
+accumulator reaches the tile's owner through global memory.  These cases make that happen on purpose (every tile split, a
+tail of tiles split after whole rounds, an odd number of K-blocks, ragged H,
+microchunks, FP8 operands) and hold the result to the same bar as every other
+path.  Also: a row block with more N-tiles than the grid has pairs takes the
+PIPELINED path instead of the fused kernel.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from synth import Workload, make_inputs, make_inputs_fp8
+
+from .gpu_util import Run, plan
+from .parity import compare
+
+pytestmark = pytest.mark.gpu
+
+fln = pytest.importorskip("decoder_layer_projection_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fln.build()
+    fln.load()
+    yield
+
+
+_REF = {}
+
+
+def _check(rb, ob, d, wl, name):
+    if wl.name not in _REF:   # the oracle once per workload (K = 8192 takes a few seconds)
+        _REF[wl.name] = oracle.proj_add_rmsnorm(d["x"], d["W"], d["r0"], d["gamma"], wl.eps, wl.norm_kind)[:2]
+    r, o = _REF[wl.name]
+    compare(rb, r, name + " residual")
+    compare(ob, o, name + " out")
+
+
+WL = Workload("split", T=520, K=8192, H=512, eps=1e-5, r_sigma=2.0, seed=31)
+
+
+# (tile, CTA target): 520 tokens = 3 row blocks of 256 (the last ragged); K = 8192 is 128 K-blocks;
+# the split decision per launch
+#   tile 128 / all SMs: 12 tiles, all split (24 pairs)
+#   tile 128 / 16 CTAs: 8 pairs, one whole round of 8 tiles, the last 4 split
+#   tile 128 / 20 CTAs: 10 pairs, 10 whole tiles, the last 2 split (2 whole tiles of their row block before)
+#   tiles 256 / 224 / 192: 6 / 9 / 9 tiles, all split (224 and 192 leave a ragged last N-tile)
+@pytest.mark.parametrize("tile,ctas", [(128, 0), (128, 16), (128, 20), (256, 0), (224, 0), (192, 0)])
+def test_split_tiles_full_parity(tile, ctas):
+    d = make_inputs(WL)
+    run = Run(d, WL.eps, WL.norm_kind)
+    rb, ob = run(plan(fln.PATH_FUSED, chunk=700, tile_n=tile, gemm_ctas=ctas))
+    _check(rb, ob, d, WL, f"split tile={tile} ctas={ctas}")
+    # deterministic: the owner adds the other half in a fixed order
+    rb2, ob2 = run(plan(fln.PATH_FUSED, chunk=700, tile_n=tile, gemm_ctas=ctas))
+    assert np.array_equal(rb, rb2) and np.array_equal(ob, ob2)
+
+
+def test_split_changes_only_the_rounding():
+    """14 CTAs (7 pairs): 12 tiles leave 5 for the last round, too many to split; 16 CTAs split 4.
+    Both meet the oracle's bar; they differ in some bits, since the split tiles add two fp32 halves (if
+    they were identical everywhere, the split would not have run)."""
+    d = make_inputs(WL)
+    run = Run(d, WL.eps, WL.norm_kind)
+    whole = run(plan(fln.PATH_FUSED, chunk=700, tile_n=128, gemm_ctas=14))
+    split = run(plan(fln.PATH_FUSED, chunk=700, tile_n=128, gemm_ctas=16))
+    _check(*whole, d, WL, "unsplit")
+    _check(*split, d, WL, "split")
+    assert not np.array_equal(whole[0], split[0])
+
+
+def test_split_odd_k_blocks_ragged_h_gemma():
+    # K = 8256: 129 K-blocks, halves of 64 and 65; H = 264: the second N-tile is 8 columns wide
+    wl = Workload("split_odd", T=300, K=8256, H=264, norm_kind=1, eps=1e-6, gamma_mode="plain", seed=32)
+    d = make_inputs(wl)
+    run = Run(d, wl.eps, wl.norm_kind)
+    for tile in (256, 128):
+        rb, ob = run(plan(fln.PATH_FUSED, chunk=300, tile_n=tile))
+        _check(rb, ob, d, wl, f"split odd K tile={tile}")
+
+
+def test_split_in_every_microchunk():
+    # chunks of 256, 256 and 8 tokens: each launch splits its tiles; the tail chunk's rows past 8 stay unwritten
+    d = make_inputs(WL)
+    run = Run(d, WL.eps, WL.norm_kind)
+    rb, ob = run(plan(fln.PATH_FUSED, chunk=256, tile_n=128))
+    _check(rb, ob, d, WL, "split chunks of 256")
+
+
+def test_split_fp8():
+    torch = pytest.importorskip("torch")
+    from .gpu_util import dev_bf16, host_bits
+    # E4M3 K-blocks hold 128 elements: K = 16384 is 128 of them
+    wl = Workload("split_fp8", T=300, K=16384, H=640, eps=1e-5, r_sigma=2.0, seed=33)
+    d = make_inputs_fp8(wl)
+    K, H = wl.K, wl.H
+    x = torch.from_numpy(np.ascontiguousarray(d["x8"])).cuda()
+    W = torch.from_numpy(np.ascontiguousarray(d["W8"])).cuda()
+    sx = torch.from_numpy(np.ascontiguousarray(d["x_scale"])).cuda()
+    sw = torch.from_numpy(np.ascontiguousarray(d["w_scale"])).cuda()
+    gamma = torch.from_numpy(np.ascontiguousarray(d["gamma"], np.float32)).cuda()
+    # four epilogue warps (eight would keep every tile whole)
+    fln.fln_set_plan(K, H, wl.norm_kind, plan(fln.PATH_FUSED, chunk=300, tile_n=128, epi_warps=4),
+                     dtype=fln.DTYPE_E4M3)
+    try:
+        r = dev_bf16(d["r0"])
+        out = torch.empty_like(r)
+        fln.fused_proj_add_rmsnorm_fp8(x, sx, W, sw, r, gamma, wl.eps, wl.norm_kind, 0, out)
+        fln.fln_device_status()
+    finally:
+        fln.fln_set_plan(K, H, wl.norm_kind, None, dtype=fln.DTYPE_E4M3)
+    ro, oo, _ = oracle.proj_add_rmsnorm_fp8(d["x8"], d["x_scale"], d["W8"], d["w_scale"], d["r0"], d["gamma"],
+                                            wl.eps, wl.norm_kind)
+    compare(host_bits(r), ro, "split fp8 residual")
+    compare(host_bits(out), oo, "split fp8 out")
+
+
+@pytest.mark.parametrize("tile", [128, 224])
+def test_row_block_wider_than_the_grid_takes_the_pipelined_path(tile):
+    # H = 2048 in 16 (tile 128) or 10 (tile 224) N-tiles on 4 pairs: the fused kernel would need every
+    # N-tile of a row block on its own pair, so the call runs GEMM -> slot -> add + norm instead
+    wl = Workload("wide_rows", T=300, K=256, H=2048, eps=1e-5, r_sigma=2.0, seed=34)
+    d = make_inputs(wl)
+    run = Run(d, wl.eps, wl.norm_kind)
+    fln.fln_profile_enable(True)
+    try:
+        rb, ob = run(plan(fln.PATH_FUSED, chunk=300, tile_n=tile, gemm_ctas=8))
+        prof = fln.fln_profile_read()
+    finally:
+        fln.fln_profile_enable(False)
+    _check(rb, ob, d, wl, f"wide rows tile={tile}")
+    assert prof["gemm_fused"]["launches"] == 0
+    assert prof["gemm_slot"]["launches"] == 1 and prof["norm_slot"]["launches"] == 1

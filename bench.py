@@ -62,6 +62,7 @@ def kernel_sources_hash(dtype, kernel):
 
 
 NCU_TRAFFIC = {
+    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "fa1e76cd037f"): 113160704 + 33056256,
     ("llama70b_down_decode", 8, "bf16", "gemm_splitk", 256, "9658cd6e0d51"): 471424256 + 3233792,
     ("llama70b_oproj_decode", 8, "bf16", "gemm_splitk", 256, "9658cd6e0d51"): 135537920 + 2888192,
     ("llama70b_down_decode", 8, "nvfp4", "gemm_splitk", 256, "75d05af169d4"): 135886080 + 2963712,

@@ -74,6 +74,11 @@ typedef enum { FLN_NORM_STANDARD = 0, FLN_NORM_GEMMA = 1 } fln_norm_kind;
  *   FUSED      per microchunk, one persistent tcgen05 GEMM whose epilogue does
  *              the residual add, the full-row sum of squares (combined across
  *              the row's N-tiles through global partial sums) and the norm.
+ *              From 128 K-blocks (K >= 8192 bf16, 16384 E4M3) a last round
+ *              of tiles that would leave half of the CTA pairs idle is split
+ *              into K-halves on two pairs (fp32 halves added in a fixed
+ *              order).  A row wider than the grid has CTA pairs (N-tiles >
+ *              pairs) runs the PIPELINED path instead.
  *   PIPELINED  per microchunk, the GEMM writes y (fp32) into one of three
  *              reusable slots on the caller's stream; the add + norm of that
  *              chunk runs on a second stream, overlapping the next GEMM.

@@ -2,7 +2,8 @@
 
 Small cases run the oracle on every element (several tiles, ragged tails in
 T, K and H); the full-size workloads compare sampled token rows that the
-oracle computes one by one.  Chunk invariance is bitwise.  Guard rows after T
+oracle computes one by one.  Chunk invariance is bitwise (K below the 128
+K-blocks from which a last round of tiles is split).  Guard rows after T
 must stay untouched on every call.
 """
 import numpy as np

@@ -7,8 +7,10 @@ o_proj prefill (T = K = H = 4096, standard RMSNorm, eps 1e-5); --config picks
 another row of the workload table.  Inputs are synthetic and seeded.
 
 Timing: W warm-up steps, then exactly K steps, each bracketed by CUDA events on
-the launching stream with an L2 flush (a 512 MiB device write) between steps,
-outside the events; a barrier and a device synchronize on both sides of the
+the launching stream with an L2 flush between steps, outside the events (a
+512 MiB device write; with --l2-flush clean, the default, it is followed by a
+512 MiB read of another buffer, so the timed step does not pay for writing back
+the dirty lines the write left in L2); a barrier and a device synchronize on both sides of the
 timed loop; the slowest rank's time counts.  The roofline fraction uses the
 dominant kernel's own per-launch CUDA-event durations, recorded by the library
 on the stream that launches it.
@@ -38,6 +40,9 @@ if ROOT not in sys.path:
 METRIC = "fused proj+add+RMSNorm TFLOP/s and tokens/s; % of roofline (tensor or HBM) on 1 GB300"
 DEFAULT_CONFIG = "llama3_8b_oproj"
 FLUSH_BYTES = 512 << 20
+L2_FLUSH_NOTE = {"write": "flushed between timed steps (512 MiB write)",
+                 "clean": "flushed between timed steps (512 MiB write, then a 512 MiB read of another buffer: "
+                          "L2 holds clean unrelated lines when a step starts)"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes per launch of the dominant kernel, from an ncu capture
@@ -45,6 +50,28 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # keyed by workload, tokens, kernel, plan tile width and the sha1 of the
 # kernel sources the capture was taken on; reported as null when the sources
 # have changed since.  Captures: profiles/ (same commands).
+class L2Flush:
+    """Evicts the step's operands from L2 between timed steps.
+
+    "write": fill a 512 MiB buffer (4x the L2).  The last L2's worth of it is
+    left dirty, and writing it back is charged to whatever runs next.
+    "clean": the same fill, then a 512 MiB read of a second buffer, which
+    evicts the dirty lines outside the timed region."""
+
+    def __init__(self, device, mode):
+        import torch
+        self.mode = mode
+        self.buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.src = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device) if mode == "clean" else None
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
+
+    def fill_(self, v):
+        self.buf.fill_(v)
+        if self.src is not None:
+            import torch
+            torch.sum(self.src, dim=0, out=self.sink)
+
+
 def kernel_sources_hash(dtype, kernel):
     """sha1 (12 hex digits) of the sources the dominant kernel (by its profile name) is built from."""
     h = hashlib.sha1()
@@ -236,7 +263,7 @@ def run_gpu(args):
     r = up(d["r0"])
     gamma = torch.from_numpy(d["gamma"]).to(device)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(device, args.l2_flush)
     stream = torch.cuda.current_stream(device)
 
     # profile the group on this device, as the pages' runtime does after the weights load
@@ -362,7 +389,7 @@ def run_gpu(args):
                    "eps": wl.eps, "global_batch_tokens": T * world, "parallelism": f"dp{world} (replicas)",
                    "plan": plan, "plan_arg": args.plan, "microchunk_arg": args.microchunk,
                    "tune_s": round(t_tune, 2),
-                   "l2": "flushed between timed steps (512 MiB write)"},
+                   "l2": L2_FLUSH_NOTE[args.l2_flush]},
         "tokens_per_s": round(tokens_per_s, 1),
         "step_roofline_frac": round(step_frac, 4),
         "roofline": roofline,
@@ -440,7 +467,7 @@ def run_gpu_moe(args):
     hg, We, r = up(d["hg"]), up(d["We"]), up(d["r0"])
     gamma = torch.from_numpy(d["gamma"]).to(device)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(device, args.l2_flush)
     stream = torch.cuda.current_stream(device)
 
     def step():
@@ -580,7 +607,7 @@ def run_gpu_moe(args):
                    "region": "MoE: routing + grouping, grouped down projection, unpermute + add + RMSNorm",
                    "norm": "gemma" if wl.norm_kind else "standard", "eps": wl.eps,
                    "global_batch_tokens": T * world, "parallelism": f"dp{world} (replicas)",
-                   "l2": "flushed between timed steps (512 MiB write)"},
+                   "l2": L2_FLUSH_NOTE[args.l2_flush]},
         "tokens_per_s": round(whole_job_value(T * args.steps, world, max_s), 1),
         "step_roofline_frac": round(t_roof / (ms_per_step * 1e-3), 4),
         "roofline": roofline,
@@ -820,6 +847,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the cpu_baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0, help="--impl reference: CPU work of the whole run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2-flush", choices=["clean", "write"], default="clean",
+                    help="between timed steps: 512 MiB write (write), or the write then a 512 MiB read (clean)")
     ap.add_argument("--dtype", choices=["bf16", "e4m3", "nvfp4", "mxfp4"], default="bf16",
                     help="operand types: bf16; e4m3 (FP8 x and W with per-token / per-channel scales); "
                          "nvfp4 (NVFP4 weights, bf16 x); mxfp4 (MXFP4 weights, bf16 x)")

@@ -469,8 +469,15 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
   CUtensorMap tmA, tmB;
   if ((rc = make_map(&tmA, c.x, c.K, c.T, 128, c.esize()))) return rc;
   if ((rc = make_map(&tmB, c.W, c.K, c.H, bn / 2, c.esize()))) return rc;
+  // Microchunks run back to back inside one persistent launch of up to 4096
+  // tokens (as many whole chunks as fit): its tiles go to the pairs in
+  // row-block-major order, so while some pairs finish a chunk's add + norm
+  // others already run the next chunk's GEMM, with no launch boundary (and no
+  // partly idle grid) between chunks.  Per-row arithmetic does not depend on
+  // the grouping.
   const int chunk = std::min(pl.microchunk_tokens, c.T);
-  const int mt_alloc = 2 * ((chunk + 255) / 256);  // 128-row blocks, rounded up to whole pairs
+  const int span = std::min(c.T, std::max(1, kMaxMicrochunk / chunk) * chunk);  // tokens per launch
+  const int mt_alloc = 2 * ((span + 255) / 256);  // 128-row blocks, rounded up to whole pairs
   const int nt = (c.H + bn - 1) / bn;
   // row partial sums: one 64-bit {generation, value} word per row and N-tile,
   // zeroed once at allocation (no launch uses generation 0)
@@ -504,9 +511,9 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
                    "cudaMalloc(split flags)")))
       return rc;
   }
-  for (int c0 = 0; c0 < c.T; c0 += chunk) {
-    const int n = std::min(chunk, c.T - c0);
-    // the chunk's residual and output rows: rows past the chunk read as zeros
+  for (int c0 = 0; c0 < c.T; c0 += span) {
+    const int n = std::min(span, c.T - c0);
+    // the launch's residual and output rows: rows past them read as zeros
     // and are never written (TMA clips every store at row n and column H)
     CUtensorMap tmR, tmRs, tmOs;
     if ((rc = make_map(&tmR, c.residual + static_cast<size_t>(c0) * c.H, c.H, n, 128))) return rc;

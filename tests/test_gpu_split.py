@@ -84,12 +84,32 @@ def test_split_odd_k_blocks_ragged_h_gemma():
         _check(rb, ob, d, wl, f"split odd K tile={tile}")
 
 
-def test_split_in_every_microchunk():
-    # chunks of 256, 256 and 8 tokens: each launch splits its tiles; the tail chunk's rows past 8 stay unwritten
+def test_split_with_small_microchunks():
+    # chunks of 256, 256 and 8 tokens run back to back in one launch of 520 tokens, whose tiles all split
     d = make_inputs(WL)
     run = Run(d, WL.eps, WL.norm_kind)
     rb, ob = run(plan(fln.PATH_FUSED, chunk=256, tile_n=128))
     _check(rb, ob, d, WL, "split chunks of 256")
+
+
+WL_LONG = Workload("split_long", T=4100, K=8192, H=256, eps=1e-5, r_sigma=2.0, seed=35)
+
+
+def test_split_in_every_launch_of_a_long_call():
+    """4100 tokens: a launch of 4096 (16 row blocks x 2 N-tiles, all split on 32 pairs of 64) and a tail
+    launch of 4 tokens (2 tiles, split), for chunks of 4096, 1024 and 256 alike (whole chunks are grouped
+    up to 4096 tokens a launch).  Rows on both sides of the launch boundary against the oracle; the
+    chunkings agree bit for bit; rows past the call stay unwritten (Run's guard rows)."""
+    d = make_inputs(WL_LONG)
+    run = Run(d, WL_LONG.eps, WL_LONG.norm_kind)
+    res = [run(plan(fln.PATH_FUSED, chunk=c, tile_n=128, gemm_ctas=128)) for c in (4096, 1024, 256)]
+    for rb, ob in res[1:]:
+        assert np.array_equal(rb, res[0][0]) and np.array_equal(ob, res[0][1])
+    rows = np.array(sorted(set([0, 1, 127, 128, 255, 256, 2047, 2048] + list(range(4088, 4100)))))
+    r, o, _ = oracle.proj_add_rmsnorm(d["x"], d["W"], d["r0"], d["gamma"], WL_LONG.eps, WL_LONG.norm_kind,
+                                      rows=rows)
+    compare(res[0][0][rows], r, "two launches residual")
+    compare(res[0][1][rows], o, "two launches out")
 
 
 def test_split_fp8():

@@ -683,10 +683,12 @@ int check_plan(const fln_plan& p) {
     return fail(FLN_ERR_INVALID_ARG, "plan.path must be FUSED or PIPELINED");
   if (p.microchunk_tokens < 1 || p.microchunk_tokens > kMaxMicrochunk)
     return fail(FLN_ERR_INVALID_ARG, "plan.microchunk_tokens must be in 1..%d", kMaxMicrochunk);
-  if (p.tile_n != 128 && p.tile_n != 192 && p.tile_n != 224 && p.tile_n != 256)
-    return fail(FLN_ERR_INVALID_ARG, "plan.tile_n must be 128, 192, 224 or 256");
+  if (p.tile_n != 64 && p.tile_n != 128 && p.tile_n != 192 && p.tile_n != 224 && p.tile_n != 256)
+    return fail(FLN_ERR_INVALID_ARG, "plan.tile_n must be 64, 128, 192, 224 or 256");
   if (p.path == FLN_PATH_PIPELINED && (p.tile_n == 192 || p.tile_n == 224))
     return fail(FLN_ERR_INVALID_ARG, "plan.tile_n 192 and 224 are available on the FUSED path only");
+  if (p.path == FLN_PATH_FUSED && p.tile_n == 64)
+    return fail(FLN_ERR_INVALID_ARG, "plan.tile_n 64 is available on the PIPELINED path only");
   if (p.gemm_ctas < 0 || p.norm_ctas < 0) return fail(FLN_ERR_INVALID_ARG, "plan CTA targets must be >= 0");
   if (p.threshold_tokens < 1 || p.threshold_tokens > kDefaultThreshold)
     return fail(FLN_ERR_INVALID_ARG, "plan.threshold_tokens must be in 1..%d", kDefaultThreshold);
@@ -1363,8 +1365,10 @@ int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, f
   bool any = false;
   std::vector<std::pair<float, fln_plan>> scanned;  // (median of 3, plan) of every candidate that passed
   for (int path : {FLN_PATH_FUSED, FLN_PATH_PIPELINED}) {
-    for (int tile : (path == FLN_PATH_FUSED ? std::vector<int>{256, 224, 192, 128} : std::vector<int>{256, 128})) {
-      for (int cch : chunks) {
+    for (int tile : (path == FLN_PATH_FUSED ? std::vector<int>{256, 224, 192, 128} : std::vector<int>{256, 128, 64})) {
+      // FUSED runs whole chunks back to back in launches of up to 4096
+      // tokens, so only the largest chunk needs timing there
+      for (int cch : (path == FLN_PATH_FUSED ? std::vector<int>{chunks.back()} : chunks)) {
         for (int g : ctas) {
           for (int nc : (path == FLN_PATH_PIPELINED ? std::vector<int>{0, ws->sms / 4} : std::vector<int>{0})) {
            for (int ew : (path == FLN_PATH_FUSED && tile >= 224 ? std::vector<int>{4, 8} : std::vector<int>{4})) {

@@ -93,7 +93,7 @@ typedef enum { FLN_PATH_FUSED = 1, FLN_PATH_PIPELINED = 2, FLN_PATH_UNFUSED = 3 
 typedef struct {
   int path;              /* fln_path used when T >= threshold_tokens (FUSED or PIPELINED) */
   int microchunk_tokens; /* 1..4096, the chunk of tokens per pipeline step */
-  int tile_n;            /* GEMM tile width on H: 128, 192 or 224 (FUSED only), 256 */
+  int tile_n;            /* GEMM tile width on H: 64 (PIPELINED only), 128, 192 or 224 (FUSED only), 256 */
   int gemm_ctas;         /* SM-count target of the persistent GEMM grid; 0 = all SMs */
   int norm_ctas;         /* CTA cap of the second-stream add + norm (PIPELINED); 0 = no cap */
   int threshold_tokens;  /* T < threshold -> UNFUSED; 1..257 (UNFUSED handles T <= 256) */

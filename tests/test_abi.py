@@ -85,6 +85,8 @@ def test_plans_thresholds_and_profiled_maximum(lib):
     assert e.value.status == fln.FLN_ERR_INVALID_ARG
     with pytest.raises(fln.FlnError):
         fln.fln_set_plan(K, H, 0, dict(bad, tile_n=192, path=fln.PATH_PIPELINED))  # 192: FUSED only
+    with pytest.raises(fln.FlnError):
+        fln.fln_set_plan(K, H, 0, dict(bad, tile_n=64))  # 64: PIPELINED only
     good = dict(bad, tile_n=128, path=fln.PATH_PIPELINED, threshold_tokens=33, tuned_max_tokens=2048)
     fln.fln_set_plan(K, H, 0, good)
     try:

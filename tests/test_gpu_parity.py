@@ -57,7 +57,7 @@ def test_tiny_config_all_paths():
 
 
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
-@pytest.mark.parametrize("path,tile", [(1, 256), (1, 224), (1, 192), (1, 128), (2, 256), (2, 128)])
+@pytest.mark.parametrize("path,tile", [(1, 256), (1, 224), (1, 192), (1, 128), (2, 256), (2, 128), (2, 64)])
 def test_small_prefill_paths_full_parity(wl, path, tile):
     d = make_inputs(wl)
     run = Run(d, wl.eps, wl.norm_kind)

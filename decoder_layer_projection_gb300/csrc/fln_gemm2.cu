@@ -209,7 +209,11 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
-    const uint64_t pol = l2_policy_evict_normal();
+    // W tiles are read again by every row block of the launch, x tiles only by
+    // the N-tiles of their own row block (within the same round): W is kept in
+    // L2 first (Llama-3-8B down_proj, 4096-token launches: 568 -> 553 us)
+    const uint64_t pol_x = l2_policy_evict_normal();
+    const uint64_t pol_w = l2_policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
@@ -228,8 +232,8 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
         uint8_t* sb = sa + C::A_BYTES;
         const uint32_t fb = map_to_cta(smem_u32(&full_bar[stage]), 0);
         if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE);
-        tma_load_2d_pair(sa, &tmA, fb, kb * KBE, a_row, pol);
-        tma_load_2d_pair(sb, &tmB, fb, kb * KBE, b_row, pol);
+        tma_load_2d_pair(sa, &tmA, fb, kb * KBE, a_row, pol_x);
+        tma_load_2d_pair(sb, &tmB, fb, kb * KBE, b_row, pol_w);
         issued_mask |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {

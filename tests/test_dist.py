@@ -64,3 +64,16 @@ def test_single_process_helpers_without_a_group():
     bench.barrier()
     assert bench.whole_job_value(10.0, 1, 2.0) == 5.0
     assert bench.rank_seed(0, 0) != bench.rank_seed(0, 1)
+
+
+def test_l2_flush_modes_on_cpu(monkeypatch):
+    # the flush writes its own buffer; "clean" also reads a second buffer (into a scalar), "write" does not
+    monkeypatch.setattr(bench, "FLUSH_BYTES", 1 << 16)
+    f = bench.L2Flush("cpu", "clean")
+    f.fill_(3.0)
+    assert torch.all(f.buf == 3.0) and f.buf.numel() == (1 << 16) // 4
+    assert float(f.sink) == float(f.src.numel())
+    g = bench.L2Flush("cpu", "write")
+    g.fill_(2.0)
+    assert g.src is None and torch.all(g.buf == 2.0)
+    assert set(bench.L2_FLUSH_NOTE) == {"clean", "write"}

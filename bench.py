@@ -667,6 +667,15 @@ def run_e2e(args, wl, d, W, gamma, device, stream, fln, sw=None):
         ho.copy_(do, non_blocking=True)
         hr_out.copy_(dr, non_blocking=True)
 
+    if args.dtype == "bf16" and not args.e2e_torch_copies:
+        # the library's host-buffer entry point: x and the residual go in and
+        # the residual and out come back in transfer chunks that overlap the
+        # compute (the residual host buffer is updated in place every step)
+        def step():  # noqa: F811
+            fln.fused_proj_add_rmsnorm_host(hx, W, hr_out, gamma, wl.eps, wl.norm_kind, args.transfer_tokens, ho,
+                                            stream)
+        hr_out.copy_(hr)
+
     for _ in range(max(2, args.warmup // 2)):
         step()
     n = max(5, args.steps // 4)
@@ -683,9 +692,13 @@ def run_e2e(args, wl, d, W, gamma, device, stream, fln, sw=None):
     s = max_over_ranks(e0.elapsed_time(e1) / 1e3, device)
     _, world, _ = dist_env()
     h2d = hx.numel() * hx.element_size() + hr.numel() * 2 + (hsx.numel() * 4 if f8 else 0)
+    via = ("fused_proj_add_rmsnorm_host (C ABI, host buffers in page-locked memory, transfer chunks of "
+           f"{args.transfer_tokens or 1024} tokens)" if args.dtype == "bf16" and not args.e2e_torch_copies else
+           "torch copies from / to page-locked host memory around the C ABI call, one stream")
     return {"value": round(whole_job_value(wl.flops() * n, world, s) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4 * T * H, "steps": n,
-            "ms_per_step": round(s * 1e3 / n, 4), "weights": "W, its scales and gamma resident on the device"}
+            "ms_per_step": round(s * 1e3 / n, 4), "weights": "W, its scales and gamma resident on the device",
+            "via": via}
 
 
 def run_comparator(args, wl, x, W, d, gamma, device, stream, fln, flush, sx=None, sw=None):
@@ -854,6 +867,10 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the cpu_baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0, help="--impl reference: CPU work of the whole run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--transfer-tokens", type=int, default=0,
+                    help="e2e: tokens per host transfer chunk of fused_proj_add_rmsnorm_host (0 = its default)")
+    ap.add_argument("--e2e-torch-copies", action="store_true",
+                    help="e2e: torch copies around the device-pointer call instead of the host-buffer entry point")
     ap.add_argument("--l2-flush", choices=["clean", "write"], default="clean",
                     help="between timed steps: 512 MiB write (write), or the write then a 512 MiB read (clean)")
     ap.add_argument("--dtype", choices=["bf16", "e4m3", "nvfp4", "mxfp4"], default="bf16",

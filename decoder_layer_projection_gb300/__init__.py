@@ -45,7 +45,7 @@ EXPORTED_SYMBOLS = (
     "fln_profile_enable", "fln_profile_read", "fln_version", "fused_proj_add_rmsnorm_noalloc",
     "fln_debug_stall_next_call", "fused_proj_add_rmsnorm_fp8", "fln_autotune_dtype", "fln_set_plan_dtype",
     "fln_get_plan_dtype", "fused_proj_add_rmsnorm_nvfp4", "fused_proj_add_rmsnorm_mxfp4", "fln_moe_route",
-    "fused_moe_down_add_rmsnorm", "fln_moe_gather",
+    "fused_moe_down_add_rmsnorm", "fln_moe_gather", "fused_proj_add_rmsnorm_host",
 )
 
 
@@ -116,6 +116,8 @@ def load(path: str | None = None):
         lib.fln_version.restype = i
         lib.fln_debug_stall_next_call.argtypes = [i]
         lib.fln_debug_stall_next_call.restype = i
+        lib.fused_proj_add_rmsnorm_host.argtypes = [vp, vp, vp, vp, f, i, i, i, i, i, vp, vp]
+        lib.fused_proj_add_rmsnorm_host.restype = i
         lib.fused_proj_add_rmsnorm_noalloc.argtypes = [vp, vp, vp, vp, f, i, i, i, i, vp, vp, vp]
         lib.fused_proj_add_rmsnorm_noalloc.restype = i
         lib.fused_proj_add_rmsnorm_fp8.argtypes = [vp, vp, i, vp, vp, i, vp, vp, f, i, i, i, i, i, vp, vp]
@@ -177,6 +179,30 @@ def fused_proj_add_rmsnorm_ptr(x_ptr, W_ptr, residual_ptr, gamma_ptr, eps, norm_
     """Raw-pointer form: returns the status code without raising."""
     return load().fused_proj_add_rmsnorm(x_ptr, W_ptr, residual_ptr, gamma_ptr, float(eps), int(norm_kind),
                                          int(T), int(K), int(H), int(microchunk_tokens), out_ptr, stream_ptr)
+
+
+def fused_proj_add_rmsnorm_host(x_host, W, residual_host, gamma, eps: float, norm_kind: int = NORM_STANDARD,
+                                transfer_tokens: int = 0, out_host=None, stream=None):
+    """The same region with x, residual (in place) and out in HOST memory (CPU
+    tensors; pinned ones let the copies overlap) and W, gamma on the device.
+    Asynchronous on `stream`: synchronize it before reading residual_host or
+    out_host.  Returns out_host."""
+    T, K = x_host.shape
+    H = W.shape[0]
+    if out_host is None:
+        import torch
+        out_host = torch.empty((T, H), dtype=residual_host.dtype, pin_memory=residual_host.is_pinned())
+    _check(load().fused_proj_add_rmsnorm_host(_ptr(x_host), _ptr(W), _ptr(residual_host), _ptr(gamma), float(eps),
+                                              int(norm_kind), int(T), int(K), int(H), int(transfer_tokens),
+                                              _ptr(out_host), _stream_ptr(stream)))
+    return out_host
+
+
+def fused_proj_add_rmsnorm_host_ptr(x_ptr, W_ptr, residual_ptr, gamma_ptr, eps, norm_kind, T, K, H,
+                                    transfer_tokens, out_ptr, stream_ptr) -> int:
+    """Raw-pointer form: returns the status code without raising."""
+    return load().fused_proj_add_rmsnorm_host(x_ptr, W_ptr, residual_ptr, gamma_ptr, float(eps), int(norm_kind),
+                                              int(T), int(K), int(H), int(transfer_tokens), out_ptr, stream_ptr)
 
 
 def fused_proj_add_rmsnorm_noalloc(x, W, residual, gamma, eps: float, norm_kind: int = NORM_STANDARD, out=None,

@@ -99,6 +99,13 @@ struct Workspace {
   cudaEvent_t ev_free[3] = {};
   cudaEvent_t ev_join = nullptr;
   unsigned int gen = 0;
+  // host-buffer entry point: three staging slots of x | residual | out rows,
+  // its copy streams and events (created on its first call)
+  __nv_bfloat16* stage = nullptr;
+  size_t stage_elems = 0;
+  cudaStream_t stream_h2d = nullptr, stream_d2h = nullptr;
+  cudaEvent_t ev_in[3] = {}, ev_done[3] = {}, ev_out[3] = {};
+  cudaEvent_t ev_start = nullptr, ev_host_join = nullptr;
   bool prepared[2][3][5] = {};     // [operand type][epilogue][tile]
   int pair_max[2][2][4] = {};      // resident CTA pairs of the fused pair kernel,
                                    // [operand type][4 / 8 epilogue warps][tile 128/192/224/256]
@@ -459,7 +466,8 @@ int gemm_grid(Workspace* ws, const fln_plan& pl, long long tiles) {
 
 int run_pipelined(Workspace* ws, const Call& c, const fln_plan& pl);
 
-// Per microchunk: one persistent CTA-pair GEMM whose epilogue does add + norm.
+// Whole microchunks back to back in persistent CTA-pair launches of up to 4096
+// tokens; the GEMM epilogue does add + norm.
 int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
   const int bn = pl.tile_n;
   int max_pairs = 0;
@@ -998,6 +1006,106 @@ int fused_proj_add_rmsnorm(const fln_bf16* x, const fln_bf16* W, fln_bf16* resid
   return run_plan(ws, c, pl);
 }
 
+// ------------------------------------------------------------------ host buffers
+namespace {
+
+constexpr int kDefaultTransferTokens = 1024;
+
+// A pointer the host reaches directly: not device memory.
+int check_host_ptr(const char* name, const void* p) {
+  if (!p) return fail(FLN_ERR_INVALID_ARG, "%s is NULL", name);
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(FLN_ERR_INVALID_ARG, "%s: cudaPointerGetAttributes failed (%s)", name, cudaGetErrorName(e));
+  }
+  if (a.type == cudaMemoryTypeDevice) return fail(FLN_ERR_INVALID_ARG, "%s is a device pointer", name);
+  return FLN_OK;
+}
+
+int host_streams(Workspace* ws) {
+  if (ws->stream_h2d) return FLN_OK;
+  FLN_CUDA(cudaStreamCreateWithFlags(&ws->stream_h2d, cudaStreamNonBlocking), "cudaStreamCreate(host copies in)");
+  FLN_CUDA(cudaStreamCreateWithFlags(&ws->stream_d2h, cudaStreamNonBlocking), "cudaStreamCreate(host copies out)");
+  for (int i = 0; i < 3; ++i) {
+    FLN_CUDA(cudaEventCreateWithFlags(&ws->ev_in[i], cudaEventDisableTiming), "cudaEventCreate");
+    FLN_CUDA(cudaEventCreateWithFlags(&ws->ev_done[i], cudaEventDisableTiming), "cudaEventCreate");
+    FLN_CUDA(cudaEventCreateWithFlags(&ws->ev_out[i], cudaEventDisableTiming), "cudaEventCreate");
+  }
+  FLN_CUDA(cudaEventCreateWithFlags(&ws->ev_start, cudaEventDisableTiming), "cudaEventCreate");
+  FLN_CUDA(cudaEventCreateWithFlags(&ws->ev_host_join, cudaEventDisableTiming), "cudaEventCreate");
+  return FLN_OK;
+}
+
+}  // namespace
+
+int fused_proj_add_rmsnorm_host(const fln_bf16* x_host, const fln_bf16* W, fln_bf16* residual_host,
+                                const float* gamma, float eps, int norm_kind, int T, int K, int H,
+                                int transfer_tokens, fln_bf16* out_host, fln_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = check_common(eps, norm_kind, T, H);
+  if (rc) return rc;
+  if (K < 8 || (K & 7)) return fail(FLN_ERR_INVALID_ARG, "K=%d must be a positive multiple of 8", K);
+  if (K > kMaxK) return fail(FLN_ERR_UNSUPPORTED, "K=%d above the supported %d", K, kMaxK);
+  if (transfer_tokens < 0 || transfer_tokens > kMaxMicrochunk)
+    return fail(FLN_ERR_INVALID_ARG, "transfer_tokens=%d outside 0..%d", transfer_tokens, kMaxMicrochunk);
+  if (T == 0) return FLN_OK;
+  if ((rc = check_host_ptr("x_host", x_host)) || (rc = check_host_ptr("residual_host", residual_host)) ||
+      (rc = check_host_ptr("out_host", out_host)) || (rc = check_ptr("W", W)) || (rc = check_ptr("gamma", gamma)))
+    return rc;
+  const size_t bx = size_t(T) * K * 2, br = size_t(T) * H * 2;
+  if (overlaps(out_host, br, x_host, bx) || overlaps(out_host, br, residual_host, br))
+    return fail(FLN_ERR_INVALID_ARG, "out_host overlaps x_host or residual_host");
+  if (overlaps(residual_host, br, x_host, bx)) return fail(FLN_ERR_INVALID_ARG, "residual_host overlaps x_host");
+  Workspace* ws = nullptr;
+  if ((rc = get_ws(&ws))) return rc;
+  if ((rc = host_streams(ws))) return rc;
+  const int tc = std::min(T, transfer_tokens > 0 ? transfer_tokens : kDefaultTransferTokens);
+  // slot layout (elements): x [tc, K] | residual [tc, H] | out [tc, H]; every
+  // part starts on a 16-byte boundary since K and H are multiples of 8
+  const size_t slot = size_t(tc) * (size_t(K) + 2 * size_t(H));
+  if ((rc = grow(&ws->stage, &ws->stage_elems, 3 * slot, false, "cudaMalloc(host staging slots)"))) return rc;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const auto* xh = reinterpret_cast<const __nv_bfloat16*>(x_host);
+  auto* rh = reinterpret_cast<__nv_bfloat16*>(residual_host);
+  auto* oh = reinterpret_cast<__nv_bfloat16*>(out_host);
+  // the copies in follow the work queued on the caller's stream before the call
+  FLN_CUDA(cudaEventRecord(ws->ev_start, cs), "cudaEventRecord(start)");
+  FLN_CUDA(cudaStreamWaitEvent(ws->stream_h2d, ws->ev_start, 0), "cudaStreamWaitEvent(start)");
+  int i = 0;
+  for (int c0 = 0; c0 < T; c0 += tc, ++i) {
+    const int s = i % 3;
+    const int n = std::min(tc, T - c0);
+    __nv_bfloat16* sx = ws->stage + s * slot;
+    __nv_bfloat16* sr = sx + size_t(tc) * K;
+    __nv_bfloat16* so = sr + size_t(tc) * H;
+    // the slot is free once its previous chunk (this call's or an earlier
+    // call's) has been copied out
+    FLN_CUDA(cudaStreamWaitEvent(ws->stream_h2d, ws->ev_out[s], 0), "cudaStreamWaitEvent(slot free)");
+    FLN_CUDA(cudaMemcpyAsync(sx, xh + size_t(c0) * K, size_t(n) * K * 2, cudaMemcpyHostToDevice, ws->stream_h2d),
+             "x chunk to the device");
+    FLN_CUDA(cudaMemcpyAsync(sr, rh + size_t(c0) * H, size_t(n) * H * 2, cudaMemcpyHostToDevice, ws->stream_h2d),
+             "residual chunk to the device");
+    FLN_CUDA(cudaEventRecord(ws->ev_in[s], ws->stream_h2d), "cudaEventRecord(chunk in)");
+    FLN_CUDA(cudaStreamWaitEvent(cs, ws->ev_in[s], 0), "cudaStreamWaitEvent(chunk in)");
+    fln_plan pl;
+    if ((rc = resolve_plan(K, H, norm_kind, FLN_DTYPE_BF16, n, 0, &pl))) return rc;
+    Call c{sx, reinterpret_cast<const __nv_bfloat16*>(W), sr, gamma, eps, norm_kind, n, K, H, so, cs};
+    if ((rc = run_plan(ws, c, pl))) return rc;
+    FLN_CUDA(cudaEventRecord(ws->ev_done[s], cs), "cudaEventRecord(chunk done)");
+    FLN_CUDA(cudaStreamWaitEvent(ws->stream_d2h, ws->ev_done[s], 0), "cudaStreamWaitEvent(chunk done)");
+    FLN_CUDA(cudaMemcpyAsync(rh + size_t(c0) * H, sr, size_t(n) * H * 2, cudaMemcpyDeviceToHost, ws->stream_d2h),
+             "residual chunk to the host");
+    FLN_CUDA(cudaMemcpyAsync(oh + size_t(c0) * H, so, size_t(n) * H * 2, cudaMemcpyDeviceToHost, ws->stream_d2h),
+             "out chunk to the host");
+    FLN_CUDA(cudaEventRecord(ws->ev_out[s], ws->stream_d2h), "cudaEventRecord(chunk out)");
+  }
+  FLN_CUDA(cudaEventRecord(ws->ev_host_join, ws->stream_d2h), "cudaEventRecord(join)");
+  FLN_CUDA(cudaStreamWaitEvent(cs, ws->ev_host_join, 0), "cudaStreamWaitEvent(join)");
+  return FLN_OK;
+}
+
 int fused_proj_add_rmsnorm_fp8(const uint8_t* x, const float* x_scale, int x_scale_per_token, const uint8_t* W,
                                const float* w_scale, int w_scale_per_channel, fln_bf16* residual,
                                const float* gamma, float eps, int norm_kind, int T, int K, int H,
@@ -1494,10 +1602,18 @@ void fln_release_workspace(void) {
     cudaFree(ws->dyn_counter);
     cudaFree(ws->w4_bf16);
     cudaFree(ws->moe_y);
+    cudaFree(ws->stage);
     for (int i = 0; i < 3; ++i) {
       cudaEventDestroy(ws->ev_ready[i]);
       cudaEventDestroy(ws->ev_free[i]);
+      if (ws->ev_in[i]) cudaEventDestroy(ws->ev_in[i]);
+      if (ws->ev_done[i]) cudaEventDestroy(ws->ev_done[i]);
+      if (ws->ev_out[i]) cudaEventDestroy(ws->ev_out[i]);
     }
+    if (ws->ev_start) cudaEventDestroy(ws->ev_start);
+    if (ws->ev_host_join) cudaEventDestroy(ws->ev_host_join);
+    if (ws->stream_h2d) cudaStreamDestroy(ws->stream_h2d);
+    if (ws->stream_d2h) cudaStreamDestroy(ws->stream_d2h);
     cudaEventDestroy(ws->ev_join);
     cudaStreamDestroy(ws->stream_b);
     delete ws;

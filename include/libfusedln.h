@@ -126,6 +126,40 @@ int fused_proj_add_rmsnorm(const fln_bf16* x, const fln_bf16* W, fln_bf16* resid
                            float eps, int norm_kind, int T, int K, int H, int microchunk_tokens, fln_bf16* out,
                            fln_stream_t stream);
 
+/*
+ * fused_proj_add_rmsnorm_host -- the same region for activations held in host
+ * memory.  The microchunk pipeline of vLLM "TPSP Design" (section 3: per chunk,
+ * compute on one stream while the chunk before is exchanged on another) with
+ * the host link in place of the collectives.
+ *
+ *   x_host         [T, K] bf16 in HOST memory (page-locked memory lets the
+ *                  copies overlap; pageable memory works, without overlap)
+ *   W, gamma       DEVICE pointers as in fused_proj_add_rmsnorm (weights stay
+ *                  resident)
+ *   residual_host  [T, H] bf16 in HOST memory, read and overwritten with r0 + y
+ *   out_host       [T, H] bf16 in HOST memory, must not overlap x_host or
+ *                  residual_host
+ *   transfer_tokens  tokens per transfer chunk: 0 = 1024, else 1..4096
+ *   eps, norm_kind, T, K, H as in fused_proj_add_rmsnorm
+ *
+ * The tokens stream through the GPU in chunks of transfer_tokens: the copy of
+ * chunk i + 1 to the device, the projection + add + norm of chunk i (on
+ * `stream`, with the group's plan for that chunk's token count) and the copy
+ * of chunk i - 1 back to the host run at the same time on three streams,
+ * through three device staging slots the library owns (allocated on first
+ * use and grown as needed; fln_release_workspace frees them).  Asynchronous
+ * on `stream` like the other calls: the copies start after the work queued
+ * on `stream` before the call, the host buffers must stay valid and unchanged
+ * until `stream` completes, and only then do residual_host and out_host hold
+ * the results.  Calls are sequential-use like the workspace (one host thread
+ * at a time).  Errors: FLN_ERR_INVALID_ARG for NULL or device host-side
+ * pointers, host or misaligned device-side pointers, bad sizes; FLN_ERR_CUDA
+ * for a failing copy or launch.
+ */
+int fused_proj_add_rmsnorm_host(const fln_bf16* x_host, const fln_bf16* W, fln_bf16* residual_host,
+                                const float* gamma, float eps, int norm_kind, int T, int K, int H,
+                                int transfer_tokens, fln_bf16* out_host, fln_stream_t stream);
+
 /* Operand element types of a projection group. */
 typedef enum { FLN_DTYPE_BF16 = 0, FLN_DTYPE_E4M3 = 1, FLN_DTYPE_NVFP4 = 2, FLN_DTYPE_MXFP4 = 3 } fln_dtype;
 

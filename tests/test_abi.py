@@ -124,6 +124,25 @@ def test_fused_rejects_bad_arguments_before_any_launch(lib, kw, status):
 
 
 @pytest.mark.parametrize("kw,status", [
+    (dict(norm_kind=2), fln.FLN_ERR_INVALID_ARG),
+    (dict(eps=-1.0), fln.FLN_ERR_INVALID_ARG),
+    (dict(K=12), fln.FLN_ERR_INVALID_ARG),
+    (dict(H=4), fln.FLN_ERR_INVALID_ARG),
+    (dict(T=-1), fln.FLN_ERR_INVALID_ARG),
+    (dict(transfer_tokens=4097), fln.FLN_ERR_INVALID_ARG),
+    (dict(transfer_tokens=-1), fln.FLN_ERR_INVALID_ARG),
+    (dict(T=0), fln.FLN_OK),                      # empty call: nothing to copy or launch
+])
+def test_host_entry_rejects_bad_arguments_before_any_copy(lib, kw, status):
+    a = dict(eps=1e-5, norm_kind=0, T=16, K=256, H=256, transfer_tokens=0)
+    a.update(kw)
+    rc = fln.fused_proj_add_rmsnorm_host_ptr(None, None, None, None, a["eps"], a["norm_kind"], a["T"], a["K"],
+                                             a["H"], a["transfer_tokens"], None, None)
+    assert rc == status, fln.fln_last_error()
+    assert fln.fln_launch_count() == 0
+
+
+@pytest.mark.parametrize("kw,status", [
     (dict(K=24), fln.FLN_ERR_INVALID_ARG),        # FP8 rows must be 16 bytes: K multiple of 16
     (dict(K=8), fln.FLN_ERR_INVALID_ARG),
     (dict(norm_kind=5), fln.FLN_ERR_INVALID_ARG),

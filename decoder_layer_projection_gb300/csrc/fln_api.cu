@@ -1051,6 +1051,12 @@ int fused_proj_add_rmsnorm_host(const fln_bf16* x_host, const fln_bf16* W, fln_b
   if (transfer_tokens < 0 || transfer_tokens > kMaxMicrochunk)
     return fail(FLN_ERR_INVALID_ARG, "transfer_tokens=%d outside 0..%d", transfer_tokens, kMaxMicrochunk);
   if (T == 0) return FLN_OK;
+  const int tc = std::min(T, transfer_tokens > 0 ? transfer_tokens : kDefaultTransferTokens);
+  {
+    // every chunk's plan resolves if the largest one does: refuse before any copy
+    fln_plan pl;
+    if ((rc = resolve_plan(K, H, norm_kind, FLN_DTYPE_BF16, tc, 0, &pl))) return rc;
+  }
   if ((rc = check_host_ptr("x_host", x_host)) || (rc = check_host_ptr("residual_host", residual_host)) ||
       (rc = check_host_ptr("out_host", out_host)) || (rc = check_ptr("W", W)) || (rc = check_ptr("gamma", gamma)))
     return rc;
@@ -1061,7 +1067,6 @@ int fused_proj_add_rmsnorm_host(const fln_bf16* x_host, const fln_bf16* W, fln_b
   Workspace* ws = nullptr;
   if ((rc = get_ws(&ws))) return rc;
   if ((rc = host_streams(ws))) return rc;
-  const int tc = std::min(T, transfer_tokens > 0 ? transfer_tokens : kDefaultTransferTokens);
   // slot layout (elements): x [tc, K] | residual [tc, H] | out [tc, H]; every
   // part starts on a 16-byte boundary since K and H are multiples of 8
   const size_t slot = size_t(tc) * (size_t(K) + 2 * size_t(H));

@@ -142,6 +142,21 @@ def test_host_entry_rejects_bad_arguments_before_any_copy(lib, kw, status):
     assert fln.fln_launch_count() == 0
 
 
+def test_host_entry_refuses_untuned_chunks_before_any_copy(lib):
+    # a group profiled up to 256 tokens: automatic chunks of 1024 exceed it, chunks of 256 do not
+    K, H = 512, 256
+    fln.fln_set_plan(K, H, 0, dict(path=fln.PATH_FUSED, microchunk_tokens=4096, tile_n=256, gemm_ctas=0,
+                                   norm_ctas=0, threshold_tokens=1, tuned_max_tokens=256))
+    try:
+        rc = fln.fused_proj_add_rmsnorm_host_ptr(None, None, None, None, 1e-5, 0, 2048, K, H, 0, None, None)
+        assert rc == fln.FLN_ERR_NOT_TUNED, fln.fln_last_error()
+        rc = fln.fused_proj_add_rmsnorm_host_ptr(None, None, None, None, 1e-5, 0, 2048, K, H, 256, None, None)
+        assert rc == fln.FLN_ERR_INVALID_ARG   # past the plan check, stopped at the NULL pointers
+    finally:
+        fln.fln_set_plan(K, H, 0, None)
+    assert fln.fln_launch_count() == 0
+
+
 @pytest.mark.parametrize("kw,status", [
     (dict(K=24), fln.FLN_ERR_INVALID_ARG),        # FP8 rows must be 16 bytes: K multiple of 16
     (dict(K=8), fln.FLN_ERR_INVALID_ARG),

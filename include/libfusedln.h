@@ -153,8 +153,9 @@ int fused_proj_add_rmsnorm(const fln_bf16* x, const fln_bf16* W, fln_bf16* resid
  * until `stream` completes, and only then do residual_host and out_host hold
  * the results.  Calls are sequential-use like the workspace (one host thread
  * at a time).  Errors: FLN_ERR_INVALID_ARG for NULL or device host-side
- * pointers, host or misaligned device-side pointers, bad sizes; FLN_ERR_CUDA
- * for a failing copy or launch.
+ * pointers, host or misaligned device-side pointers, bad sizes;
+ * FLN_ERR_NOT_TUNED, before any copy, when a transfer chunk exceeds the
+ * group's profiled token maximum; FLN_ERR_CUDA for a failing copy or launch.
  */
 int fused_proj_add_rmsnorm_host(const fln_bf16* x_host, const fln_bf16* W, fln_bf16* residual_host,
                                 const float* gamma, float eps, int norm_kind, int T, int K, int H,

@@ -30,7 +30,8 @@
  *   - Tensors are row-major with the last dimension contiguous.  bf16 tensors
  *     are passed as pointers to their 16-bit storage (fln_bf16).  gamma is fp32.
  *   - Pointers are CUDA device pointers on the current device, 16-byte
- *     aligned.  The caller owns every tensor; the library never frees them.
+ *     aligned (fused_proj_add_rmsnorm_host takes its activations in host
+ *     memory).  The caller owns every tensor; the library never frees them.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
  *     Work the library puts on its internal second stream is joined back into
  *     `stream` before the call returns; nothing is synchronised on the host.
@@ -77,10 +78,10 @@ typedef enum { FLN_NORM_STANDARD = 0, FLN_NORM_GEMMA = 1 } fln_norm_kind;
  *              run back to back inside one launch of up to 4096 tokens (as
  *              many whole chunks as fit; tiles in row-block order, so one
  *              chunk's add + norm overlaps the next chunk's GEMM on other
- *              CTA pairs).  From 128 K-blocks (K >= 8192 bf16, 16384 E4M3) a last round
- *              of tiles that would leave half of the CTA pairs idle is split
- *              into K-halves on two pairs (fp32 halves added in a fixed
- *              order).  A row wider than the grid has CTA pairs (N-tiles >
+ *              CTA pairs).  From 128 K-blocks (K >= 8192 bf16, 16384 E4M3)
+ *              a last round of tiles that would leave half of the CTA pairs
+ *              idle is split into K-halves on two pairs (fp32 halves added
+ *              in a fixed order).  A row wider than the grid has CTA pairs (N-tiles >
  *              pairs) runs the PIPELINED path instead.
  *   PIPELINED  per microchunk, the GEMM writes y (fp32) into one of three
  *              reusable slots on the caller's stream; the add + norm of that

@@ -110,6 +110,22 @@ NCU_TRAFFIC = {
 FP8_OVER_BF16 = 2.0
 
 
+def bench_config(wl, operands, world, l2_mode, extra=None):
+    """The workload description both arms print in `config` (identical keys and values)."""
+    c = {"workload": wl.name, "T": wl.T, "K": wl.K, "H": wl.H, "operands": operands,
+         "norm": "gemma" if wl.norm_kind else "standard", "eps": wl.eps, "global_batch_tokens": wl.T * world,
+         "parallelism": f"dp{world} (replicas)", "l2": L2_FLUSH_NOTE[l2_mode]}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def moe_config(wl, E, k, world, l2_mode):
+    return bench_config(wl, "bf16", world, l2_mode, {
+        "experts": E, "top_k": k,
+        "region": "MoE: routing + grouping, grouped down projection, unpermute + add + RMSNorm"})
+
+
 # ------------------------------------------------------------------ distributed helpers
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
@@ -329,16 +345,18 @@ def run_gpu(args):
             prof = fln.fln_profile_read()
             fln.fln_profile_enable(False)
         fln.fln_device_status(stream)
-        return sum(st.elapsed_time(en) for st, en in zip(starts, ends)) / 1e3, nl, prof
+        step_ms = [st.elapsed_time(en) for st, en in zip(starts, ends)]
+        return sum(step_ms) / 1e3, nl, prof, step_ms
 
     # pass 1: the headline number, nothing recorded between the library's launches
     sampler = ClockSampler(local_rank)
     sampler.start()
-    local_s, launches, _ = timed_pass(False)
+    local_s, launches, _, head_step_ms = timed_pass(False)
     clocks = sampler.stop()
     sampler = None
-    # pass 2: the same K steps with per-kernel events on each kernel's own stream (roofline)
-    prof_s, _, prof = timed_pass(True)
+    # pass 2: the same K steps with per-kernel events on each kernel's own stream (which kernel
+    # dominates, and its time when a step launches more than one kernel)
+    prof_s, _, prof, _ = timed_pass(True)
     max_s = max_over_ranks(local_s, device)
     ms_per_step = max_s * 1e3 / args.steps
     flops = wl.flops()
@@ -351,6 +369,14 @@ def run_gpu(args):
     kp = prof[kname]
     avg_launch_ms = kp["total_ms"] / max(kp["launches"], 1)
     launches_per_step = kp["launches"] / args.steps
+    if launches == args.steps and kp["launches"] == args.steps:
+        # one library launch per step: the headline pass's step events, recorded on the stream that
+        # launches the kernel, bracket exactly that launch
+        avg_launch_ms = statistics.fmean(head_step_ms)
+        kernel_timing = "headline pass: each step's CUDA events bracket the kernel's one launch on its stream"
+    else:
+        kernel_timing = ("second timed pass of the same K steps with per-kernel CUDA events on each kernel's "
+                         "stream (a step launches more than one kernel)")
     tokens_per_launch = T / launches_per_step
     ob = 1.0 if f8 else 2.0  # bytes per x element (and per W element, except NVFP4)
     wb = 0.5 + (1.0 / 32.0 if mx else 1.0 / 16.0) if w4 else ob  # bytes per W element
@@ -375,7 +401,7 @@ def run_gpu(args):
                 "peak_source": (f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback")
                 + (" bf16 x 2, the nominal dense FP8/BF16 ratio" if f8 and bound == "tensor" else ""),
                 "kernel_ms_per_launch": round(avg_launch_ms, 5), "launches_per_step": launches_per_step,
-                "measured": "second timed pass of the same K steps with per-kernel CUDA events",
+                "measured": kernel_timing,
                 "profiled_ms_per_step": round(prof_s * 1e3 / args.steps, 5)}
     # full-step roofline: the slower of FLOPs at tensor peak and bytes at HBM bandwidth
     t_roof = max(flops / (tensor_peak * 1e12),
@@ -390,12 +416,8 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
-        "config": {"workload": wl.name, "T": T, "K": K, "H": H, "operands": args.dtype,
-                   "norm": "gemma" if wl.norm_kind else "standard",
-                   "eps": wl.eps, "global_batch_tokens": T * world, "parallelism": f"dp{world} (replicas)",
-                   "plan": plan, "plan_arg": args.plan, "microchunk_arg": args.microchunk,
-                   "tune_s": round(t_tune, 2),
-                   "l2": L2_FLUSH_NOTE[args.l2_flush]},
+        "config": bench_config(wl, args.dtype, world, args.l2_flush),
+        "plan": dict(plan, plan_arg=args.plan, microchunk_arg=args.microchunk, tune_s=round(t_tune, 2)),
         "tokens_per_s": round(tokens_per_s, 1),
         "step_roofline_frac": round(step_frac, 4),
         "roofline": roofline,
@@ -405,6 +427,9 @@ def run_gpu(args):
         "comparator_unfused_cublas": comparator,
         "clocks": clocks,
     }
+    if (world == 1 and not args.no_table and args.config == DEFAULT_CONFIG and args.dtype == "bf16"
+            and not args.tokens):
+        line["configs"] = run_table(args, fln, device, stream, flush, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, d, args.cpu_seconds)
     if world > 1:
@@ -609,11 +634,7 @@ def run_gpu_moe(args):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "T": T, "K": K, "H": H, "experts": E, "top_k": k,
-                   "region": "MoE: routing + grouping, grouped down projection, unpermute + add + RMSNorm",
-                   "norm": "gemma" if wl.norm_kind else "standard", "eps": wl.eps,
-                   "global_batch_tokens": T * world, "parallelism": f"dp{world} (replicas)",
-                   "l2": L2_FLUSH_NOTE[args.l2_flush]},
+        "config": moe_config(wl, E, k, world, args.l2_flush),
         "tokens_per_s": round(whole_job_value(T * args.steps, world, max_s), 1),
         "step_roofline_frac": round(t_roof / (ms_per_step * 1e-3), 4),
         "roofline": roofline,
@@ -740,6 +761,148 @@ def run_comparator(args, wl, x, W, d, gamma, device, stream, fln, flush, sx=None
             "what": what}
 
 
+# ------------------------------------------------------------------ the other workloads
+# Every large workload of the table besides the headline one: the Llama-3-8B
+# down projection, the Gemma-2-9B down projection, and the 70B decode sweep
+# (o_proj and down_proj at each token count).  The tiny workload is a parity
+# case only.
+TABLE_CASES = ([("llama3_8b_down", 0), ("gemma2_9b_down", 0)] +
+               [(n, t) for n in ("llama70b_oproj_decode", "llama70b_down_decode") for t in (1, 8, 32, 128, 256)])
+PATH_NAMES = {1: "FUSED", 2: "PIPELINED", 3: "UNFUSED"}
+
+
+def kernel_roofline(kname, wl, T_launch, ms, peaks):
+    """Roofline of one launch of a kernel: the slower of its FLOPs at the tensor peak and its
+    algorithmic bytes at the HBM bandwidth decides the bound; returns (bound, achieved, unit, frac)."""
+    K, H = wl.K, wl.H
+    if kname in ("gemm_fused", "gemm_slot", "gemm_splitk"):
+        flops = 2.0 * T_launch * K * H
+        nbytes = 2.0 * H * K + 2.0 * T_launch * K + (6.0 * T_launch * H + 4.0 * H if kname == "gemm_fused" else 0.0)
+    else:
+        flops = 5.0 * T_launch * H
+        nbytes = 6.0 * T_launch * H + 4.0 * H
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    s = ms * 1e-3
+    if t_tensor >= t_hbm:
+        return "tensor", flops / s / 1e12, "TFLOP/s", t_tensor / s
+    return "hbm", nbytes / s / 1e9, "GB/s", t_hbm / s
+
+
+def run_table(args, fln, device, stream, flush, peaks):
+    """Each case: the tuned plan, K timed steps (L2 flushed between them, the headline's timing), the
+    dominant kernel's per-launch time and roofline, and the unfused cuBLAS GEMM + add_rmsnorm comparator."""
+    import numpy as np
+    import torch
+    from synth import make_inputs, workload
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    rows = []
+    tuned = set()
+    sampler = ClockSampler(device.index)
+    sampler.start()
+    sampler.mark_begin()
+    t_start = time.time()
+    for name, T in TABLE_CASES:
+        wl = workload(name)
+        if T:
+            wl = wl.with_tokens(T)
+        T, K, H = wl.T, wl.K, wl.H
+        d = make_inputs(wl)
+        x, W, r = up(d["x"]), up(d["W"]), up(d["r0"])
+        gamma = torch.from_numpy(d["gamma"]).to(device)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        group = (K, H, wl.norm_kind)
+        if group not in tuned:
+            # decode groups are profiled once up to 256 tokens, so the token threshold decides the path
+            fln.fln_autotune(K, H, wl.norm_kind, 256 if "decode" in name else T, stream)
+            tuned.add(group)
+        plan = fln.fln_get_plan(K, H, wl.norm_kind, T)
+
+        def step():
+            fln.fused_proj_add_rmsnorm(x, W, r, gamma, wl.eps, wl.norm_kind, 0, out, stream)
+
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            step()
+
+        def timed(profile):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            if profile:
+                fln.fln_profile_enable(True)
+            n0 = fln.fln_launch_count()
+            torch.cuda.synchronize(device)
+            for i, (a, b) in enumerate(ev):
+                flush.fill_(float(i))
+                a.record(stream)
+                step()
+                b.record(stream)
+            torch.cuda.synchronize(device)
+            nl = fln.fln_launch_count() - n0
+            prof = None
+            if profile:
+                prof = fln.fln_profile_read()
+                fln.fln_profile_enable(False)
+            fln.fln_device_status(stream)
+            return [a.elapsed_time(b) for a, b in ev], nl, prof
+
+        step_ms, nl, _ = timed(False)
+        _, _, prof = timed(True)
+        ms = statistics.fmean(step_ms)
+        kname = max(prof, key=lambda k: prof[k]["total_ms"])
+        kp = prof[kname]
+        if nl == args.steps and kp["launches"] == args.steps:
+            kms, ktiming = ms, "headline-style pass (one launch per step)"
+        else:
+            kms, ktiming = kp["total_ms"] / kp["launches"], "second pass, per-kernel events"
+        lps = kp["launches"] / args.steps
+        bound, achieved, unit, kfrac = kernel_roofline(kname, wl, T / lps, kms, peaks)
+        t_roof = max(wl.flops() / (peaks["bf16_tflops"] * 1e12), wl.algorithmic_bytes(2) / (peaks["hbm_gbs"] * 1e9))
+        src_hash = kernel_sources_hash("bf16", kname)
+        traffic = NCU_TRAFFIC.get((name, T, "bf16", kname, plan["tile_n"], src_hash))
+        # comparator: cuBLAS GEMM (bf16 out) then add_rmsnorm, same flush, same timing
+        r2 = up(d["r0"])
+        out2 = torch.empty_like(out)
+        cm = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            y = torch.matmul(x, W.t())
+            fln.add_rmsnorm(y, r2, gamma, wl.eps, wl.norm_kind, out2, stream)
+            b.record(stream)
+            cm.append((a, b))
+        torch.cuda.synchronize(device)
+        cms = statistics.fmean(a.elapsed_time(b) for a, b in cm[args.warmup:])
+        rows.append({
+            "workload": name, "T": T, "K": K, "H": H, "norm": "gemma" if wl.norm_kind else "standard",
+            "path": PATH_NAMES.get(3 if T < plan["threshold_tokens"] else plan["path"]),
+            "plan": {k: plan[k] for k in ("path", "microchunk_tokens", "tile_n", "gemm_ctas", "norm_ctas",
+                                          "threshold_tokens", "epi_warps")},
+            "ms_per_step": round(ms, 5), "tflops": round(wl.flops() / (ms * 1e-3) / 1e12, 2),
+            "tokens_per_s": round(T / (ms * 1e-3), 1), "step_roofline_frac": round(t_roof / (ms * 1e-3), 4),
+            "launches_per_step": nl / args.steps,
+            "kernel": kname, "kernel_ms_per_launch": round(kms, 5), "kernel_timing": ktiming,
+            "roofline": {"bound": bound, "achieved": round(achieved, 2), "unit": unit, "frac": round(kfrac, 4),
+                         "traffic": traffic},
+            "kernel_time_ms": {k: round(v["total_ms"] / args.steps, 5) for k, v in prof.items() if v["launches"]},
+            "comparator_unfused_cublas": {"ms_per_step": round(cms, 5),
+                                          "tflops": round(wl.flops() / (cms * 1e-3) / 1e12, 2)},
+            "speedup_vs_comparator": round(cms / ms, 4),
+        })
+        del x, W, r, out, r2, out2, y
+        torch.cuda.empty_cache()
+    sampler.mark_end()
+    clocks = sampler.stop()
+    return {"cases": rows, "clocks": clocks, "wall_s": round(time.time() - t_start, 1),
+            "what": "each case with its tuned plan (decode groups profiled up to 256 tokens), the same timing "
+                    "and L2 flush as the headline; roofline of the dominant kernel: the slower of its FLOPs "
+                    "at the tensor peak and its algorithmic bytes at the HBM bandwidth (measured peaks)"}
+
+
 # ------------------------------------------------------------------ CPU oracle
 def _oracle_rows_timed(wl, d, rows, nthreads=0):
     import numpy as np
@@ -804,8 +967,7 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total * 1e3 / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "K": wl.K, "H": wl.H,
-                                            "operands": args.dtype},
+            "data": "synthetic", "config": bench_config(wl, args.dtype, world, args.l2_flush),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -845,8 +1007,7 @@ def run_reference_moe(args):
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total * 1e3 / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "K": wl.K, "H": wl.H, "experts": E,
-                                            "top_k": k},
+            "data": "synthetic", "config": moe_config(wl, E, k, world, args.l2_flush),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -867,6 +1028,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the cpu_baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0, help="--impl reference: CPU work of the whole run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-table", action="store_true",
+                    help="skip the other workloads' record (run with the default workload at N = 1)")
     ap.add_argument("--transfer-tokens", type=int, default=0,
                     help="e2e: tokens per host transfer chunk of fused_proj_add_rmsnorm_host (0 = its default)")
     ap.add_argument("--e2e-torch-copies", action="store_true",

@@ -1571,15 +1571,32 @@ int fln_autotune_dtype(int K, int H, int norm_kind, int dtype, int max_tokens, f
 
 int fln_device_status(fln_stream_t stream) {
   std::lock_guard<std::mutex> lk(g_mu);
-  Workspace* ws = nullptr;
-  int rc = get_ws(&ws);
-  if (rc) return rc;
+  int dev = 0;
+  FLN_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
   FLN_CUDA(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)), "cudaStreamSynchronize");
-  FLN_CUDA(cudaStreamSynchronize(ws->stream_b), "cudaStreamSynchronize(internal stream)");
   unsigned int word = 0;
-  FLN_CUDA(cudaMemcpy(&word, ws->err_word, sizeof word, cudaMemcpyDeviceToHost), "read device error word");
+  // the workspace's error word, if this device has a workspace (the status
+  // call itself never creates one, so callers of the no-allocation entry
+  // point can use it)
+  auto it = g_ws.find(dev);
+  if (it != g_ws.end()) {
+    Workspace* ws = it->second;
+    FLN_CUDA(cudaStreamSynchronize(ws->stream_b), "cudaStreamSynchronize(internal stream)");
+    unsigned int w = 0;
+    FLN_CUDA(cudaMemcpy(&w, ws->err_word, sizeof w, cudaMemcpyDeviceToHost), "read device error word");
+    if (w) FLN_CUDA(cudaMemset(ws->err_word, 0, sizeof w), "clear device error word");
+    word |= w;
+  }
+  // the no-allocation entry point's word in its static scratch, which
+  // collects the error bits of calls made without a caller-owned word
+  if (dev >= 0 && dev < kNoAllocMaxDevices && g_noalloc_dev[dev].ready) {
+    unsigned int w = 0;
+    unsigned char* sc = g_noalloc_dev[dev].scratch;
+    FLN_CUDA(cudaMemcpy(&w, sc, sizeof w, cudaMemcpyDeviceToHost), "read no-allocation error word");
+    if (w) FLN_CUDA(cudaMemset(sc, 0, sizeof w), "clear no-allocation error word");
+    word |= w;
+  }
   if (word) {
-    FLN_CUDA(cudaMemset(ws->err_word, 0, sizeof word), "clear device error word");
     if (word & FLN_DEVERR_BAD_INDEX)
       return fail(FLN_ERR_INVALID_ARG, "a kernel met a device index out of range (device error bits 0x%x)", word);
     return fail(FLN_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (device error bits 0x%x)", word);
@@ -1696,6 +1713,12 @@ int fused_proj_add_rmsnorm_noalloc(const fln_bf16* x, const fln_bf16* W, fln_bf1
   }
   NoAllocDevice* d = nullptr;
   if ((rc = noalloc_setup(&d))) return rc;
+  // The N-tiles of a row block wait for one another's row statistics, so they
+  // must fall on distinct CTAs that are resident together: one CTA per SM,
+  // tiles dealt round-robin, which holds when a row block has at most as many
+  // N-tiles as the GPU has SMs.
+  if (nt > d->sms)
+    return fail(FLN_ERR_UNSUPPORTED, "no-allocation path: %d N-tiles per row block exceed the %d SMs", nt, d->sms);
   CUtensorMap tmA, tmB;
   if ((rc = make_map(&tmA, x, K, T, 128))) return rc;
   if ((rc = make_map(&tmB, W, K, H, kNoAllocTile))) return rc;
@@ -1724,6 +1747,8 @@ int fused_proj_add_rmsnorm_noalloc(const fln_bf16* x, const fln_bf16* W, fln_bf1
     if (++d->gen == 0) ++d->gen;
     p.gen = d->gen;
     p.err = err_word;
+    p.stall_rowstat = g_stall_next ? 1 : 0;
+    g_stall_next = false;
     const int G = std::max(1, std::min(d->sms, p.num_m_tiles * nt));
     cudaError_t e = launch_gemm(EPI_FUSED_NORM, kNoAllocTile, 0, tmA, tmB, p, G, s);
     if (e != cudaSuccess) return cuda_fail(e, "no-allocation fused GEMM launch");

@@ -429,9 +429,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           bool ok = true;
           for (int j = lane; j < nN; j += 32) {
             const unsigned int* f = &p.flags[w.m_tile * nN + j];
-            if (ld_acquire_gpu(f) != p.gen) {
+            // (the test switch makes flag 0 wait for a value nobody publishes)
+            const unsigned int want = (p.stall_rowstat && j == 0) ? p.gen + 1u : p.gen;
+            if (ld_acquire_gpu(f) != want) {
               const uint64_t t0 = globaltimer_ns();
-              while (ld_acquire_gpu(f) != p.gen) {
+              while (ld_acquire_gpu(f) != want) {
                 if (*abort_flag || globaltimer_ns() - t0 > FLN_WAIT_TIMEOUT_NS) {
                   ok = false;
                   break;

@@ -361,7 +361,10 @@ int fln_set_plan_dtype(int K, int H, int norm_kind, int dtype, const fln_plan* p
 int fln_get_plan_dtype(int K, int H, int norm_kind, int dtype, int T, int microchunk_tokens, fln_plan* plan);
 
 /* Synchronise `stream` and the internal stream, read and clear the device
- * error word.  FLN_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait;
+ * error words of the current device: the workspace's (if the device has a
+ * workspace; this call never creates one) and the one in the static scratch
+ * of fused_proj_add_rmsnorm_noalloc (if that entry point has run on the
+ * device).  FLN_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait;
  * FLN_ERR_INVALID_ARG if an MoE kernel met a device-resident index out of
  * range (offsets that are not a grouping of the T * k rows, a row_of entry
  * outside [0, T * k), a row_token entry outside [0, T)): the kernel then
@@ -417,18 +420,30 @@ int fln_profile_read(fln_profile_stats* stats);
  * creates a stream or an event.
  *
  *   x, W, residual, gamma, eps, norm_kind, T, K, H, out, stream: as in
- *   fused_proj_add_rmsnorm.  It always runs the FUSED path (tile width 256,
- *   chunks of 4096 tokens, one CTA per SM); plans, tuning, the token threshold
- *   and the overrides do not apply.
+ *   fused_proj_add_rmsnorm.  It always runs one kernel: the single-CTA
+ *   tcgen05 GEMM with the fused add + norm epilogue (tile 128 x 256, chunks
+ *   of 4096 tokens, one CTA per SM, row statistics exchanged through the
+ *   static scratch).  That is not the CTA-pair kernel of the FUSED path, so
+ *   its results agree with fused_proj_add_rmsnorm within the parity
+ *   tolerance (max-abs 2e-2 or one bf16 ulp, mean-abs 2e-3, both against the
+ *   fp64 reference), not bit for bit.  Plans, tuning, the token threshold and
+ *   the overrides do not apply.
  *   device_error: NULL, or a device pointer to one 4-byte word owned by the
  *   caller; a kernel that gives up a bounded wait ORs its error bits into it
- *   (the caller clears it and reads it after synchronising).
+ *   (the caller clears it and reads it after synchronising).  With NULL the
+ *   bits go to a word in the static scratch instead, which fln_device_status
+ *   reads and clears (that call allocates nothing either).  A bounded wait
+ *   gives up only if the kernel's CTAs cannot all be resident at once (for
+ *   example while other streams hold SMs); the rows it did not finish are
+ *   left unwritten.
  *
  * Scratch: a static device array of 1 057 024 bytes, held by every GPU that
  * loads the library until the process exits.  It holds the row statistics of
  * at most 2048 tiles: ceil(min(T, 4096) / 128) * ceil(H / 256) <= 2048, i.e.
  * H <= 16384 once T >= 3969.  Larger problems return FLN_ERR_UNSUPPORTED with a
- * message before anything is launched.
+ * message before anything is launched, as do rows with more 256-wide N-tiles
+ * than the GPU has SMs (the N-tiles of a row block must run on distinct,
+ * co-resident CTAs).
  * The first call on a device looks up where the array lives on that device
  * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make that
  * first call before any stream capture.

@@ -77,3 +77,34 @@ def test_l2_flush_modes_on_cpu(monkeypatch):
     g.fill_(2.0)
     assert g.src is None and torch.all(g.buf == 2.0)
     assert set(bench.L2_FLUSH_NOTE) == {"clean", "write"}
+
+
+def test_reference_arm_prints_the_gpu_arms_config():
+    """Both arms describe the workload with the same dict, so a line-by-line comparison of their
+    `config` matches (the plan the GPU arm tuned is reported beside it, not inside)."""
+    import argparse
+    from synth import workload
+    args = argparse.Namespace(config="tiny", tokens=0, dtype="bf16", steps=1, warmup=3, ref_seconds=0.5,
+                              l2_flush="clean")
+    line = bench.run_reference(args)
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.bench_config(workload("tiny"), "bf16", 1, "clean")
+    assert "plan" not in line["config"]
+
+
+def test_kernel_roofline_picks_the_slower_resource():
+    from synth import workload
+    peaks = {"bf16_tflops": 1000.0, "hbm_gbs": 5000.0}
+    wl = workload("llama3_8b_oproj")
+    # 4096^3 prefill: FLOPs dominate; achieved = FLOPs / time
+    bound, ach, unit, frac = bench.kernel_roofline("gemm_fused", wl, 4096, 0.2, peaks)
+    assert (bound, unit) == ("tensor", "TFLOP/s")
+    assert ach == pytest.approx(2 * 4096 ** 3 / 0.2e-3 / 1e12)
+    assert frac == pytest.approx(2 * 4096 ** 3 / 1e15 / 0.2e-3)
+    # 8 tokens of a 70B o_proj: the weight bytes dominate
+    wd = workload("llama70b_oproj_decode")
+    bound, ach, unit, frac = bench.kernel_roofline("gemm_splitk", wd, 8, 0.03, peaks)
+    nbytes = 2 * 8192 * 8192 + 2 * 8 * 8192
+    assert (bound, unit) == ("hbm", "GB/s")
+    assert ach == pytest.approx(nbytes / 0.03e-3 / 1e9)
+    assert frac == pytest.approx(nbytes / 5e12 / 0.03e-3)

@@ -23,6 +23,7 @@ FLN_ERR_UNSUPPORTED = -2
 FLN_ERR_CUDA = -3
 FLN_ERR_DEVICE_TIMEOUT = -4
 FLN_ERR_NOT_TUNED = -5
+FLN_ERR_COMM = -6
 
 NORM_STANDARD = 0
 NORM_GEMMA = 1
@@ -46,6 +47,8 @@ EXPORTED_SYMBOLS = (
     "fln_debug_stall_next_call", "fused_proj_add_rmsnorm_fp8", "fln_autotune_dtype", "fln_set_plan_dtype",
     "fln_get_plan_dtype", "fused_proj_add_rmsnorm_nvfp4", "fused_proj_add_rmsnorm_mxfp4", "fln_moe_route",
     "fused_moe_down_add_rmsnorm", "fln_moe_gather", "fused_proj_add_rmsnorm_host",
+    "fln_tp_unique_id", "fln_tp_comm_init", "fln_tp_comm_destroy", "fln_tp_layout", "fln_tp_chunk_rows",
+    "fused_proj_rs_add_rmsnorm_ag",
 )
 
 
@@ -138,6 +141,19 @@ def load(path: str | None = None):
         lib.fln_set_plan_dtype.restype = i
         lib.fln_get_plan_dtype.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Plan)]
         lib.fln_get_plan_dtype.restype = i
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.fln_tp_unique_id.argtypes = [vp]
+        lib.fln_tp_unique_id.restype = i
+        lib.fln_tp_comm_init.argtypes = [i, i, vp, ctypes.POINTER(vp)]
+        lib.fln_tp_comm_init.restype = i
+        lib.fln_tp_comm_destroy.argtypes = [vp]
+        lib.fln_tp_comm_destroy.restype = i
+        lib.fln_tp_layout.argtypes = [i, i, i, ip, ip, ip]
+        lib.fln_tp_layout.restype = i
+        lib.fln_tp_chunk_rows.argtypes = [i, i, i, i, i, ip, ip, ip]
+        lib.fln_tp_chunk_rows.restype = i
+        lib.fused_proj_rs_add_rmsnorm_ag.argtypes = [vp, vp, vp, vp, f, i, i, i, i, i, vp, vp, vp]
+        lib.fused_proj_rs_add_rmsnorm_ag.restype = i
         _lib = lib
         return lib
 
@@ -410,3 +426,81 @@ def fln_moe_gather(x, row_token, k: int, out=None, stream=None):
     _check(load().fln_moe_gather(_ptr(x), _ptr(row_token), int(T), int(k), int(H), _ptr(out), _stream_ptr(stream)))
     return out
 
+
+
+# ------------------------------------------------------------------ TPSP region across ranks
+def _nccl_in_process():
+    """The TP calls use the NCCL that PyTorch loads into the process."""
+    import torch  # noqa: F401  (loads libnccl with the CUDA libraries)
+
+
+def fln_tp_unique_id() -> bytes:
+    """128-byte NCCL unique id for fln_tp_comm_init (made on one rank, sent to the others)."""
+    _nccl_in_process()
+    buf = ctypes.create_string_buffer(128)
+    _check(load().fln_tp_unique_id(buf))
+    return buf.raw
+
+
+class TpComm:
+    """One rank's TP communicator handle (current CUDA device); close() frees it."""
+
+    def __init__(self, nranks: int, rank: int, unique_id: bytes | None = None):
+        _nccl_in_process()
+        h = ctypes.c_void_p()
+        idbuf = None if unique_id is None else ctypes.create_string_buffer(bytes(unique_id), 128)
+        _check(load().fln_tp_comm_init(int(nranks), int(rank), idbuf, ctypes.byref(h)))
+        self.handle = h
+        self.nranks, self.rank = int(nranks), int(rank)
+
+    def close(self):
+        if self.handle:
+            _check(load().fln_tp_comm_destroy(self.handle))
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+        return False
+
+
+def fln_tp_layout(T: int, nranks: int, microchunk_tokens: int = 0) -> tuple:
+    """(shard rows S, chunk tokens per rank, number of chunks); host only."""
+    a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(load().fln_tp_layout(int(T), int(nranks), int(microchunk_tokens), ctypes.byref(a), ctypes.byref(b),
+                                ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def fln_tp_chunk_rows(T: int, nranks: int, microchunk_tokens: int, chunk: int, rank: int) -> tuple:
+    """(first token, block rows, valid rows) of chunk `chunk` of rank `rank`; host only."""
+    a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(load().fln_tp_chunk_rows(int(T), int(nranks), int(microchunk_tokens), int(chunk), int(rank),
+                                    ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def fused_proj_rs_add_rmsnorm_ag(x, W, residual_shard, gamma, eps: float, norm_kind: int, comm: TpComm,
+                                 microchunk_tokens: int = 0, out=None, stream=None):
+    """One rank's TPSP region: x [T,K] and W [H,K] are this rank's K-shards (bf16), residual_shard
+    [ceil(T/P), H] its token shard (bf16, in place); returns out [T,H] bf16, the gathered normalised
+    tensor."""
+    T, K = x.shape
+    H = W.shape[0]
+    if out is None:
+        import torch
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _check(load().fused_proj_rs_add_rmsnorm_ag(_ptr(x), _ptr(W), _ptr(residual_shard), _ptr(gamma), float(eps),
+                                               int(norm_kind), int(T), int(K), int(H), int(microchunk_tokens),
+                                               _ptr(out), comm.handle, _stream_ptr(stream)))
+    return out
+
+
+def fused_proj_rs_add_rmsnorm_ag_ptr(x_ptr, W_ptr, residual_ptr, gamma_ptr, eps, norm_kind, T, K, H,
+                                     microchunk_tokens, out_ptr, comm_handle, stream_ptr) -> int:
+    """Raw-pointer form: returns the status code without raising."""
+    return load().fused_proj_rs_add_rmsnorm_ag(x_ptr, W_ptr, residual_ptr, gamma_ptr, float(eps), int(norm_kind),
+                                               int(T), int(K), int(H), int(microchunk_tokens), out_ptr,
+                                               comm_handle, stream_ptr)

@@ -986,6 +986,36 @@ int noalloc_setup(NoAllocDevice** out) {
 
 }  // namespace
 
+// ------------------------------------------------------------------ helpers shared with fln_tp.cu
+namespace fln {
+int api_fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+int api_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+int api_check_ptr(const char* name, const void* p) { return check_ptr(name, p); }
+int api_check_common(float eps, int kind, int T, int H) { return check_common(eps, kind, T, H); }
+bool api_overlaps(const void* a, size_t na, const void* b, size_t nb) { return overlaps(a, na, b, nb); }
+int api_make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  return make_map(m, base, inner, rows, box_rows, 2);
+}
+void api_count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+int api_device_error_word(unsigned int** word) {
+  Workspace* ws = nullptr;
+  int rc = get_ws(&ws);
+  if (rc) return rc;
+  *word = ws->err_word;
+  return FLN_OK;
+}
+void api_lock() { g_mu.lock(); }
+void api_unlock() { g_mu.unlock(); }
+}  // namespace fln
+
 // ====================================================================== C ABI
 extern "C" {
 

@@ -73,6 +73,18 @@ __device__ __forceinline__ WorkItem dyn_item(const GemmParams& p, int j) {
   return w;
 }
 
+// x row (TMA coordinate) of an m-tile's first row, and the slot row of its
+// row rl: plain (a_row0 + tile * 128, tile * 128 + rl) or, with rank-major
+// blocks, block b = tile / blk_m_tiles at x rows a_row0 + b * blk_stride and
+// slot rows b * blk_rows (rows of a block past blk_rows are not stored)
+__device__ __forceinline__ int a_row_of(const GemmParams& p, int m_tile) {
+  if (p.blk_m_tiles > 0) {
+    const int b = m_tile / p.blk_m_tiles;
+    return p.a_row0 + b * p.blk_stride + (m_tile - b * p.blk_m_tiles) * BM;
+  }
+  return p.a_row0 + m_tile * BM;
+}
+
 template <int EPI>
 struct Scheduler {
   const GemmParams& p;
@@ -280,7 +292,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t issued_parity = 0;   // parity of that load's phase
     bool ok = true;
     while (ok && src.next_producer(w, ok, wq_full, wq_empty, wq, abort_flag)) {
-      const int a_row = p.a_row0 + w.m_tile * BM;
+      const int a_row = a_row_of(p, w.m_tile);
       const int b_row = w.n_tile * BN;
       for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
         if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_EMPTY)) {
@@ -487,15 +499,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       } else if (EPI == EPI_STORE_F32) {
         const int n0 = w.n_tile * BN;
-        float* yrow = p.yout + static_cast<size_t>(row) * static_cast<size_t>(p.ld);
-        // FP8: this row's token scale
+        int srow = row;  // slot row
+        bool vslot = vrow;
+        if (p.blk_m_tiles > 0) {
+          const int blk = w.m_tile / p.blk_m_tiles;
+          const int local = (w.m_tile - blk * p.blk_m_tiles) * BM + rl;
+          srow = blk * p.blk_rows + local;
+          vslot = local < p.blk_rows;
+        }
+        float* yrow = p.yout + static_cast<size_t>(srow) * static_cast<size_t>(p.ld);
+        // FP8: this row's token scale (FP8 launches use no blocks)
         const float sxr =
-            (F8 && vrow) ? __ldg(p.x_scale + static_cast<size_t>(p.a_row0 + row) * p.x_scale_stride) : 0.f;
+            (F8 && vslot) ? __ldg(p.x_scale + static_cast<size_t>(p.a_row0 + row) * p.x_scale_stride) : 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           float v[16];
           tmem_ld16(tb + static_cast<uint32_t>(c), v);
-          if (vrow) {
+          if (vslot) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int col = n0 + c + 8 * h;

@@ -47,6 +47,13 @@ struct GemmParams {
   int stall_rowstat;        // test switch: wait for a generation nobody publishes (bounded wait runs out)
   // store-f32 epilogue
   float* yout;              // [M, ld] fp32 slot, local rows
+  // rank-major blocks of rows (store-f32 only; 0 = none): the launch's m-tiles
+  // form blocks of blk_m_tiles tiles; block b reads x rows a_row0 + b *
+  // blk_stride + local and stores slot rows b * blk_rows + local, local <
+  // blk_rows (the TP region's slot: every rank's rows of one microchunk)
+  int blk_m_tiles = 0;
+  int blk_rows = 0;
+  int blk_stride = 0;
   // split-K swap epilogue.  Each m-tile's first kb_static K-blocks are split
   // statically (stream-K over the grid); the remaining K-blocks form dyn_cpm
   // chunks of dyn_kc blocks, handed out at run time through an atomic counter.
@@ -103,6 +110,7 @@ struct NormParams {
   int row0;                     // global row of local row 0 (residual/out/y_bf16)
   int H;
   int pdl;                      // launched as a programmatic dependent of the preceding kernel
+  int out_local = 0;            // out rows are local to the launch (out + t * H), not row0 + t
   float y_scale = 1.0f;         // the addend is multiplied by this (1 = identity)
   // FP8 split-K: scale the summed partials by x_scale[(row0 + t) * stride] *
   // w_scale[h * stride] (null: no scaling)
@@ -171,6 +179,20 @@ cudaError_t launch_fp4_to_bf16(int fmt, const uint8_t* Wq, const uint8_t* S, __n
 
 enum NormSource : int { NORM_SRC_BF16 = 0, NORM_SRC_F32 = 1, NORM_SRC_SPLITK = 2 };
 cudaError_t launch_add_rmsnorm(NormSource src, const NormParams& p, int grid_cap, cudaStream_t stream);
+
+// Host helpers of the C ABI (fln_api.cu) that the TP region (fln_tp.cu) uses:
+// the thread's last-error message, argument checks, tensor maps (bf16, 128-byte
+// boxes with 128-byte swizzle), the launch counter and the library's lock.
+int api_fail(int code, const char* fmt, ...);
+int api_cuda_fail(cudaError_t e, const char* what);
+int api_check_ptr(const char* name, const void* p);
+int api_check_common(float eps, int kind, int T, int H);
+bool api_overlaps(const void* a, size_t na, const void* b, size_t nb);
+int api_make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+void api_count_launch();
+int api_device_error_word(unsigned int** word);  // the current device's workspace error word (created if needed)
+void api_lock();
+void api_unlock();
 
 // split-K bookkeeping shared by the GEMM and the reducer: the CTA whose
 // unit range [c*U/G, (c+1)*U/G) contains unit u.  32-bit arithmetic: the host

@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(NT) fln_add_rmsnorm_kernel(const NormParams p)
     __syncthreads();
     const float rstd = rsqrtf(row_total / static_cast<float>(p.H) + p.eps);
     __nv_bfloat16* rw = p.residual + grow * p.H;
-    __nv_bfloat16* ow = p.out + grow * p.H;
+    __nv_bfloat16* ow = p.out + (p.out_local ? static_cast<size_t>(t) : grow) * p.H;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       const int vi = v * NT + tid;
@@ -254,7 +254,8 @@ __global__ void __launch_bounds__(256) fln_add_rmsnorm_cluster_kernel(const Norm
 #pragma unroll
     for (int j = 0; j < 8; ++j) o[j] = r[j] * rstd * (p.norm_kind ? 1.0f + g[j] : g[j]);
     *reinterpret_cast<uint4*>(p.residual + grow * p.H + h) = f32x8_to_bf16(r);
-    __stcs(reinterpret_cast<uint4*>(p.out + grow * p.H + h), f32x8_to_bf16(o));
+    __stcs(reinterpret_cast<uint4*>(p.out + (p.out_local ? static_cast<size_t>(t) : grow) * p.H + h),
+           f32x8_to_bf16(o));
   }
 }
 

@@ -65,7 +65,8 @@ typedef enum {
   FLN_ERR_UNSUPPORTED = -2,    /* valid but outside what the kernels support (e.g. H > 32768) */
   FLN_ERR_CUDA = -3,           /* a CUDA runtime call or launch failed */
   FLN_ERR_DEVICE_TIMEOUT = -4, /* a kernel's bounded wait expired (reported by fln_device_status) */
-  FLN_ERR_NOT_TUNED = -5       /* automatic choice requested for T above the tuned token maximum */
+  FLN_ERR_NOT_TUNED = -5,      /* automatic choice requested for T above the tuned token maximum */
+  FLN_ERR_COMM = -6            /* the collective library (NCCL) is missing or a collective failed */
 } fln_status;
 
 typedef enum { FLN_NORM_STANDARD = 0, FLN_NORM_GEMMA = 1 } fln_norm_kind;
@@ -457,6 +458,78 @@ int fln_profile_read(fln_profile_stats* stats);
 int fused_proj_add_rmsnorm_noalloc(const fln_bf16* x, const fln_bf16* W, fln_bf16* residual, const float* gamma,
                                    float eps, int norm_kind, int T, int K, int H, fln_bf16* out,
                                    unsigned int* device_error, fln_stream_t stream);
+
+/*
+ * The TPSP region across P tensor-parallel ranks (vLLM "TPSP Design": section
+ * 1 "Motivation", section 3 "Microchunk pipeline", section 4 "Constraints").
+ * Each rank holds a K-shard of the projection's input and weight; the
+ * AllReduce after the row-parallel projection becomes a ReduceScatter over
+ * tokens, the residual add and norm run on the rank's token shard only, and an
+ * AllGather hands every rank the full normalised [T, H] tensor:
+ *
+ *   y_p   = x_p . W_p^T                      (this rank's partial projection, all T tokens)
+ *   y     = sum_p y_p                        (ReduceScatter: rank p receives its token shard)
+ *   r_p  += y[shard p];  o_p = RMSNorm(r_p)  (local, rank p's tokens only)
+ *   out   = AllGather(o_p)                   ([T, H] on every rank)
+ *
+ * Token partition: S = ceil(T / P) rows per rank, rank p owning tokens
+ * [p S, min((p + 1) S, T)) (the last shards are padded: their rows past T are
+ * never read or written).  A microchunk of c tokens per rank (c <= 4096) is
+ * chunk i of every shard at once: rank p's shard rows [i c, i c + n_i),
+ * n_i = min(c, S - i c).  Per chunk: the GEMM writes the partial y of every
+ * rank's rows into a rank-major fp32 slot [P, n_i, H] on the caller's stream;
+ * on the communicator's second stream the ReduceScatter (fp32 sum), the add +
+ * norm of this rank's valid rows and the AllGather (bf16) follow, and the
+ * gathered rows are written to `out` in token order; three slots guarded by
+ * events let the next chunks' GEMMs overlap.  The collectives are NCCL's,
+ * found at run time in the process (PyTorch loads it) or at the path in the
+ * environment variable FLN_NCCL_LIBRARY; without it these calls return
+ * FLN_ERR_COMM.  bf16 operands only.
+ */
+typedef struct fln_tp_comm fln_tp_comm;  /* one rank's communicator, stream, slots and events */
+
+/* Writes a 128-byte unique id (on one rank; the caller hands it to the others). */
+int fln_tp_unique_id(void* id);
+
+/* Collective over the nranks ranks (each calls it with the same id and its own
+ * rank, with its device current).  nranks = 1 may pass id = NULL (no
+ * rendezvous).  The handle belongs to the current device; free it with
+ * fln_tp_comm_destroy. */
+int fln_tp_comm_init(int nranks, int rank, const void* id, fln_tp_comm** comm);
+int fln_tp_comm_destroy(fln_tp_comm* comm);
+
+/* Host-only partition of T tokens over nranks ranks in microchunks of
+ * microchunk_tokens per rank (0 = 1024, the default; at most 4096): shard rows
+ * S, the chunk size used and the number of chunks; and, for chunk `chunk` of
+ * rank `rank`, its first token, its block rows n_i (the same on every rank)
+ * and how many of those rows are valid tokens (< T).  Needs no GPU. */
+int fln_tp_layout(int T, int nranks, int microchunk_tokens, int* shard_rows, int* chunk_tokens, int* num_chunks);
+int fln_tp_chunk_rows(int T, int nranks, int microchunk_tokens, int chunk, int rank, int* token0, int* rows,
+                      int* valid);
+
+/*
+ * fused_proj_rs_add_rmsnorm_ag -- one rank's part of the TPSP region.
+ *
+ *   x               [T, K] bf16, this rank's K-shard of the projection input (all T tokens)
+ *   W               [H, K] bf16, this rank's K-shard of the weight (F.linear layout)
+ *   residual_shard  [S, H] bf16, this rank's token shard of the residual (S = ceil(T / P));
+ *                   its valid rows are read and overwritten with r + y, rows past T untouched
+ *   gamma, eps, norm_kind   as in fused_proj_add_rmsnorm
+ *   T               tokens of the whole batch (the same on every rank)
+ *   microchunk_tokens  per rank, 0 = 1024, else 1..4096
+ *   out             [T, H] bf16, the gathered normalised tensor (every rank)
+ *   comm            this rank's handle (current device); stream: the caller's stream
+ *
+ * Every rank calls it with the same T, H and microchunk_tokens; the calls are
+ * collective.  Asynchronous on `stream`; the communicator's second stream is
+ * joined back before return.  Sequential use per communicator.  The norm is
+ * computed from the fp32 sum, as in fused_proj_add_rmsnorm.  Errors:
+ * FLN_ERR_INVALID_ARG (pointers, sizes, a communicator of another device),
+ * FLN_ERR_COMM (a collective failed), FLN_ERR_CUDA.
+ */
+int fused_proj_rs_add_rmsnorm_ag(const fln_bf16* x, const fln_bf16* W, fln_bf16* residual_shard,
+                                 const float* gamma, float eps, int norm_kind, int T, int K, int H,
+                                 int microchunk_tokens, fln_bf16* out, fln_tp_comm* comm, fln_stream_t stream);
 
 /* Test switch for failure reporting: with enable != 0, the next launch of
  * the FUSED path waits, in its exchange of row statistics, for a value that no

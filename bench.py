@@ -251,6 +251,8 @@ def run_gpu(args):
 
     fln.build()
     fln.load()
+    if args.splitk_tail >= 0:
+        fln.fln_set_splitk_tail_tokens(args.splitk_tail)
     wl = workload(args.config)
     if args.tokens:
         wl = wl.with_tokens(args.tokens)
@@ -1028,6 +1030,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the cpu_baseline sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0, help="--impl reference: CPU work of the whole run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splitk-tail", type=int, default=-1,
+                    help="UNFUSED calls of at most this many tokens reduce in the split-K GEMM's tail "
+                         "(0 = separate reducer kernel; -1 = the library's default)")
     ap.add_argument("--no-table", action="store_true",
                     help="skip the other workloads' record (run with the default workload at N = 1)")
     ap.add_argument("--transfer-tokens", type=int, default=0,

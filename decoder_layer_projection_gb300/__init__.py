@@ -48,7 +48,7 @@ EXPORTED_SYMBOLS = (
     "fln_get_plan_dtype", "fused_proj_add_rmsnorm_nvfp4", "fused_proj_add_rmsnorm_mxfp4", "fln_moe_route",
     "fused_moe_down_add_rmsnorm", "fln_moe_gather", "fused_proj_add_rmsnorm_host",
     "fln_tp_unique_id", "fln_tp_comm_init", "fln_tp_comm_destroy", "fln_tp_layout", "fln_tp_chunk_rows",
-    "fused_proj_rs_add_rmsnorm_ag",
+    "fused_proj_rs_add_rmsnorm_ag", "fln_set_splitk_tail_tokens",
 )
 
 
@@ -141,6 +141,8 @@ def load(path: str | None = None):
         lib.fln_set_plan_dtype.restype = i
         lib.fln_get_plan_dtype.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Plan)]
         lib.fln_get_plan_dtype.restype = i
+        lib.fln_set_splitk_tail_tokens.argtypes = [i]
+        lib.fln_set_splitk_tail_tokens.restype = i
         ip = ctypes.POINTER(ctypes.c_int)
         lib.fln_tp_unique_id.argtypes = [vp]
         lib.fln_tp_unique_id.restype = i
@@ -371,6 +373,11 @@ def fln_profile_read() -> dict:
 def fln_debug_stall_next_call(enable: bool = True):
     """Test switch: the next FUSED launch's bounded row-statistics wait runs out."""
     _check(load().fln_debug_stall_next_call(1 if enable else 0))
+
+
+def fln_set_splitk_tail_tokens(max_tokens: int):
+    """UNFUSED calls with at most max_tokens tokens reduce, add and normalise in the split-K GEMM's tail."""
+    _check(load().fln_set_splitk_tail_tokens(int(max_tokens)))
 
 
 def fln_version() -> int:

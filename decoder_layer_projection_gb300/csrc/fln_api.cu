@@ -106,7 +106,11 @@ struct Workspace {
   cudaStream_t stream_h2d = nullptr, stream_d2h = nullptr;
   cudaEvent_t ev_in[3] = {}, ev_done[3] = {}, ev_out[3] = {};
   cudaEvent_t ev_start = nullptr, ev_host_join = nullptr;
-  bool prepared[2][3][5] = {};     // [operand type][epilogue][tile]
+  bool prepared[2][4][5] = {};     // [operand type][epilogue][tile]
+  unsigned long long* tail_words = nullptr;  // fused split-K tail: per m-tile {gen, deliveries}, then {gen, reduced}
+  size_t tail_word_count = 0;
+  float* rowstat = nullptr;                  // fused split-K tail: per token and m-tile sums of squares
+  size_t rowstat_floats = 0;
   int pair_max[2][2][4] = {};      // resident CTA pairs of the fused pair kernel,
                                    // [operand type][4 / 8 epilogue warps][tile 128/192/224/256]
 };
@@ -124,6 +128,10 @@ std::map<GroupKey, fln_plan> g_plans;
 int g_override_chunk = 0;
 int g_override_threshold = 0;
 bool g_stall_next = false;  // test switch, see fln_debug_stall_next_call
+// UNFUSED calls up to this many tokens reduce in the split-K GEMM's tail; 0 by
+// default: on the 70B decode shapes the separate reducer launched as a
+// programmatic dependent was faster at every token count (1-256)
+int g_splitk_tail_tokens = 0;
 
 struct ProfRec {
   int kind;
@@ -343,9 +351,13 @@ int round_bn_tokens(int T) {
   return 256;
 }
 
-// T <= 256: split-K GEMM with H on the MMA's M side, then reduce + add + norm.
+// T <= 256: split-K GEMM with H on the MMA's M side, then reduce + add + norm
+// (in the GEMM's own tail, or by a separate reducer launched as its
+// programmatic dependent).
 int run_unfused(Workspace* ws, const Call& c) {
   const int bn = round_bn_tokens(c.T);
+  const bool tail = !c.w4 && c.T <= g_splitk_tail_tokens;
+  const EpilogueKind epi = tail ? EPI_SPLITK_FUSED : EPI_SPLITK_SWAP;
   int rc = FLN_OK;
   if (c.w4) {
     const int bi = bn_index(bn);
@@ -353,7 +365,7 @@ int run_unfused(Workspace* ws, const Call& c) {
       FLN_CUDA(w4_gemm_prepare(bn, c.w4_fmt), "cudaFuncSetAttribute(max dynamic shared memory)");
       ws->prepared_w4[c.w4_fmt][bi] = true;
     }
-  } else if ((rc = prepare_kernel(ws, bn, EPI_SPLITK_SWAP, c.f8))) {
+  } else if ((rc = prepare_kernel(ws, bn, epi, c.f8))) {
     return rc;
   }
   CUtensorMap tmA, tmB;
@@ -422,6 +434,34 @@ int run_unfused(Workspace* ws, const Call& c) {
   p.w4_nblk = c.w4_fmt ? c.K / 32 : c.K / 16;  // scale bytes per row
   p.err = ws->err_word;
   p.dyn_counter = ws->dyn_counter;
+  if (tail) {
+    // per m-tile delivery counts and the reduced-m-tile count, generation-tagged
+    // (zeroed once; a launch's new generation starts them from zero), and the
+    // per-token sums of squares of each m-tile
+    if ((rc = grow(&ws->tail_words, &ws->tail_word_count, static_cast<size_t>(p.num_m_tiles) + 2, true,
+                   "cudaMalloc(split-K tail counters)")) ||
+        (rc = grow(&ws->rowstat, &ws->rowstat_floats, static_cast<size_t>(c.T) * p.num_m_tiles, false,
+                   "cudaMalloc(split-K tail row sums)")))
+      return rc;
+    p.tile_arrivals = ws->tail_words;
+    p.tiles_done = ws->tail_words + p.num_m_tiles;
+    p.rowstat = ws->rowstat;
+    p.residual = c.residual;
+    p.out = c.out;
+    p.gamma = c.gamma;
+    p.eps = c.eps;
+    p.norm_kind = c.kind;
+    p.ld = c.H;
+    p.y_scale = c.y_scale;
+    set_scales(p, c);
+    if (++ws->gen == 0) ++ws->gen;
+    p.gen = ws->gen;
+    p.stall_rowstat = g_stall_next ? 1 : 0;
+    g_stall_next = false;
+    return launch_counted(FLN_KERNEL_GEMM_SPLITK, c.stream,
+                          [&] { return launch_gemm(EPI_SPLITK_FUSED, bn, c.f8, tmA, tmB, p, G, c.stream); },
+                          "split-K GEMM launch (reduce + add + norm in its tail)");
+  }
   rc = launch_counted(FLN_KERNEL_GEMM_SPLITK, c.stream,
                       [&] {
                         return c.w4 ? launch_w4_gemm_splitk(bn, c.w4_fmt, tmA, tmB, p, G, c.stream)
@@ -1614,7 +1654,13 @@ int fln_device_status(fln_stream_t stream) {
     FLN_CUDA(cudaStreamSynchronize(ws->stream_b), "cudaStreamSynchronize(internal stream)");
     unsigned int w = 0;
     FLN_CUDA(cudaMemcpy(&w, ws->err_word, sizeof w, cudaMemcpyDeviceToHost), "read device error word");
-    if (w) FLN_CUDA(cudaMemset(ws->err_word, 0, sizeof w), "clear device error word");
+    if (w) {
+      FLN_CUDA(cudaMemset(ws->err_word, 0, sizeof w), "clear device error word");
+      // a launch that gave up may have left the split-K tail's counters mid-count
+      if (ws->tail_words)
+        FLN_CUDA(cudaMemset(ws->tail_words, 0, ws->tail_word_count * sizeof(unsigned long long)),
+                 "clear split-K tail counters");
+    }
     word |= w;
   }
   // the no-allocation entry point's word in its static scratch, which
@@ -1652,6 +1698,8 @@ void fln_release_workspace(void) {
     for (int i = 0; i < 3; ++i) cudaFree(ws->slots[i]);
     cudaFree(ws->partial);
     cudaFree(ws->dyn_counter);
+    cudaFree(ws->tail_words);
+    cudaFree(ws->rowstat);
     cudaFree(ws->w4_bf16);
     cudaFree(ws->moe_y);
     cudaFree(ws->stage);
@@ -1707,6 +1755,14 @@ int fln_profile_read(fln_profile_stats* st) {
 }
 
 int fln_version(void) { return 100; }
+
+int fln_set_splitk_tail_tokens(int max_tokens) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (max_tokens < 0 || max_tokens > kMaxUnfusedTokens)
+    return fail(FLN_ERR_INVALID_ARG, "split-K tail tokens %d outside 0..%d", max_tokens, kMaxUnfusedTokens);
+  g_splitk_tail_tokens = max_tokens;
+  return FLN_OK;
+}
 
 int fln_debug_stall_next_call(int enable) {
   std::lock_guard<std::mutex> lk(g_mu);

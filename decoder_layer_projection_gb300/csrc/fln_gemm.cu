@@ -42,14 +42,16 @@ __host__ __device__ constexpr int stage_bytes(int bn) { return A_TILE_BYTES + bn
 // As many ring stages as fit in the 227 KiB a CTA may use (at most 16): the
 // decode shapes stream W from HBM and need many bytes in flight per SM.
 __host__ __device__ constexpr int stages_for(int bn) {
-  return (232448 - 512 - 1024) / stage_bytes(bn) > 16 ? 16 : (232448 - 512 - 1024) / stage_bytes(bn);
+  return (232448 - 2560) / stage_bytes(bn) > 16 ? 16 : (232448 - 2560) / stage_bytes(bn);
 }
 __host__ __device__ constexpr int tmem_cols_for(int bn) {
   return (2 * bn) <= 32 ? 32 : (2 * bn) <= 64 ? 64 : (2 * bn) <= 128 ? 128 : (2 * bn) <= 256 ? 256 : 512;
 }
+// per-token 1 / rms of the fused split-K tail (up to 256 tokens)
+constexpr int TAIL_SMEM = 1024;
 __host__ __device__ constexpr int smem_bytes_for(int bn) {
-  // ring + barriers/flags/work queue (512 B) + alignment slack for the 1024-byte swizzle base
-  return stages_for(bn) * stage_bytes(bn) + 512 + 1024;
+  // ring + barriers/flags/work queue (512 B) + tail scratch + alignment slack for the 1024-byte swizzle base
+  return stages_for(bn) * stage_bytes(bn) + 512 + TAIL_SMEM + 1024;
 }
 
 // One unit of work: an output tile and the K-block range it accumulates.
@@ -92,7 +94,7 @@ struct Scheduler {
   long long u, u_end;  // decode: stream-K unit cursor
 
   __device__ explicit Scheduler(const GemmParams& prm) : p(prm) {
-    if (EPI == EPI_SPLITK_SWAP) {
+    if (is_splitk(EPI)) {
       const long long U = p.units_total;
       u = U * blockIdx.x / gridDim.x;
       u_end = U * (blockIdx.x + 1) / gridDim.x;
@@ -104,7 +106,7 @@ struct Scheduler {
   }
 
   __device__ bool next(WorkItem& w) {
-    if (EPI == EPI_SPLITK_SWAP) {
+    if (is_splitk(EPI)) {
       // static part: units (m-tile, K-block < kb_static) in m-major order
       if (u >= u_end) return false;
       const int KB = p.kb_static;
@@ -145,7 +147,7 @@ struct WorkSource {
   int q = 0;
   __device__ explicit WorkSource(const GemmParams& prm) : sched(prm) {}
 
-  __device__ bool has_dynamic() const { return EPI == EPI_SPLITK_SWAP && sched.p.dyn_cpm > 0; }
+  __device__ bool has_dynamic() const { return is_splitk(EPI) && sched.p.dyn_cpm > 0; }
 
   // one draw; returns the chunk id or -1 past the end
   __device__ int draw() {
@@ -220,6 +222,170 @@ struct WorkSource {
   }
 };
 
+
+// ------------------------------------------------------------------ fused split-K tail
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// {gen, count} word: add one delivery for launch generation gen; returns the
+// count after it (a word left by another launch counts from zero).  Only the
+// claim of a word that holds another generation is a compare-and-swap; once
+// the word carries gen, every add is one hardware atomic (a swap loop with
+// every CTA of the grid adding at once would retry once per CTA, each retry a
+// round trip to L2).
+__device__ __forceinline__ unsigned int tagged_add_one(unsigned long long* w, unsigned int gen) {
+  unsigned long long cur = ld_relaxed_gpu_u64(w);
+  while (static_cast<unsigned int>(cur >> 32) != gen) {
+    const unsigned long long prev = atomicCAS(w, cur, (static_cast<unsigned long long>(gen) << 32) | 1ull);
+    if (prev == cur) return 1u;
+    cur = prev;  // someone else changed it: claimed it for gen (then add below) or added to it
+  }
+  return static_cast<unsigned int>(atomicAdd(w, 1ull)) + 1u;
+}
+
+// partial slots that deliver to m-tile m: the static split's CTAs, then the dynamic chunks
+__device__ __forceinline__ int splitk_static_slots(const GemmParams& p, int m) {
+  const long long KB = p.kb_static;
+  const int a = splitk_cta_of_unit(static_cast<long long>(m) * KB, p.units_total, gridDim.x);
+  const int b = splitk_cta_of_unit(static_cast<long long>(m + 1) * KB - 1, p.units_total, gridDim.x);
+  return b - a + 1;
+}
+
+// The last delivery of m-tile m (128 epilogue threads): y = sum of its slots in
+// slot order, scaled; r = r0 + y; bf16 r to the residual, fp32 r into slot 0
+// (read back by the normalisation), the m-tile's sum of squares per token to
+// rowstat[t, m].  Warp wid takes tokens wid, wid + 4, ...; a lane covers four
+// consecutive hidden indices.
+template <int F8>
+__device__ void splitk_reduce_mtile(const GemmParams& p, int m, int ep_tid) {
+  const int lane = ep_tid & 31, wid = ep_tid >> 5;
+  const int n = splitk_static_slots(p, m);
+  const int total = n + p.dyn_cpm;
+  const int h0 = m * BM + lane * 4;
+  const bool hv = h0 < p.M;  // M = H, a multiple of 8: the four columns are all valid or all not
+  float sw[4] = {1.f, 1.f, 1.f, 1.f};
+  if (F8 && hv) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sw[j] = __ldg(p.w_scale + static_cast<size_t>(h0 + j) * p.w_scale_stride);
+  }
+  const size_t tile_base = static_cast<size_t>(m) * p.slot_stride * p.N * BM;
+  const size_t slot_step = static_cast<size_t>(p.N) * BM;
+  // four tokens per warp at a time (wid, wid + 4, wid + 8, wid + 12 of each group of 16), their
+  // residual and slot loads all in flight together: one L2 round trip per four tokens
+  constexpr int U = 4;
+  for (int t0 = 0; t0 < p.N; t0 += 4 * U) {
+    int tt[U];
+    bool tv[U];
+    uint2 u[U];
+    float4 acc[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      tt[k] = t0 + wid + 4 * k;
+      tv[k] = tt[k] < p.N;
+      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      u[k] = make_uint2(0u, 0u);
+      if (tv[k] && hv) u[k] = *reinterpret_cast<const uint2*>(p.residual + static_cast<size_t>(tt[k]) * p.ld + h0);
+    }
+#pragma unroll 2
+    for (int s = 0; s < total; ++s) {
+      const int slot = s < n ? s : p.max_split + (s - n);
+      const float* src = p.partial + tile_base + slot * slot_step + lane * 4;
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        if (tv[k]) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(tt[k]) * BM));
+          acc[k].x += v.x;
+          acc[k].y += v.y;
+          acc[k].z += v.z;
+          acc[k].w += v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      if (!tv[k]) continue;  // warp-uniform
+      const int t = tt[k];
+      float ss = 0.f;
+      if (hv) {
+        float sx = p.y_scale;
+        if (F8) sx *= __ldg(p.x_scale + static_cast<size_t>(t) * p.x_scale_stride);
+        float r[4];
+        r[0] = __uint_as_float(u[k].x << 16) + acc[k].x * (sx * sw[0]);
+        r[1] = __uint_as_float(u[k].x & 0xFFFF0000u) + acc[k].y * (sx * sw[1]);
+        r[2] = __uint_as_float(u[k].y << 16) + acc[k].z * (sx * sw[2]);
+        r[3] = __uint_as_float(u[k].y & 0xFFFF0000u) + acc[k].w * (sx * sw[3]);
+        *reinterpret_cast<uint2*>(p.residual + static_cast<size_t>(t) * p.ld + h0) =
+            make_uint2(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]));
+        __stcg(reinterpret_cast<float4*>(p.partial + tile_base + static_cast<size_t>(t) * BM + lane * 4),
+               make_float4(r[0], r[1], r[2], r[3]));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ss = fmaf(r[j], r[j], ss);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) p.rowstat[static_cast<size_t>(t) * p.num_m_tiles + m] = ss;
+    }
+  }
+}
+
+// After every m-tile is reduced: this CTA's slice of the T x H outputs,
+// out = r * rstd[t] * g, vectors of eight columns; rstd from the m-tiles'
+// sums of squares of the token in a fixed order.
+__device__ void splitk_normalise_slice(const GemmParams& p, int ep_tid, float* rstd_s) {
+  const int H8 = p.M >> 3;
+  const long long V = static_cast<long long>(p.N) * H8;
+  const long long v0 = V * blockIdx.x / gridDim.x, v1 = V * (blockIdx.x + 1) / gridDim.x;
+  const int ta = static_cast<int>(v0 / H8), tb = v1 > v0 ? static_cast<int>((v1 - 1) / H8) : ta - 1;
+  const int lane = ep_tid & 31, wid = ep_tid >> 5;
+  const size_t tile_step = static_cast<size_t>(p.slot_stride) * p.N * BM;
+  // this thread's first vector: its r and gamma loads go out with the row statistics' loads
+  float4 fa = make_float4(0.f, 0.f, 0.f, 0.f), fb = fa, fg0 = fa, fg1 = fa;
+  const long long vf = v0 + ep_tid;
+  if (vf < v1) {
+    const int t = static_cast<int>(vf / H8);
+    const int h = static_cast<int>(vf - static_cast<long long>(t) * H8) * 8;
+    const float4* rp =
+        reinterpret_cast<const float4*>(p.partial + (h >> 7) * tile_step + static_cast<size_t>(t) * BM + (h & 127));
+    fa = __ldcg(rp);
+    fb = __ldcg(rp + 1);
+    fg0 = __ldg(reinterpret_cast<const float4*>(p.gamma + h));
+    fg1 = __ldg(reinterpret_cast<const float4*>(p.gamma + h + 4));
+  }
+  for (int t = ta + wid; t <= tb; t += 4) {
+    float ss = 0.f;
+    for (int m = lane; m < p.num_m_tiles; m += 32) ss += __ldcg(p.rowstat + static_cast<size_t>(t) * p.num_m_tiles + m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) rstd_s[t - ta] = rsqrtf(ss / static_cast<float>(p.M) + p.eps);
+  }
+  named_bar_sync(1, 128);
+  for (long long v = vf; v < v1; v += 128) {
+    const int t = static_cast<int>(v / H8);
+    const int h = static_cast<int>(v - static_cast<long long>(t) * H8) * 8;
+    float4 a = fa, b = fb, g0 = fg0, g1 = fg1;
+    if (v != vf) {
+      const float4* rp =
+          reinterpret_cast<const float4*>(p.partial + (h >> 7) * tile_step + static_cast<size_t>(t) * BM + (h & 127));
+      a = __ldcg(rp);
+      b = __ldcg(rp + 1);
+      g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + h));
+      g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + h + 4));
+    }
+    const float rs = rstd_s[t - ta];
+    const float r[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    float o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = r[j] * rs * (p.norm_kind ? 1.0f + g[j] : g[j]);
+    __stcs(reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * p.ld + h), f32x8_to_bf16(o));
+  }
+}
+
 template <int BN, int EPI, int F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fln_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -243,12 +409,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* epi_abort = abort_flag + 1;
   volatile int* wq = epi_abort + 1;     // 4 queued chunk ids (-1 = no more)
+  volatile int* tail_last = wq + 4;     // fused split-K tail: this delivery was the m-tile's last
+  float* tail_rstd = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full_bar) + 512);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // the split-K reducer may be scheduled right away: it waits for this grid to
   // finish before it reads anything
-  if (EPI == EPI_SPLITK_SWAP) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (is_splitk(EPI)) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -282,8 +450,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    const uint64_t pol_a = (EPI == EPI_SPLITK_SWAP) ? l2_policy_evict_first() : l2_policy_evict_normal();
-    const uint64_t pol_b = (EPI == EPI_SPLITK_SWAP) ? l2_policy_evict_last() : l2_policy_evict_last();
+    const uint64_t pol_a = is_splitk(EPI) ? l2_policy_evict_first() : l2_policy_evict_normal();
+    const uint64_t pol_b = l2_policy_evict_last();
     WorkSource<EPI> src(p);
     WorkItem w;
     int stage = 0;
@@ -556,6 +724,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
       ++local;
+      if (EPI == EPI_SPLITK_FUSED) {
+        // the partial is delivered; the m-tile's last delivery reduces the m-tile.  The CTA
+        // barrier orders every thread's partial stores before thread 0's release fence, which
+        // makes them visible before its count (and its acquire fence after the count makes the
+        // other deliveries' partials visible to the threads after the next barrier).
+        named_bar_sync(1, 128);
+        if (ep_tid == 0) {
+          fence_acq_rel_gpu();
+          const unsigned int cnt = tagged_add_one(&p.tile_arrivals[w.m_tile], p.gen);
+          fence_acq_rel_gpu();
+          const bool last = cnt == static_cast<unsigned int>(splitk_static_slots(p, w.m_tile) + p.dyn_cpm);
+          // the last delivery puts the word back to zero (a graph replay reuses the generation)
+          if (last) st_relaxed_gpu_u64(&p.tile_arrivals[w.m_tile], 0ull);
+          *tail_last = last ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        if (*tail_last) {
+          splitk_reduce_mtile<F8>(p, w.m_tile, ep_tid);
+          named_bar_sync(1, 128);
+          if (ep_tid == 0) {
+            fence_acq_rel_gpu();
+            tagged_add_one(p.tiles_done, p.gen);
+          }
+        }
+      }
+    }
+    if (EPI == EPI_SPLITK_FUSED) {
+      // every m-tile reduced (a bounded wait), then this CTA's slice of the outputs
+      bool ok = true;
+      if (ep_tid == 0) {
+        // (the test switch waits for one m-tile more than there are)
+        const unsigned long long want = (static_cast<unsigned long long>(p.gen) << 32) |
+                                        static_cast<unsigned int>(p.num_m_tiles + (p.stall_rowstat ? 1 : 0));
+        if (*abort_flag) {
+          ok = false;
+        } else if (ld_acquire_u64(p.tiles_done) != want) {
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_u64(p.tiles_done) != want) {
+            if (*abort_flag || globaltimer_ns() - t0 > FLN_WAIT_TIMEOUT_NS) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ok && !*abort_flag) {
+            atomicOr(p.err, FLN_DEVERR_TIMEOUT_ROWSTAT);
+            *abort_flag = 1;
+          }
+        }
+        if (ok && tagged_add_one(p.tiles_done + 1, p.gen) == gridDim.x) {
+          // the last CTA past the wait: every CTA has read the count, put both words back to zero
+          st_relaxed_gpu_u64(p.tiles_done, 0ull);
+          st_relaxed_gpu_u64(p.tiles_done + 1, 0ull);
+        }
+        fence_acq_rel_gpu();
+      }
+      if (!named_bar_any(1, 128, !ok)) splitk_normalise_slice(p, ep_tid, tail_rstd);
     }
   }
 
@@ -608,6 +832,7 @@ cudaError_t gemm_prepare(int bn, EpilogueKind epi, int f8) {
     switch (epi) {
       case EPI_STORE_F32: FLN_BN_SWITCH(bn, EPI_STORE_F32, 1, prepare_one)
       case EPI_SPLITK_SWAP: FLN_BN_SWITCH(bn, EPI_SPLITK_SWAP, 1, prepare_one)
+      case EPI_SPLITK_FUSED: FLN_BN_SWITCH(bn, EPI_SPLITK_FUSED, 1, prepare_one)
       default: return cudaErrorInvalidValue;
     }
   }
@@ -615,6 +840,7 @@ cudaError_t gemm_prepare(int bn, EpilogueKind epi, int f8) {
     case EPI_FUSED_NORM: FLN_BN_SWITCH(bn, EPI_FUSED_NORM, 0, prepare_one)
     case EPI_STORE_F32: FLN_BN_SWITCH(bn, EPI_STORE_F32, 0, prepare_one)
     case EPI_SPLITK_SWAP: FLN_BN_SWITCH(bn, EPI_SPLITK_SWAP, 0, prepare_one)
+    case EPI_SPLITK_FUSED: FLN_BN_SWITCH(bn, EPI_SPLITK_FUSED, 0, prepare_one)
   }
   return cudaErrorInvalidValue;
 }
@@ -636,6 +862,7 @@ cudaError_t launch_gemm(EpilogueKind epi, int bn, int f8, const CUtensorMap& tmA
     switch (epi) {
       case EPI_STORE_F32: FLN_BN_LAUNCH(bn, EPI_STORE_F32, 1)
       case EPI_SPLITK_SWAP: FLN_BN_LAUNCH(bn, EPI_SPLITK_SWAP, 1)
+      case EPI_SPLITK_FUSED: FLN_BN_LAUNCH(bn, EPI_SPLITK_FUSED, 1)
       default: return cudaErrorInvalidValue;
     }
   }
@@ -643,6 +870,7 @@ cudaError_t launch_gemm(EpilogueKind epi, int bn, int f8, const CUtensorMap& tmA
     case EPI_FUSED_NORM: FLN_BN_LAUNCH(bn, EPI_FUSED_NORM, 0)
     case EPI_STORE_F32: FLN_BN_LAUNCH(bn, EPI_STORE_F32, 0)
     case EPI_SPLITK_SWAP: FLN_BN_LAUNCH(bn, EPI_SPLITK_SWAP, 0)
+    case EPI_SPLITK_FUSED: FLN_BN_LAUNCH(bn, EPI_SPLITK_FUSED, 0)
   }
   return cudaErrorInvalidValue;
 }

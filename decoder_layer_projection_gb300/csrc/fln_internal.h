@@ -23,7 +23,16 @@ enum EpilogueKind : int {
   // partial y^T tiles (fp32) go to a partial buffer, reduced by the
   // add + norm kernel.
   EPI_SPLITK_SWAP = 2,
+  // The same split, with the reduction, residual add and norm in the GEMM's
+  // own tail: the last CTA to deliver a partial of an m-tile sums the m-tile's
+  // partial slots (fixed order), adds the residual, keeps fp32 r and each
+  // token's sum of squares over the m-tile's 128 columns; once every m-tile
+  // is reduced (a grid-wide count, bounded wait: the grid is at most one CTA
+  // per SM, so every CTA is resident while the GPU runs nothing else), each
+  // CTA normalises a slice of the [T, H] outputs.
+  EPI_SPLITK_FUSED = 3,
 };
+__host__ __device__ constexpr bool is_splitk(int epi) { return epi == EPI_SPLITK_SWAP || epi == EPI_SPLITK_FUSED; }
 
 struct GemmParams {
   int M;             // valid rows of the A operand in this launch
@@ -65,6 +74,15 @@ struct GemmParams {
   int dyn_cpm;              // dynamic chunks per m-tile (0: none)
   int dyn_kc;               // K-blocks per dynamic chunk
   unsigned int* dyn_counter;  // chunk counter: zero before and after every launch
+  // split-K with the fused tail: per m-tile {gen, deliveries} words, then
+  // tiles_done[0] = {gen, m-tiles reduced} and tiles_done[1] = {gen, CTAs past
+  // the wait} (each word is put back to zero by its last user, so graph
+  // replays start from zero), and per-token sums of squares [N, num_m_tiles]
+  // (the residual, out, gamma, eps and norm fields above hold the norm's
+  // arguments; ld = M = H)
+  unsigned long long* tile_arrivals;
+  unsigned long long* tiles_done;
+  float* rowstat;
   // FP8 (E4M3) operands: the accumulator of (token t, hidden h) is scaled by
   // x_scale[t * x_scale_stride] * w_scale[h * w_scale_stride] (stride 0: one
   // scale for the tensor); t is the global token row.  Unused for bf16.  The

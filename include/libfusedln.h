@@ -531,12 +531,28 @@ int fused_proj_rs_add_rmsnorm_ag(const fln_bf16* x, const fln_bf16* W, fln_bf16*
                                  const float* gamma, float eps, int norm_kind, int T, int K, int H,
                                  int microchunk_tokens, fln_bf16* out, fln_tp_comm* comm, fln_stream_t stream);
 
-/* Test switch for failure reporting: with enable != 0, the next launch of
- * the FUSED path waits, in its exchange of row statistics, for a value that no
+/* The UNFUSED path's split reduction (bf16 and FP8 operands): calls with at
+ * most max_tokens tokens sum the split-K partials, add the residual and
+ * normalise in the split-K GEMM's own tail (the last CTA to deliver a part of
+ * a 128-row block of W reduces that block; after a grid-wide count every CTA
+ * normalises a slice of the outputs: the grid is at most one CTA per SM, and
+ * its bounded waits report FLN_ERR_DEVICE_TIMEOUT if other work keeps CTAs
+ * from being resident together, as for the FUSED path);
+ * larger calls use a separate reduce + add + norm kernel launched as the
+ * GEMM's programmatic dependent.  0 (the default) = always the separate
+ * kernel, which measured faster on the 70B decode shapes at 1-256 tokens; at
+ * most 256.  Both give results within the parity tolerance of each other (the
+ * summation order of the row statistics differs). */
+int fln_set_splitk_tail_tokens(int max_tokens);
+
+/* Test switch for failure reporting: with enable != 0, the next launch that
+ * exchanges row statistics between CTAs (the FUSED path, the no-allocation
+ * entry point, or the UNFUSED path's split-K tail) waits for a value that no
  * CTA publishes.  That bounded wait gives up after about two seconds, the
- * kernel unwinds without writing the affected rows, and fln_device_status
- * returns FLN_ERR_DEVICE_TIMEOUT; the device stays usable.  The switch clears
- * itself after one launch.  No fault, trap or unbounded wait is involved. */
+ * kernel unwinds without writing the affected outputs, and fln_device_status
+ * returns FLN_ERR_DEVICE_TIMEOUT (and puts the tail's counters back to zero);
+ * the device stays usable.  The switch clears itself after one launch.  No
+ * fault, trap or unbounded wait is involved. */
 int fln_debug_stall_next_call(int enable);
 
 /* Library version: major * 10000 + minor * 100 + patch. */

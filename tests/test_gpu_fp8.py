@@ -146,23 +146,33 @@ def test_tensor_scale_equals_repeated_token_scale_bitwise():
 
 @pytest.mark.parametrize("wl", SMALL[:3], ids=lambda w: w.name)
 @pytest.mark.parametrize("T", [1, 7, 16, 33, 128, 256])
-def test_small_unfused_full_parity(wl, T):
+@pytest.mark.parametrize("tail", [256, 0], ids=["tail", "reducer"])
+def test_small_unfused_full_parity(wl, T, tail):
     d = make_inputs_fp8(wl, T=T)
     run = Run8(d, wl.eps, wl.norm_kind)
-    rb, ob = run(unfused())
-    check(rb, ob, d, wl, name=f"{wl.name} fp8 unfused T={T}")
+    fln.fln_set_splitk_tail_tokens(tail)
+    try:
+        rb, ob = run(unfused())
+    finally:
+        fln.fln_set_splitk_tail_tokens(0)
+    check(rb, ob, d, wl, name=f"{wl.name} fp8 unfused T={T} tail={tail}")
 
 
 @pytest.mark.parametrize("T", [1, 9, 32, 64])
-def test_unfused_dynamic_chunks(T):
+@pytest.mark.parametrize("tail", [256, 0], ids=["tail", "reducer"])
+def test_unfused_dynamic_chunks(T, tail):
     # K >= 16384: at <= 32 tokens the last fifth of each m-tile's K-blocks is drawn at run time
     wl = Workload("deep_k_fp8", T=64, K=16400, H=392, eps=1e-5, r_sigma=2.0, seed=13)
     d = make_inputs_fp8(wl, T=T)
     run = Run8(d, wl.eps, wl.norm_kind)
-    rb, ob = run(unfused())
-    check(rb, ob, d, wl, name=f"deep_k fp8 unfused T={T}")
-    rb2, ob2 = run(unfused())
-    assert np.array_equal(rb, rb2) and np.array_equal(ob, ob2)
+    fln.fln_set_splitk_tail_tokens(tail)
+    try:
+        rb, ob = run(unfused())
+        check(rb, ob, d, wl, name=f"deep_k fp8 unfused T={T} tail={tail}")
+        rb2, ob2 = run(unfused())
+        assert np.array_equal(rb, rb2) and np.array_equal(ob, ob2)
+    finally:
+        fln.fln_set_splitk_tail_tokens(0)
 
 
 def test_chunk_invariance_is_bitwise():

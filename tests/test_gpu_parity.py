@@ -88,13 +88,30 @@ def test_epilogue_width_does_not_change_the_layout_of_work():
         assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+class tail_tokens:
+    """Within the block, UNFUSED calls of at most n tokens reduce in the split-K GEMM's tail (0: the
+    separate reducer kernel for every call)."""
+
+    def __init__(self, n):
+        self.n = n
+
+    def __enter__(self):
+        fln.fln_set_splitk_tail_tokens(self.n)
+
+    def __exit__(self, *exc):
+        fln.fln_set_splitk_tail_tokens(0)
+        return False
+
+
 @pytest.mark.parametrize("wl", SMALL[:3], ids=lambda w: w.name)
 @pytest.mark.parametrize("T", [1, 7, 16, 33, 128, 256])
-def test_small_unfused_full_parity(wl, T):
+@pytest.mark.parametrize("tail", [256, 0], ids=["tail", "reducer"])
+def test_small_unfused_full_parity(wl, T, tail):
     d = make_inputs(wl, T=T)
     run = Run(d, wl.eps, wl.norm_kind)
-    rb, ob = run(UNFUSED)
-    check_rows(rb, ob, d, wl, name=f"{wl.name} unfused T={T}")
+    with tail_tokens(tail):
+        rb, ob = run(UNFUSED)
+    check_rows(rb, ob, d, wl, name=f"{wl.name} unfused T={T} tail={tail}")
 
 
 # K long enough (>= 256 K-blocks) that for <= 32 tokens the split-K GEMM hands
@@ -107,20 +124,25 @@ DEEP = [
 
 @pytest.mark.parametrize("wl", DEEP, ids=lambda w: w.name)
 @pytest.mark.parametrize("T", [1, 9, 32, 64])
-def test_unfused_dynamic_chunks_full_parity(wl, T):
+@pytest.mark.parametrize("tail", [256, 0], ids=["tail", "reducer"])
+def test_unfused_dynamic_chunks_full_parity(wl, T, tail):
     d = make_inputs(wl, T=T)
     run = Run(d, wl.eps, wl.norm_kind)
-    rb, ob = run(UNFUSED)
-    check_rows(rb, ob, d, wl, name=f"{wl.name} unfused T={T}")
-    # the chunk counter returns to zero after every launch: repeats are bitwise equal
-    for _ in range(3):
-        rb2, ob2 = run(UNFUSED)
-        assert np.array_equal(rb, rb2) and np.array_equal(ob, ob2)
+    with tail_tokens(tail):
+        rb, ob = run(UNFUSED)
+        check_rows(rb, ob, d, wl, name=f"{wl.name} unfused T={T} tail={tail}")
+        # the chunk counter (and the tail's counters) return to zero after every launch: repeats are
+        # bitwise equal
+        for _ in range(3):
+            rb2, ob2 = run(UNFUSED)
+            assert np.array_equal(rb, rb2) and np.array_equal(ob, ob2)
 
 
-def test_unfused_graph_replay_is_bitwise():
+@pytest.mark.parametrize("tail", [0, 256], ids=["reducer", "tail"])
+def test_unfused_graph_replay_is_bitwise(tail):
     """The split-K path captured in a CUDA graph and replayed gives the eager
-    result on every replay (nothing of one launch is baked into the next)."""
+    result on every replay (nothing of one launch is baked into the next: the
+    dynamic-chunk counter and the tail's counters return to zero)."""
     import torch
     from .gpu_util import dev_bf16, host_bits
     wl = DEEP[0]
@@ -130,6 +152,7 @@ def test_unfused_graph_replay_is_bitwise():
     gamma = torch.from_numpy(np.ascontiguousarray(d["gamma"], np.float32)).cuda()
     r0 = dev_bf16(d["r0"])
     fln.fln_set_plan(wl.K, wl.H, wl.norm_kind, UNFUSED)
+    fln.fln_set_splitk_tail_tokens(tail)
     try:
         r = r0.clone()
         out = torch.empty_like(r)
@@ -152,7 +175,8 @@ def test_unfused_graph_replay_is_bitwise():
             assert np.array_equal(host_bits(r), r_eager) and np.array_equal(host_bits(out), o_eager)
     finally:
         fln.fln_set_plan(wl.K, wl.H, wl.norm_kind, None)
-    check_rows(r_eager, o_eager, d, wl, name="graph replay")
+        fln.fln_set_splitk_tail_tokens(0)
+    check_rows(r_eager, o_eager, d, wl, name=f"graph replay tail={tail}")
 
 
 def test_chunk_invariance_is_bitwise():
@@ -315,8 +339,10 @@ def test_full_size_chunk_sweep_bitwise():
 def test_full_size_decode_every_row(name, T):
     wl, d, ref_r, ref_o = _full(name, T)
     run = Run(d, wl.eps, wl.norm_kind)
-    rb, ob = run(UNFUSED)
-    _check_full(rb, ob, ref_r, ref_o, f"{name} T={T} unfused")
+    for tail in (256, 0):
+        with tail_tokens(tail):
+            rb, ob = run(UNFUSED)
+        _check_full(rb, ob, ref_r, ref_o, f"{name} T={T} unfused tail={tail}")
     rb, ob = run(plan(fln.PATH_FUSED, chunk=T))
     _check_full(rb, ob, ref_r, ref_o, f"{name} T={T} fused")
 

@@ -771,6 +771,37 @@ def run_comparator(args, wl, x, W, d, gamma, device, stream, fln, flush, sx=None
 TABLE_CASES = ([("llama3_8b_down", 0), ("gemma2_9b_down", 0)] +
                [(n, t) for n in ("llama70b_oproj_decode", "llama70b_down_decode") for t in (1, 8, 32, 128, 256)])
 PATH_NAMES = {1: "FUSED", 2: "PIPELINED", 3: "UNFUSED"}
+# the extensions of the region (FP8 operands, FP4 weights, the MoE region), measured by the same code
+# as their own bench lines and summarised in the table
+EXTRA_CASES = [("llama3_8b_oproj", 0, "e4m3"), ("llama3_8b_down", 0, "e4m3"),
+               ("llama70b_oproj_decode", 8, "e4m3"), ("llama70b_down_decode", 8, "e4m3"),
+               ("llama70b_oproj_decode", 8, "nvfp4"), ("llama70b_down_decode", 8, "nvfp4"),
+               ("llama70b_oproj_decode", 8, "mxfp4"), ("llama70b_down_decode", 8, "mxfp4"),
+               ("mixtral_8x7b_down_decode", 0, "moe"), ("mixtral_8x7b_down", 0, "moe")]
+
+
+def summarize_line(line):
+    """The figures of a workload's own bench line that the table keeps."""
+    c, rf = line["config"], line["roofline"]
+    comp = line.get("comparator_unfused_cublas") or {}
+    out = {"workload": c["workload"], "T": c["T"], "K": c["K"], "H": c["H"], "operands": c.get("operands", "bf16"),
+           "ms_per_step": line["ms_per_step"], "tflops": line["value"], "tokens_per_s": line["tokens_per_s"],
+           "step_roofline_frac": line["step_roofline_frac"], "kernel": rf["kernel"],
+           "kernel_ms_per_launch": rf["kernel_ms_per_launch"], "kernel_timing": rf["measured"],
+           "roofline": {k: rf[k] for k in ("bound", "achieved", "unit", "frac", "traffic", "peak_source")},
+           "kernel_time_ms": line["kernel_time_ms"], "e2e_tflops": line["e2e"]["value"],
+           "gpu_launches_per_step": line["gpu_launches"] / line["steps"]}
+    if "plan" in line:
+        out["plan"] = {k: line["plan"][k] for k in ("path", "microchunk_tokens", "tile_n", "gemm_ctas",
+                                                     "threshold_tokens", "epi_warps")}
+    if "experts" in c:
+        out.update(experts=c["experts"], top_k=c["top_k"], experts_used=rf.get("experts_used"))
+    if "ms_per_step" in comp:
+        out["comparator_unfused_cublas"] = {"ms_per_step": comp["ms_per_step"], "tflops": comp["value"]}
+        out["speedup_vs_comparator"] = round(comp["ms_per_step"] / line["ms_per_step"], 4)
+    else:
+        out["comparator_unfused_cublas"] = comp
+    return out
 
 
 def kernel_roofline(kname, wl, T_launch, ms, peaks):
@@ -897,12 +928,21 @@ def run_table(args, fln, device, stream, flush, peaks):
         })
         del x, W, r, out, r2, out2, y
         torch.cuda.empty_cache()
+    for name, T, dtype in EXTRA_CASES:
+        import argparse
+        sub = argparse.Namespace(**vars(args))
+        sub.config, sub.tokens, sub.dtype = name, T, dtype
+        sub.no_cpu_baseline, sub.no_table, sub.plan, sub.microchunk = True, True, "auto", 0
+        rows.append(summarize_line(run_gpu_moe(sub) if dtype == "moe" else run_gpu(sub)))
+        torch.cuda.empty_cache()
     sampler.mark_end()
     clocks = sampler.stop()
     return {"cases": rows, "clocks": clocks, "wall_s": round(time.time() - t_start, 1),
-            "what": "each case with its tuned plan (decode groups profiled up to 256 tokens), the same timing "
-                    "and L2 flush as the headline; roofline of the dominant kernel: the slower of its FLOPs "
-                    "at the tensor peak and its algorithmic bytes at the HBM bandwidth (measured peaks)"}
+            "what": "bf16 cases: each with its tuned plan (decode groups profiled up to 256 tokens), the same "
+                    "timing and L2 flush as the headline; roofline of the dominant kernel: the slower of its "
+                    "FLOPs at the tensor peak and its algorithmic bytes at the HBM bandwidth (measured peaks). "
+                    "FP8, FP4 and MoE cases: the figures of each one's own bench line (bench.py --config C "
+                    "--dtype D), run in this process"}
 
 
 # ------------------------------------------------------------------ CPU oracle

@@ -76,7 +76,7 @@ typedef enum { FLN_NORM_STANDARD = 0, FLN_NORM_GEMMA = 1 } fln_norm_kind;
  *   FUSED      one persistent tcgen05 GEMM whose epilogue does the residual
  *              add, the full-row sum of squares (combined across the row's
  *              N-tiles through global partial sums) and the norm.  Microchunks
- *              run back to back inside one launch of up to 4096 tokens (as
+ *              run back to back inside one launch of up to 16384 tokens (as
  *              many whole chunks as fit; tiles in row-block order, so one
  *              chunk's add + norm overlaps the next chunk's GEMM on other
  *              CTA pairs).  From 128 K-blocks (K >= 8192 bf16, 16384 E4M3)

@@ -101,9 +101,11 @@ def test_every_tile_is_covered_once_and_every_launch_completes():
     assert n_split > 100   # the grid exercises the split often
 
 
-@pytest.mark.parametrize("rb,nt,cap", [(8, 16, 76), (16, 16, 72), (3, 4, 16), (3, 4, 20)])
+@pytest.mark.parametrize("rb,nt,cap", [(32, 16, 76), (32, 16, 72), (32, 16, 64), (16, 16, 76), (8, 19, 76),
+                                        (64, 2, 64), (3, 4, 16), (3, 4, 20)])
 def test_launch_shapes_of_the_workloads(rb, nt, cap):
-    # Llama-3-8B down_proj (4096-token launches, 256-wide tiles on 76 pairs) and others
+    # Llama-3-8B down_proj (one 8192-token launch, 256-wide tiles on 76, 72 or 64 pairs), o_proj (4096
+    # tokens), Gemma-2-9B (192-wide tiles), the 16384-token launch of the split test, and others
     tiles, S, pairs = plan(rb, nt, cap)
     assert covers_exactly_once(tiles, S, pairs)
     assert runs_to_completion(tiles, nt, S, pairs)

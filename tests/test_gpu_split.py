@@ -92,20 +92,20 @@ def test_split_with_small_microchunks():
     _check(rb, ob, d, WL, "split chunks of 256")
 
 
-WL_LONG = Workload("split_long", T=4100, K=8192, H=256, eps=1e-5, r_sigma=2.0, seed=35)
+WL_LONG = Workload("split_long", T=16388, K=8192, H=256, eps=1e-5, r_sigma=2.0, seed=35)
 
 
 def test_split_in_every_launch_of_a_long_call():
-    """4100 tokens: a launch of 4096 (16 row blocks x 2 N-tiles, all split on 32 pairs of 64) and a tail
+    """16388 tokens: a launch of 16384 (64 row-pair blocks x 2 N-tiles on 64 pairs, no split) and a tail
     launch of 4 tokens (2 tiles, split), for chunks of 4096, 1024 and 256 alike (whole chunks are grouped
-    up to 4096 tokens a launch).  Rows on both sides of the launch boundary against the oracle; the
-    chunkings agree bit for bit; rows past the call stay unwritten (Run's guard rows)."""
+    up to 16384 tokens a launch).  Every row against the oracle; the chunkings agree bit for bit; rows
+    past the call stay unwritten (Run's guard rows)."""
     d = make_inputs(WL_LONG)
     run = Run(d, WL_LONG.eps, WL_LONG.norm_kind)
     res = [run(plan(fln.PATH_FUSED, chunk=c, tile_n=128, gemm_ctas=128)) for c in (4096, 1024, 256)]
     for rb, ob in res[1:]:
         assert np.array_equal(rb, res[0][0]) and np.array_equal(ob, res[0][1])
-    rows = np.array(sorted(set([0, 1, 127, 128, 255, 256, 2047, 2048] + list(range(4088, 4100)))))
+    rows = np.arange(WL_LONG.T)
     r, o, _ = oracle.proj_add_rmsnorm(d["x"], d["W"], d["r0"], d["gamma"], WL_LONG.eps, WL_LONG.norm_kind,
                                       rows=rows)
     compare(res[0][0][rows], r, "two launches residual")

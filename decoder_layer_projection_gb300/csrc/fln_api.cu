@@ -39,6 +39,7 @@ namespace {
 
 constexpr int kMaxMicrochunk = 4096;   // per-call chunk cap ("TPSP Design", section 4)
 constexpr int kSplitMinKBlocks = 128;   // fused pair kernel: K-blocks from which a last round is split
+constexpr int kSplitMinKBlocksTwoGroups = 32;  // the same with eight epilogue warps (two groups)
 // FUSED: whole microchunks run back to back in one launch of at most this many
 // tokens (the microchunk itself stays <= 4096).  One launch of 8192 tokens of
 // the Llama-3-8B down projection instead of two of 4096: 560 -> 526 us (one
@@ -555,7 +556,10 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
   // K-block mainloop's time at BN = 256) plus the hand-off; measured on
   // 4096-token chunks at 152 CTAs: K = 4096 (64 K-blocks) 108 -> 116 us,
   // K = 14336 (224 K-blocks) 636 -> 582 us.
-  const bool may_split = ew == 4 && c.k_blocks() >= kSplitMinKBlocks;
+  // With eight epilogue warps the helper's half never waits behind its pair's
+  // previous tile (the other group holds that one), so shorter K loops split
+  // too, and the round before needs no guard.
+  const bool may_split = c.k_blocks() >= (ew == 8 ? kSplitMinKBlocksTwoGroups : kSplitMinKBlocks);
   if (may_split) {
     // split halves of at most cap / 2 tiles: fp32 128 x bn per CTA, four flag words per CTA
     if ((rc = grow(&ws->split_buf, &ws->split_floats, static_cast<size_t>(cap) * 128 * bn, false,
@@ -605,7 +609,7 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
     // last x pairs of the round before.
     const long long rem = tiles % cap;
     const long long x = (tiles - rem) % nt;
-    p.split_tiles = (may_split && rem > 0 && 2 * rem + x <= cap) ? static_cast<int>(rem) : 0;
+    p.split_tiles = (may_split && rem > 0 && 2 * rem + (ew == 8 ? 0 : x) <= cap) ? static_cast<int>(rem) : 0;
     p.split_buf = ws->split_buf;
     p.split_flags = ws->split_flags;
     const int pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, tiles + p.split_tiles)));

@@ -31,6 +31,9 @@
 // stores), the second half's pair writes its fp32 accumulator to global
 // memory (L2) and announces it with a {launch generation, 1} word per lane
 // quarter; the owner adds it to its own accumulator before the residual.
+// With two epilogue groups the helper's half goes out before the helper
+// takes the output-staging token, so it never waits for its pair's previous
+// tile (the host then needs no guard on the round before).
 //
 // FP8 (E4M3) operands: the same kernel with kind::f8f6f4 MMAs over 128-byte
 // K-blocks of 128 elements; phase 1 scales the accumulator by the token's and
@@ -166,9 +169,7 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
   const int nN = p.num_n_tiles;
   const int num_pm = (p.num_m_tiles + 1) / 2;
   const int total = num_pm * nN;
-  // split tiles only with one epilogue group (the two groups' staging hand-off
-  // assumes every unit stores)
-  const int S = EW == 4 ? p.split_tiles : 0;
+  const int S = p.split_tiles;
   const int units = total + S;
   const int KB = p.num_k_blocks;
 
@@ -404,6 +405,19 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
         __threadfence();
         __syncwarp();
         if (lane == 0) st_release_gpu_u64(p.split_flags + split_slot * 4 + q, tag | 1ull);
+        if (NG == 2) {
+          // two groups: hand the quarter's output staging on in unit order (this unit stores
+          // nothing).  Taken only after the half is out, so the owner never waits for this
+          // pair's previous tile, whose norm may need that very half.
+          bool okh = true;
+          if (lane == 0) {
+            if (local >= 1)
+              okh = mbar_wait(&stg_done[q], static_cast<uint32_t>(local - 1) & 1u, abort_flag, p.err,
+                              FLN_DEVERR_TIMEOUT_ACC);
+            if (okh) mbar_arrive(&stg_done[q]);
+          }
+          if (!__shfl_sync(0xffffffffu, okh ? 1 : 0, 0)) failed = true;
+        }
         continue;
       }
 

@@ -79,10 +79,10 @@ typedef enum { FLN_NORM_STANDARD = 0, FLN_NORM_GEMMA = 1 } fln_norm_kind;
  *              run back to back inside one launch of up to 16384 tokens (as
  *              many whole chunks as fit; tiles in row-block order, so one
  *              chunk's add + norm overlaps the next chunk's GEMM on other
- *              CTA pairs).  From 128 K-blocks (K >= 8192 bf16, 16384 E4M3)
- *              a last round of tiles that would leave half of the CTA pairs
- *              idle is split into K-halves on two pairs (fp32 halves added
- *              in a fixed order).  A row wider than the grid has CTA pairs (N-tiles >
+ *              CTA pairs).  From 128 K-blocks (K >= 8192 bf16, 16384 E4M3;
+ *              32 K-blocks with eight epilogue warps) a last round of tiles
+ *              that would leave half of the CTA pairs idle is split into
+ *              K-halves on two pairs (fp32 halves added in a fixed order).  A row wider than the grid has CTA pairs (N-tiles >
  *              pairs) runs the PIPELINED path instead.
  *   PIPELINED  per microchunk, the GEMM writes y (fp32) into one of three
  *              reusable slots on the caller's stream; the add + norm of that

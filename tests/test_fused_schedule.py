@@ -120,3 +120,99 @@ def test_the_rule_keeps_pairs_from_waiting_on_work_behind_them():
     for rb, nt, cap in stalls:
         tiles, S, pairs = plan(rb, nt, cap)
         assert runs_to_completion(tiles, nt, S, pairs)
+
+
+# ---------------------------------------------------------------- two epilogue groups
+# With eight epilogue warps a pair's k-th unit goes to group k % 2 and to TMEM buffer k % 2: its MMAs
+# start once the pair's previous unit's MMAs are done and unit k - 2 has released the buffer (its
+# epilogue is complete); a group works through its own units in order; a whole or owner unit publishes
+# its row sums (an owner only once its helper's half is out), waits for its row block, then takes the
+# quarter's output staging from unit k - 1 and hands it on; a helper unit publishes its half as soon as
+# its MMAs are done and its group is free, and only then takes and hands on the staging.  So a helper
+# never waits for its pair's previous tile, and the split needs no guard on whole tiles.
+def split_tiles_two_groups(tiles, nt, cap):
+    rem = tiles % cap
+    return rem if (rem > 0 and 2 * rem <= cap) else 0
+
+
+def runs_to_completion_two_groups(tiles, nt, S, pairs, helper_token_first=False):
+    queues = [[unit_at(u, tiles, S, 2) for u in range(p, tiles + S, pairs)] for p in range(pairs)]
+    mma = [[False] * len(q) for q in queues]
+    done = [[False] * len(q) for q in queues]        # epilogue complete: buffer released, staging handed on
+    phase1 = [[False] * len(q) for q in queues]
+    published = [False] * tiles
+    helper_out = [False] * tiles
+    while True:
+        moved = False
+        for p, q in enumerate(queues):
+            for k, (role, t, _, _) in enumerate(q):
+                if not mma[p][k] and (k == 0 or mma[p][k - 1]) and (k < 2 or done[p][k - 2]):
+                    mma[p][k] = moved = True
+                group_free = mma[p][k] and (k < 2 or done[p][k - 2])
+                if not group_free or done[p][k]:
+                    continue
+                token = k == 0 or done[p][k - 1]
+                if role == "helper":
+                    if helper_token_first:
+                        if token:
+                            helper_out[t] = done[p][k] = moved = True
+                        continue
+                    if not helper_out[t]:
+                        helper_out[t] = moved = True
+                    if token:
+                        done[p][k] = moved = True
+                    continue
+                if not phase1[p][k] and (role == "whole" or helper_out[t]):
+                    phase1[p][k] = published[t] = moved = True
+                rb = t // nt
+                if phase1[p][k] and token and all(published[rb * nt + n] for n in range(nt)):
+                    done[p][k] = moved = True
+        if all(all(d) for d in done):
+            return True
+        if not moved:
+            return False
+
+
+def test_two_groups_split_every_tile_covered_once_and_every_launch_completes():
+    n_split = 0
+    for rb, nt, cap in GRID:
+        tiles = rb * nt
+        S = split_tiles_two_groups(tiles, nt, cap)
+        pairs = max(1, min(cap, tiles + S))
+        n_split += S > 0
+        assert covers_exactly_once(tiles, S, pairs), (rb, nt, cap)
+        assert runs_to_completion_two_groups(tiles, nt, S, pairs), (rb, nt, cap)
+        assert runs_to_completion_two_groups(tiles, nt, 0, max(1, min(cap, tiles))), (rb, nt, cap)
+    assert n_split > 200
+
+
+@pytest.mark.parametrize("rb,nt,cap,splits", [(16, 16, 76, True), (8, 14, 76, True), (8, 16, 76, False),
+                                               (32, 16, 76, False), (16, 16, 72, False)])
+def test_two_groups_split_on_the_workloads(rb, nt, cap, splits):
+    # o_proj 4096^3 on 76 pairs (28 split tiles), Gemma-2-9B with 256-wide (36 split tiles) and 224-wide
+    # tiles, down_proj; a last round with more than half of the pairs busy is not split
+    tiles = rb * nt
+    S = split_tiles_two_groups(tiles, nt, cap)
+    assert (S > 0) == splits
+    assert runs_to_completion_two_groups(tiles, nt, S, min(cap, tiles + S))
+
+
+def test_one_group_split_without_the_guard_stalls_where_two_groups_do_not():
+    # the shapes where the one-group kernel needs the guard are safe with two groups
+    stalls = [(rb, nt, cap) for rb, nt, cap in GRID
+              if not runs_to_completion(*(lambda t, s, p: (t, nt, s, p))(*plan(rb, nt, cap, guard=False)))]
+    assert stalls
+    for rb, nt, cap in stalls:
+        tiles = rb * nt
+        S = split_tiles(tiles, nt, cap, guard=False)
+        assert runs_to_completion_two_groups(tiles, nt, S, max(1, min(cap, tiles + S)))
+
+
+def test_a_helper_that_takes_the_staging_first_can_stall():
+    # the order matters: a helper that waited for the output staging before publishing its half would
+    # wait for its pair's previous tile, whose norm may need that very half
+    stalls = [(rb, nt, cap) for rb, nt, cap in GRID
+              if split_tiles_two_groups(rb * nt, nt, cap) and not runs_to_completion_two_groups(
+                  rb * nt, nt, split_tiles_two_groups(rb * nt, nt, cap),
+                  max(1, min(cap, rb * nt + split_tiles_two_groups(rb * nt, nt, cap))), helper_token_first=True)]
+    assert len(stalls) > 100

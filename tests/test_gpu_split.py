@@ -1,8 +1,9 @@
 """GPU parity of the fused pair kernel's split last round, through the C ABI.
 
 When the last round of a launch's tiles would leave at least half of the
-CTA pairs idle and K spans at least 128 K-blocks, each of its tiles is
-computed as two halves of its K-blocks on two pairs; the second half's fp32
+CTA pairs idle and K spans at least 128 K-blocks (32 with eight epilogue
+warps), each of its tiles is computed as two halves of its K-blocks on two
+pairs; the second half's fp32
 accumulator reaches the tile's owner through global memory.  These cases make that happen on purpose (every tile split, a
 tail of tiles split after whole rounds, an odd number of K-blocks, ragged H,
 microchunks, FP8 operands) and hold the result to the same bar as every other
@@ -92,6 +93,41 @@ def test_split_with_small_microchunks():
     _check(rb, ob, d, WL, "split chunks of 256")
 
 
+# Eight epilogue warps (two groups on alternate tiles): a helper's half goes out before it takes the
+# output staging, so the split runs from 32 K-blocks and with no guard on the round before.
+WL8 = Workload("split_two_groups", T=520, K=2048, H=512, eps=1e-5, r_sigma=2.0, seed=36)
+WL8_GUARD = Workload("split_two_groups_guard", T=700, K=2048, H=2048, norm_kind=1, eps=1e-6, gamma_mode="plain",
+                     seed=37)
+
+
+# (workload, tile, CTA target): WL8 has 3 x 2 tiles (256) or 3 x 3 (224): all split on the full grid; on 8
+# CTAs (4 pairs) 4 whole tiles then 2 split.  WL8_GUARD: 3 x 8 tiles on 10 pairs, 20 whole then 4 split,
+# with 4 whole tiles of the split row block in the round before (the one-group kernel would not split).
+@pytest.mark.parametrize("wl,tile,ctas", [(WL8, 256, 0), (WL8, 224, 0), (WL8, 256, 8), (WL8_GUARD, 256, 20)],
+                         ids=["256-all", "224-all", "256-tail", "guard"])
+def test_two_group_split_full_parity(wl, tile, ctas):
+    d = make_inputs(wl)
+    run = Run(d, wl.eps, wl.norm_kind)
+    rb, ob = run(plan(fln.PATH_FUSED, chunk=1024, tile_n=tile, gemm_ctas=ctas, epi_warps=8))
+    _check(rb, ob, d, wl, f"two-group split tile={tile} ctas={ctas}")
+    rb2, ob2 = run(plan(fln.PATH_FUSED, chunk=1024, tile_n=tile, gemm_ctas=ctas, epi_warps=8))
+    assert np.array_equal(rb, rb2) and np.array_equal(ob, ob2)
+    # four epilogue warps do not split at 32 K-blocks: the same bar, other rounding on the split tiles
+    w4 = run(plan(fln.PATH_FUSED, chunk=1024, tile_n=tile, gemm_ctas=ctas, epi_warps=4))
+    _check(*w4, d, wl, f"one group tile={tile} ctas={ctas}")
+    assert not np.array_equal(rb, w4[0])
+
+
+def test_two_group_split_with_microchunks_and_repeats():
+    # chunks of 128 tokens grouped in one launch; repeated calls agree bit for bit (generation-tagged halves)
+    d = make_inputs(WL8)
+    run = Run(d, WL8.eps, WL8.norm_kind)
+    res = [run(plan(fln.PATH_FUSED, chunk=c, tile_n=256, epi_warps=8)) for c in (128, 520, 128)]
+    for rb, ob in res[1:]:
+        assert np.array_equal(rb, res[0][0]) and np.array_equal(ob, res[0][1])
+    _check(*res[0], d, WL8, "two-group split, chunks of 128")
+
+
 WL_LONG = Workload("split_long", T=16388, K=8192, H=256, eps=1e-5, r_sigma=2.0, seed=35)
 
 
@@ -112,7 +148,8 @@ def test_split_in_every_launch_of_a_long_call():
     compare(res[0][1][rows], o, "two launches out")
 
 
-def test_split_fp8():
+@pytest.mark.parametrize("tile,ew", [(128, 4), (256, 8)])
+def test_split_fp8(tile, ew):
     torch = pytest.importorskip("torch")
     from .gpu_util import dev_bf16, host_bits
     # E4M3 K-blocks hold 128 elements: K = 16384 is 128 of them
@@ -124,8 +161,8 @@ def test_split_fp8():
     sx = torch.from_numpy(np.ascontiguousarray(d["x_scale"])).cuda()
     sw = torch.from_numpy(np.ascontiguousarray(d["w_scale"])).cuda()
     gamma = torch.from_numpy(np.ascontiguousarray(d["gamma"], np.float32)).cuda()
-    # four epilogue warps (eight would keep every tile whole)
-    fln.fln_set_plan(K, H, wl.norm_kind, plan(fln.PATH_FUSED, chunk=300, tile_n=128, epi_warps=4),
+    # one epilogue group from 128 K-blocks, two groups from 32: both split every tile here
+    fln.fln_set_plan(K, H, wl.norm_kind, plan(fln.PATH_FUSED, chunk=300, tile_n=tile, epi_warps=ew),
                      dtype=fln.DTYPE_E4M3)
     try:
         r = dev_bf16(d["r0"])
@@ -136,8 +173,8 @@ def test_split_fp8():
         fln.fln_set_plan(K, H, wl.norm_kind, None, dtype=fln.DTYPE_E4M3)
     ro, oo, _ = oracle.proj_add_rmsnorm_fp8(d["x8"], d["x_scale"], d["W8"], d["w_scale"], d["r0"], d["gamma"],
                                             wl.eps, wl.norm_kind)
-    compare(host_bits(r), ro, "split fp8 residual")
-    compare(host_bits(out), oo, "split fp8 out")
+    compare(host_bits(r), ro, f"split fp8 tile={tile} ew={ew} residual")
+    compare(host_bits(out), oo, f"split fp8 tile={tile} ew={ew} out")
 
 
 @pytest.mark.parametrize("tile", [128, 224])

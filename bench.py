@@ -47,9 +47,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes per launch of the dominant kernel, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum, one launch, -s 5 -c 1),
-# keyed by workload, tokens, kernel, plan tile width and the sha1 of the
-# kernel sources the capture was taken on; reported as null when the sources
-# have changed since.  Captures: profiles/ (same commands).
+# keyed by workload, tokens, kernel, plan tile width (0 for the split-K
+# kernels, whose tile follows the token count) and the sha1 of the kernel
+# sources the capture was taken on; reported as null when the sources have
+# changed since.  Captures: profiles/ (same commands).
 class L2Flush:
     """Evicts the step's operands from L2 between timed steps.
 
@@ -89,22 +90,22 @@ def kernel_sources_hash(dtype, kernel):
 
 
 NCU_TRAFFIC = {
-    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "dad09e7e8342"): 108679168 + 32381952,
-    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 224, "dad09e7e8342"): 112590336 + 37060864,
-    ("llama3_8b_down", 8192, "bf16", "gemm_fused", 256, "dad09e7e8342"): 645383680 + 57627904,
-    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 192, "dad09e7e8342"): 278785024 + 17946368,
-    ("llama3_8b_oproj", 4096, "e4m3", "gemm_fused", 224, "dad09e7e8342"): 67497728 + 17090304,
-    ("llama70b_down_decode", 8, "e4m3", "gemm_splitk", 256, "9658cd6e0d51"): 236315392 + 3085312,
-    ("llama70b_oproj_decode", 8, "e4m3", "gemm_splitk", 256, "9658cd6e0d51"): 67211776 + 167424,
-    ("llama70b_down_decode", 8, "bf16", "gemm_splitk", 256, "9658cd6e0d51"): 471424256 + 3233792,
-    ("llama70b_oproj_decode", 8, "bf16", "gemm_splitk", 256, "9658cd6e0d51"): 135537920 + 2888192,
-    ("llama70b_down_decode", 8, "nvfp4", "gemm_splitk", 256, "75d05af169d4"): 135886080 + 2963712,
-    ("llama70b_oproj_decode", 8, "nvfp4", "gemm_splitk", 256, "75d05af169d4"): 37937152 + 0,
-    ("llama70b_down_decode", 8, "mxfp4", "gemm_splitk", 256, "75d05af169d4"): 128547072 + 2881536,
-    ("llama70b_oproj_decode", 8, "mxfp4", "gemm_splitk", 256, "75d05af169d4"): 35841280 + 0,
+    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "31c03f66903d"): 108776960 + 32363776,
+    ("llama3_8b_down", 8192, "bf16", "gemm_fused", 256, "31c03f66903d"): 1248116224 + 122408448,
+    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 256, "31c03f66903d"): 286641152 + 22163456,
+    ("llama70b_down_decode", 8, "bf16", "gemm_splitk", 0, "abf134257120"): 471433472 + 3321856,
+    ("llama70b_oproj_decode", 8, "bf16", "gemm_splitk", 0, "abf134257120"): 135542016 + 3136256,
+    ("llama70b_down_decode", 8, "nvfp4", "gemm_splitk", 0, "75d05af169d4"): 135886080 + 2963712,
+    ("llama70b_oproj_decode", 8, "nvfp4", "gemm_splitk", 0, "75d05af169d4"): 37937152 + 0,
+    ("llama70b_down_decode", 8, "mxfp4", "gemm_splitk", 0, "75d05af169d4"): 128547072 + 2881536,
+    ("llama70b_oproj_decode", 8, "mxfp4", "gemm_splitk", 0, "75d05af169d4"): 35841280 + 0,
     ("mixtral_8x7b_down_decode", 8, "moe", "moe_gemm", 256, "ea0f5d1ffc77"): 822708224 + 2672640,
     ("mixtral_8x7b_down", 4096, "moe", "moe_gemm", 256, "ea0f5d1ffc77"): 1323357952 + 135113472,
 }
+def traffic_tile(kname, plan):
+    return plan["tile_n"] if kname in ("gemm_fused", "gemm_slot") else 0
+
+
 # FP8 (E4M3) dense peak: the measured bf16 peak times NVIDIA's nominal dense
 # FP8 / BF16 ratio (4.5 / 2.25 PFLOP/s); no FP8 GEMM peak is measured
 FP8_OVER_BF16 = 2.0
@@ -396,7 +397,7 @@ def run_gpu(args):
         achieved = (tokens_per_launch * H * 6.0 + 4.0 * H) / (avg_launch_ms * 1e-3) / 1e9
         bound, unit, peak = "hbm", "GB/s", peaks["hbm_gbs"]
     src_hash = kernel_sources_hash(args.dtype, kname)
-    traffic = NCU_TRAFFIC.get((args.config, T, args.dtype, kname, plan["tile_n"], src_hash))
+    traffic = NCU_TRAFFIC.get((args.config, T, args.dtype, kname, traffic_tile(kname, plan), src_hash))
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
                 "kernel": kname,
@@ -895,7 +896,7 @@ def run_table(args, fln, device, stream, flush, peaks):
         bound, achieved, unit, kfrac = kernel_roofline(kname, wl, T / lps, kms, peaks)
         t_roof = max(wl.flops() / (peaks["bf16_tflops"] * 1e12), wl.algorithmic_bytes(2) / (peaks["hbm_gbs"] * 1e9))
         src_hash = kernel_sources_hash("bf16", kname)
-        traffic = NCU_TRAFFIC.get((name, T, "bf16", kname, plan["tile_n"], src_hash))
+        traffic = NCU_TRAFFIC.get((name, T, "bf16", kname, traffic_tile(kname, plan), src_hash))
         # comparator: cuBLAS GEMM (bf16 out) then add_rmsnorm, same flush, same timing
         r2 = up(d["r0"])
         out2 = torch.empty_like(out)

@@ -6,7 +6,7 @@
   (K and H tails, experts without rows, one expert, k = 1..4), the same bar
   as the dense paths (tests/parity.py), guard rows after T untouched;
 * routing then the region chained on the device;
-* the Mixtral-8x7B down shape at decode and at 512 tokens on sampled rows;
+* the Mixtral-8x7B down shape at decode, 512 and 4096 tokens, every row;
 * argument checks.
 """
 import numpy as np
@@ -145,23 +145,15 @@ def test_route_then_region_on_device():
     compare(host_bits(out), oo, "chained out")
 
 
-@pytest.mark.parametrize("name,T", [("mixtral_8x7b_down_decode", 8), ("mixtral_8x7b_down", 512)])
-def test_full_size_sampled_rows(name, T):
+@pytest.mark.parametrize("name,T", [("mixtral_8x7b_down_decode", 8), ("mixtral_8x7b_down", 512),
+                                    ("mixtral_8x7b_down", 4096)])
+def test_full_size_every_row(name, T):
+    # every token of the Mixtral-8x7B down region against the oracle (4096 tokens: the bench workload)
     wl, E, k = MOE_CONFIGS[name]
     d = make_inputs_moe(wl, E, k, T=T)
     run = RunMoe(d, E, wl.eps, wl.norm_kind)
     rb, ob = run()
-    rows = sorted({0, 1, T // 2, T - 1} | set(np.random.default_rng(T).choice(T, size=min(4, T), replace=False).tolist()))
-    sel = np.array(rows, np.int64)
-    # the oracle on the sampled tokens alone: their (token, slot) rows regrouped; each token's result
-    # depends only on its own rows, gates and residual
-    ids_s = d["ids"][sel]
-    off_s, tok_s, slot_s, row_of_s = oracle.moe_permute(ids_s, E)
-    hg_s = d["hg"][run.row_of[sel[tok_s], slot_s]]
-    r, o, _ = oracle.moe_down_region(hg_s, off_s, row_of_s, d["wt"][sel], d["We"], d["r0"][sel], d["gamma"], wl.eps,
-                                     wl.norm_kind)
-    compare(rb[sel], r, f"{name} T={T} residual")
-    compare(ob[sel], o, f"{name} T={T} out")
+    run.check(rb, ob, f"{name} T={T}")
 
 
 def test_rejects_bad_arguments():

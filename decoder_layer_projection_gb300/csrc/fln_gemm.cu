@@ -223,6 +223,10 @@ struct WorkSource {
 };
 
 
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ------------------------------------------------------------------ fused split-K tail
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
@@ -443,10 +447,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(tmem_holder, TMEM_COLS);
     tmem_relinquish();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_holder;
+  // The producer lane initialised the barriers itself and needs no tensor
+  // memory, so warp 0 only arrives at the start barrier and streams at once;
+  // the other warps wait there for the barriers and the TMEM address.
+  if (warp == 0) {
+    __syncwarp();
+    named_bar_arrive(2, NUM_THREADS);
+  } else {
+    tc_fence_before();
+    named_bar_sync(2, NUM_THREADS);
+    tc_fence_after();
+  }
+  const uint32_t tmem_base = warp == 0 ? 0u : *tmem_holder;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer

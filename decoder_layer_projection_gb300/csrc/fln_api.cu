@@ -117,8 +117,8 @@ struct Workspace {
   size_t tail_word_count = 0;
   float* rowstat = nullptr;                  // fused split-K tail: per token and m-tile sums of squares
   size_t rowstat_floats = 0;
-  int pair_max[2][2][4] = {};      // resident CTA pairs of the fused pair kernel,
-                                   // [operand type][4 / 8 epilogue warps][tile 128/192/224/256]
+  int pair_max[2][3][4] = {};      // resident CTA pairs of the pair kernel, [operand type]
+                                   // [4 / 8 epilogue warps / slot GEMM][tile 128/192/224/256]
 };
 
 std::mutex g_mu;
@@ -232,7 +232,7 @@ int pair_index(int bn) { return bn == 128 ? 0 : bn == 192 ? 1 : bn == 224 ? 2 : 
 int prepare_pair(Workspace* ws, int bn, int f8, int ew, int* max_pairs) {
   const int i = pair_index(bn);
   if (i < 0) return fail(FLN_ERR_UNSUPPORTED, "fused tile width %d", bn);
-  const int e = ew == 8 ? 1 : 0;
+  const int e = ew == 8 ? 1 : ew == 0 ? 2 : 0;
   if (ws->pair_max[f8][e][i] == 0) {
     int mp = 0;
     FLN_CUDA(pair_gemm_prepare(bn, f8, ew, &mp), "pair kernel set-up (shared memory limit, resident clusters)");
@@ -624,14 +624,18 @@ int run_fused(Workspace* ws, const Call& c, const fln_plan& pl) {
 }
 
 // Per microchunk: GEMM -> slot (caller's stream), add + norm of the slot on
-// the library's second stream; three slots guarded by events.
+// the library's second stream; three slots guarded by events.  Tiles 128 and
+// 256 run the slot GEMM on CTA pairs (the fused kernel's mainloop), tile 64 on
+// single CTAs.
 int run_pipelined(Workspace* ws, const Call& c, const fln_plan& pl) {
   const int bn = pl.tile_n;
-  int rc = prepare_kernel(ws, bn, EPI_STORE_F32, c.f8);
+  const bool pair_slot = bn == 128 || bn == 256;
+  int max_pairs = 0;
+  int rc = pair_slot ? prepare_pair(ws, bn, c.f8, 0, &max_pairs) : prepare_kernel(ws, bn, EPI_STORE_F32, c.f8);
   if (rc) return rc;
   CUtensorMap tmA, tmB;
   if ((rc = make_map(&tmA, c.x, c.K, c.T, 128, c.esize()))) return rc;
-  if ((rc = make_map(&tmB, c.W, c.K, c.H, bn, c.esize()))) return rc;
+  if ((rc = make_map(&tmB, c.W, c.K, c.H, pair_slot ? bn / 2 : bn, c.esize()))) return rc;
   const int chunk = std::min(pl.microchunk_tokens, c.T);
   const size_t slot_need = static_cast<size_t>(chunk) * c.H;
   if (slot_need > ws->slot_floats) {
@@ -664,10 +668,22 @@ int run_pipelined(Workspace* ws, const Call& c, const fln_plan& pl) {
     p.ld = c.H;
     p.yout = ws->slots[s];
     p.err = ws->err_word;
-    const int G = gemm_grid(ws, pl, static_cast<long long>(p.num_m_tiles) * nt);
-    rc = launch_counted(FLN_KERNEL_GEMM_SLOT, c.stream,
-                        [&] { return launch_gemm(EPI_STORE_F32, bn, c.f8, tmA, tmB, p, G, c.stream); },
-                        "slot GEMM launch");
+    if (pair_slot) {
+      int cap = max_pairs;
+      if (pl.gemm_ctas > 0) cap = std::min(cap, std::max(1, pl.gemm_ctas / 2));
+      const long long tiles = static_cast<long long>((p.num_m_tiles + 1) / 2) * nt;
+      const int pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, tiles)));
+      rc = launch_counted(FLN_KERNEL_GEMM_SLOT, c.stream,
+                          [&] {
+                            return launch_gemm_pair_fused(bn, c.f8, 0, tmA, tmB, tmA, tmA, tmA, p, pairs, c.stream);
+                          },
+                          "slot GEMM launch");
+    } else {
+      const int G = gemm_grid(ws, pl, static_cast<long long>(p.num_m_tiles) * nt);
+      rc = launch_counted(FLN_KERNEL_GEMM_SLOT, c.stream,
+                          [&] { return launch_gemm(EPI_STORE_F32, bn, c.f8, tmA, tmB, p, G, c.stream); },
+                          "slot GEMM launch");
+    }
     if (rc) return rc;
     FLN_CUDA(cudaEventRecord(ws->ev_ready[s], c.stream), "cudaEventRecord(slot ready)");
     FLN_CUDA(cudaStreamWaitEvent(ws->stream_b, ws->ev_ready[s], 0), "cudaStreamWaitEvent(slot ready)");

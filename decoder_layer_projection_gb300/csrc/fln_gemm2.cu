@@ -140,6 +140,9 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
                          const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmRs,
                          const __grid_constant__ CUtensorMap tmOs, const GemmParams p) {
   using C = Cfg<BN>;
+  // EW = 0: the PIPELINED path's slot GEMM -- the same mainloop, an epilogue
+  // that writes the fp32 accumulator to the slot (no residual, no norm)
+  constexpr bool SLOT = EW == 0;
   constexpr int STAGES = C::STAGES;
   constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(2 * BM, BN) : idesc_bf16_f32(2 * BM, BN);
   constexpr int KBE = kblock_elems(F8);  // elements of K per 128-byte K-block
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
   const int nN = p.num_n_tiles;
   const int num_pm = (p.num_m_tiles + 1) / 2;
   const int total = num_pm * nN;
-  const int S = p.split_tiles;
+  const int S = SLOT ? 0 : p.split_tiles;
   const int units = total + S;
   const int KB = p.num_k_blocks;
 
@@ -194,9 +197,11 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
     fence_proxy_async_smem();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmR);
-    tma_prefetch_desc(&tmRs);
-    tma_prefetch_desc(&tmOs);
+    if (!SLOT) {
+      tma_prefetch_desc(&tmR);
+      tma_prefetch_desc(&tmRs);
+      tma_prefetch_desc(&tmOs);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
@@ -251,7 +256,7 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
         }
       }
     }
-  } else if (warp == 6 && lane == 0) {
+  } else if (warp == 6 && lane == 0 && !SLOT) {
     // ------------------------------------------------------------ residual loader (both CTAs)
     // (a warp of its own: a lane spinning on a barrier would steal issue
     // slots from a producer or MMA lane of the same warp)
@@ -344,7 +349,7 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
     // pair's k-th tile uses TMEM buffer k % 2, i.e. always its group's.  The
     // groups share each quarter's output staging rows, passed on from tile to
     // tile in order through one mbarrier per quarter.
-    constexpr int NG = EW / 4;    // epilogue groups
+    constexpr int NG = SLOT ? 1 : EW / 4;  // epilogue groups
     const int q = warp & 3;       // TMEM lane quarter of this warp
     const int grp = warp >= 7 ? 1 : 0;
     const int rl = q * 32 + lane;  // row within this CTA's 128 rows
@@ -388,6 +393,44 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
       // fp32 halves of split tiles: [chunk of 32 columns][quad i of 4 columns][row of this CTA][4], so
       // that each 16-byte access of a warp covers 512 contiguous bytes
       float* const half = p.split_buf + split_slot * (static_cast<size_t>(BN) * BM);
+      if (SLOT) {
+        // slot GEMM: y (scaled like the fused path) to the launch's fp32 rows [M, ld]
+        const int row = mtile * BM + rl;
+        const bool vrow = row < p.M;
+        float sxr = p.y_scale;
+        if (F8 && vrow) sxr = __ldg(p.x_scale + static_cast<size_t>(p.a_row0 + row) * p.x_scale_stride);
+        float* yrow = p.yout + static_cast<size_t>(row) * static_cast<size_t>(p.ld);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tb + static_cast<uint32_t>(c * 32), v);
+          if (vrow) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int col = n0 + c * 32 + 8 * i;
+              if (col < p.N) {
+                float sc[8];
+                if (F8) {
+                  load_scale8(p.w_scale, p.w_scale_stride, col, true, sc);
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) sc[j] *= sxr;
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) sc[j] = sxr;
+                }
+                float4* d = reinterpret_cast<float4*>(yrow + col);
+                d[0] = make_float4(v[8 * i] * sc[0], v[8 * i + 1] * sc[1], v[8 * i + 2] * sc[2], v[8 * i + 3] * sc[3]);
+                d[1] = make_float4(v[8 * i + 4] * sc[4], v[8 * i + 5] * sc[5], v[8 * i + 6] * sc[6],
+                                   v[8 * i + 7] * sc[7]);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_leader + static_cast<uint32_t>(b * 8));
+        continue;
+      }
       if (w.role == UNIT_HELPER) {
         // second K-half: the raw accumulator goes to the owner (scales and the residual are the owner's)
 #pragma unroll 1
@@ -700,7 +743,7 @@ static cudaError_t prepare_pair_bn(int* max_pairs) {
 }
 
 // The instantiated variants: every tile width with four epilogue warps, tile
-// widths 224 and 256 also with eight.
+// widths 224 and 256 also with eight; the slot GEMM (ew = 0) for 128 and 256.
 struct PairArgs {
   const CUtensorMap *tmA, *tmB, *tmR, *tmRs, *tmOs;
   const GemmParams* p;
@@ -717,6 +760,13 @@ static cudaError_t run_variant(const PairArgs& a) {
 
 template <int F8>
 static cudaError_t dispatch_bn(int bn, int ew, const PairArgs& a) {
+  if (ew == 0) {  // slot GEMM of the PIPELINED path
+    switch (bn) {
+      case 128: return run_variant<128, F8, 0>(a);
+      case 256: return run_variant<256, F8, 0>(a);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (ew == 8) {
     switch (bn) {
       case 224: return run_variant<224, F8, 8>(a);

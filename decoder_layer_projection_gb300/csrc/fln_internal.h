@@ -158,7 +158,10 @@ cudaError_t gemm_prepare(int bn, EpilogueKind epi, int f8);  // sets max dynamic
 // boxes), tmRs / tmOs the chunk's residual and output rows in 32 x 64 boxes
 // (stores).
 // ew: epilogue warps per CTA, 4 (every tile width) or 8 (two groups of four on
-// alternate tiles; tile widths 224, 256).
+// alternate tiles; tile widths 224, 256); ew = 0 runs the same kernel as the
+// PIPELINED path's slot GEMM (tile widths 128, 256): the fp32 accumulator,
+// scaled, to p.yout [M, ld] (launch-local rows), no residual, no norm, no
+// split (tmR, tmRs, tmOs are not used).
 cudaError_t pair_gemm_prepare(int bn, int f8, int ew, int* max_pairs);
 cudaError_t launch_gemm_pair_fused(int bn, int f8, int ew, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                    const CUtensorMap& tmR, const CUtensorMap& tmRs, const CUtensorMap& tmOs,

@@ -90,11 +90,16 @@ def kernel_sources_hash(dtype, kernel):
 
 
 NCU_TRAFFIC = {
-    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "31c03f66903d"): 108776960 + 32363776,
-    ("llama3_8b_down", 8192, "bf16", "gemm_fused", 256, "31c03f66903d"): 1248116224 + 122408448,
-    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 256, "31c03f66903d"): 286641152 + 22163456,
-    ("llama70b_down_decode", 8, "bf16", "gemm_splitk", 0, "abf134257120"): 471433472 + 3321856,
-    ("llama70b_oproj_decode", 8, "bf16", "gemm_splitk", 0, "abf134257120"): 135542016 + 3136256,
+    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "d17edc8821c6"): 108715776 + 32147712,
+    ("llama3_8b_down", 8192, "bf16", "gemm_fused", 256, "d17edc8821c6"): 1245283072 + 122326016,
+    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 192, "d17edc8821c6"): 278793216 + 17995008,
+    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 256, "d17edc8821c6"): 286488064 + 22124800,
+    ("llama70b_down_decode", 8, "bf16", "gemm_splitk", 0, "384cbfdf0b50"): 471428352 + 3621120,
+    ("llama70b_oproj_decode", 8, "bf16", "gemm_splitk", 0, "384cbfdf0b50"): 135542016 + 2951936,
+    ("llama3_8b_oproj", 4096, "e4m3", "gemm_fused", 224, "d17edc8821c6"): 67530240 + 17053696,
+    ("llama3_8b_down", 8192, "e4m3", "gemm_fused", 256, "d17edc8821c6"): 542484992 + 110922752,
+    ("llama70b_oproj_decode", 8, "e4m3", "gemm_splitk", 0, "384cbfdf0b50"): 67211008 + 72704,
+    ("llama70b_down_decode", 8, "e4m3", "gemm_splitk", 0, "384cbfdf0b50"): 236310016 + 3079680,
     ("llama70b_down_decode", 8, "nvfp4", "gemm_splitk", 0, "75d05af169d4"): 135886080 + 2963712,
     ("llama70b_oproj_decode", 8, "nvfp4", "gemm_splitk", 0, "75d05af169d4"): 37937152 + 0,
     ("llama70b_down_decode", 8, "mxfp4", "gemm_splitk", 0, "75d05af169d4"): 128547072 + 2881536,

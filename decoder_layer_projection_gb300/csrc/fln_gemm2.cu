@@ -487,6 +487,23 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
         for (int c2 = 0; c2 < halves; ++c2) {
           float v[32];
           const uint32_t ta = tb + static_cast<uint32_t>(g * 64 + c2 * 32);
+          // the residual rows and (FP8) the scales first: their latency then
+          // overlaps the TMEM load's
+          uint4 rin[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) rin[h] = *reinterpret_cast<const uint4*>(box + swz(rl, c2 * 4 + h));
+          float scl[32];
+          if (F8) {
+            // dequantisation: y = acc * (sx[token] * sw[column])
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int cc = n0 + g * 64 + c2 * 32 + 8 * h;
+              float sw[8];
+              load_scale8(p.w_scale, p.w_scale_stride, cc, cc < p.N, sw);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) scl[8 * h + j] = sxr * sw[j];
+            }
+          }
           tmem_ld32(ta, v);
           if (w.role == UNIT_OWNER) {
             // the other K-half of the accumulator (fixed order: this half + that half)
@@ -501,15 +518,8 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
             }
           }
           if (F8) {
-            // dequantise: y = acc * (sx[token] * sw[column])
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const int cc = n0 + g * 64 + c2 * 32 + 8 * h;
-              float sw[8];
-              load_scale8(p.w_scale, p.w_scale_stride, cc, cc < p.N, sw);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) v[8 * h + j] *= sxr * sw[j];
-            }
+            for (int j = 0; j < 32; ++j) v[j] *= scl[j];
           } else {
             // a tensor scale of the weights (NVFP4 dequantised to bf16); 1 otherwise
 #pragma unroll
@@ -519,7 +529,7 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
           for (int h = 0; h < 4; ++h) {
             uint4* rp = reinterpret_cast<uint4*>(box + swz(rl, c2 * 4 + h));
             float f[8];
-            bf16x8_to_f32(*rp, f);
+            bf16x8_to_f32(rin[h], f);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float r = f[j] + v[8 * h + j];
@@ -624,29 +634,32 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           if (c2 < halves) {
+            // gamma first: its latency then overlaps the TMEM load's
+            float gw[32];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int cc = n0 + g * 64 + (c2 * 4 + h) * 8;
+              if (cc < p.N) {
+                const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc));
+                const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc + 4));
+                gw[8 * h] = g0.x; gw[8 * h + 1] = g0.y; gw[8 * h + 2] = g0.z; gw[8 * h + 3] = g0.w;
+                gw[8 * h + 4] = g1.x; gw[8 * h + 5] = g1.y; gw[8 * h + 6] = g1.z; gw[8 * h + 7] = g1.w;
+              } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) gw[8 * h + j] = 0.f;
+              }
+            }
             float v[32];
             tmem_ld32(tb + static_cast<uint32_t>(g * 64 + c2 * 32), v);
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-              const int chunk = c2 * 4 + h;
-              const int cc = n0 + g * 64 + chunk * 8;
-              float gw[8];
-              if (cc < p.N) {
-                const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc));
-                const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc + 4));
-                gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
-                gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
-              } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) gw[j] = 0.f;
-              }
               float o[8];
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const float gj = p.norm_kind ? 1.0f + gw[j] : gw[j];
+                const float gj = p.norm_kind ? 1.0f + gw[8 * h + j] : gw[8 * h + j];
                 o[j] = v[8 * h + j] * rstd * gj;
               }
-              ob[chunk] = f32x8_to_bf16(o);
+              ob[c2 * 4 + h] = f32x8_to_bf16(o);
             }
           }
         }

@@ -68,9 +68,13 @@ struct Cfg {
   static constexpr int NBOX = 3;                         // residual boxes in flight
   static constexpr int OSTAGE = 4 * 32 * 128;            // 32 rows x 64 bf16 output staging per warp
   static constexpr int E_BYTES = NBOX * BOX + OSTAGE;
-  static constexpr int RAW_STAGES = (SMEM_LIMIT - 1024 - BAR_BYTES - E_BYTES) / STAGE;
+  // the tile's gamma and weight scales in shared memory, [2 groups][2 tiles][2 vectors][BN] fp32:
+  // where they fit beside the ring without costing a stage (every width but 256)
+  static constexpr bool VEC = BN != 256 || false;
+  static constexpr int VEC_BYTES = VEC ? 32 * BN : 0;
+  static constexpr int RAW_STAGES = (SMEM_LIMIT - 1024 - BAR_BYTES - E_BYTES - VEC_BYTES) / STAGE;
   static constexpr int STAGES = RAW_STAGES > 8 ? 8 : RAW_STAGES;
-  static constexpr int SMEM = STAGES * STAGE + E_BYTES + BAR_BYTES + 1024;
+  static constexpr int SMEM = STAGES * STAGE + E_BYTES + BAR_BYTES + VEC_BYTES + 1024;
   static constexpr int TMEM_COLS = (2 * BN) <= 256 ? 256 : 512;
   static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256, "tile width");
   static_assert(STAGES >= 4, "pipeline depth");
@@ -162,6 +166,7 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(stg_done + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* epi_abort = abort_flag + 1;
+  float* const svec = reinterpret_cast<float*>(sE + C::E_BYTES + BAR_BYTES);  // C::VEC only
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -375,6 +380,19 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
       const int n0 = nt * BN;
       const int col_end = min(p.N, n0 + BN);
       const int wrow0 = mtile * BM + q * 32;  // this warp's first row in the chunk
+      // this tile's gamma [BN] and weight scales [BN] (C::VEC): the group's
+      // tiles alternate between two slots, so a warp may fill the next slot
+      // while the group's other warps still read this one; the group barrier
+      // below orders the fill before every read
+      float* const vslot = svec + ((grp * 2 + (NG == 2 ? (local >> 1) & 1 : local & 1)) * 2) * BN;
+      if (C::VEC && !SLOT && w.role != UNIT_HELPER) {
+        for (int c = rl; c < BN; c += BM) {
+          const int cc = n0 + c;
+          const bool vc = cc < p.N;
+          vslot[c] = vc ? __ldg(p.gamma + cc) : 0.f;
+          if (F8) vslot[BN + c] = vc ? __ldg(p.w_scale + (p.w_scale_stride ? cc : 0)) : 0.f;
+        }
+      }
       // All epilogue threads decide together whether to continue: a thread
       // that leaves alone would strand the others at a named barrier.
       bool stop = failed;
@@ -499,7 +517,14 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
             for (int h = 0; h < 4; ++h) {
               const int cc = n0 + g * 64 + c2 * 32 + 8 * h;
               float sw[8];
-              load_scale8(p.w_scale, p.w_scale_stride, cc, cc < p.N, sw);
+              if (C::VEC) {
+                const float4* sv = reinterpret_cast<const float4*>(vslot + BN + g * 64 + c2 * 32 + 8 * h);
+                const float4 a = sv[0], bq = sv[1];
+                sw[0] = a.x; sw[1] = a.y; sw[2] = a.z; sw[3] = a.w;
+                sw[4] = bq.x; sw[5] = bq.y; sw[6] = bq.z; sw[7] = bq.w;
+              } else {
+                load_scale8(p.w_scale, p.w_scale_stride, cc, cc < p.N, sw);
+              }
 #pragma unroll
               for (int j = 0; j < 8; ++j) scl[8 * h + j] = sxr * sw[j];
             }
@@ -639,7 +664,12 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
               const int cc = n0 + g * 64 + (c2 * 4 + h) * 8;
-              if (cc < p.N) {
+              if (C::VEC) {
+                const float4* gv = reinterpret_cast<const float4*>(vslot + g * 64 + (c2 * 4 + h) * 8);
+                const float4 g0 = gv[0], g1 = gv[1];
+                gw[8 * h] = g0.x; gw[8 * h + 1] = g0.y; gw[8 * h + 2] = g0.z; gw[8 * h + 3] = g0.w;
+                gw[8 * h + 4] = g1.x; gw[8 * h + 5] = g1.y; gw[8 * h + 6] = g1.z; gw[8 * h + 7] = g1.w;
+              } else if (cc < p.N) {
                 const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc));
                 const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma + cc + 4));
                 gw[8 * h] = g0.x; gw[8 * h + 1] = g0.y; gw[8 * h + 2] = g0.z; gw[8 * h + 3] = g0.w;

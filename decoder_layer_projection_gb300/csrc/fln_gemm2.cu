@@ -385,6 +385,10 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
       // while the group's other warps still read this one; the group barrier
       // below orders the fill before every read
       float* const vslot = svec + ((grp * 2 + (NG == 2 ? (local >> 1) & 1 : local & 1)) * 2) * BN;
+      // FP8: this row's token scale (rows past the chunk have a zero accumulator)
+      float sxr = 0.f;
+      if (F8 && !SLOT && w.role != UNIT_HELPER && wrow0 + lane < p.M)
+        sxr = __ldg(p.x_scale + static_cast<size_t>(p.a_row0 + wrow0 + lane) * p.x_scale_stride);
       if (C::VEC && !SLOT && w.role != UNIT_HELPER) {
         for (int c = rl; c < BN; c += BM) {
           const int cc = n0 + c;
@@ -415,8 +419,8 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
         // slot GEMM: y (scaled like the fused path) to the launch's fp32 rows [M, ld]
         const int row = mtile * BM + rl;
         const bool vrow = row < p.M;
-        float sxr = p.y_scale;
-        if (F8 && vrow) sxr = __ldg(p.x_scale + static_cast<size_t>(p.a_row0 + row) * p.x_scale_stride);
+        float ysc = p.y_scale;
+        if (F8 && vrow) ysc = __ldg(p.x_scale + static_cast<size_t>(p.a_row0 + row) * p.x_scale_stride);
         float* yrow = p.yout + static_cast<size_t>(row) * static_cast<size_t>(p.ld);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -431,10 +435,10 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
                 if (F8) {
                   load_scale8(p.w_scale, p.w_scale_stride, col, true, sc);
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) sc[j] *= sxr;
+                  for (int j = 0; j < 8; ++j) sc[j] *= ysc;
                 } else {
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) sc[j] = sxr;
+                  for (int j = 0; j < 8; ++j) sc[j] = ysc;
                 }
                 float4* d = reinterpret_cast<float4*>(yrow + col);
                 d[0] = make_float4(v[8 * i] * sc[0], v[8 * i + 1] * sc[1], v[8 * i + 2] * sc[2], v[8 * i + 3] * sc[3]);
@@ -492,10 +496,6 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
       // zeros: acc and r0 are 0.
       float ss = 0.f;
       int pending = -1;  // box whose TMA store may still be reading it (freed one box later)
-      // FP8: this row's token scale (rows past the chunk have a zero accumulator)
-      float sxr = 0.f;
-      if (F8 && wrow0 + lane < p.M)
-        sxr = __ldg(p.x_scale + static_cast<size_t>(p.a_row0 + wrow0 + lane) * p.x_scale_stride);
 #pragma unroll 1
       for (int g = 0; g < G; ++g, ++s) {
         const int halves = (BN - g * 64) >= 64 ? 2 : 1;  // 32-column halves of this box inside the tile

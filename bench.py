@@ -77,7 +77,7 @@ def kernel_sources_hash(dtype, kernel):
     """sha1 (12 hex digits) of the sources the dominant kernel (by its profile name) is built from."""
     h = hashlib.sha1()
     if dtype == "moe":
-        files = ["fln_moe.cu", "fln_ptx.cuh"]
+        files = ["fln_moe.cu", "fln_gemm2.cu", "fln_ptx.cuh"]
     elif kernel == "gemm_fused":
         files = ["fln_gemm2.cu", "fln_ptx.cuh"]
     elif kernel == "gemm_splitk" and dtype in ("nvfp4", "mxfp4"):
@@ -104,8 +104,8 @@ NCU_TRAFFIC = {
     ("llama70b_oproj_decode", 8, "nvfp4", "gemm_splitk", 0, "75d05af169d4"): 37937152 + 0,
     ("llama70b_down_decode", 8, "mxfp4", "gemm_splitk", 0, "75d05af169d4"): 128547072 + 2881536,
     ("llama70b_oproj_decode", 8, "mxfp4", "gemm_splitk", 0, "75d05af169d4"): 35841280 + 0,
-    ("mixtral_8x7b_down_decode", 8, "moe", "moe_gemm", 256, "ea0f5d1ffc77"): 822708224 + 2672640,
-    ("mixtral_8x7b_down", 4096, "moe", "moe_gemm", 256, "ea0f5d1ffc77"): 1323357952 + 135113472,
+    ("mixtral_8x7b_down_decode", 8, "moe", "moe_gemm", 256, "6266342f59fb"): 822599168 + 3301120,
+    ("mixtral_8x7b_down", 4096, "moe", "moe_gemm", 256, "6266342f59fb"): 1398003200 + 122324992,
 }
 def traffic_tile(kname, plan):
     return plan["tile_n"] if kname in ("gemm_fused", "gemm_slot") else 0

@@ -1252,6 +1252,9 @@ int fused_proj_add_rmsnorm_nvfp4(const fln_bf16* x, const uint8_t* W, const uint
 
 namespace {
 constexpr int kMoeMaxE = 256, kMoeMaxK = 8, kMoeMaxH = 16384;
+// grouped rows per expert (on average) from which the MoE GEMM runs on CTA
+// pairs; below, the single-CTA kernel's 128-row tiles waste less on short groups
+constexpr int kMoePairRowsPerExpert = 256;
 
 int check_moe_shape(int T, int E, int k) {
   if (T < 0 || T > kMaxT) return fail(FLN_ERR_INVALID_ARG, "T=%d outside [0, %d]", T, kMaxT);
@@ -1329,13 +1332,36 @@ int fused_moe_down_add_rmsnorm(const fln_bf16* hg, const int* offsets, const int
   }
   CUtensorMap tmA, tmB;
   if ((rc = make_map(&tmA, hg, K, R, 128))) return rc;
-  if ((rc = make_map(&tmB, We, K, static_cast<uint64_t>(E) * H, 256))) return rc;
-  rc = launch_counted(FLN_KERNEL_MOE_GEMM, s,
-                      [&] {
-                        return launch_moe_grouped_gemm(tmA, tmB, offsets, E, static_cast<int>(R), H, K, ws->moe_y,
-                                                       ws->err_word, ws->err_word + 1, ws->sms, s);
-                      },
-                      "MoE grouped GEMM launch");
+  if (R >= static_cast<size_t>(kMoePairRowsPerExpert) * E) {
+    // many rows per expert: the pair kernel's slot GEMM over the grouping
+    // (256-row blocks on CTA pairs, each CTA loading half of a 256-wide W tile)
+    int max_pairs = 0;
+    if ((rc = prepare_pair(ws, 256, 0, 0, &max_pairs))) return rc;
+    if ((rc = make_map(&tmB, We, K, static_cast<uint64_t>(E) * H, 128))) return rc;
+    GemmParams p{};
+    p.M = static_cast<int>(R);
+    p.N = H;
+    p.K = K;
+    p.num_n_tiles = (H + 255) / 256;
+    p.num_k_blocks = (K + 63) / 64;
+    p.ld = H;
+    p.yout = ws->moe_y;
+    p.err = ws->err_word;
+    p.moe_off = offsets;
+    p.moe_E = E;
+    p.moe_bad = ws->err_word + 1;
+    rc = launch_counted(FLN_KERNEL_MOE_GEMM, s,
+                        [&] { return launch_gemm_pair_fused(256, 0, 0, tmA, tmB, tmA, tmA, tmA, p, max_pairs, s); },
+                        "MoE grouped GEMM launch (CTA pairs)");
+  } else {
+    if ((rc = make_map(&tmB, We, K, static_cast<uint64_t>(E) * H, 256))) return rc;
+    rc = launch_counted(FLN_KERNEL_MOE_GEMM, s,
+                        [&] {
+                          return launch_moe_grouped_gemm(tmA, tmB, offsets, E, static_cast<int>(R), H, K, ws->moe_y,
+                                                         ws->err_word, ws->err_word + 1, ws->sms, s);
+                        },
+                        "MoE grouped GEMM launch");
+  }
   if (rc) return rc;
   return launch_counted(FLN_KERNEL_MOE_NORM, s,
                         [&] {

@@ -138,6 +138,46 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Where tile t of a launch lives: this CTA's first A row and B row, its
+// first output row and the end of its valid rows, and the tile's first
+// column.  Dense: row-pair block t / nN of the launch and N-tile t % nN.
+// Grouped (slot mode with offsets): tiles of expert e are tb[e] ..
+// tb[e + 1] - 1, row blocks fastest (the pairs of a round then stream the same
+// W tiles), each row block starting at off[e] + 256 m.
+struct TileAt {
+  int a_row, b_row, out_row, row_end, n0;
+};
+
+template <int BN>
+__device__ __forceinline__ TileAt tile_at(const GemmParams& p, int t, int nN, uint32_t rank, const int* g_off,
+                                          const int* g_tb) {
+  TileAt r;
+  if (g_off == nullptr) {
+    const int pm = t / nN, nt = t % nN;
+    r.a_row = p.a_row0 + pm * 2 * BM + static_cast<int>(rank) * BM;
+    r.b_row = nt * BN + static_cast<int>(rank) * (BN / 2);
+    r.out_row = (pm * 2 + static_cast<int>(rank)) * BM;
+    r.row_end = p.M;
+    r.n0 = nt * BN;
+    return r;
+  }
+  int lo = 0, hi = p.moe_E - 1;  // the last expert e with tb[e] <= t (experts without rows own no tiles)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (g_tb[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const int e = lo, local = t - g_tb[e];
+  const int mb = (g_off[e + 1] - g_off[e] + 2 * BM - 1) / (2 * BM);  // row blocks of the expert
+  const int nt = local / mb, m = local - nt * mb;
+  r.a_row = g_off[e] + m * 2 * BM + static_cast<int>(rank) * BM;
+  r.b_row = e * p.N + nt * BN + static_cast<int>(rank) * (BN / 2);
+  r.out_row = r.a_row;
+  r.row_end = g_off[e + 1];
+  r.n0 = nt * BN;
+  return r;
+}
+
 template <int BN, int F8, int EW>
 __global__ void __launch_bounds__(threads_for(EW), 1)
     fln_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -176,7 +216,35 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
   const int num_pairs = static_cast<int>(nclusters_x());
   const int nN = p.num_n_tiles;
   const int num_pm = (p.num_m_tiles + 1) / 2;
-  const int total = num_pm * nN;
+  // grouped slot GEMM: the offsets and the tiles before each expert, in the
+  // residual boxes' space (slot mode has no residual); checked before any
+  // barrier, TMEM or peer is touched, identically in both CTAs of a pair
+  const bool grouped = SLOT && p.moe_off != nullptr;
+  int* const g_off = grouped ? reinterpret_cast<int*>(sE) : nullptr;
+  int* const g_tb = grouped ? g_off + 257 : nullptr;
+  if (grouped) {
+    const int E = p.moe_E;
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) g_off[e] = p.moe_off[e];
+    __syncthreads();
+    bool okg = threadIdx.x != 0 || (g_off[0] == 0 && g_off[E] == p.M);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) okg = okg && g_off[e] <= g_off[e + 1];
+    okg = __syncthreads_and(okg);
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+      *p.moe_bad = okg ? 0u : 1u;
+      if (!okg) atomicOr(p.err, FLN_DEVERR_BAD_INDEX);
+    }
+    if (!okg) return;
+    if (threadIdx.x == 0) {
+      int run = 0;
+      for (int e = 0; e < E; ++e) {
+        g_tb[e] = run;
+        run += (g_off[e + 1] - g_off[e] + 2 * BM - 1) / (2 * BM) * nN;
+      }
+      g_tb[E] = run;
+    }
+    __syncthreads();
+  }
+  const int total = grouped ? g_tb[p.moe_E] : num_pm * nN;
   const int S = SLOT ? 0 : p.split_tiles;
   const int units = total + S;
   const int KB = p.num_k_blocks;
@@ -231,9 +299,8 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
     bool ok = true;
     for (int u = pair_id; ok && u < units; u += num_pairs) {
       const Unit w = unit_at(u, total, S, KB);
-      const int pm = w.t / nN, nt = w.t % nN;
-      const int a_row = p.a_row0 + pm * 2 * BM + static_cast<int>(rank) * BM;
-      const int b_row = nt * BN + static_cast<int>(rank) * (BN / 2);
+      const TileAt ta = tile_at<BN>(p, w.t, nN, rank, g_off, g_tb);
+      const int a_row = ta.a_row, b_row = ta.b_row;
       for (int kb = w.kb0; kb < w.kb1; ++kb) {
         if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, FLN_DEVERR_TIMEOUT_EMPTY)) {
           ok = false;
@@ -416,9 +483,12 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
       // that each 16-byte access of a warp covers 512 contiguous bytes
       float* const half = p.split_buf + split_slot * (static_cast<size_t>(BN) * BM);
       if (SLOT) {
-        // slot GEMM: y (scaled like the fused path) to the launch's fp32 rows [M, ld]
-        const int row = mtile * BM + rl;
-        const bool vrow = row < p.M;
+        // slot GEMM: y (scaled like the fused path) to the fp32 rows [M, ld]
+        // (launch-local rows; grouped: rows at their grouped positions)
+        const TileAt ta = tile_at<BN>(p, t, nN, rank, g_off, g_tb);
+        const int row = ta.out_row + rl;
+        const bool vrow = row < ta.row_end;
+        const int n0 = ta.n0;
         float ysc = p.y_scale;
         if (F8 && vrow) ysc = __ldg(p.x_scale + static_cast<size_t>(p.a_row0 + row) * p.x_scale_stride);
         float* yrow = p.yout + static_cast<size_t>(row) * static_cast<size_t>(p.ld);

@@ -106,6 +106,16 @@ struct GemmParams {
   int split_tiles;
   float* split_buf;
   unsigned long long* split_flags;
+  // pair kernel, slot mode: a grouped (MoE) GEMM when moe_off is set.  Rows
+  // [moe_off[e], moe_off[e + 1]) of A times expert e's rows [e N, (e + 1) N)
+  // of B, in row blocks of 256 that never cross an expert's end; y rows go to
+  // their grouped positions in yout [M, ld].  The offsets are checked on the
+  // device first: unless 0 = off[0] <= ... <= off[E] = M, nothing is written,
+  // *moe_bad is set to 1 (else 0) and the device error word gets the
+  // bad-index bit.  E <= 256.
+  const int* moe_off = nullptr;
+  int moe_E = 0;
+  unsigned int* moe_bad = nullptr;
 };
 
 struct NormParams {

@@ -4,7 +4,9 @@
   bit for bit, gates within fp32 rounding, with planted equal logits;
 * the grouped down projection + unpermute + add + norm on ragged shapes
   (K and H tails, experts without rows, one expert, k = 1..4), the same bar
-  as the dense paths (tests/parity.py), guard rows after T untouched;
+  as the dense paths (tests/parity.py), guard rows after T untouched, on
+  single CTAs and (256 or more rows per expert) on CTA pairs, with bad
+  offsets caught on both;
 * routing then the region chained on the device;
 * the Mixtral-8x7B down shape at decode, 512 and 4096 tokens, every row;
 * argument checks.
@@ -111,6 +113,56 @@ def test_down_region_parity(case):
     run.check(rb, ob, wl.name)
     rb2, ob2 = run()
     assert np.array_equal(rb, rb2) and np.array_equal(ob, ob2)
+
+
+# At least 256 grouped rows per expert on average: the grouped GEMM runs on CTA pairs (256-row blocks that
+# stop at each expert's end, 256-wide W tiles split between the two CTAs)
+PAIR = [
+    (Workload("moe_pair_ragged", T=600, K=200, H=264, eps=1e-5, r_sigma=2.0, seed=7), 2, 1),
+    (Workload("moe_pair_gemma", T=300, K=448, H=520, norm_kind=1, eps=1e-6, gamma_mode="plain", seed=8), 4, 4),
+    (Workload("moe_pair_top3", T=700, K=136, H=384, eps=1e-5, r_sigma=2.0, seed=9), 8, 3),
+]
+
+
+@pytest.mark.parametrize("case", PAIR, ids=lambda c: c[0].name)
+def test_down_region_parity_on_cta_pairs(case):
+    wl, E, k = case
+    assert wl.T * k >= 256 * E
+    d = make_inputs_moe(wl, E, k)
+    run = RunMoe(d, E, wl.eps, wl.norm_kind)
+    rb, ob = run()
+    run.check(rb, ob, wl.name)
+    rb2, ob2 = run()
+    assert np.array_equal(rb, rb2) and np.array_equal(ob, ob2)
+
+
+def test_expert_without_rows_on_cta_pairs():
+    wl = Workload("moe_pair_empty", T=1100, K=256, H=384, eps=1e-5, r_sigma=2.0, seed=10)
+    d = dict(make_inputs_moe(wl, 4, 1))
+    g = np.random.default_rng(10)
+    d["ids"] = g.choice([0, 1, 3], size=(wl.T, 1)).astype(np.int32)
+    run = RunMoe(d, 4, wl.eps, wl.norm_kind)
+    assert run.offsets[2] == run.offsets[3] and wl.T >= 256 * 4
+    rb, ob = run()
+    run.check(rb, ob, "expert without rows, CTA pairs")
+
+
+def test_bad_offsets_on_cta_pairs_write_nothing():
+    wl, E, k = PAIR[0]
+    d = make_inputs_moe(wl, E, k)
+    run = RunMoe(d, E, wl.eps, wl.norm_kind)
+    T, H = d["r0"].shape
+    good = run.offsets
+    for bad in (np.array([0, good[1], good[2] + 128], np.int32), np.array([0, good[2], good[1]], np.int32)):
+        r = dev_bf16(d["r0"])
+        out = dev_bf16(np.full((T, H), 0x7FC2, np.uint16))
+        fln.fused_moe_down_add_rmsnorm(run.hg, torch.from_numpy(bad).cuda(), torch.from_numpy(run.row_of).cuda(),
+                                       torch.from_numpy(d["wt"]).cuda(), run.We, r, run.gamma, wl.eps,
+                                       wl.norm_kind, out=out)
+        _expect_bad_index()
+        assert np.array_equal(host_bits(r), d["r0"]) and np.all(host_bits(out) == 0x7FC2)
+    rb, ob = run()
+    run.check(rb, ob, "after bad offsets, CTA pairs")
 
 
 def test_expert_without_rows():

@@ -90,14 +90,14 @@ def kernel_sources_hash(dtype, kernel):
 
 
 NCU_TRAFFIC = {
-    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "24525b694e96"): 112253952 + 33777408,
-    ("llama3_8b_down", 8192, "bf16", "gemm_fused", 256, "24525b694e96"): 1175215104 + 122487040,
-    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 192, "24525b694e96"): 278710784 + 17981696,
-    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 256, "24525b694e96"): 286444800 + 22294784,
+    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "77aa50ccbcdc"): 109771264 + 33087232,
+    ("llama3_8b_down", 8192, "bf16", "gemm_fused", 256, "77aa50ccbcdc"): 1174534656 + 122550016,
+    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 192, "77aa50ccbcdc"): 278787840 + 18025216,
+    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 256, "77aa50ccbcdc"): 286511872 + 22354432,
     ("llama70b_down_decode", 8, "bf16", "gemm_splitk", 0, "384cbfdf0b50"): 471428352 + 3621120,
     ("llama70b_oproj_decode", 8, "bf16", "gemm_splitk", 0, "384cbfdf0b50"): 135542016 + 2951936,
-    ("llama3_8b_oproj", 4096, "e4m3", "gemm_fused", 224, "24525b694e96"): 67465472 + 17224704,
-    ("llama3_8b_down", 8192, "e4m3", "gemm_fused", 256, "24525b694e96"): 562207744 + 111489280,
+    ("llama3_8b_oproj", 4096, "e4m3", "gemm_fused", 224, "77aa50ccbcdc"): 67456512 + 17328384,
+    ("llama3_8b_down", 8192, "e4m3", "gemm_fused", 256, "77aa50ccbcdc"): 535526400 + 110201088,
     ("llama70b_oproj_decode", 8, "e4m3", "gemm_splitk", 0, "384cbfdf0b50"): 67211008 + 72704,
     ("llama70b_down_decode", 8, "e4m3", "gemm_splitk", 0, "384cbfdf0b50"): 236310016 + 3079680,
     ("llama70b_down_decode", 8, "nvfp4", "gemm_splitk", 0, "75d05af169d4"): 135886080 + 2963712,

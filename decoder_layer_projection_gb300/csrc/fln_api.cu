@@ -276,9 +276,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D tensor [rows, inner] (inner contiguous) of bf16 (esize 2) or E4M3
-// codes (esize 1) read in boxes of 128 bytes x box_rows with 128-byte
-// swizzle; out-of-range elements read 0.
+// 2-D tensor [rows, inner] (inner contiguous) of bf16 (esize 2), E4M3
+// codes (esize 1) or fp32 (esize 4) in boxes of 128 bytes x box_rows with
+// 128-byte swizzle; out-of-range elements read 0 (and are not stored).
 int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows, int esize = 2) {
   auto enc = encode_fn();
   if (!enc) return fail(FLN_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
@@ -286,7 +286,9 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, ui
   cuuint64_t strides[1] = {inner * static_cast<uint64_t>(esize)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt = esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = esize == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -673,9 +675,12 @@ int run_pipelined(Workspace* ws, const Call& c, const fln_plan& pl) {
       if (pl.gemm_ctas > 0) cap = std::min(cap, std::max(1, pl.gemm_ctas / 2));
       const long long tiles = static_cast<long long>((p.num_m_tiles + 1) / 2) * nt;
       const int pairs = static_cast<int>(std::max<long long>(1, std::min<long long>(cap, tiles)));
+      // the slot's rows of this chunk, stored in 32 x 32 fp32 boxes (clipped at row n and column H)
+      CUtensorMap tmY;
+      if ((rc = make_map(&tmY, ws->slots[s], c.H, n, 32, 4))) return rc;
       rc = launch_counted(FLN_KERNEL_GEMM_SLOT, c.stream,
                           [&] {
-                            return launch_gemm_pair_fused(bn, c.f8, 0, tmA, tmB, tmA, tmA, tmA, p, pairs, c.stream);
+                            return launch_gemm_pair_fused(bn, c.f8, 0, tmA, tmB, tmA, tmA, tmY, p, pairs, c.stream);
                           },
                           "slot GEMM launch");
     } else {

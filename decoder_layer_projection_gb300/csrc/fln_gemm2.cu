@@ -273,8 +273,8 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
     if (!SLOT) {
       tma_prefetch_desc(&tmR);
       tma_prefetch_desc(&tmRs);
-      tma_prefetch_desc(&tmOs);
     }
+    if (!SLOT || p.moe_off == nullptr) tma_prefetch_desc(&tmOs);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
@@ -492,28 +492,71 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
         float ysc = p.y_scale;
         if (F8 && vrow) ysc = __ldg(p.x_scale + static_cast<size_t>(p.a_row0 + row) * p.x_scale_stride);
         float* yrow = p.yout + static_cast<size_t>(row) * static_cast<size_t>(p.ld);
+        if (!grouped) {
+          // dense slot: each 32-column chunk of the warp's 32 rows goes out
+          // through shared memory (two 4 KiB buffers a warp, in the residual
+          // boxes' space) in one TMA store of whole 128-byte lines; the tensor
+          // map clips rows past the chunk and columns past H
+          uint8_t* const stg = sE + q * 8192;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(tb + static_cast<uint32_t>(c * 32), v);
-          if (vrow) {
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(tb + static_cast<uint32_t>(c * 32), v);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int col = n0 + c * 32 + 8 * i;
-              if (col < p.N) {
-                float sc[8];
-                if (F8) {
-                  load_scale8(p.w_scale, p.w_scale_stride, col, true, sc);
+              float sc[8];
+              if (F8) {
+                load_scale8(p.w_scale, p.w_scale_stride, col, col < p.N, sc);
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) sc[j] *= ysc;
-                } else {
+                for (int j = 0; j < 8; ++j) sc[j] *= ysc;
+              } else {
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) sc[j] = ysc;
+                for (int j = 0; j < 8; ++j) sc[j] = ysc;
+              }
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[8 * i + j] *= sc[j];
+            }
+            uint8_t* const buf = stg + (c & 1) * 4096;
+            if (lane == 0 && c >= 2) bulk_wait_group_read<1>();  // the store of two chunks ago has read buf
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<float4*>(buf + swz(lane, k)) =
+                  make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmOs, buf, n0 + c * 32, ta.out_row + q * 32);
+              bulk_commit_group();
+            }
+          }
+          if (lane == 0) bulk_wait_group_read<0>();  // both buffers free for the warp's next tile
+        } else {
+          // grouped: rows stop at the expert's end, inside a box, so each lane stores its own row
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(tb + static_cast<uint32_t>(c * 32), v);
+            if (vrow) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int col = n0 + c * 32 + 8 * i;
+                if (col < p.N) {
+                  float sc[8];
+                  if (F8) {
+                    load_scale8(p.w_scale, p.w_scale_stride, col, true, sc);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) sc[j] *= ysc;
+                  } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) sc[j] = ysc;
+                  }
+                  float4* d = reinterpret_cast<float4*>(yrow + col);
+                  d[0] = make_float4(v[8 * i] * sc[0], v[8 * i + 1] * sc[1], v[8 * i + 2] * sc[2], v[8 * i + 3] * sc[3]);
+                  d[1] = make_float4(v[8 * i + 4] * sc[4], v[8 * i + 5] * sc[5], v[8 * i + 6] * sc[6],
+                                     v[8 * i + 7] * sc[7]);
                 }
-                float4* d = reinterpret_cast<float4*>(yrow + col);
-                d[0] = make_float4(v[8 * i] * sc[0], v[8 * i + 1] * sc[1], v[8 * i + 2] * sc[2], v[8 * i + 3] * sc[3]);
-                d[1] = make_float4(v[8 * i + 4] * sc[4], v[8 * i + 5] * sc[5], v[8 * i + 6] * sc[6],
-                                   v[8 * i + 7] * sc[7]);
               }
             }
           }

@@ -90,22 +90,22 @@ def kernel_sources_hash(dtype, kernel):
 
 
 NCU_TRAFFIC = {
-    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "77aa50ccbcdc"): 109771264 + 33087232,
-    ("llama3_8b_down", 8192, "bf16", "gemm_fused", 256, "77aa50ccbcdc"): 1174534656 + 122550016,
-    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 192, "77aa50ccbcdc"): 278787840 + 18025216,
-    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 256, "77aa50ccbcdc"): 286511872 + 22354432,
+    ("llama3_8b_oproj", 4096, "bf16", "gemm_fused", 256, "04894e535244"): 109651456 + 33146880,
+    ("llama3_8b_down", 8192, "bf16", "gemm_fused", 256, "04894e535244"): 1209827584 + 122526720,
+    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 192, "04894e535244"): 278789632 + 18013440,
+    ("gemma2_9b_down", 2048, "bf16", "gemm_fused", 256, "04894e535244"): 286519808 + 22036480,
     ("llama70b_down_decode", 8, "bf16", "gemm_splitk", 0, "384cbfdf0b50"): 471428352 + 3621120,
     ("llama70b_oproj_decode", 8, "bf16", "gemm_splitk", 0, "384cbfdf0b50"): 135542016 + 2951936,
-    ("llama3_8b_oproj", 4096, "e4m3", "gemm_fused", 224, "77aa50ccbcdc"): 67456512 + 17328384,
-    ("llama3_8b_down", 8192, "e4m3", "gemm_fused", 256, "77aa50ccbcdc"): 535526400 + 110201088,
+    ("llama3_8b_oproj", 4096, "e4m3", "gemm_fused", 224, "04894e535244"): 67461376 + 17776384,
+    ("llama3_8b_down", 8192, "e4m3", "gemm_fused", 256, "04894e535244"): 541988352 + 110707456,
     ("llama70b_oproj_decode", 8, "e4m3", "gemm_splitk", 0, "384cbfdf0b50"): 67211008 + 72704,
     ("llama70b_down_decode", 8, "e4m3", "gemm_splitk", 0, "384cbfdf0b50"): 236310016 + 3079680,
     ("llama70b_down_decode", 8, "nvfp4", "gemm_splitk", 0, "75d05af169d4"): 135886080 + 2963712,
     ("llama70b_oproj_decode", 8, "nvfp4", "gemm_splitk", 0, "75d05af169d4"): 37937152 + 0,
     ("llama70b_down_decode", 8, "mxfp4", "gemm_splitk", 0, "75d05af169d4"): 128547072 + 2881536,
     ("llama70b_oproj_decode", 8, "mxfp4", "gemm_splitk", 0, "75d05af169d4"): 35841280 + 0,
-    ("mixtral_8x7b_down_decode", 8, "moe", "moe_gemm", 256, "6266342f59fb"): 822599168 + 3301120,
-    ("mixtral_8x7b_down", 4096, "moe", "moe_gemm", 256, "6266342f59fb"): 1398003200 + 122324992,
+    ("mixtral_8x7b_down_decode", 8, "moe", "moe_gemm", 256, "b78e8675c0a1"): 822593536 + 2991872,
+    ("mixtral_8x7b_down", 4096, "moe", "moe_gemm", 256, "b78e8675c0a1"): 1400630016 + 123581440,
 }
 def traffic_tile(kname, plan):
     return plan["tile_n"] if kname in ("gemm_fused", "gemm_slot") else 0

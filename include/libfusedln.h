@@ -307,7 +307,9 @@ int fln_moe_gather(const fln_bf16* x, const int* row_token, int T, int k, int H,
  *
  * y is kept in fp32 in the library workspace ([T * k, H]); the grouped GEMM
  * is a persistent tcgen05 kernel over (expert, 128-row tile, 256-column tile)
- * items read from the device offsets, so no host synchronisation is needed.
+ * items read from the device offsets (with T * k >= 256 E: over (expert,
+ * 256-row block, 256-column tile) tiles on CTA pairs), so no host
+ * synchronisation is needed.
  * Offsets that are not a grouping of the T * k rows (0 first, T * k last,
  * non-decreasing) make the call write nothing, a row_of entry outside
  * [0, T * k) leaves that token's residual and out rows untouched; either
